@@ -1,0 +1,276 @@
+"""fp64 reference definitions of (Block) Attention Residuals.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): never imported by the
+product path, and sharing no code with the CUDA kernels.
+
+Sources cited (page title, then the section / equation on it):
+
+* [Deep-dive 2] "Kimi K3 deep-dive series (2): AttnRes and Stable LatentMoE",
+  §1 (plain residual), §2 (pseudo-code and the a_l / r_l formula), §2.1 (the
+  four-source worked example), §3 (Block AttnRes, nine sources).
+* [Tutorial] Kimi K3 chaptered tutorial (kimi.papertok.ai), ch. 0.11
+  (RMSNorm: square, mean, square root), ch. 4.2 (Eq. 8-9: pseudo-query,
+  keys = values = layer outputs, phi(q, k) = exp(q^T RMSNorm(k))), ch. 4.3
+  (Eq. 10: the two-case value list, the final output aggregating all block
+  representations), ch. 4.5 (12-layer blocks, incomplete last block, nine
+  sources counting the embedding).
+* [Parts 6] "Kimi K3 model structure (6): inputs and parts", list of odd
+  facts (RMSNorm eps = 1e-5 model-wide).
+* [Atlas] "LLM Atlas · Kimi K3", §07 Attention Residuals (alpha_{i->l} and
+  h_l = sum_i alpha v_i), §28 workbench "save per block, not per layer"
+  (ceil(L/S) + embedding sources), and the reduced study's train-time forward
+  intervention (uniform mixer: zero logits give the mean of the sources).
+
+Everything is float64.  Inputs of any float dtype are widened exactly
+(bf16 and fp32 values are exactly representable in fp64).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Callable, Sequence
+
+import numpy as np
+
+EPS = 1e-5  # [Parts 6]: RMSNorm eps is 1e-5 throughout the model
+
+
+# --------------------------------------------------------------------------
+# One aggregation: a_l = softmax(w_l RMSNorm(H)^T), r_l = a_l H   [Deep-dive 2 §2]
+# --------------------------------------------------------------------------
+
+def rms(h: np.ndarray, eps: float = EPS) -> np.ndarray:
+    """Root mean square over the last axis, eps added to the mean square.
+
+    [Tutorial ch. 0.11]: square each value, take the mean, take the square
+    root.  The eps of [Parts 6] goes inside the root (the usual RMSNorm
+    placement; the pages do not print the formula)."""
+    h = np.asarray(h, dtype=np.float64)
+    return np.sqrt(np.mean(h * h, axis=-1) + eps)
+
+
+def rmsnorm(h: np.ndarray, eps: float = EPS) -> np.ndarray:
+    """RMSNorm with no learned gain, as in the pseudo-code of [Deep-dive 2 §2]."""
+    h = np.asarray(h, dtype=np.float64)
+    return h / rms(h, eps)[..., None]
+
+
+def depth_attention(H: Sequence[np.ndarray] | np.ndarray, w: np.ndarray,
+                    eps: float = EPS) -> tuple[np.ndarray, np.ndarray]:
+    """Depth-wise attention of one layer over its sources.
+
+    H: the S sources, stacked as [S, T, d] (or a list of S arrays [T, d]);
+    w: the layer's pseudo-query [d].
+    Returns (r [T, d], a [T, S]), both float64:
+
+        keys   = RMSNorm(H)                       (per source row, no gain)
+        logits = w . keys                          (no temperature)
+        a      = softmax over the S sources
+        r      = sum_s a_s H_s                     (values are the raw sources)
+
+    [Deep-dive 2 §2] pseudo-code and formula; [Tutorial ch. 4.2] Eq. 8-9;
+    [Atlas §07] alpha_{i->l}.  The softmax subtracts the per-token maximum
+    logit first, which leaves it unchanged mathematically.
+    """
+    H = np.stack([np.asarray(h, dtype=np.float64) for h in H]) if not isinstance(H, np.ndarray) \
+        else np.asarray(H, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    if H.ndim != 3:
+        raise ValueError("H must be [S, T, d]")
+    keys = rmsnorm(H, eps)                                   # [S, T, d]
+    logits = np.einsum("std,d->ts", keys, w)                 # [T, S]
+    logits = logits - logits.max(axis=1, keepdims=True)
+    e = np.exp(logits)
+    a = e / e.sum(axis=1, keepdims=True)                     # [T, S]
+    r = np.einsum("ts,std->td", a, H)                        # [T, d]
+    return r, a
+
+
+# --------------------------------------------------------------------------
+# Block bookkeeping: which sources layer l sees   [Tutorial ch. 4.3 Eq. 10]
+# --------------------------------------------------------------------------
+
+def block_index(layer: int, block_size: int) -> int:
+    """Block n (1-based) that layer `layer` (1-based) belongs to."""
+    return (layer - 1) // block_size + 1
+
+
+def position_in_block(layer: int, block_size: int) -> int:
+    """Position i (1-based) of layer `layer` inside its block."""
+    return (layer - 1) % block_size + 1
+
+
+def num_blocks(num_layers: int, block_size: int) -> int:
+    """N = ceil(L / B); the last block may be incomplete ([Tutorial ch. 4.5])."""
+    return -(-num_layers // block_size)
+
+
+def block_layers(n: int, block_size: int, num_layers: int) -> range:
+    """The layers whose outputs are summed into block representation b_n."""
+    first = (n - 1) * block_size + 1
+    last = min(n * block_size, num_layers)
+    return range(first, last + 1)
+
+
+def value_list(layer: int, block_size: int, num_layers: int) -> list[tuple]:
+    """Eq. 10's value list for `layer` in 1..L, or the final output for L+1.
+
+    Entries, in source order:
+      ("embed",)                      b_0 = h_0, the token embedding
+      ("block", k, first, last)       b_k = sum of outputs of layers first..last
+      ("partial", n, first, last)     the current block's partial sum over
+                                      layers first..last (only when non-empty:
+                                      the block's first layer gets no zero
+                                      source)
+    [Tutorial ch. 4.3]: layer i of block n reads [b_0 .. b_{n-1}] when i = 1
+    and [b_0 .. b_{n-1}, b_n^{i-1}] when i >= 2; the final output layer reads
+    all N block representations ([Tutorial ch. 4.3], last paragraph).
+    """
+    L, B = num_layers, block_size
+    if not (1 <= layer <= L + 1):
+        raise ValueError("layer out of range")
+    out: list[tuple] = [("embed",)]
+    if layer == L + 1:
+        for k in range(1, num_blocks(L, B) + 1):
+            lay = block_layers(k, B, L)
+            out.append(("block", k, lay[0], lay[-1]))
+        return out
+    n, i = block_index(layer, B), position_in_block(layer, B)
+    for k in range(1, n):
+        lay = block_layers(k, B, L)
+        out.append(("block", k, lay[0], lay[-1]))
+    if i >= 2:
+        first = (n - 1) * B + 1
+        out.append(("partial", n, first, layer - 1))
+    return out
+
+
+def num_sources(layer: int, block_size: int, num_layers: int) -> int:
+    """Number of sources layer `layer` attends over (len of the value list)."""
+    return len(value_list(layer, block_size, num_layers))
+
+
+# --------------------------------------------------------------------------
+# Storage rounding (the stack stores every tensor it writes in bf16 or fp32)
+# --------------------------------------------------------------------------
+
+_BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value, ties to even,
+    returned as float64.  bfloat16 keeps 8 significant bits and fp32's
+    exponent range (subnormal quantum 2^-133); overflow gives +-inf."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)                       # x = m 2^e, 0.5 <= |m| < 1
+    q = np.maximum(e - 8, -133)              # quantum exponent of x's binade
+    y = np.ldexp(np.rint(np.ldexp(x, -q)), q)  # rint: round half to even
+    return np.where(np.abs(y) > _BF16_MAX, np.copysign(np.inf, x), y)
+
+
+def round_fp32(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to float32 (IEEE, ties to even), returned as float64."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def _identity(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# The synthetic layer body that stands in for KDA/MLA + MoE in the stack
+# --------------------------------------------------------------------------
+
+def synthetic_layer(x: np.ndarray, g: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """F_l(x) = tanh(x * g_l) * s_l, per channel (a stand-in layer body, not
+    part of the method)."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.tanh(x * np.asarray(g, np.float64)) * np.asarray(s, np.float64)
+
+
+# --------------------------------------------------------------------------
+# Stacks
+# --------------------------------------------------------------------------
+
+@dataclass
+class StackTrace:
+    """Everything a stack forward produced, per layer (index 0 = layer 1)."""
+    r: list = field(default_factory=list)          # r_l [T, d], l = 1..L+1 (as stored)
+    a: list = field(default_factory=list)          # a_l [T, S_l], l = 1..L+1
+    v: list = field(default_factory=list)          # v_l = F_l(r_l) [T, d], l = 1..L (as stored)
+    final_sources: list = field(default_factory=list)  # sources of the final aggregation
+
+
+def _fold_sum(terms: list, store: Callable) -> np.ndarray:
+    """Sum of the terms in order, each running total stored (rounded) once:
+    ((t1 + t2) -> store) + t3 -> store ...  (plain sum when store is exact)."""
+    acc = terms[0]
+    for t in terms[1:]:
+        acc = store(acc + t)
+    return acc
+
+
+def block_stack_forward(h0: np.ndarray, W: np.ndarray, layer_fn: Callable[[int, np.ndarray], np.ndarray],
+                        num_layers: int, block_size: int, eps: float = EPS,
+                        store: Callable | None = None) -> StackTrace:
+    """Block AttnRes forward through L layers and the final aggregation.
+
+    Layer l (1..L) aggregates the sources of `value_list(l)` with pseudo-query
+    W[l-1], giving r_l; the layer body then gives v_l = layer_fn(l, r_l), the
+    layer's OUTPUT (not r_l + v_l: keys and values are the layer outputs,
+    [Tutorial ch. 4.2], and b_n is the sum of the outputs of block n,
+    [Tutorial ch. 4.3]).  After layer L the final aggregation (l = L+1) uses
+    W[L] over [h_0, b_1 .. b_N].
+
+    Every source is rebuilt from the list of layer outputs for each layer
+    (b_k and the partial sum are sums over explicit layer ranges).  `store`
+    models storage rounding (e.g. `round_bf16`): it is applied to every
+    tensor the stack writes (r_l, v_l, and each running total of a block sum);
+    None means exact fp64 throughout.
+    """
+    store = store or _identity
+    L, B = num_layers, block_size
+    W = np.asarray(W, dtype=np.float64)
+    h0 = np.asarray(h0, dtype=np.float64)
+    outputs = {0: h0}                               # v_0 = h_0
+    tr = StackTrace()
+    for layer in range(1, L + 2):
+        srcs = []
+        for entry in value_list(layer, B, L):
+            if entry[0] == "embed":
+                srcs.append(h0)
+            else:
+                _, _, first, last = entry
+                srcs.append(_fold_sum([outputs[j] for j in range(first, last + 1)], store))
+        r, a = depth_attention(np.stack(srcs), W[layer - 1], eps)
+        r = store(r)
+        tr.r.append(r)
+        tr.a.append(a)
+        if layer <= L:
+            v = store(layer_fn(layer, r))
+            outputs[layer] = v
+            tr.v.append(v)
+        else:
+            tr.final_sources = srcs
+    return tr
+
+
+def full_stack_forward(h0: np.ndarray, W: np.ndarray, layer_fn: Callable[[int, np.ndarray], np.ndarray],
+                       num_layers: int, eps: float = EPS) -> StackTrace:
+    """Full AttnRes: layer l attends over [h_0, v_1 .. v_{l-1}] (every earlier
+    layer output, [Deep-dive 2 §2] H_<l; [Tutorial ch. 4.2]); the final output
+    over [h_0, v_1 .. v_L].  Exact fp64; written separately from the block
+    version so the two can check each other."""
+    W = np.asarray(W, dtype=np.float64)
+    history = [np.asarray(h0, dtype=np.float64)]
+    tr = StackTrace()
+    for layer in range(1, num_layers + 2):
+        r, a = depth_attention(np.stack(history), W[layer - 1], eps)
+        tr.r.append(r)
+        tr.a.append(a)
+        if layer <= num_layers:
+            v = np.asarray(layer_fn(layer, r), dtype=np.float64)
+            tr.v.append(v)
+            history.append(v)
+        else:
+            tr.final_sources = list(history)
+    return tr

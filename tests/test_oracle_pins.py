@@ -1,0 +1,363 @@
+"""Pins of the fp64 oracle to what the pages and the mathematics fix.
+
+Each test is chosen so that a plausible mistake in the oracle (a dropped
+term, a wrong axis, a transposed operand, eps in the wrong place, a 1/sqrt(d)
+temperature, normalised values instead of raw ones, an off-by-one in the
+block bookkeeping) fails at least one of them.  None of them calls the CUDA
+path.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.conftest import read_golden
+
+RNG = np.random.default_rng(12345)
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def _orth_to(w, y):
+    """Component of y orthogonal to w."""
+    return y - (y @ w) / (w @ w) * w
+
+
+def _sources_with_logits(w, z, d, T=1, eps=O.EPS, ms=1.0, rng=RNG):
+    """Sources h_s (s = 0..S-1) whose RMSNorm logits against w are exactly z_s.
+
+    h_s = c_s u + y_s with u = w / |w|^2 (so w.h_s = c_s) and y_s orthogonal
+    to w, scaled so that mean(h_s^2) = ms; then rms = sqrt(ms + eps) and
+    choosing c_s = z_s sqrt(ms + eps) gives logit z_s.
+    """
+    u = w / (w @ w)
+    H = np.empty((len(z), T, d))
+    for s, zs in enumerate(z):
+        c = zs * math.sqrt(ms + eps)
+        for t in range(T):
+            y = _orth_to(w, rng.standard_normal(d))
+            need = d * ms - c * c * (u @ u)
+            assert need > 0
+            y *= math.sqrt(need / (y @ y))
+            H[s, t] = c * u + y
+    return H
+
+
+# ------------------------------------------------- worked example (§2.1) ---
+
+def test_worked_example_four_sources(golden_dir):
+    rows = read_golden(os.path.join(golden_dir, "worked_example_4src.txt"))
+    a_page = np.array([float(r[1]) for r in rows])
+    assert [int(r[0]) for r in rows] == [0, 1, 2, 3]
+    assert abs(a_page.sum() - 1.0) < 1e-15
+    d = 256
+    w = RNG.standard_normal(d) / math.sqrt(d)
+    H = _sources_with_logits(w, np.log(a_page), d, T=3)
+    r, a = O.depth_attention(H, w)
+    np.testing.assert_allclose(a, np.tile(a_page, (3, 1)), rtol=0, atol=1e-12)
+    # r_4 = 0.05 h_0 + 0.10 h_1 + 0.70 h_2 + 0.15 h_3, from the page's weights
+    r_page = 0.05 * H[0] + 0.10 * H[1] + 0.70 * H[2] + 0.15 * H[3]
+    np.testing.assert_allclose(r, r_page, rtol=1e-12, atol=1e-12 * np.abs(H).max())
+
+
+# ------------------------------------------------ definitions & closed forms -
+
+def test_rms_closed_form_constant_rows():
+    # a constant row c*1 has mean square c^2; eps goes inside the root
+    for c in [0.0, 1e-3, 0.5, -2.0, 37.0]:
+        for eps in [0.0, 1e-5, 0.25]:
+            h = np.full((1, 64), c)
+            assert abs(O.rms(h, eps)[0] - math.sqrt(c * c + eps)) <= 1e-15 * max(1, abs(c))
+    # mean over the channel axis, not over tokens: rows with different scales
+    h = np.stack([np.full(16, 1.0), np.full(16, 3.0)])
+    np.testing.assert_allclose(O.rms(h, 0.0), [1.0, 3.0], rtol=1e-15)
+
+
+def test_logits_closed_form_constant_sources():
+    # h_s[t] = c_{s,t} * 1 (all channels equal): logit = c sum(w) / sqrt(c^2 + eps),
+    # with no 1/sqrt(d) temperature; weights follow.
+    d, S, T = 48, 3, 5
+    w = RNG.standard_normal(d)
+    c = RNG.uniform(-3, 3, size=(S, T))
+    H = np.repeat(c[:, :, None], d, axis=2)
+    for eps in [0.0, 1e-5, 0.5]:
+        z = (c * w.sum() / np.sqrt(c * c + eps)).T          # [T, S]
+        a_cf = np.exp(z - z.max(1, keepdims=True))
+        a_cf /= a_cf.sum(1, keepdims=True)
+        r_cf = (a_cf * c.T).sum(1)                          # every channel of r equals this
+        r, a = O.depth_attention(H, w, eps)
+        np.testing.assert_allclose(a, a_cf, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(r, np.repeat(r_cf[:, None], d, 1), rtol=1e-13, atol=1e-15)
+
+
+def test_single_source_returns_it_exactly():
+    # layer 1 of a block stack sees only h_0: weight 1, r = h_0 bit for bit
+    h = RNG.standard_normal((1, 7, 33))
+    r, a = O.depth_attention(h, RNG.standard_normal(33))
+    assert np.array_equal(a, np.ones((7, 1)))
+    assert np.array_equal(r, h[0])
+
+
+def test_zero_query_is_uniform_mean():
+    # uniform mixer: zero logits -> w_i = 1/N -> output = sum_i source_i / N
+    S, T, d = 5, 4, 24
+    H = RNG.standard_normal((S, T, d)) * RNG.uniform(0.1, 10, size=(S, 1, 1))
+    r, a = O.depth_attention(H, np.zeros(d))
+    np.testing.assert_allclose(a, np.full((T, S), 1.0 / S), rtol=1e-15)
+    np.testing.assert_allclose(r, H.mean(0), rtol=1e-13, atol=1e-14)
+
+
+def test_dominant_logit_selects_that_source():
+    d = 128
+    w = RNG.standard_normal(d)          # |w|^2 ~ d leaves room for logit 45
+    for j in range(4):
+        z = np.zeros(4)
+        z[j] = 45.0                          # other weights ~ e^-45 ~ 3e-20
+        H = _sources_with_logits(w, z, d, T=2)
+        r, a = O.depth_attention(H, w)
+        np.testing.assert_allclose(a[:, j], 1.0, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(r, H[j], rtol=0, atol=1e-15 * np.abs(H).max() * 8)
+
+
+def test_values_are_raw_sources_not_normalised():
+    # scaling a source by k keeps its weight (with eps = 0) but scales its
+    # contribution to r by k: values are the un-normalised sources
+    d, S, T = 32, 3, 4
+    H = RNG.standard_normal((S, T, d))
+    w = RNG.standard_normal(d) / math.sqrt(d)
+    r0, a0 = O.depth_attention(H, w, eps=0.0)
+    H2 = H.copy()
+    H2[1] *= 7.0
+    r1, a1 = O.depth_attention(H2, w, eps=0.0)
+    np.testing.assert_allclose(a1, a0, rtol=1e-13)
+    np.testing.assert_allclose(r1 - r0, 6.0 * a0[:, 1:2] * H[1], rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------- invariants ---
+
+def test_weights_nonnegative_sum_to_one_and_convex_hull():
+    for S in [1, 2, 4, 9, 17]:
+        H = RNG.standard_normal((S, 6, 40)) * RNG.uniform(0.01, 100, size=(S, 6, 1))
+        w = RNG.standard_normal(40) * 0.5
+        r, a = O.depth_attention(H, w)
+        assert (a >= 0).all()
+        np.testing.assert_allclose(a.sum(1), 1.0, rtol=0, atol=1e-15)
+        lo, hi = H.min(0), H.max(0)
+        tol = 1e-13 * np.abs(H).max()
+        assert (r >= lo - tol).all() and (r <= hi + tol).all()
+
+
+def test_permuting_sources_permutes_weights_keeps_output():
+    S, T, d = 6, 5, 20
+    H = RNG.standard_normal((S, T, d))
+    w = RNG.standard_normal(d)
+    r, a = O.depth_attention(H, w)
+    perm = RNG.permutation(S)
+    rp, ap = O.depth_attention(H[perm], w)
+    np.testing.assert_allclose(ap, a[:, perm], rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(rp, r, rtol=1e-13, atol=1e-14)
+
+
+def test_rescaling_one_source_leaves_weights_unchanged():
+    # the purpose of the RMSNorm keys: a large-norm source cannot dominate
+    # merely by its norm.  Exact at eps = 0; with eps > 0 the change is tiny
+    # but not zero (eps is really used).
+    S, T, d = 4, 3, 64
+    H = RNG.standard_normal((S, T, d))
+    w = RNG.standard_normal(d) / math.sqrt(d)
+    _, a0 = O.depth_attention(H, w, eps=0.0)
+    for k in [1e-3, 0.5, 3.0, 1e4]:
+        H2 = H.copy()
+        H2[2] *= k
+        _, a1 = O.depth_attention(H2, w, eps=0.0)
+        np.testing.assert_allclose(a1, a0, rtol=1e-13, atol=1e-16)
+    _, a_eps = O.depth_attention(H, w, eps=1e-5)
+    H2 = H.copy()
+    H2[2] *= 1e-2                      # mean square 1e-4: eps now matters (~5%)
+    _, a_eps2 = O.depth_attention(H2, w, eps=1e-5)
+    diff = np.abs(a_eps2 - a_eps).max()
+    assert 1e-6 < diff < 0.1
+
+
+# -------------------------------------------------------- bf16 rounding pin -
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    x = np.concatenate([
+        RNG.standard_normal(20000) * 10.0 ** RNG.integers(-30, 30, 20000),
+        RNG.standard_normal(2000),
+        [0.0, -0.0, 1.0, -1.0, 3.4e38, -3.4e38, 1e-40, -1e-42],
+    ]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_bf16(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_round_bf16_ties_to_even():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: rounds to 1 (even)
+    assert O.round_bf16(np.array([1 + 2 ** -8]))[0] == 1.0
+    # 1 + 3*2^-8 is halfway between 1 + 2^-7 and 1 + 2^-6: rounds up (even)
+    assert O.round_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6
+    # just above a tie rounds away
+    assert O.round_bf16(np.array([1 + 2 ** -8 + 2 ** -40]))[0] == 1 + 2 ** -7
+    assert O.round_bf16(np.array([-(1 + 2 ** -8 + 2 ** -40)]))[0] == -(1 + 2 ** -7)
+
+
+# ------------------------------------------------ block bookkeeping (Eq. 10) -
+
+def test_k3_block_layout_and_source_counts(golden_dir):
+    g = {r[0]: int(r[1]) for r in read_golden(os.path.join(golden_dir, "k3_block_layout.txt"))}
+    L, B = g["num_layers"], g["block_size"]
+    assert O.num_blocks(L, B) == g["num_blocks"]
+    assert len(O.block_layers(g["num_blocks"], B, L)) == g["last_block_layers"]
+    assert list(O.block_layers(8, B, L)) == list(range(85, 94))
+    counts = [O.num_sources(l, B, L) for l in range(1, L + 2)]
+    # the final aggregation sees the embedding plus all 8 block representations
+    assert counts[-1] == g["block_sources"] == math.ceil(L / B) + 1
+    assert max(counts) == g["block_sources"]
+    # Full AttnRes (block size 1): L outputs + embedding at the top
+    assert O.num_sources(L + 1, 1, L) == g["full_sources"] == L + 1
+    # derived totals: 12n + 11 per full block n = 1..7, 8*9 + 8 for the last
+    assert sum(counts[:L]) == 493
+    assert counts[0] == 1 and counts[1] == 2 and counts[11] == 2
+    assert counts[12] == 2 and counts[13] == 3          # layer 13 opens block 2
+    assert counts[84] == 8 and counts[85] == 9           # layer 85 opens block 8
+    # the site's per-token state estimate
+    d = g["hidden"]
+    assert abs(L * d - g["full_values_per_token_approx"]) / g["full_values_per_token_approx"] < 0.01
+    assert abs(9 * d - g["block_values_per_token_approx"]) / g["block_values_per_token_approx"] < 0.01
+    assert abs(L * d * 2 / 1e6 - 1.3) < 0.05 and abs(9 * d * 2 / 1e3 - 129) < 1
+
+
+def test_value_list_two_cases():
+    L, B = 93, 12
+    # first layer of block 3: [b_0, b_1, b_2], no empty partial
+    assert O.value_list(25, B, L) == [("embed",), ("block", 1, 1, 12), ("block", 2, 13, 24)]
+    # layer 3 of block 3: ... plus the partial sum of layers 25, 26
+    assert O.value_list(27, B, L)[-1] == ("partial", 3, 25, 26)
+    # final output: embedding plus the 8 blocks, the last one layers 85..93
+    fin = O.value_list(94, B, L)
+    assert fin[0] == ("embed",) and fin[-1] == ("block", 8, 85, 93) and len(fin) == 9
+    # block size 1 is Full AttnRes: layer l sees the embedding and l-1 outputs
+    for l in range(1, 8):
+        vl = O.value_list(l, 1, 7)
+        assert vl == [("embed",)] + [("block", k, k, k) for k in range(1, l)]
+    with pytest.raises(ValueError):
+        O.value_list(0, B, L)
+    with pytest.raises(ValueError):
+        O.value_list(L + 2, B, L)
+
+
+# --------------------------------------------------------- synthetic layer --
+
+def test_synthetic_layer_closed_forms():
+    g = np.array([2.0, -0.5, 1.0])
+    s = np.array([0.1, 0.2, 0.05])
+    assert np.array_equal(O.synthetic_layer(np.zeros(3), g, s), np.zeros(3))
+    x = np.arctanh(0.5) / g                      # tanh(x g) = 0.5
+    np.testing.assert_allclose(O.synthetic_layer(x, g, s), 0.5 * s, rtol=1e-15)
+    np.testing.assert_allclose(O.synthetic_layer(-x, g, s), -0.5 * s, rtol=1e-15)
+
+
+# ---------------------------------------------------------------- stacks ----
+
+def _tiny_stack(L, d, T, seed):
+    rng = np.random.default_rng(seed)
+    h0 = rng.standard_normal((T, d))
+    W = rng.standard_normal((L + 1, d)) / math.sqrt(d)
+    G = rng.standard_normal((L, d))
+    Sc = rng.uniform(0.05, 0.2, size=(L, d))
+    fn = lambda l, x: O.synthetic_layer(x, G[l - 1], Sc[l - 1])
+    return h0, W, G, Sc, fn
+
+
+def test_block_size_one_equals_full_attnres():
+    L, d, T = 6, 16, 3
+    h0, W, G, Sc, fn = _tiny_stack(L, d, T, 7)
+    blk = O.block_stack_forward(h0, W, fn, L, 1)
+    full = O.full_stack_forward(h0, W, fn, L)
+    for l in range(L + 1):
+        np.testing.assert_allclose(blk.a[l], full.a[l], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(blk.r[l], full.r[l], rtol=1e-13, atol=1e-14)
+    for s_b, s_f in zip(blk.final_sources, full.final_sources):
+        np.testing.assert_allclose(s_b, s_f, rtol=1e-13, atol=1e-14)
+
+
+def test_block_size_at_least_L_is_embedding_plus_partial():
+    # one block holding every layer: layer l >= 2 sees [h_0, v_1 + .. + v_{l-1}]
+    L, d, T = 5, 12, 2
+    h0, W, G, Sc, fn = _tiny_stack(L, d, T, 8)
+    tr = O.block_stack_forward(h0, W, fn, L, L)
+    for l in range(2, L + 1):
+        part = sum(tr.v[j - 1] for j in range(1, l))
+        r, a = O.depth_attention(np.stack([h0, part]), W[l - 1])
+        np.testing.assert_allclose(tr.r[l - 1], r, rtol=1e-13, atol=1e-14)
+    assert len(tr.final_sources) == 2
+    np.testing.assert_allclose(tr.final_sources[1], sum(tr.v), rtol=1e-13, atol=1e-14)
+
+
+def test_stack_rounding_mode_stores_bf16_values():
+    L, d, T = 7, 16, 3
+    h0, W, G, Sc, fn = _tiny_stack(L, d, T, 9)
+    h0 = O.round_bf16(h0)
+    tr = O.block_stack_forward(h0, W, fn, L, 3, store=O.round_bf16)
+    for x in tr.r + tr.v + tr.final_sources:
+        assert np.array_equal(O.round_bf16(x), x)
+    ex = O.block_stack_forward(h0, W, fn, L, 3)
+    # rounding only perturbs at the bf16 level
+    np.testing.assert_allclose(tr.r[-1], ex.r[-1], rtol=0.05, atol=0.05)
+
+
+def _brute_force_stack(h0, W, G, Sc, L, B, eps=O.EPS):
+    """Independent high-precision stack, written as a running-state machine
+    from the two cases of Eq. 10 (the oracle instead rebuilds every source
+    from explicit layer ranges).  mpmath at 40 digits, one token at a time."""
+    mpmath = pytest.importorskip("mpmath")
+    mp = mpmath.mp
+    mp.dps = 40
+    T, d = h0.shape
+    out_r, out_a = [], []
+    for t in range(T):
+        emb = [mp.mpf(float(x)) for x in h0[t]]
+        blocks = []              # completed block representations
+        partial = None           # running sum of the current block, None if empty
+        rs, as_ = [], []
+        for layer in range(1, L + 2):
+            srcs = [emb] + blocks + ([partial] if partial is not None else [])
+            wq = [mp.mpf(float(x)) for x in W[layer - 1]]
+            z = []
+            for h in srcs:
+                ms = mp.fsum(x * x for x in h) / d
+                z.append(mp.fsum(a * b for a, b in zip(wq, h)) / mp.sqrt(ms + mp.mpf(eps)))
+            m = max(z)
+            e = [mp.exp(zz - m) for zz in z]
+            tot = mp.fsum(e)
+            a = [ee / tot for ee in e]
+            r = [mp.fsum(a[s] * srcs[s][c] for s in range(len(srcs))) for c in range(d)]
+            rs.append([float(x) for x in r])
+            as_.append([float(x) for x in a])
+            if layer == L + 1:
+                break
+            v = [mp.tanh(r[c] * mp.mpf(float(G[layer - 1, c]))) * mp.mpf(float(Sc[layer - 1, c]))
+                 for c in range(d)]
+            partial = v if partial is None else [p + q for p, q in zip(partial, v)]
+            if layer % B == 0 or layer == L:      # the block ends here
+                blocks.append(partial)
+                partial = None
+        out_r.append(rs)
+        out_a.append(as_)
+    return out_r, out_a
+
+
+@pytest.mark.parametrize("L,B", [(4, 1), (5, 2), (7, 3), (6, 3), (7, 2)])
+def test_block_stack_matches_brute_force(L, B):
+    d, T = 8, 2
+    h0, W, G, Sc, fn = _tiny_stack(L, d, T, 100 + 10 * L + B)
+    tr = O.block_stack_forward(h0, W, fn, L, B)
+    br, ba = _brute_force_stack(h0, W, G, Sc, L, B)
+    for l in range(L + 1):
+        for t in range(T):
+            np.testing.assert_allclose(tr.r[l][t], br[t][l], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(tr.a[l][t], ba[t][l], rtol=1e-12, atol=1e-14)

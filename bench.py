@@ -1,0 +1,471 @@
+"""Benchmark of the Block AttnRes depth-aggregation hot path on GB300.
+
+One step = one `attnres_aggregate` launch over the K3-width single-layer
+workload: T=4096 tokens, d=7168, S=9 bf16 sources [h_0, b_1..b_7, partial]
+(fp32 arithmetic, bf16 output r, fp32 weights).  Inputs are resident in HBM
+when the timed region starts; three input sets of 528 MB each (each larger
+than the 129 MB L2) are rotated, so no step reads what the previous one left
+in L2.
+
+Printed (rank 0, one JSON line): tokens/s of the whole job, the roofline of
+the aggregation kernel (algorithmic bytes / CUDA-event launch time against
+the measured HBM copy bandwidth), an end-to-end figure through the public
+API with host buffers (pinned H2D of the sources, D2H of r and the weights
+inside the timed region), the fp64 oracle timed on the host cores on a
+bounded sample, the SM clocks sampled during the timed region, and the
+secondary workloads (93-layer prefill and decode stacks, 128K-token long
+context).
+
+`--impl reference` times the fp64 CPU oracle instead (the only reference
+implementation of this method here), on the same workload and metric.
+
+Multi-GPU (torchrun, one rank per GPU): every rank aggregates its own batch
+of 4096 tokens (tokens are independent, so the path shards with no data
+exchange: weak scaling); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "AttnRes depth-aggregation tokens/s & HBM GB/s (% of peak), d=7168, 9 sources"
+T_MAIN, D_MAIN, S_MAIN = 4096, 7168, 9
+WORKLOAD = "block_attnres_single_layer_T4096_d7168_S9"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "aggregate_ring_T4096_d7168_S9.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "depth_wise_attention_block_gb300", "csrc", f)
+                  for f in ("aggregate.cu", "device_common.cuh")]
+
+
+def algorithmic_bytes(T: int, d: int, S: int, esz: int = 2) -> int:
+    """Each source row read once, r written once (bf16), weights once (fp32);
+    the 28 KB pseudo-query is negligible and not counted."""
+    return T * (S * d * esz + d * esz + S * 4)
+
+
+# ------------------------------------------------------------------ dist ---
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks ---
+
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+            0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (read-only)
+    during the timed region; falls back to nvidia-smi."""
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._h = None
+        self._smi = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            assert nv.nvmlInit_v2() == 0
+            h = ctypes.c_void_p()
+            bus = torch.cuda.get_device_properties(device_index)
+            busid = "%08x:%02x:%02x.0" % (getattr(bus, "pci_domain_id", 0), bus.pci_bus_id, bus.pci_device_id)
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(busid.encode(), ctypes.byref(h)) != 0:
+                assert nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(h)) == 0
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._h = nv, h
+        except Exception:
+            self._nvml = None
+
+    def _poll(self):
+        nv, h = self._nvml, self._h
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._thr = threading.Thread(target=self._poll, daemon=True)
+            self._thr.start()
+        else:
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100", "-i", "0"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self._smi = None
+        return self
+
+    def __exit__(self, *exc):
+        if self._nvml is not None:
+            self._stop.set()
+            self._thr.join()
+        elif self._smi is not None:
+            self._smi.terminate()
+            out, _ = self._smi.communicate(timeout=5)
+            for line in out.strip().splitlines():
+                try:
+                    sm, mx, rs = [x.strip() for x in line.split(",")]
+                    self.samples.append((int(sm), int(rs, 16)))
+                    self.max_mhz = int(mx)
+                except ValueError:
+                    pass
+
+    def summary(self) -> dict:
+        reasons = set()
+        for _, rs in self.samples:
+            for bit, name in _REASONS.items():
+                if rs & bit and name != "gpu_idle":
+                    reasons.add(name)
+        sms = [s for s, _ in self.samples]
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sms),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+
+# ------------------------------------------------------------------ peaks ---
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per launch of the aggregation kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()
+    try:
+        kv = {}
+        with open(PROFILE_SUMMARY) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith(("kernel_source_sha256", "dram_bytes_per_launch")):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip().strip("`")
+        if kv.get("kernel_source_sha256") == digest:
+            return int(kv["dram_bytes_per_launch"]), digest
+    except Exception:
+        pass
+    return None, digest
+
+
+# ------------------------------------------------------------- CPU oracle ---
+
+def time_oracle(H_cpu: torch.Tensor, w_cpu: torch.Tensor, budget_s: float, chunk: int = 64):
+    """Run the fp64 oracle over consecutive token chunks of the workload for
+    about `budget_s` seconds; returns (tokens, seconds)."""
+    import oracle as O
+    w64 = w_cpu.double().numpy()
+    T = H_cpu.shape[1]
+    tokens, t0 = 0, time.perf_counter()
+    start = 0
+    while True:
+        h = H_cpu[:, start:start + chunk].double().numpy()
+        O.depth_attention(h, w64)
+        tokens += h.shape[1]
+        start = (start + chunk) % T
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return tokens, el
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    inp = W.block_bf16(T=T_MAIN, d=D_MAIN, seed=1, device="cpu")
+    # calibrate the per-step sample so warm-up + steps end within ~2 minutes
+    tok, el = time_oracle(inp.H, inp.w, 2.0, chunk=16)
+    rate = tok / el
+    per_step = max(1, int(rate * 110.0 / max(1, args.steps + args.warmup)))
+    per_step = min(per_step, T_MAIN)
+    import oracle as O
+    w64 = inp.w.double().numpy()
+    start = 0
+
+    def step():
+        nonlocal start
+        idx = [(start + i) % T_MAIN for i in range(per_step)]
+        start = (start + per_step) % T_MAIN
+        O.depth_attention(inp.H[:, idx].double().numpy(), w64)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    sample = f"{per_step} consecutive tokens of the {T_MAIN}-token workload per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_MAIN, "d": D_MAIN, "S": S_MAIN, "storage": "bf16",
+                   "tokens_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- GPU arm ---
+
+def bench_main(args, A, W, dev, ws):
+    """Timed steps of the main workload; returns the measurement dict."""
+    sets = [W.block_bf16(T=T_MAIN, d=D_MAIN, seed=1 + 1000 * k, device=dev) for k in range(3)]
+    r = torch.empty((T_MAIN, D_MAIN), dtype=torch.bfloat16, device=dev)
+    a = torch.empty((T_MAIN, S_MAIN), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % len(sets)]
+        A.attnres_aggregate(s.H, s.w, r, a, dev_err=err, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(dev.index or 0)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with sampler:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    per_launch = [s.elapsed_time(e) for s, e in ev]           # ms
+    region_ms = ev[0][0].elapsed_time(ev[-1][1])
+    assert int(err.item()) == 0, "device error flag set"
+    return {"region_ms": region_ms, "launch_ms_mean": statistics.fmean(per_launch),
+            "launch_ms_median": statistics.median(per_launch), "wall_s": t_wall, "clocks": sampler.summary(),
+            "launches": K, "sets": sets}
+
+
+def bench_e2e(args, A, dev, sets):
+    """Through the public API with host buffers: pinned H2D of the sources
+    and the query, the aggregation, D2H of r and the weights, every step."""
+    s = sets[0]
+    H_host = torch.empty(s.H.shape, dtype=s.H.dtype, pin_memory=True)
+    H_host.copy_(s.H)
+    w_host = s.w.cpu().pin_memory()
+    r_host = torch.empty((T_MAIN, D_MAIN), dtype=torch.bfloat16, pin_memory=True)
+    a_host = torch.empty((T_MAIN, S_MAIN), dtype=torch.float32, pin_memory=True)
+    H_dev, w_dev = torch.empty_like(s.H), torch.empty_like(s.w)
+    r_dev = torch.empty((T_MAIN, D_MAIN), dtype=torch.bfloat16, device=dev)
+    a_dev = torch.empty((T_MAIN, S_MAIN), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    K = max(3, min(args.steps, 30))
+    for _ in range(3):
+        A.aggregate_host(H_host, w_host, r_host, a_host, H_dev, w_dev, r_dev, a_dev, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        A.aggregate_host(H_host, w_host, r_host, a_host, H_dev, w_dev, r_dev, a_dev, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    h2d = H_host.numel() * H_host.element_size() + w_host.numel() * 4
+    d2h = r_host.numel() * 2 + a_host.numel() * 4
+    return {"value": T_MAIN / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K}
+
+
+def bench_stacks(A, W, dev, peak):
+    from depth_wise_attention_block_gb300.stack import StackForward
+    out = {}
+    for name, T, seed, graph, reps in (("stack_prefill_T2048", 2048, 2, False, 10),
+                                        ("stack_decode_T64", 64, 3, True, 50)):
+        stk = W.stack(T=T, seed=seed, device=dev)
+        fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size)
+        fwd.run()
+        if graph:
+            fwd.capture()
+        for _ in range(3):
+            fwd.run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fwd.run()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = fwd.bytes_moved() / (ms * 1e-3) / 1e9
+        out[name] = {"ms_per_forward": ms, "tokens_per_s": T / (ms * 1e-3), "layers": stk.num_layers,
+                     "us_per_layer": 1e3 * ms / (stk.num_layers + 1), "launches_per_forward": fwd.launches_per_forward(),
+                     "cuda_graph": graph, "bytes_per_forward": fwd.bytes_moved(), "achieved_gbs": gbs,
+                     "frac_of_hbm_peak": gbs / peak}
+        del fwd, stk
+        torch.cuda.empty_cache()
+    return out
+
+
+def bench_long(A, W, dev, peak, reps=8):
+    inp = W.block_T131072_d7168(device=dev)
+    T = inp.H.shape[1]
+    r = torch.empty((T, D_MAIN), dtype=torch.bfloat16, device=dev)
+    a = torch.empty((T, S_MAIN), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        A.attnres_aggregate(inp.H, inp.w, r, a)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        A.attnres_aggregate(inp.H, inp.w, r, a)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    gbs = algorithmic_bytes(T, D_MAIN, S_MAIN) / (ms * 1e-3) / 1e9
+    del inp, r, a
+    torch.cuda.empty_cache()
+    return {"block_attnres_single_layer_T131072_d7168_S9": {
+        "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": algorithmic_bytes(T, D_MAIN, S_MAIN),
+        "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}}
+
+
+def run_gpu(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import depth_wise_attention_block_gb300 as A
+    import workloads as W
+
+    peak, peak_src = hbm_peak()
+    m = bench_main(args, A, W, dev, ws)
+    region_ms = max_over_ranks(m["region_ms"], ws, dev)
+    launch_ms = max_over_ranks(m["launch_ms_mean"], ws, dev)
+    ms_per_step = region_ms / args.steps
+    value = ws * T_MAIN * args.steps / (region_ms * 1e-3)
+    bytes_launch = algorithmic_bytes(T_MAIN, D_MAIN, S_MAIN)
+    achieved = bytes_launch / (launch_ms * 1e-3) / 1e9
+    traffic, digest = profiled_traffic()
+
+    e2e = bench_e2e(args, A, dev, m["sets"])
+    e2e_ms = max_over_ranks(e2e["ms_per_step"], ws, dev)
+    e2e["value"] = ws * T_MAIN / (e2e_ms * 1e-3)
+    del m["sets"]
+    torch.cuda.empty_cache()
+
+    extras = {}
+    if not args.no_extras:
+        extras.update(bench_stacks(A, W, dev, peak))
+        extras.update(bench_long(A, W, dev, peak))
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        inp = W.block_bf16(T=T_MAIN, d=D_MAIN, seed=1, device="cpu")
+        tok, el = time_oracle(inp.H, inp.w, args.cpu_seconds)
+        cpu = {"value": tok / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{tok} tokens of the {T_MAIN}-token workload in 64-token chunks "
+                         f"(single-threaded numpy fp64, {el:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": T_MAIN, "d": D_MAIN, "S": S_MAIN, "storage": "bf16",
+                       "out": "r bf16 + weights fp32", "seed": 1,
+                       "l2": "inputs larger than L2: 3 rotated input sets of 528 MB each",
+                       "parallelism": f"token-sharded x{ws}, no data exchange"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "agg_ring_kernel<bf16,bf16,2,false>",
+                         "algorithmic_bytes_per_launch": bytes_launch, "peak_source": peak_src,
+                         "launch_ms_mean": launch_ms, "launch_ms_median": m["launch_ms_median"]},
+            "hbm_gbs_achieved": achieved,
+            "e2e": e2e,
+            "gpu_launches": m["launches"],
+            "clocks": m["clocks"],
+            "cpu_baseline": cpu,
+            "secondary": extras,
+            "gpu": torch.cuda.get_device_name(dev),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extras", action="store_true", help="skip the stack and long-context workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""Block Attention Residuals (Block AttnRes) depth aggregation for GB300.
+
+A thin Python binding of ``libattnres`` (C ABI in ``include/attnres.h``);
+the functions keep the C names.  torch supplies device memory and streams
+only: tensors are passed as device pointers, the current torch CUDA stream
+is used unless one is given, and every step of the computation runs in the
+library's sm_103a kernels.  Importing raises if the library is missing.
+
+What is computed ("Kimi K3 deep-dive series (2): AttnRes and Stable
+LatentMoE", §2; Kimi K3 chaptered tutorial, ch. 4.3 Eq. 10):
+    a_l = softmax_s(w_l . RMSNorm(h_s)),  r_l = sum_s a_l[s] h_s
+over the sources [h_0, b_1 .. b_{n-1}, partial sum of the current block].
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+import torch
+
+from . import _native as _N
+from ._native import (  # noqa: F401
+    ATTNRES_BF16,
+    ATTNRES_DEFAULT_EPS,
+    ATTNRES_DEVERR_WAIT_TIMEOUT,
+    ATTNRES_F32,
+    ATTNRES_MAX_BLOCKS,
+    ATTNRES_MAX_SOURCES,
+    AttnresError,
+    LIB_PATH,
+)
+
+__all__ = [
+    "attnres_aggregate", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
+    "attnres_layer_step", "attnres_synthetic_layer", "attnres_version", "AttnResState",
+    "aggregate_host", "dtype_code", "AttnresError",
+]
+
+_DT = {torch.float32: ATTNRES_F32, torch.bfloat16: ATTNRES_BF16}
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    try:
+        return _DT[dt]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {dt}; use float32 or bfloat16") from None
+
+
+def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None, contiguous=True) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def attnres_version() -> int:
+    return _N.lib.attnres_version()
+
+
+def attnres_num_sources(layer_idx: int, block_size: int, num_layers: int) -> int:
+    """Sources of layer `layer_idx` (L+1 = the final output aggregation)."""
+    return _N.check(_N.lib.attnres_num_sources(layer_idx, block_size, num_layers), "attnres_num_sources")
+
+
+def attnres_aggregate(sources: Sequence[torch.Tensor] | torch.Tensor, w_l: torch.Tensor, out_r: torch.Tensor,
+                      out_weights: torch.Tensor | None = None, eps: float = ATTNRES_DEFAULT_EPS,
+                      dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """One layer of depth-wise attention.
+
+    sources: S CUDA tensors [T, d] (float32 or bfloat16, one dtype), or one
+    [S, T, d] tensor; w_l: [d] float32; out_r: [T, d] float32/bfloat16;
+    out_weights: [T, S] float32 or None; dev_err: int32 [1] or None.
+    """
+    if isinstance(sources, torch.Tensor):
+        if sources.dim() != 3:
+            raise ValueError("a stacked sources tensor must be [S, T, d]")
+        srcs = list(sources.unbind(0))
+    else:
+        srcs = list(sources)
+    if not srcs:
+        raise ValueError("need at least one source")
+    T, d = srcs[0].shape
+    dt = srcs[0].dtype
+    for i, s in enumerate(srcs):
+        if s.shape != (T, d) or s.dtype != dt:
+            raise ValueError(f"source {i}: expected [{T}, {d}] {dt}, got {list(s.shape)} {s.dtype}")
+    ptrs = (ctypes.c_void_p * len(srcs))(*[_dev_ptr(s, f"sources[{i}]") for i, s in enumerate(srcs)])
+    if out_r.shape != (T, d):
+        raise ValueError("out_r must be [T, d]")
+    if out_weights is not None and out_weights.shape != (T, len(srcs)):
+        raise ValueError("out_weights must be [T, S]")
+    rc = _N.lib.attnres_aggregate(
+        ptrs, len(srcs), T, d, dtype_code(dt), _dev_ptr(w_l, "w_l", torch.float32), float(eps),
+        _dev_ptr(out_r, "out_r"), dtype_code(out_r.dtype), _dev_ptr(out_weights, "out_weights", torch.float32),
+        _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
+    _N.check(rc, "attnres_aggregate")
+
+
+class AttnResState:
+    """Resident depth sources of one batch (embedding, block sums, partial).
+
+    Holds the torch buffers (so they outlive the C struct's pointers) and the
+    `attnres_state` struct the C ABI updates.
+    """
+
+    def __init__(self, h0: torch.Tensor, block_reps: Sequence[torch.Tensor], partial: torch.Tensor,
+                 num_layers: int, block_size: int, eps: float = ATTNRES_DEFAULT_EPS):
+        T, d = h0.shape
+        for i, b in enumerate(list(block_reps) + [partial]):
+            if b.shape != (T, d) or b.dtype != h0.dtype:
+                raise ValueError(f"state buffer {i} must be [{T}, {d}] {h0.dtype}")
+        self.h0, self.block_reps, self.partial = h0, list(block_reps), partial
+        self.num_layers, self.block_size = num_layers, block_size
+        self.struct = _N.AttnresState()
+        reps = (ctypes.c_void_p * max(1, len(self.block_reps)))(
+            *[_dev_ptr(b, f"block_reps[{i}]") for i, b in enumerate(self.block_reps)])
+        rc = _N.lib.attnres_state_init(ctypes.byref(self.struct), _dev_ptr(h0, "h0"), reps, len(self.block_reps),
+                                       _dev_ptr(partial, "partial"), T, d, dtype_code(h0.dtype), num_layers,
+                                       block_size, float(eps))
+        _N.check(rc, "attnres_state_init")
+
+    @classmethod
+    def allocate(cls, h0: torch.Tensor, num_layers: int, block_size: int, eps: float = ATTNRES_DEFAULT_EPS):
+        n_blocks = -(-num_layers // block_size)
+        reps = [torch.empty_like(h0) for _ in range(n_blocks)]
+        return cls(h0, reps, torch.empty_like(h0), num_layers, block_size, eps)
+
+    @property
+    def folded(self) -> int:
+        return self.struct.folded
+
+    def reset(self) -> None:
+        _N.check(_N.lib.attnres_state_reset(ctypes.byref(self.struct)), "attnres_state_reset")
+
+
+def attnres_layer_sources(state: AttnResState, layer_idx: int) -> list[int]:
+    """Device pointers of layer `layer_idx`'s sources, in order."""
+    out = (ctypes.c_void_p * ATTNRES_MAX_SOURCES)()
+    n = ctypes.c_int(0)
+    _N.check(_N.lib.attnres_layer_sources(ctypes.byref(state.struct), layer_idx, out, ctypes.byref(n)),
+             "attnres_layer_sources")
+    return [out[i] for i in range(n.value)]
+
+
+def attnres_block_step(state: AttnResState, F_out: torch.Tensor, layer_idx: int,
+                       dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Fold layer `layer_idx`'s output into the partial sum / block representation."""
+    rc = _N.lib.attnres_block_step(ctypes.byref(state.struct), _dev_ptr(F_out, "F_out", state.h0.dtype), layer_idx,
+                                   _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
+    _N.check(rc, "attnres_block_step")
+
+
+def attnres_layer_step(state: AttnResState, F_prev: torch.Tensor | None, w_l: torch.Tensor, layer_idx: int,
+                       out_r: torch.Tensor, out_weights: torch.Tensor | None = None,
+                       dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Fused: fold F_prev = v_{l-1}, then aggregate layer `layer_idx`."""
+    rc = _N.lib.attnres_layer_step(
+        ctypes.byref(state.struct), _dev_ptr(F_prev, "F_prev", state.h0.dtype),
+        _dev_ptr(w_l, "w_l", torch.float32), layer_idx, _dev_ptr(out_r, "out_r", state.h0.dtype),
+        _dev_ptr(out_weights, "out_weights", torch.float32), _dev_ptr(dev_err, "dev_err", torch.int32),
+        _stream_ptr(stream))
+    _N.check(rc, "attnres_layer_step")
+
+
+def attnres_synthetic_layer(x: torch.Tensor, g: torch.Tensor, s: torch.Tensor, out: torch.Tensor,
+                            stream=None) -> None:
+    """Stand-in layer body out = tanh(x * g) * s (drives a stack; not the method)."""
+    T, d = x.shape
+    rc = _N.lib.attnres_synthetic_layer(_dev_ptr(x, "x"), _dev_ptr(g, "g", torch.float32),
+                                        _dev_ptr(s, "s", torch.float32), _dev_ptr(out, "out", x.dtype), T, d,
+                                        dtype_code(x.dtype), _stream_ptr(stream))
+    _N.check(rc, "attnres_synthetic_layer")
+
+
+def aggregate_host(H_host: torch.Tensor, w_host: torch.Tensor, r_host: torch.Tensor, a_host: torch.Tensor | None,
+                   H_dev: torch.Tensor, w_dev: torch.Tensor, r_dev: torch.Tensor, a_dev: torch.Tensor | None,
+                   eps: float = ATTNRES_DEFAULT_EPS, stream=None) -> None:
+    """One aggregation from and to host memory: copy the [S, T, d] sources
+    and w in (pinned host -> device), aggregate, copy r (and the weights)
+    back.  The device buffers are the caller's; everything is asynchronous
+    on `stream` (synchronise before reading r_host)."""
+    st = stream if stream is not None else torch.cuda.current_stream()
+    with torch.cuda.stream(st):
+        H_dev.copy_(H_host, non_blocking=True)
+        w_dev.copy_(w_host, non_blocking=True)
+        attnres_aggregate(H_dev, w_dev, r_dev, a_dev, eps=eps, stream=st)
+        r_host.copy_(r_dev, non_blocking=True)
+        if a_host is not None and a_dev is not None:
+            a_host.copy_(a_dev, non_blocking=True)

@@ -1,0 +1,598 @@
+// Depth-wise attention over the sources of one layer (Block AttnRes).
+//
+// Per token t, with S sources h_s = src_s[t, :] of d channels and the
+// layer's pseudo-query w ("Kimi K3 deep-dive series (2): AttnRes and Stable
+// LatentMoE", §2; eps from "Kimi K3 model structure (6)", odd facts):
+//     z_s = (w . h_s) / sqrt(mean_c h_s[c]^2 + eps)     (w . RMSNorm(h_s))
+//     a   = softmax_s(z)
+//     r   = sum_s a_s h_s                                (raw sources)
+// All arithmetic is fp32; bf16 is a storage format only.
+//
+// Two kernels:
+//
+//  agg_ring_kernel  (the hot path: S <= 9, 16-byte aligned rows of at most
+//      2 x 448 16-byte vectors, e.g. d = 7168 bf16).  One persistent CTA per
+//      SM.  A producer warp streams every source row of the CTA's tokens
+//      into a ring of shared-memory slots with TMA bulk copies
+//      (cp.async.bulk, completion on an mbarrier per slot).  448 consumer
+//      threads each own the same 16-byte vectors of every row: they copy
+//      their vectors of each landed row into registers and release the slot
+//      at once, so the ring (up to ~225 KB per SM) is almost entirely bytes
+//      in flight.  Dot products and sums of squares for all S sources are
+//      reduced with warp shuffles and one cross-warp step (2 named
+//      barriers per token); the weighted sum is then formed from registers.
+//      Every source byte is read from HBM exactly once.
+//
+//  agg_generic_kernel  (everything else: S up to 128, any d, any pointer
+//      alignment).  One CTA per token, plain loads, two passes over the
+//      token's rows (the second mostly from L2).
+//
+// Both can fuse the block bookkeeping: the last source is formed on the fly
+// as round(prev + F) (or F), written out as the new partial sum / block
+// representation, and used, already rounded, as a source.
+#include <math.h>
+
+#include "attnres.h"
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace attnres {
+
+// ------------------------------------------------------------ ring kernel --
+
+constexpr int kRingConsumerWarps = 14;
+constexpr int kRingConsumers = kRingConsumerWarps * 32;  // 448
+constexpr int kRingThreads = kRingConsumers + 32;        // + one producer warp
+constexpr int kRingSmax = 9;                             // K3: embedding + 7 blocks + partial
+constexpr int kRingMaxVpt = 2;                           // 16-byte vectors per thread per row
+constexpr int kRingMaxSlots = 32;
+constexpr int kRingBarrierId = 1;                        // named barrier of the consumers
+
+struct RingShared {
+  uint64_t full[kRingMaxSlots];   // slot holds a landed row
+  uint64_t empty[kRingMaxSlots];  // every consumer warp has taken its part of the row
+  float red[kRingConsumerWarps][2 * kRingSmax];
+  float a[kRingSmax + 1];
+  int abort_flag;
+};
+constexpr int kRingHeaderBytes = (int)((sizeof(RingShared) + 127) / 128 * 128);
+
+struct RingParams {
+  const char* src[kRingSmax];
+  const char* fuse_prev;
+  const char* fuse_F;
+  char* fuse_dst;
+  const float* w;
+  char* out_r;
+  float* out_a;
+  int* dev_err;
+  long long T;
+  int d;
+  int n_stored;
+  int S;
+  int nvec;       // 16-byte vectors per source row
+  int row_bytes;  // bytes per source row
+  int out_row_bytes;
+  int nslots;
+  float eps;
+};
+
+template <typename Tin>
+struct Vec;
+template <>
+struct Vec<bf16_t> {
+  static constexpr int kElems = 8;
+  static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int kElems = 4;
+  static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+// store EPV output values of vector `vec` of an output row
+template <typename Tout, int EPV>
+__device__ __forceinline__ void store_out(char* row, int vec, const float* acc) {
+  if constexpr (sizeof(Tout) == 2 && EPV == 8) {
+    *reinterpret_cast<uint4*>(row + (size_t)vec * 16) = Vec<bf16_t>::pack(acc);
+  } else if constexpr (sizeof(Tout) == 2 && EPV == 4) {
+    *reinterpret_cast<uint2*>(row + (size_t)vec * 8) =
+        make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+  } else if constexpr (sizeof(Tout) == 4 && EPV == 8) {
+    uint4* o = reinterpret_cast<uint4*>(row + (size_t)vec * 32);
+    o[0] = Vec<float>::pack(acc);
+    o[1] = Vec<float>::pack(acc + 4);
+  } else {
+    *reinterpret_cast<uint4*>(row + (size_t)vec * 16) = Vec<float>::pack(acc);
+  }
+}
+
+template <typename Tin, typename Tout, int VPT, bool FUSED>
+__global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_constant__ RingParams p) {
+  constexpr int EPV = Vec<Tin>::kElems;
+  extern __shared__ __align__(128) unsigned char smem[];
+  RingShared& sh = *reinterpret_cast<RingShared*>(smem);
+  const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int nslots = p.nslots;
+  const long long T = p.T;
+
+  if (tid == 0) {
+    for (int k = 0; k < nslots; ++k) {
+      mbar_init(smem_addr(&sh.full[k]), 1);
+      mbar_init(smem_addr(&sh.empty[k]), kRingConsumerWarps);
+    }
+    sh.abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kRingConsumerWarps) {
+    // ----------------------------------------------------------- producer --
+    if (lane == 0) {
+      const int rows = p.n_stored + (FUSED ? (p.fuse_prev ? 2 : 1) : 0);
+      uint32_t slot = 0, lap = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        const long long off = t * (long long)p.row_bytes;
+        for (int j = 0; j < rows; ++j) {
+          const char* g;
+          if (j < p.n_stored) g = p.src[j] + off;
+          else if (FUSED && p.fuse_prev && j == p.n_stored) g = p.fuse_prev + off;
+          else g = p.fuse_F + off;
+          // first lap: parity 1 of a fresh barrier counts as complete
+          if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_addr(&sh.full[slot]);
+          mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
+          bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+          ++issued;
+          if (++slot == (uint32_t)nslots) {
+            slot = 0;
+            ++lap;
+          }
+        }
+      }
+      if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+      // Every issued copy must have landed before this CTA exits: wait on the
+      // latest armed phase of each slot (already-consumed phases pass at once).
+      const long long armed_slots = issued < nslots ? issued : nslots;
+      for (int k = 0; k < armed_slots; ++k) {
+        const long long uses = (issued - 1 - k) / nslots + 1;
+        mbar_wait_bounded(smem_addr(&sh.full[k]), (uint32_t)((uses - 1) & 1));
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers --
+  float wreg[VPT][EPV];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * kRingConsumers;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) wreg[k][e] = (v < p.nvec) ? __ldg(p.w + v * EPV + e) : 0.f;
+  }
+
+  const int S = p.S;
+  uint32_t slot = 0, lap = 0;
+  bool ok = true;
+
+  // take this thread's vectors of the next landed row, then release the slot
+  auto consume = [&](uint4* dst) {
+    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u)) ok = false;
+    const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * kRingConsumers;
+      dst[k] = (ok && v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&sh.empty[slot]));
+    if (++slot == (uint32_t)nslots) {
+      slot = 0;
+      ++lap;
+    }
+  };
+
+  for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+    uint4 x[kRingSmax][VPT];
+    float dot[kRingSmax], ss[kRingSmax];
+#pragma unroll
+    for (int s = 0; s < kRingSmax; ++s) {
+      dot[s] = 0.f;
+      ss[s] = 0.f;
+      if (s < S) {
+        if (!FUSED || s < p.n_stored) {
+          consume(x[s]);
+        } else {
+          // the fused source: round(prev + F), stored as the new partial / b_n
+          uint4 pv[VPT], fv[VPT];
+          if (p.fuse_prev) consume(pv);
+          consume(fv);
+          char* drow = p.fuse_dst + t * (long long)p.row_bytes;
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * kRingConsumers;
+            if (v < p.nvec) {
+              float f[EPV];
+              Vec<Tin>::unpack(fv[k], f);
+              if (p.fuse_prev) {
+                float q[EPV];
+                Vec<Tin>::unpack(pv[k], q);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) f[e] = q[e] + f[e];
+              }
+              if (!ok) {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) f[e] = __int_as_float(0x7fc00000);
+              }
+              x[s][k] = Vec<Tin>::pack(f);  // one rounding to the storage type
+              *reinterpret_cast<uint4*>(drow + (size_t)v * 16) = x[s][k];
+            } else {
+              x[s][k] = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          float f[EPV];
+          Vec<Tin>::unpack(x[s][k], f);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            dot[s] = fmaf(wreg[k][e], f[e], dot[s]);
+            ss[s] = fmaf(f[e], f[e], ss[s]);
+          }
+        }
+      }
+    }
+
+    // ---- reduce dot / sum of squares of every source over the CTA
+#pragma unroll
+    for (int s = 0; s < kRingSmax; ++s) {
+      if (s < S) {
+        dot[s] = warp_sum(dot[s]);
+        ss[s] = warp_sum(ss[s]);
+      }
+    }
+    const bool warp_failed = __any_sync(0xffffffffu, !ok);
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < kRingSmax; ++s) {
+        if (s < S) {
+          sh.red[warp][2 * s] = dot[s];
+          sh.red[warp][2 * s + 1] = ss[s];
+        }
+      }
+      if (warp_failed) sh.abort_flag = 1;
+    }
+    named_barrier_sync(kRingBarrierId, kRingConsumers);
+
+    // ---- logits and the depth softmax (warp 0; lane 2s holds source s)
+    if (warp == 0) {
+      float v = 0.f;
+      if (lane < 2 * S) {
+#pragma unroll
+        for (int w = 0; w < kRingConsumerWarps; ++w) v += sh.red[w][lane];
+      }
+      const float sumsq = __shfl_down_sync(0xffffffffu, v, 1);
+      const bool is_src = lane < 2 * S && (lane & 1) == 0;
+      const float z = is_src ? v / sqrtf(sumsq / (float)p.d + p.eps) : -INFINITY;
+      const float m = warp_max(z);
+      const float e = is_src ? expf(z - m) : 0.f;
+      const float tot = warp_sum(e);
+      if (is_src) {
+        float a = e / tot;
+        if (*(volatile int*)&sh.abort_flag) a = __int_as_float(0x7fc00000);
+        sh.a[lane >> 1] = a;
+        if (p.out_a) p.out_a[t * S + (lane >> 1)] = a;
+      }
+    }
+    named_barrier_sync(kRingBarrierId, kRingConsumers);
+
+    // ---- r = sum_s a_s h_s from the registers
+    const bool abort = *(volatile int*)&sh.abort_flag != 0;
+    float as[kRingSmax];
+#pragma unroll
+    for (int s = 0; s < kRingSmax; ++s) as[s] = (s < S) ? sh.a[s] : 0.f;
+    char* orow = p.out_r + t * (long long)p.out_row_bytes;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * kRingConsumers;
+      if (v < p.nvec) {
+        float acc[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int s = 0; s < kRingSmax; ++s) {
+          if (s < S) {
+            float f[EPV];
+            Vec<Tin>::unpack(x[s][k], f);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[e] = fmaf(as[s], f[e], acc[e]);
+          }
+        }
+        if (abort) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) acc[e] = __int_as_float(0x7fc00000);
+        }
+        store_out<Tout, EPV>(orow, v, acc);
+      }
+    }
+    if (abort) {
+      if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+  }
+}
+
+// --------------------------------------------------------- generic kernel --
+
+constexpr int kGenThreads = 256;
+
+struct GenericParams {
+  const char* src[kMaxSources];
+  const char* fuse_prev;
+  const char* fuse_F;
+  char* fuse_dst;
+  const float* w;
+  char* out_r;
+  float* out_a;
+  long long T;
+  int d;
+  int n_stored;
+  int S;
+  float eps;
+};
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kGenThreads) agg_generic_kernel(const __grid_constant__ GenericParams p) {
+  __shared__ float s_red[kGenThreads / 32][2];
+  __shared__ float s_za[kMaxSources];  // logits, then weights
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int d = p.d, S = p.S;
+  for (long long t = blockIdx.x; t < p.T; t += gridDim.x) {
+    const long long row = t * (long long)d;
+    // pass 1: logit of every source (forming the fused source on the way)
+    for (int s = 0; s < S; ++s) {
+      float dot = 0.f, ss = 0.f;
+      if (s < p.n_stored) {
+        const Tin* h = reinterpret_cast<const Tin*>(p.src[s]) + row;
+        for (int c = tid; c < d; c += kGenThreads) {
+          const float x = load_elem(h + c);
+          dot = fmaf(p.w[c], x, dot);
+          ss = fmaf(x, x, ss);
+        }
+      } else {
+        const Tin* F = reinterpret_cast<const Tin*>(p.fuse_F) + row;
+        const Tin* P = p.fuse_prev ? reinterpret_cast<const Tin*>(p.fuse_prev) + row : nullptr;
+        Tin* D = reinterpret_cast<Tin*>(p.fuse_dst) + row;
+        for (int c = tid; c < d; c += kGenThreads) {
+          float x = load_elem(F + c);
+          if (P) x = round_to<Tin>(load_elem(P + c) + x);
+          store_elem(D + c, x);
+          dot = fmaf(p.w[c], x, dot);
+          ss = fmaf(x, x, ss);
+        }
+      }
+      dot = warp_sum(dot);
+      ss = warp_sum(ss);
+      if (lane == 0) {
+        s_red[warp][0] = dot;
+        s_red[warp][1] = ss;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float dd = 0.f, sq = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGenThreads / 32; ++w) {
+          dd += s_red[w][0];
+          sq += s_red[w][1];
+        }
+        s_za[s] = dd / sqrtf(sq / (float)d + p.eps);
+      }
+      __syncthreads();
+    }
+    // depth softmax over the S logits
+    if (warp == 0) {
+      float m = -INFINITY;
+      for (int s = lane; s < S; s += 32) m = fmaxf(m, s_za[s]);
+      m = warp_max(m);
+      float tot = 0.f;
+      for (int s = lane; s < S; s += 32) tot += expf(s_za[s] - m);
+      tot = warp_sum(tot);
+      for (int s = lane; s < S; s += 32) {
+        const float a = expf(s_za[s] - m) / tot;
+        s_za[s] = a;
+        if (p.out_a) p.out_a[t * S + s] = a;
+      }
+    }
+    __syncthreads();
+    // pass 2: weighted sum of the raw sources
+    for (int c = tid; c < d; c += kGenThreads) {
+      float acc = 0.f;
+      for (int s = 0; s < S; ++s) {
+        const Tin* h = (s < p.n_stored) ? reinterpret_cast<const Tin*>(p.src[s]) + row
+                                        : reinterpret_cast<const Tin*>(p.fuse_dst) + row;
+        acc = fmaf(s_za[s], load_elem(h + c), acc);
+      }
+      store_elem(reinterpret_cast<Tout*>(p.out_r) + row + c, acc);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- launch --
+
+cudaError_t device_info(DeviceInfo* info) {
+  constexpr int kMaxDevices = 64;
+  static DeviceInfo cache[kMaxDevices];
+  static bool have[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && have[dev]) {
+    *info = cache[dev];
+    return cudaSuccess;
+  }
+  DeviceInfo di{};
+  e = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) {
+    cache[dev] = di;
+    have[dev] = true;
+  }
+  *info = di;
+  return cudaSuccess;
+}
+
+template <typename Tin, typename Tout, int VPT, bool FUSED>
+static cudaError_t launch_ring_t(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
+  constexpr int kMaxDevices = 64;
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto kern = agg_ring_kernel<Tin, Tout, VPT, FUSED>;
+  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+    DeviceInfo di;
+    e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+  }
+  kern<<<grid, kRingThreads, smem, stream>>>(rp);
+  return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+static cudaError_t launch_ring_vpt(const RingParams& rp, int vpt, bool fused, int grid, int smem,
+                                   cudaStream_t stream) {
+  if (vpt == 1) {
+    return fused ? launch_ring_t<Tin, Tout, 1, true>(rp, grid, smem, stream)
+                 : launch_ring_t<Tin, Tout, 1, false>(rp, grid, smem, stream);
+  }
+  return fused ? launch_ring_t<Tin, Tout, 2, true>(rp, grid, smem, stream)
+               : launch_ring_t<Tin, Tout, 2, false>(rp, grid, smem, stream);
+}
+
+template <typename Tin, typename Tout>
+static cudaError_t launch_generic_t(const GenericParams& gp, int grid, cudaStream_t stream) {
+  agg_generic_kernel<Tin, Tout><<<grid, kGenThreads, 0, stream>>>(gp);
+  return cudaGetLastError();
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
+  *path = kPathNone;
+  if (a.T <= 0) return cudaSuccess;
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+
+  const bool in_bf16 = a.src_dtype == ATTNRES_BF16;
+  const bool out_bf16 = a.out_dtype == ATTNRES_BF16;
+  const int esz = in_bf16 ? 2 : 4;
+  const int osz = out_bf16 ? 2 : 4;
+  const int S = a.S();
+  const bool fused = a.fuse_F != nullptr;
+  const long long row_bytes = (long long)a.d * esz;
+  const int epv = 16 / esz;
+
+  // ---- can the ring kernel take it?
+  bool ring = S <= kRingSmax && row_bytes % 16 == 0;
+  const long long nvec = row_bytes / 16;
+  const int vpt = (int)((nvec + kRingConsumers - 1) / kRingConsumers);
+  ring = ring && vpt >= 1 && vpt <= kRingMaxVpt;
+  for (int s = 0; ring && s < a.n_stored; ++s) ring = aligned16(a.src[s]);
+  if (ring && fused) ring = aligned16(a.fuse_F) && aligned16(a.fuse_dst) && (!a.fuse_prev || aligned16(a.fuse_prev));
+  const int out_store = epv * osz > 16 ? 16 : epv * osz;  // widest single store of an output vector
+  if (ring) ring = (reinterpret_cast<uintptr_t>(a.out_r) % out_store) == 0;
+  int nslots = 0;
+  if (ring) {
+    const long long avail = (long long)di.max_smem_optin - kRingHeaderBytes;
+    nslots = (int)(avail / row_bytes);
+    if (nslots > kRingMaxSlots) nslots = kRingMaxSlots;
+    ring = nslots >= 1;
+  }
+
+  if (ring) {
+    RingParams rp{};
+    for (int s = 0; s < a.n_stored; ++s) rp.src[s] = static_cast<const char*>(a.src[s]);
+    rp.fuse_prev = static_cast<const char*>(a.fuse_prev);
+    rp.fuse_F = static_cast<const char*>(a.fuse_F);
+    rp.fuse_dst = static_cast<char*>(a.fuse_dst);
+    rp.w = a.w;
+    rp.out_r = static_cast<char*>(a.out_r);
+    rp.out_a = a.out_a;
+    rp.dev_err = a.dev_err;
+    rp.T = a.T;
+    rp.d = a.d;
+    rp.n_stored = a.n_stored;
+    rp.S = S;
+    rp.nvec = (int)nvec;
+    rp.row_bytes = (int)row_bytes;
+    rp.out_row_bytes = (int)((long long)a.d * osz);
+    rp.nslots = nslots;
+    rp.eps = a.eps;
+    const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
+    const int smem = kRingHeaderBytes + nslots * (int)row_bytes;
+    *path = kPathRing;
+    if (in_bf16) {
+      return out_bf16 ? launch_ring_vpt<bf16_t, bf16_t>(rp, vpt, fused, grid, smem, a.stream)
+                      : launch_ring_vpt<bf16_t, float>(rp, vpt, fused, grid, smem, a.stream);
+    }
+    return out_bf16 ? launch_ring_vpt<float, bf16_t>(rp, vpt, fused, grid, smem, a.stream)
+                    : launch_ring_vpt<float, float>(rp, vpt, fused, grid, smem, a.stream);
+  }
+
+  GenericParams gp{};
+  for (int s = 0; s < a.n_stored; ++s) gp.src[s] = static_cast<const char*>(a.src[s]);
+  gp.fuse_prev = static_cast<const char*>(a.fuse_prev);
+  gp.fuse_F = static_cast<const char*>(a.fuse_F);
+  gp.fuse_dst = static_cast<char*>(a.fuse_dst);
+  gp.w = a.w;
+  gp.out_r = static_cast<char*>(a.out_r);
+  gp.out_a = a.out_a;
+  gp.T = a.T;
+  gp.d = a.d;
+  gp.n_stored = a.n_stored;
+  gp.S = S;
+  gp.eps = a.eps;
+  const long long max_grid = (long long)di.sm_count * 8;
+  const int grid = (int)(a.T < max_grid ? a.T : max_grid);
+  *path = kPathGeneric;
+  if (in_bf16) {
+    return out_bf16 ? launch_generic_t<bf16_t, bf16_t>(gp, grid, a.stream)
+                    : launch_generic_t<bf16_t, float>(gp, grid, a.stream);
+  }
+  return out_bf16 ? launch_generic_t<float, bf16_t>(gp, grid, a.stream)
+                  : launch_generic_t<float, float>(gp, grid, a.stream);
+}
+
+}  // namespace attnres

@@ -1,0 +1,279 @@
+// The C ABI of libattnres (declared in include/attnres.h): argument
+// checking, the host-side block bookkeeping of a stack (which sources layer
+// l reads, where the folded layer output goes), and dispatch to the kernels.
+//
+// Block bookkeeping follows the Kimi K3 chaptered tutorial (kimi.papertok.ai),
+// ch. 4.3 Eq. 10 (two-case value list; no source for an empty partial sum;
+// the final output layer aggregates all block representations) and ch. 4.5
+// (an incomplete last block).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <string>
+
+#include "attnres.h"
+#include "launch.h"
+
+using namespace attnres;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return ATTNRES_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTNRES_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool valid_dtype(int dt) { return dt == ATTNRES_F32 || dt == ATTNRES_BF16; }
+
+int dtype_bytes(int dt) { return dt == ATTNRES_BF16 ? 2 : 4; }
+
+// T * d * 4 must stay well inside int64 (element offsets are 64-bit).
+bool size_ok(int64_t T, int d) { return T >= 0 && d >= 1 && T <= (((int64_t)1) << 40) / d; }
+
+int num_blocks(int L, int B) { return (L + B - 1) / B; }
+
+// Where folding layer p's output goes, and what the partial sum held before.
+struct FoldPlan {
+  int block;        // n: block of layer p (1-based)
+  bool has_prev;    // partial sum non-empty before folding v_p
+  bool ends_block;  // p is the last layer of block n
+};
+
+FoldPlan fold_plan(int p, int B, int L) {
+  FoldPlan f;
+  f.block = (p - 1) / B + 1;
+  const int first = (f.block - 1) * B + 1;
+  f.has_prev = p > first;
+  f.ends_block = (p % B == 0) || (p == L);
+  return f;
+}
+
+int check_state(const attnres_state* st) {
+  if (!st) return fail(ATTNRES_EINVAL, "state is NULL");
+  if (!st->h0 || !st->partial) return fail(ATTNRES_EINVAL, "state h0/partial is NULL");
+  if (!valid_dtype(st->dtype)) return fail(ATTNRES_EDTYPE, "state dtype %d", st->dtype);
+  if (!size_ok(st->T, st->d)) return fail(ATTNRES_EINVAL, "state T=%lld d=%d", (long long)st->T, st->d);
+  if (st->num_layers < 1 || st->block_size < 1) return fail(ATTNRES_EINVAL, "state L/B");
+  if (num_blocks(st->num_layers, st->block_size) > ATTNRES_MAX_BLOCKS) return fail(ATTNRES_ERANGE, "too many blocks");
+  if (st->folded < 0 || st->folded > st->num_layers) return fail(ATTNRES_ESTATE, "state folded=%d", st->folded);
+  return ATTNRES_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attnres_version(void) { return (1 << 16) | 0; }
+
+const char* attnres_status_string(int status) {
+  switch (status) {
+    case ATTNRES_OK: return "ATTNRES_OK";
+    case ATTNRES_EINVAL: return "ATTNRES_EINVAL: invalid argument";
+    case ATTNRES_EDTYPE: return "ATTNRES_EDTYPE: unsupported dtype";
+    case ATTNRES_ERANGE: return "ATTNRES_ERANGE: size out of range";
+    case ATTNRES_ECUDA: return "ATTNRES_ECUDA: CUDA error";
+    case ATTNRES_ESTATE: return "ATTNRES_ESTATE: stack call out of order";
+    default: return "unknown attnres status";
+  }
+}
+
+const char* attnres_last_error(void) { return g_last_error.c_str(); }
+
+int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int src_dtype, const float* w_l, float eps,
+                      void* out_r, int out_dtype, float* out_weights, int* dev_err, void* stream) {
+  if (!sources) return fail(ATTNRES_EINVAL, "sources is NULL");
+  if (S < 1) return fail(ATTNRES_EINVAL, "S=%d < 1", S);
+  if (S > ATTNRES_MAX_SOURCES) return fail(ATTNRES_ERANGE, "S=%d > %d", S, ATTNRES_MAX_SOURCES);
+  if (!valid_dtype(src_dtype) || !valid_dtype(out_dtype)) return fail(ATTNRES_EDTYPE, "dtype %d/%d", src_dtype, out_dtype);
+  if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
+  if (!w_l || !out_r) return fail(ATTNRES_EINVAL, "w_l/out_r is NULL");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  for (int s = 0; s < S; ++s)
+    if (!sources[s]) return fail(ATTNRES_EINVAL, "sources[%d] is NULL", s);
+  if (T == 0) return ok();
+  AggArgs a{};
+  for (int s = 0; s < S; ++s) a.src[s] = sources[s];
+  a.n_stored = S;
+  a.T = T;
+  a.d = d;
+  a.src_dtype = src_dtype;
+  a.w = w_l;
+  a.eps = eps;
+  a.out_r = out_r;
+  a.out_dtype = out_dtype;
+  a.out_a = out_weights;
+  a.dev_err = dev_err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  AggPath path;
+  cudaError_t e = launch_aggregate(a, &path);
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate launch");
+  return ok();
+}
+
+int attnres_state_init(attnres_state* st, const void* h0, void* const* block_reps, int n_block_reps, void* partial,
+                       int64_t T, int d, int dtype, int num_layers, int block_size, float eps) {
+  if (!st || !h0 || !partial || !block_reps) return fail(ATTNRES_EINVAL, "NULL argument");
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (!size_ok(T, d)) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (num_layers < 1 || block_size < 1) return fail(ATTNRES_EINVAL, "num_layers/block_size must be >= 1");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  const int N = num_blocks(num_layers, block_size);
+  if (N > ATTNRES_MAX_BLOCKS) return fail(ATTNRES_ERANGE, "ceil(L/B)=%d > %d", N, ATTNRES_MAX_BLOCKS);
+  if (n_block_reps < N) return fail(ATTNRES_EINVAL, "need %d block buffers, got %d", N, n_block_reps);
+  memset(st, 0, sizeof(*st));
+  st->h0 = h0;
+  for (int k = 0; k < N; ++k) {
+    if (!block_reps[k]) return fail(ATTNRES_EINVAL, "block_reps[%d] is NULL", k);
+    if (block_reps[k] == partial || block_reps[k] == h0) return fail(ATTNRES_EINVAL, "block_reps[%d] aliases", k);
+    for (int j = 0; j < k; ++j)
+      if (block_reps[j] == block_reps[k]) return fail(ATTNRES_EINVAL, "block_reps[%d] == block_reps[%d]", j, k);
+    st->block_reps[k] = block_reps[k];
+  }
+  if (partial == h0) return fail(ATTNRES_EINVAL, "partial aliases h0");
+  st->partial = partial;
+  st->T = T;
+  st->d = d;
+  st->dtype = dtype;
+  st->num_layers = num_layers;
+  st->block_size = block_size;
+  st->eps = eps;
+  st->folded = 0;
+  return ok();
+}
+
+int attnres_state_reset(attnres_state* st) {
+  if (!st) return fail(ATTNRES_EINVAL, "state is NULL");
+  st->folded = 0;
+  return ok();
+}
+
+int attnres_num_sources(int layer_idx, int block_size, int num_layers) {
+  if (block_size < 1 || num_layers < 1) return fail(ATTNRES_EINVAL, "block_size/num_layers must be >= 1");
+  if (layer_idx < 1 || layer_idx > num_layers + 1) return fail(ATTNRES_EINVAL, "layer_idx %d outside 1..L+1", layer_idx);
+  if (layer_idx == num_layers + 1) return num_blocks(num_layers, block_size) + 1;
+  const int n = (layer_idx - 1) / block_size + 1;
+  const int i = (layer_idx - 1) % block_size + 1;
+  return n + (i >= 2 ? 1 : 0);
+}
+
+int attnres_layer_sources(const attnres_state* st, int layer_idx, const void** out_ptrs, int* out_S) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (!out_ptrs || !out_S) return fail(ATTNRES_EINVAL, "NULL output");
+  const int L = st->num_layers, B = st->block_size;
+  if (layer_idx < 1 || layer_idx > L + 1) return fail(ATTNRES_EINVAL, "layer_idx %d outside 1..L+1", layer_idx);
+  if (st->folded != layer_idx - 1)
+    return fail(ATTNRES_ESTATE, "layer %d needs %d folded layer outputs, state has %d", layer_idx, layer_idx - 1,
+                st->folded);
+  int S = 0;
+  out_ptrs[S++] = st->h0;
+  const int f = st->folded;
+  int completed = 0;
+  bool partial = false;
+  if (f > 0) {
+    const FoldPlan fp = fold_plan(f, B, L);
+    completed = fp.ends_block ? fp.block : fp.block - 1;
+    partial = !fp.ends_block;
+  }
+  for (int k = 0; k < completed; ++k) out_ptrs[S++] = st->block_reps[k];
+  if (partial) out_ptrs[S++] = st->partial;
+  *out_S = S;
+  return ok();
+}
+
+int attnres_block_step(attnres_state* st, const void* F_out, int layer_idx, int* dev_err, void* stream) {
+  (void)dev_err;  // the fold kernel has no waits
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (!F_out) return fail(ATTNRES_EINVAL, "F_out is NULL");
+  const int L = st->num_layers, B = st->block_size;
+  if (layer_idx < 1 || layer_idx > L) return fail(ATTNRES_EINVAL, "layer_idx %d outside 1..L", layer_idx);
+  if (st->folded != layer_idx - 1)
+    return fail(ATTNRES_ESTATE, "block_step(%d) needs folded == %d, state has %d", layer_idx, layer_idx - 1,
+                st->folded);
+  const FoldPlan fp = fold_plan(layer_idx, B, L);
+  void* dst = fp.ends_block ? st->block_reps[fp.block - 1] : st->partial;
+  const void* prev = fp.has_prev ? st->partial : nullptr;
+  cudaError_t e = launch_fold(prev, F_out, dst, st->T * (int64_t)st->d, st->dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_block_step launch");
+  st->folded = layer_idx;
+  return ok();
+}
+
+int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, int layer_idx, void* out_r,
+                       float* out_weights, int* dev_err, void* stream) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (!w_l || !out_r) return fail(ATTNRES_EINVAL, "w_l/out_r is NULL");
+  const int L = st->num_layers, B = st->block_size;
+  if (layer_idx < 1 || layer_idx > L + 1) return fail(ATTNRES_EINVAL, "layer_idx %d outside 1..L+1", layer_idx);
+  if ((layer_idx == 1) != (F_prev == nullptr)) return fail(ATTNRES_EINVAL, "F_prev must be NULL exactly at layer 1");
+  const int need = layer_idx >= 2 ? layer_idx - 2 : 0;
+  if (st->folded != need)
+    return fail(ATTNRES_ESTATE, "layer_step(%d) needs folded == %d, state has %d", layer_idx, need, st->folded);
+  if (out_r == st->partial || out_r == st->h0) return fail(ATTNRES_EINVAL, "out_r aliases the state");
+
+  AggArgs a{};
+  a.T = st->T;
+  a.d = st->d;
+  a.src_dtype = st->dtype;
+  a.w = w_l;
+  a.eps = st->eps;
+  a.out_r = out_r;
+  a.out_dtype = st->dtype;
+  a.out_a = out_weights;
+  a.dev_err = dev_err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.src[0] = st->h0;
+  a.n_stored = 1;
+  if (layer_idx >= 2) {
+    const int p = layer_idx - 1;
+    const FoldPlan fp = fold_plan(p, B, L);
+    for (int k = 0; k < fp.block - 1; ++k) a.src[a.n_stored++] = st->block_reps[k];
+    a.fuse_prev = fp.has_prev ? st->partial : nullptr;
+    a.fuse_F = F_prev;
+    a.fuse_dst = fp.ends_block ? st->block_reps[fp.block - 1] : st->partial;
+    for (int k = 0; k < num_blocks(L, B); ++k)
+      if (out_r == st->block_reps[k]) return fail(ATTNRES_EINVAL, "out_r aliases block_reps[%d]", k);
+  }
+  if (a.S() != attnres_num_sources(layer_idx, B, L))
+    return fail(ATTNRES_ESTATE, "internal: source count mismatch at layer %d", layer_idx);
+  if (st->T > 0) {
+    AggPath path;
+    cudaError_t e = launch_aggregate(a, &path);
+    if (e != cudaSuccess) return cuda_fail(e, "attnres_layer_step launch");
+  }
+  if (layer_idx >= 2) st->folded = layer_idx - 1;
+  return ok();
+}
+
+int attnres_synthetic_layer(const void* x, const float* g, const float* s, void* out, int64_t T, int d, int dtype,
+                            void* stream) {
+  if (!x || !g || !s || !out) return fail(ATTNRES_EINVAL, "NULL argument");
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (!size_ok(T, d)) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  cudaError_t e = launch_synthetic_layer(x, g, s, out, T, d, dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_synthetic_layer launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+// Elementwise kernels of the stack:
+//
+//  fold_kernel        the block bookkeeping on its own (Kimi K3 chaptered
+//                     tutorial, ch. 4.3 Eq. 10 and ch. 4.6): the output v of
+//                     a layer is added to the running partial sum of its
+//                     block, dst = round(prev + v), or copied when the
+//                     partial sum is empty.  The fused path in aggregate.cu
+//                     does the same arithmetic inside the aggregation.
+//  synth_layer_kernel the stand-in layer body F(x) = tanh(x * g) * s used to
+//                     drive a stack without trained weights.
+//
+// Both are HBM-bound streams: 16-byte vector accesses when every pointer is
+// 16-byte aligned and rows hold whole vectors, scalar accesses otherwise;
+// grid-stride loops over a grid sized to the SM count.
+#include <math.h>
+
+#include "attnres.h"
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace attnres {
+
+constexpr int kEwThreads = 256;
+constexpr int kEwCtasPerSm = 4;
+
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<bf16_t> {
+  static constexpr int kElems = 8;
+  static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+};
+template <>
+struct Vec16<float> {
+  static constexpr int kElems = 4;
+  static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+// ------------------------------------------------------------------ fold --
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kEwThreads) fold_kernel(const T* prev, const T* F, T* dst,
+                                                          long long n) {
+  // dst may alias prev (the partial sum is updated in place)
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if constexpr (VEC) {
+    constexpr int E = Vec16<T>::kElems;
+    const long long nv = n / E;
+    const uint4* F4 = reinterpret_cast<const uint4*>(F);
+    const uint4* P4 = reinterpret_cast<const uint4*>(prev);
+    uint4* D4 = reinterpret_cast<uint4*>(dst);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+      float f[E];
+      Vec16<T>::unpack(F4[i], f);
+      if (prev) {
+        float q[E];
+        Vec16<T>::unpack(P4[i], q);
+#pragma unroll
+        for (int e = 0; e < E; ++e) f[e] = q[e] + f[e];
+      }
+      D4[i] = Vec16<T>::pack(f);
+    }
+  } else {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+      float x = load_elem(F + i);
+      if (prev) x = load_elem(prev + i) + x;
+      store_elem(dst + i, x);
+    }
+  }
+}
+
+// ------------------------------------------------------- synthetic layer --
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, const float* __restrict__ g,
+                                                                 const float* __restrict__ s, T* out,
+                                                                 long long T_, int d) {
+  const long long n = T_ * (long long)d;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if constexpr (VEC) {
+    constexpr int E = Vec16<T>::kElems;
+    const int vrow = d / E;  // vectors per row (d % E == 0 here)
+    const long long nv = n / E;
+    const uint4* X4 = reinterpret_cast<const uint4*>(x);
+    uint4* O4 = reinterpret_cast<uint4*>(out);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+      const int c0 = (int)(i % vrow) * E;
+      float f[E];
+      Vec16<T>::unpack(X4[i], f);
+#pragma unroll
+      for (int e = 0; e < E; ++e) f[e] = tanhf(f[e] * __ldg(g + c0 + e)) * __ldg(s + c0 + e);
+      O4[i] = Vec16<T>::pack(f);
+    }
+  } else {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+      const int c = (int)(i % d);
+      store_elem(out + i, tanhf(load_elem(x + i) * g[c]) * s[c]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launch --
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int ew_grid(long long work_items) {
+  DeviceInfo di;
+  if (device_info(&di) != cudaSuccess) di.sm_count = 1;
+  const long long cap = (long long)di.sm_count * kEwCtasPerSm;
+  long long g = (work_items + kEwThreads - 1) / kEwThreads;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+template <typename T>
+static cudaError_t launch_fold_t(const void* prev, const void* F, void* dst, long long n, cudaStream_t st) {
+  constexpr int E = 16 / (int)sizeof(T);
+  const bool vec = n % E == 0 && al16(F) && al16(dst) && (!prev || al16(prev));
+  const T* P = static_cast<const T*>(prev);
+  const T* Fp = static_cast<const T*>(F);
+  T* D = static_cast<T*>(dst);
+  if (vec) fold_kernel<T, true><<<ew_grid(n / E), kEwThreads, 0, st>>>(P, Fp, D, n);
+  else fold_kernel<T, false><<<ew_grid(n), kEwThreads, 0, st>>>(P, Fp, D, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold(const void* prev, const void* F, void* dst, int64_t n, int dtype, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  return dtype == ATTNRES_BF16 ? launch_fold_t<bf16_t>(prev, F, dst, n, stream)
+                               : launch_fold_t<float>(prev, F, dst, n, stream);
+}
+
+template <typename T>
+static cudaError_t launch_synth_t(const void* x, const float* g, const float* s, void* out, long long T_, int d,
+                                  cudaStream_t st) {
+  constexpr int E = 16 / (int)sizeof(T);
+  const long long n = T_ * (long long)d;
+  const bool vec = d % E == 0 && al16(x) && al16(out);
+  const T* X = static_cast<const T*>(x);
+  T* O = static_cast<T*>(out);
+  if (vec) synth_layer_kernel<T, true><<<ew_grid(n / E), kEwThreads, 0, st>>>(X, g, s, O, T_, d);
+  else synth_layer_kernel<T, false><<<ew_grid(n), kEwThreads, 0, st>>>(X, g, s, O, T_, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_synthetic_layer(const void* x, const float* g, const float* s, void* out, int64_t T, int d,
+                                   int dtype, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  return dtype == ATTNRES_BF16 ? launch_synth_t<bf16_t>(x, g, s, out, T, d, stream)
+                               : launch_synth_t<float>(x, g, s, out, T, d, stream);
+}
+
+}  // namespace attnres

@@ -1,0 +1,58 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attnres {
+
+constexpr int kMaxSources = 128;
+
+// One aggregation launch, possibly with the block bookkeeping fused in.
+//
+// Stored sources src[0 .. n_stored-1] are read as they are.  When fuse_F is
+// non-null one more source follows them, formed on the fly as
+//     x = round(fuse_prev + fuse_F)   (or fuse_F alone when fuse_prev is null)
+// written to fuse_dst and used, already rounded, as source n_stored.
+struct AggArgs {
+  const void* src[kMaxSources];
+  int n_stored;
+  const void* fuse_prev;
+  const void* fuse_F;
+  void* fuse_dst;
+  int64_t T;
+  int d;
+  int src_dtype;  // attnres_dtype (stored sources, fused rows, fuse_dst)
+  const float* w;
+  float eps;
+  void* out_r;
+  int out_dtype;
+  float* out_a;   // [T, S] or null
+  int* dev_err;
+  cudaStream_t stream;
+
+  int S() const { return n_stored + (fuse_F ? 1 : 0); }
+};
+
+// Which kernel a launch took (for tests and the bench).
+enum AggPath { kPathNone = 0, kPathRing = 1, kPathGeneric = 2 };
+
+// Launch; returns cudaSuccess or the launch error.  *path gets the kernel.
+cudaError_t launch_aggregate(const AggArgs& a, AggPath* path);
+
+// dst = prev ? round(prev + F) : F over n = T*d elements of dtype.
+cudaError_t launch_fold(const void* prev, const void* F, void* dst, int64_t n, int dtype,
+                        cudaStream_t stream);
+
+// out = round(tanh(x * g[c]) * s[c]) over [T, d].
+cudaError_t launch_synthetic_layer(const void* x, const float* g, const float* s, void* out,
+                                   int64_t T, int d, int dtype, cudaStream_t stream);
+
+// Per-device properties, cached.
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;
+};
+cudaError_t device_info(DeviceInfo* info);
+
+}  // namespace attnres

@@ -1,0 +1,103 @@
+"""Synthetic L-layer Block AttnRes stack forward on the GPU.
+
+Per layer l = 1..L: one fused `attnres_layer_step` (fold v_{l-1} into the
+partial sum or emit b_n at a block boundary, then aggregate layer l), then
+the stand-in layer body v_l = tanh(r_l * g_l) * s_l.  After layer L, the
+final output aggregation (l = L+1) folds v_L into the last block and
+aggregates [h_0, b_1 .. b_N] (Kimi K3 chaptered tutorial, ch. 4.3: the final
+output layer aggregates all block representations).  2L+1 launches per
+forward; `capture()` records them into one CUDA graph so a decode-sized
+forward is not bound by launch latency.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (
+    AttnResState,
+    attnres_layer_step,
+    attnres_num_sources,
+    attnres_synthetic_layer,
+)
+
+
+class StackForward:
+    """Buffers and launch sequence of one stack forward over T tokens.
+
+    h0: [T, d] embedding (bf16 or fp32); W: [L+1, d] fp32 pseudo-queries
+    (row L is the final aggregation's); G, Sc: [L, d] fp32 gains and scales
+    of the synthetic layer body.  Outputs: `r` ([T, d], the final residual
+    stream after `run()`), `weights[l-1]` ([T, S_l] fp32, l = 1..L+1).
+    """
+
+    def __init__(self, h0, W, G, Sc, num_layers: int, block_size: int, eps: float = 1e-5,
+                 keep_weights: bool = True, dev_err: torch.Tensor | None = None):
+        self.L, self.B = num_layers, block_size
+        T, d = h0.shape
+        self.T, self.d = T, d
+        self.W, self.G, self.Sc = W, G, Sc
+        self.state = AttnResState.allocate(h0, num_layers, block_size, eps)
+        self.r = torch.empty_like(h0)
+        self.F = torch.empty_like(h0)
+        self.S = [attnres_num_sources(l, block_size, num_layers) for l in range(1, num_layers + 2)]
+        self.weights = None
+        if keep_weights:
+            flat = torch.empty(T * sum(self.S), dtype=torch.float32, device=h0.device)
+            self.weights, off = [], 0
+            for s in self.S:
+                self.weights.append(flat[off:off + T * s].view(T, s))
+                off += T * s
+        self.dev_err = dev_err
+        self.graph = None
+
+    def launches_per_forward(self) -> int:
+        return 2 * self.L + 1
+
+    def _issue(self, stream=None) -> None:
+        self.state.reset()
+        for l in range(1, self.L + 2):
+            attnres_layer_step(self.state, self.F if l > 1 else None, self.W[l - 1], l, self.r,
+                               self.weights[l - 1] if self.weights is not None else None,
+                               dev_err=self.dev_err, stream=stream)
+            if l <= self.L:
+                attnres_synthetic_layer(self.r, self.G[l - 1], self.Sc[l - 1], self.F, stream=stream)
+
+    def run(self, stream=None) -> torch.Tensor:
+        """One forward (replays the captured graph if there is one)."""
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self._issue(stream)
+        return self.r
+
+    def capture(self) -> None:
+        """Record the whole forward into a CUDA graph (after one eager run)."""
+        self._issue()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._issue()
+        self.graph = g
+
+    def bytes_moved(self) -> int:
+        """Minimum HBM bytes one forward must move (every source row, F row,
+        partial/b_n row read once; r, F, partial/b_n and weights written once)."""
+        esz = self.state.h0.element_size()
+        row = self.T * self.d * esz
+        total = 0
+        for l in range(1, self.L + 2):
+            S = self.S[l - 1]
+            if l == 1:
+                total += row + row                       # read h_0, write r
+            else:
+                p = l - 1
+                first = (p - 1) // self.B * self.B + 1
+                has_prev = p > first
+                total += (S - 1) * row                   # stored sources
+                total += row * (2 if has_prev else 1)    # partial (if any) + F_{l-1}
+                total += row                             # new partial / b_n
+                total += row                             # r_l
+            total += self.T * S * 4                      # weights
+            if l <= self.L:
+                total += 2 * row + 2 * self.d * 4        # F_l: read r, write F (+ g, s)
+        return total

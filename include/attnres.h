@@ -1,0 +1,198 @@
+/*
+ * attnres.h -- C ABI of libattnres: Block Attention Residuals (Block AttnRes)
+ * depth aggregation on NVIDIA GB300 (sm_103a).
+ *
+ * What the operations compute (sources cited by page title and section):
+ *
+ *  - [Deep-dive 2] "Kimi K3 deep-dive series (2): AttnRes and Stable
+ *    LatentMoE", §2: for one token and layer l with sources H (S rows of d)
+ *    and a learned pseudo-query w_l,
+ *        a_l = softmax_s( w_l . RMSNorm(H_s) ),     r_l = sum_s a_l[s] H_s,
+ *    RMSNorm without a gain, no temperature, values are the raw sources.
+ *    [Atlas] "LLM Atlas · Kimi K3", §07 Attention Residuals, states the same
+ *    weights alpha_{i->l} and h_l = sum_i alpha_{i->l} v_i.
+ *  - [Parts 6] "Kimi K3 model structure (6): inputs and parts", odd facts:
+ *    RMSNorm eps = 1e-5 model-wide.  Here rms(h) = sqrt(mean_c h_c^2 + eps).
+ *  - [Tutorial] Kimi K3 chaptered tutorial (kimi.papertok.ai), ch. 4.3,
+ *    Eq. 10: layers are split into blocks of B layers; a completed block is
+ *    kept as the SUM of its layers' outputs b_n; layer i of block n reads
+ *    [b_0 .. b_{n-1}] if i = 1 and [b_0 .. b_{n-1}, partial] if i >= 2,
+ *    where b_0 is the embedding h_0 and the partial sum holds the outputs of
+ *    layers 1..i-1 of block n.  The final output layer aggregates all block
+ *    representations.  Ch. 4.5: K3 uses B = 12 over 93 layers (the 8th block
+ *    has 9 layers), so at most 9 sources.  Ch. 4.6: block representations
+ *    are produced once at the block boundary and then stay resident.
+ *
+ * Conventions for every call:
+ *  - Tensors are row-major [T, d] (token-major, channel contiguous) in device
+ *    memory; `sources` / `block_reps` are HOST arrays of DEVICE pointers.
+ *  - The caller owns and allocates every buffer.  The library allocates no
+ *    device memory and keeps no device-side global state.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream) and never synchronise the device.
+ *  - Argument errors are detected on the host before any launch and return
+ *    a negative attnres_status; nothing is written then.  A failed launch
+ *    returns ATTNRES_ECUDA; attnres_last_error() gives the CUDA message
+ *    (per host thread).
+ *  - dev_err (nullable): a device int32 the kernels OR error bits into
+ *    (ATTNRES_DEVERR_*); they never clear it.  Every spin-wait inside the
+ *    kernels has a time limit; when one runs out the kernel sets the bit,
+ *    writes NaN to the affected outputs, drains its own copies and returns.
+ *  - Any pointer alignment and any d >= 1 is accepted; rows that start on a
+ *    16-byte boundary with 16-byte-multiple row length take the bulk-copy
+ *    (TMA) path, others a plain-load kernel (still on the GPU).
+ */
+#ifndef ATTNRES_H
+#define ATTNRES_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTNRES_OK = 0,
+  ATTNRES_EINVAL = -1, /* null pointer, non-positive size, bad eps */
+  ATTNRES_EDTYPE = -2, /* dtype code not one of attnres_dtype */
+  ATTNRES_ERANGE = -4, /* S > ATTNRES_MAX_SOURCES, too many blocks, T*d overflow */
+  ATTNRES_ECUDA = -5,  /* a CUDA runtime call or launch failed */
+  ATTNRES_ESTATE = -6  /* stack call out of order (see attnres_state) */
+} attnres_status;
+
+typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
+
+/* bits ORed into *dev_err by the kernels */
+#define ATTNRES_DEVERR_WAIT_TIMEOUT 0x1 /* a bounded wait on a copy gave up */
+
+#define ATTNRES_MAX_SOURCES 128
+#define ATTNRES_MAX_BLOCKS (ATTNRES_MAX_SOURCES - 1)
+#define ATTNRES_DEFAULT_EPS 1e-5f
+
+/* ------------------------------------------------------------------------
+ * attnres_aggregate -- one layer of depth-wise attention ([Deep-dive 2] §2).
+ *
+ *   for every token t in [0, T):
+ *     z[s]  = (sum_c w_l[c] * src_s[t,c]) / sqrt(mean_c src_s[t,c]^2 + eps)
+ *     a[t,:] = softmax_s(z)                         (fp32)
+ *     r[t,c] = sum_s a[t,s] * src_s[t,c]            (fp32 accumulate)
+ *
+ * sources     host array of S device pointers, each [T, d] of src_dtype
+ *             (a [S, T, d] slab: sources[s] = base + s*T*d elements)
+ * S           1 .. ATTNRES_MAX_SOURCES
+ * T, d        T >= 0 (T = 0 launches nothing), d >= 1
+ * src_dtype   ATTNRES_F32 or ATTNRES_BF16
+ * w_l         device [d] fp32 pseudo-query
+ * eps         > 0 or 0 (1e-5 in K3)
+ * out_r       device [T, d] of out_dtype; bf16 is rounded to nearest even
+ * out_weights device [T, S] fp32, or NULL to skip
+ * Each source row is read from device memory once.  out_r may not alias a
+ * source.  Returns ATTNRES_OK or a negative attnres_status.
+ * ---------------------------------------------------------------------- */
+int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int src_dtype,
+                      const float* w_l, float eps, void* out_r, int out_dtype,
+                      float* out_weights, int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Stack state: the resident depth sources of one batch of T tokens.
+ * ([Tutorial] ch. 4.3-4.6: b_0 = embedding, b_1 .. b_N completed block sums
+ * kept resident, one running partial sum of the current block.)
+ *
+ * The caller allocates the buffers (each [T, d] of `dtype`) and fills the
+ * struct with attnres_state_init; the library only updates `folded`.
+ * `folded` = number of layer outputs v_1 .. v_folded already folded into the
+ * partial sum / block representations.  Layer outputs must be folded in
+ * order: attnres_block_step(p) needs folded == p-1; attnres_layer_step(l)
+ * needs folded == l-2 (it folds v_{l-1} itself); attnres_layer_sources(l)
+ * needs folded == l-1.  Anything else returns ATTNRES_ESTATE.
+ * ---------------------------------------------------------------------- */
+typedef struct attnres_state {
+  const void* h0;                          /* device [T, d]: b_0, the embedding */
+  void* block_reps[ATTNRES_MAX_BLOCKS];    /* block_reps[k-1] = b_k, k = 1..N */
+  void* partial;                           /* device [T, d]: running partial sum */
+  int64_t T;
+  int d;
+  int dtype;                               /* attnres_dtype of every buffer */
+  int num_layers;                          /* L */
+  int block_size;                          /* B */
+  float eps;
+  int folded;                              /* progress, maintained by the library */
+} attnres_state;
+
+/* Fill *st.  n_block_reps must be >= ceil(L/B) (ATTNRES_ERANGE if
+ * ceil(L/B) > ATTNRES_MAX_BLOCKS).  Buffers must not alias each other.
+ * Host only; sets folded = 0. */
+int attnres_state_init(attnres_state* st, const void* h0, void* const* block_reps,
+                       int n_block_reps, void* partial, int64_t T, int d, int dtype,
+                       int num_layers, int block_size, float eps);
+
+/* Rewind to layer 1 (folded = 0).  Host only; buffers are left as they are. */
+int attnres_state_reset(attnres_state* st);
+
+/* Number of sources layer `layer_idx` (1..L, or L+1 for the final output
+ * aggregation) reads: n + [i >= 2] for layer i of block n, ceil(L/B) + 1 for
+ * L+1 ([Tutorial] ch. 4.3 Eq. 10; [Atlas] §28 workbench: ceil(L/S) +
+ * embedding).  Host only, pure.  Negative status on bad arguments. */
+int attnres_num_sources(int layer_idx, int block_size, int num_layers);
+
+/* Host only: the device pointers of layer `layer_idx`'s sources in order
+ * [h_0, b_1 .. b_{n-1}, partial (if non-empty)] into out_ptrs (capacity
+ * ATTNRES_MAX_SOURCES), their count into *out_S.  Needs folded ==
+ * layer_idx - 1.  With attnres_block_step this gives the unfused path:
+ * block_step(p) then aggregate(layer_sources(p+1)). */
+int attnres_layer_sources(const attnres_state* st, int layer_idx, const void** out_ptrs,
+                          int* out_S);
+
+/* ------------------------------------------------------------------------
+ * attnres_block_step -- fold layer `layer_idx`'s output v = F_out into the
+ * block bookkeeping ([Tutorial] ch. 4.3, 4.6):
+ *   new = (partial non-empty) ? partial + v : v      (fp32 add, one rounding)
+ *   if layer_idx ends its block (layer_idx % B == 0 or layer_idx == L):
+ *        b_n = new, partial becomes empty
+ *   else partial = new
+ * F_out: device [T, d] of st->dtype.  Needs folded == layer_idx - 1;
+ * advances folded.  One elementwise launch.
+ * ---------------------------------------------------------------------- */
+int attnres_block_step(attnres_state* st, const void* F_out, int layer_idx, int* dev_err,
+                       void* stream);
+
+/* ------------------------------------------------------------------------
+ * attnres_layer_step -- the fused hot path of one layer: fold F_prev =
+ * v_{l-1} (exactly as attnres_block_step(l-1) would, same rounding, written
+ * to the partial sum or to b_n) and aggregate layer l over its sources,
+ * using the freshly formed partial / b_n as the last source without reading
+ * it back.  One launch.
+ *   layer_idx  1..L+1 (L+1 = the final output aggregation over [h_0, b_1..b_N])
+ *   F_prev     device [T, d] of st->dtype; NULL exactly when layer_idx == 1
+ *   w_l        device [d] fp32 pseudo-query of this layer
+ *   out_r      device [T, d] of st->dtype (must not alias the state's buffers)
+ *   out_weights device [T, S_l] fp32 or NULL
+ * Needs folded == max(layer_idx - 2, 0); advances folded to layer_idx - 1.
+ * Bit-identical to block_step(l-1) + aggregate(layer_sources(l)).
+ * ---------------------------------------------------------------------- */
+int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, int layer_idx,
+                       void* out_r, float* out_weights, int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * attnres_synthetic_layer -- the stand-in layer body used to drive a stack
+ * forward without trained weights (not part of the method):
+ *   out[t,c] = tanh(x[t,c] * g[c]) * s[c], fp32 math, rounded to `dtype`.
+ * x, out: device [T, d] of dtype (may alias); g, s: device [d] fp32.
+ * ---------------------------------------------------------------------- */
+int attnres_synthetic_layer(const void* x, const float* g, const float* s, void* out, int64_t T,
+                            int d, int dtype, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* attnres_status_string(int status);
+
+/* Detail of the last error returned on this host thread ("" if none). */
+const char* attnres_last_error(void);
+
+/* ABI version: (major << 16) | minor. */
+int attnres_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNRES_H */

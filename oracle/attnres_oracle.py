@@ -200,13 +200,19 @@ class StackTrace:
     final_sources: list = field(default_factory=list)  # sources of the final aggregation
 
 
-def _fold_sum(terms: list, store: Callable) -> np.ndarray:
-    """Sum of the terms in order, each running total stored (rounded) once:
-    ((t1 + t2) -> store) + t3 -> store ...  (plain sum when store is exact)."""
-    acc = terms[0]
-    for t in terms[1:]:
-        acc = store(acc + t)
-    return acc
+def _range_sum(outputs: dict, first: int, last: int, store: Callable, memo: dict) -> np.ndarray:
+    """Sum of the layer outputs v_first .. v_last, added in layer order with
+    every running total stored (rounded) once:
+        ((v_first + v_{first+1}) -> store) + v_{first+2} -> store ...
+    (a plain sum when `store` is exact).  Memoised per range: the sum over
+    first..last is the stored sum over first..last-1 plus v_last."""
+    key = (first, last)
+    if key not in memo:
+        if last == first:
+            memo[key] = outputs[first]
+        else:
+            memo[key] = store(_range_sum(outputs, first, last - 1, store, memo) + outputs[last])
+    return memo[key]
 
 
 def block_stack_forward(h0: np.ndarray, W: np.ndarray, layer_fn: Callable[[int, np.ndarray], np.ndarray],
@@ -221,7 +227,7 @@ def block_stack_forward(h0: np.ndarray, W: np.ndarray, layer_fn: Callable[[int, 
     [Tutorial ch. 4.3]).  After layer L the final aggregation (l = L+1) uses
     W[L] over [h_0, b_1 .. b_N].
 
-    Every source is rebuilt from the list of layer outputs for each layer
+    Every source is looked up from the list of layer outputs for each layer
     (b_k and the partial sum are sums over explicit layer ranges).  `store`
     models storage rounding (e.g. `round_bf16`): it is applied to every
     tensor the stack writes (r_l, v_l, and each running total of a block sum);
@@ -232,6 +238,7 @@ def block_stack_forward(h0: np.ndarray, W: np.ndarray, layer_fn: Callable[[int, 
     W = np.asarray(W, dtype=np.float64)
     h0 = np.asarray(h0, dtype=np.float64)
     outputs = {0: h0}                               # v_0 = h_0
+    memo: dict = {}
     tr = StackTrace()
     for layer in range(1, L + 2):
         srcs = []
@@ -240,7 +247,7 @@ def block_stack_forward(h0: np.ndarray, W: np.ndarray, layer_fn: Callable[[int, 
                 srcs.append(h0)
             else:
                 _, _, first, last = entry
-                srcs.append(_fold_sum([outputs[j] for j in range(first, last + 1)], store))
+                srcs.append(_range_sum(outputs, first, last, store, memo))
         r, a = depth_attention(np.stack(srcs), W[layer - 1], eps)
         r = store(r)
         tr.r.append(r)

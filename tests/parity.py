@@ -1,0 +1,80 @@
+"""Tolerances and comparison helpers of the GPU-vs-oracle parity tests.
+
+The bars (all written out here, used by every parity test):
+
+* weights a[t, s] (fp32 on the GPU): |a_gpu - a_ref| <= 1e-5 absolute;
+* fp32 outputs r: |r_gpu - r_ref| <= 1e-5 * (|r_ref| + sum_s a_s |h_s|),
+  i.e. 1e-5 relative to the condition scale of the weighted sum, so that
+  outputs that cancel to near zero do not fail spuriously;
+* bf16 outputs r (bf16 storage, fp32 accumulation):
+  |r_gpu - r_ref| <= ulp_bf16(r_ref) + 1e-3 * M_t with M_t = max_{s,c}
+  |h_s[t, c]| per token (the largest source magnitude of that token).
+
+r_ref and a_ref are the fp64 oracle's results on the very bytes the GPU
+read.  Nothing here computes the method itself.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+
+A_ATOL = 1e-5
+R_F32_RTOL = 1e-5
+R_BF16_MABS = 1e-3
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def ulp_bf16(x: np.ndarray) -> np.ndarray:
+    """Spacing of bfloat16 values in the binade of |x| (2^-133 at zero)."""
+    _, e = np.frexp(np.abs(x))
+    q = np.maximum(e - 8, -133)
+    return np.where(x == 0, 2.0 ** -133, np.ldexp(1.0, q))
+
+
+def oracle_aggregate(H: torch.Tensor, w: torch.Tensor, eps: float, chunk: int = 256):
+    """Oracle on a (possibly large) [S, T, d] tensor, token chunk by chunk.
+    Returns (r_ref [T, d], a_ref [T, S], cond [T, d], M [T]) in fp64, where
+    cond = sum_s a_s |h_s| and M = max_{s,c} |h_s|."""
+    S, T, d = H.shape
+    w64 = to64(w)
+    r = np.empty((T, d))
+    a = np.empty((T, S))
+    cond = np.empty((T, d))
+    M = np.empty(T)
+    for t0 in range(0, T, chunk):
+        h = to64(H[:, t0:t0 + chunk])
+        rr, aa = O.depth_attention(h, w64, eps)
+        r[t0:t0 + chunk] = rr
+        a[t0:t0 + chunk] = aa
+        cond[t0:t0 + chunk] = np.einsum("ts,std->td", aa, np.abs(h))
+        M[t0:t0 + chunk] = np.abs(h).max(axis=(0, 2))
+    return r, a, cond, M
+
+
+def check_weights(a_gpu: np.ndarray, a_ref: np.ndarray) -> float:
+    err = np.abs(a_gpu - a_ref)
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= A_ATOL, f"weights off by {worst:.3g} > {A_ATOL}"
+    return worst
+
+
+def check_r(r_gpu: np.ndarray, r_ref: np.ndarray, out_dtype: torch.dtype, cond: np.ndarray | None = None,
+            M: np.ndarray | None = None) -> dict:
+    """Assert the output bar; return error statistics."""
+    err = np.abs(r_gpu - r_ref)
+    if out_dtype == torch.float32:
+        bound = R_F32_RTOL * (np.abs(r_ref) + cond)
+        ratio = err / np.maximum(bound, np.finfo(np.float64).tiny)
+        assert (err <= bound).all(), f"fp32 r: worst error {ratio.max():.3g} x the bound"
+        return {"max_abs": float(err.max(initial=0)), "worst_ratio": float(ratio.max(initial=0))}
+    ulp = ulp_bf16(r_ref)
+    bound = ulp + R_BF16_MABS * M[:, None]
+    ratio = err / bound
+    assert (err <= bound).all(), f"bf16 r: worst error {ratio.max():.3g} x the bound"
+    return {"max_abs": float(err.max(initial=0)), "max_ulps": float((err / ulp).max(initial=0)),
+            "worst_ratio": float(ratio.max(initial=0))}

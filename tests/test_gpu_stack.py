@@ -1,0 +1,148 @@
+"""GPU parity of the fused stack path (attnres_layer_step + the block
+bookkeeping) against the fp64 oracle run with the same storage rounding.
+
+The oracle runs the whole stack on its own (free-running): it never sees a
+GPU result.  Per token the stack is independent of every other token, so at
+full size the oracle runs on sampled tokens only.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from tests.parity import A_ATOL, R_BF16_MABS, R_F32_RTOL, to64, ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    import depth_wise_attention_block_gb300 as A
+    return A
+
+
+def _oracle_stack(stk: W.Stack, tokens=None, store=O.round_bf16):
+    h0 = to64(stk.h0 if tokens is None else stk.h0[tokens])
+    G, Sc, Wq = to64(stk.G), to64(stk.Sc), to64(stk.W)
+    fn = lambda l, x: O.synthetic_layer(x, G[l - 1], Sc[l - 1])
+    return O.block_stack_forward(h0, Wq, fn, stk.num_layers, stk.block_size, store=store)
+
+
+def _gpu_stack(A, stk: W.Stack, graph=False):
+    from depth_wise_attention_block_gb300.stack import StackForward
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, dev_err=err)
+    if graph:
+        fwd.capture()
+    fwd.run()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return fwd
+
+
+def _layer_bar(ref_sources, r_ref, dtype):
+    """Per-element bound of one layer's output (see tests/parity.py)."""
+    if dtype == torch.float32:
+        return R_F32_RTOL * (np.abs(r_ref) + np.abs(np.stack(ref_sources)).max(0))
+    M = np.abs(np.stack(ref_sources)).max(axis=(0, 2))
+    return ulp_bf16(r_ref) + R_BF16_MABS * M[:, None]
+
+
+def _check_stack(fwd, tr, tokens, dtype, weight_tol):
+    """Every layer's weights and the final output against the oracle trace."""
+    worst_a, worst_r = 0.0, 0.0
+    L = fwd.L
+    for l in range(1, L + 2):
+        a = to64(fwd.weights[l - 1][tokens])
+        worst_a = max(worst_a, float(np.abs(a - tr.a[l - 1]).max()))
+    assert worst_a <= weight_tol, f"weights off by {worst_a:.3g}"
+    r = to64(fwd.r[tokens])
+    bound = _layer_bar(tr.final_sources, tr.r[-1], dtype)
+    err = np.abs(r - tr.r[-1])
+    worst_r = float((err / bound).max())
+    assert worst_r <= 1.0, f"final output off by {worst_r:.3g} x the bound"
+    # the resident block representations after the forward
+    for k, b in enumerate(fwd.state.block_reps):
+        ref = tr.final_sources[k + 1]
+        bb = _layer_bar([ref], ref, dtype)
+        assert (np.abs(to64(b[tokens]) - ref) <= bb).all(), f"block rep {k + 1}"
+    return worst_a, worst_r
+
+
+@pytest.mark.parametrize("L,B,T,d,dtype", [
+    (7, 3, 6, 64, torch.bfloat16),      # ring kernel, 3 blocks, the last incomplete
+    (12, 1, 5, 40, torch.float32),      # block size 1 = Full AttnRes; S reaches 13 (generic kernel)
+    (9, 4, 7, 7168, torch.bfloat16),    # K3 width, ring, 2 vectors per thread
+    (5, 9, 3, 24, torch.float32),       # one block holds every layer
+])
+def test_tiny_stacks_every_layer(A, L, B, T, d, dtype):
+    stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=31 + L + B, device="cuda", dtype=dtype)
+    fwd = _gpu_stack(A, stk)
+    store = O.round_bf16 if dtype == torch.bfloat16 else O.round_fp32
+    tr = _oracle_stack(stk, store=store)
+    tol = A_ATOL if dtype == torch.float32 else 1e-4
+    _check_stack(fwd, tr, slice(None), dtype, tol)
+
+
+def test_fused_equals_unfused_bit_for_bit(A):
+    L, B, T, d = 14, 4, 33, 7168
+    stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=77, device="cuda")
+    fused = _gpu_stack(A, stk)
+    # unfused: block_step, then aggregate over layer_sources
+    st = A.AttnResState.allocate(stk.h0, L, B)
+    r = torch.empty_like(stk.h0)
+    F = torch.empty_like(stk.h0)
+    for l in range(1, L + 2):
+        if l > 1:
+            A.attnres_block_step(st, F, l - 1)
+        ptrs = A.attnres_layer_sources(st, l)
+        bufs = {t.data_ptr(): t for t in [st.h0, st.partial] + st.block_reps}
+        srcs = [bufs[p] for p in ptrs]
+        a = torch.empty((T, len(srcs)), dtype=torch.float32, device="cuda")
+        A.attnres_aggregate(srcs, stk.W[l - 1], r, a)
+        assert torch.equal(a, fused.weights[l - 1]), f"layer {l} weights differ"
+        if l <= L:
+            A.attnres_synthetic_layer(r, stk.G[l - 1], stk.Sc[l - 1], F)
+    torch.cuda.synchronize()
+    assert torch.equal(r, fused.r)
+    for b1, b2 in zip(st.block_reps, fused.state.block_reps):
+        assert torch.equal(b1, b2)
+
+
+def test_cuda_graph_replay_matches_eager(A):
+    stk = W.stack(T=64, num_layers=20, block_size=12, seed=5, device="cuda")
+    eager = _gpu_stack(A, stk)
+    graphed = _gpu_stack(A, stk, graph=True)
+    graphed.run()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.r, graphed.r)
+    for a1, a2 in zip(eager.weights, graphed.weights):
+        assert torch.equal(a1, a2)
+
+
+def test_decode_stack_T64_every_token(A):
+    stk = W.stack_T64(device="cuda")
+    fwd = _gpu_stack(A, stk, graph=True)
+    tr = _oracle_stack(stk)
+    wa, wr = _check_stack(fwd, tr, slice(None), torch.bfloat16, 1e-4)
+    print(f"decode stack T=64: worst weight error {wa:.3g}, worst output error {wr:.3g} x bound")
+
+
+def test_prefill_stack_T2048_sampled_tokens(A):
+    stk = W.stack_T2048(device="cuda")
+    fwd = _gpu_stack(A, stk)
+    tokens = torch.tensor([0, 1, 151, 152, 1000, 1023, 2046, 2047], device="cuda")
+    tr = _oracle_stack(stk, tokens)
+    wa, wr = _check_stack(fwd, tr, tokens, torch.bfloat16, 1e-4)
+    print(f"prefill stack T=2048: worst weight error {wa:.3g}, worst output error {wr:.3g} x bound")
+
+
+def test_bytes_model_counts_k3_sources(A):
+    stk = W.stack(T=8, d=64, seed=1, device="cuda")
+    from depth_wise_attention_block_gb300.stack import StackForward
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, 93, 12)
+    assert sum(fwd.S[:93]) == 493 and fwd.S[-1] == 9
+    assert fwd.bytes_moved() > 0

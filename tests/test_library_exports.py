@@ -1,0 +1,150 @@
+"""The C-ABI library builds, loads and exports every symbol include/attnres.h
+declares; its host-only logic (source counts, source lists, argument and
+order checks) behaves as specified.  No compute call: runs without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def native():
+    from depth_wise_attention_block_gb300 import build as B
+    if not os.path.exists(B.LIB_PATH):
+        B.build()
+    from depth_wise_attention_block_gb300 import _native
+    return _native
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "attnres.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attnres_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(native):
+    declared = _declared_functions()
+    assert len(declared) >= 10
+    for name in declared:
+        assert hasattr(native.lib, name), name
+    assert sorted(native.EXPORTED) == declared
+
+
+def test_abi_version_and_status_strings(native):
+    v = native.lib.attnres_version()
+    assert v >> 16 == 1
+    for code in [0, -1, -2, -4, -5, -6]:
+        assert native.lib.attnres_status_string(code).startswith(b"ATTNRES_")
+    assert b"unknown" in native.lib.attnres_status_string(12345)
+
+
+@pytest.mark.parametrize("L,B", [(93, 12), (7, 3), (6, 1), (5, 5), (5, 9), (1, 1), (13, 4)])
+def test_num_sources_matches_the_value_list(native, L, B):
+    for l in range(1, L + 2):
+        assert native.lib.attnres_num_sources(l, B, L) == O.num_sources(l, B, L)
+    assert native.lib.attnres_num_sources(L + 1, B, L) == -(-L // B) + 1
+    assert native.lib.attnres_num_sources(0, B, L) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_num_sources(L + 2, B, L) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_num_sources(1, 0, L) == native.ATTNRES_EINVAL
+
+
+def _fake_state(native, L, B, T=4, d=8, dtype=1):
+    """State over fake (never dereferenced) device pointers."""
+    N = -(-L // B)
+    st = native.AttnresState()
+    h0, partial = 0x10000, 0x20000
+    reps = (ctypes.c_void_p * N)(*[0x100000 * (k + 1) for k in range(N)])
+    rc = native.lib.attnres_state_init(ctypes.byref(st), h0, reps, N, partial, T, d, dtype, L, B, 1e-5)
+    assert rc == 0, native.lib.attnres_last_error()
+    return st, h0, partial, list(reps)
+
+
+@pytest.mark.parametrize("L,B", [(93, 12), (7, 3), (6, 1), (5, 9)])
+def test_layer_sources_follow_eq10(native, L, B):
+    st, h0, partial, reps = _fake_state(native, L, B)
+    assert st.T == 4 and st.d == 8 and st.dtype == 1 and st.num_layers == L and st.block_size == B
+    assert abs(st.eps - 1e-5) < 1e-12 and st.folded == 0
+    out = (ctypes.c_void_p * 128)()
+    n = ctypes.c_int()
+    for l in range(1, L + 2):
+        st.folded = l - 1   # as if v_1 .. v_{l-1} had been folded
+        assert native.lib.attnres_layer_sources(ctypes.byref(st), l, out, ctypes.byref(n)) == 0
+        got = [out[i] for i in range(n.value)]
+        want = []
+        for e in O.value_list(l, B, L):
+            if e[0] == "embed":
+                want.append(h0)
+            elif e[0] == "block":
+                want.append(reps[e[1] - 1])
+            else:
+                want.append(partial)
+        assert got == want, (l, got, want)
+
+
+def test_stack_calls_enforce_order(native):
+    L, B = 7, 3
+    st, *_ = _fake_state(native, L, B)
+    out = (ctypes.c_void_p * 128)()
+    n = ctypes.c_int()
+    # sources of layer 3 need v_1, v_2 folded
+    assert native.lib.attnres_layer_sources(ctypes.byref(st), 3, out, ctypes.byref(n)) == native.ATTNRES_ESTATE
+    # block_step(2) before block_step(1)
+    assert native.lib.attnres_block_step(ctypes.byref(st), 0x999, 2, None, None) == native.ATTNRES_ESTATE
+    # layer_step: F_prev must be NULL exactly at layer 1; layer 3 needs folded == 1
+    assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, 1, 0x777, None, None, None) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 2, 0x777, None, None, None) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, 3, 0x777, None, None, None) == native.ATTNRES_ESTATE
+    assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, L + 2, 0x777, None, None, None) == native.ATTNRES_EINVAL
+    # out_r may not alias the state
+    st.folded = 0
+    assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 1, 0x20000, None, None, None) == native.ATTNRES_EINVAL
+    assert b"alias" in native.lib.attnres_last_error()
+    assert st.folded == 0
+    assert native.lib.attnres_state_reset(ctypes.byref(st)) == 0
+
+
+def test_state_init_rejects_bad_arguments(native):
+    st = native.AttnresState()
+    reps = (ctypes.c_void_p * 3)(0x1000, 0x2000, 0x3000)
+    init = native.lib.attnres_state_init
+    assert init(ctypes.byref(st), None, reps, 3, 0x50, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
+    assert init(ctypes.byref(st), 0x40, reps, 2, 0x50, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL  # need 3
+    assert init(ctypes.byref(st), 0x40, reps, 3, 0x50, 4, 8, 7, 7, 3, 1e-5) == native.ATTNRES_EDTYPE
+    assert init(ctypes.byref(st), 0x40, reps, 3, 0x50, 4, 0, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
+    assert init(ctypes.byref(st), 0x40, reps, 3, 0x1000, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL  # alias
+    assert init(ctypes.byref(st), 0x40, reps, 3, 0x50, 4, 8, 1, 7, 3, -1.0) == native.ATTNRES_EINVAL
+    many = (ctypes.c_void_p * 200)(*range(0x1000, 0x1000 + 200 * 16, 16))
+    assert init(ctypes.byref(st), 0x40, many, 200, 0x50, 4, 8, 1, 200, 1, 1e-5) == native.ATTNRES_ERANGE
+
+
+def test_aggregate_rejects_bad_arguments_before_any_launch(native):
+    agg = native.lib.attnres_aggregate
+    src = (ctypes.c_void_p * 3)(0x1000, 0x2000, 0x3000)
+    ok_args = dict(S=3, T=4, d=8, sdt=1, w=0x4000, eps=1e-5, r=0x5000, odt=1)
+
+    def call(**kw):
+        a = {**ok_args, **kw}
+        return agg(kw.get("src", src), a["S"], a["T"], a["d"], a["sdt"], a["w"], a["eps"], a["r"], a["odt"],
+                   None, None, None)
+
+    assert call(S=0) == native.ATTNRES_EINVAL
+    assert call(S=129) == native.ATTNRES_ERANGE
+    assert call(sdt=5) == native.ATTNRES_EDTYPE
+    assert call(odt=-1) == native.ATTNRES_EDTYPE
+    assert call(T=-1) == native.ATTNRES_EINVAL
+    assert call(d=0) == native.ATTNRES_EINVAL
+    assert call(w=None) == native.ATTNRES_EINVAL
+    assert call(r=None) == native.ATTNRES_EINVAL
+    assert call(eps=float("nan")) == native.ATTNRES_EINVAL
+    assert call(eps=-1e-5) == native.ATTNRES_EINVAL
+    assert call(T=1 << 40, d=7168) == native.ATTNRES_ERANGE
+    assert call(src=(ctypes.c_void_p * 3)(0x1000, None, 0x3000)) == native.ATTNRES_EINVAL
+    assert b"sources[1]" in native.lib.attnres_last_error()
+    assert agg(None, 3, 4, 8, 1, 0x4000, 1e-5, 0x5000, 1, None, None, None) == native.ATTNRES_EINVAL
+    # T = 0 is a valid empty problem: nothing is launched
+    assert call(T=0) == 0

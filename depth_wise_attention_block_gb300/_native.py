@@ -63,7 +63,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"libattnres.so not found at {LIB_PATH}; build it first "
-            "(python -m depth_wise_attention_block_gb300.build). There is no CPU fallback.")
+            "(python depth_wise_attention_block_gb300/build.py). There is no CPU fallback.")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     sp = ctypes.POINTER(AttnresState)

@@ -53,7 +53,10 @@ struct RingShared {
   uint64_t empty[kRingMaxSlots];  // every consumer warp has taken its part of the row
   float red[kRingConsumerWarps][2 * kRingSmax];
   float a[kRingSmax + 1];
-  int abort_flag;
+  // set (never cleared) when a wait of the token loop's iteration i gave up;
+  // indexed by i & 1 so a fast warp flagging iteration i+1 cannot be seen
+  // by a slow warp still reading the flag of iteration i
+  int abort_flag[2];
 };
 constexpr int kRingHeaderBytes = (int)((sizeof(RingShared) + 127) / 128 * 128);
 
@@ -140,7 +143,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
       mbar_init(smem_addr(&sh.full[k]), 1);
       mbar_init(smem_addr(&sh.empty[k]), kRingConsumerWarps);
     }
-    sh.abort_flag = 0;
+    sh.abort_flag[0] = 0;
+    sh.abort_flag[1] = 0;
     mbar_fence_init();
   }
   __syncthreads();
@@ -216,7 +220,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     }
   };
 
-  for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+  int iter = 0;
+  for (long long t = blockIdx.x; t < T; t += gridDim.x, ++iter) {
+    volatile int* abort_flag = &sh.abort_flag[iter & 1];
     uint4 x[kRingSmax][VPT];
     float dot[kRingSmax], ss[kRingSmax];
 #pragma unroll
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
           sh.red[warp][2 * s + 1] = ss[s];
         }
       }
-      if (warp_failed) sh.abort_flag = 1;
+      if (warp_failed) *abort_flag = 1;
     }
     named_barrier_sync(kRingBarrierId, kRingConsumers);
 
@@ -304,7 +310,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
       const float tot = warp_sum(e);
       if (is_src) {
         float a = e / tot;
-        if (*(volatile int*)&sh.abort_flag) a = __int_as_float(0x7fc00000);
+        if (*abort_flag) a = __int_as_float(0x7fc00000);
         sh.a[lane >> 1] = a;
         if (p.out_a) p.out_a[t * S + (lane >> 1)] = a;
       }
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     named_barrier_sync(kRingBarrierId, kRingConsumers);
 
     // ---- r = sum_s a_s h_s from the registers
-    const bool abort = *(volatile int*)&sh.abort_flag != 0;
+    const bool abort = *abort_flag != 0;
     float as[kRingSmax];
 #pragma unroll
     for (int s = 0; s < kRingSmax; ++s) as[s] = (s < S) ? sh.a[s] : 0.f;

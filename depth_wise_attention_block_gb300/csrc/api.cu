@@ -43,8 +43,6 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 bool valid_dtype(int dt) { return dt == ATTNRES_F32 || dt == ATTNRES_BF16; }
 
-int dtype_bytes(int dt) { return dt == ATTNRES_BF16 ? 2 : 4; }
-
 // T * d * 4 must stay well inside int64 (element offsets are 64-bit).
 bool size_ok(int64_t T, int d) { return T >= 0 && d >= 1 && T <= (((int64_t)1) << 40) / d; }
 
@@ -105,11 +103,11 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
   if (!valid_dtype(src_dtype) || !valid_dtype(out_dtype)) return fail(ATTNRES_EDTYPE, "dtype %d/%d", src_dtype, out_dtype);
   if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
   if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
-  if (!w_l || !out_r) return fail(ATTNRES_EINVAL, "w_l/out_r is NULL");
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  if (T == 0) return ok();  // empty problem: nothing is read or written, buffers may be NULL
+  if (!w_l || !out_r) return fail(ATTNRES_EINVAL, "w_l/out_r is NULL");
   for (int s = 0; s < S; ++s)
     if (!sources[s]) return fail(ATTNRES_EINVAL, "sources[%d] is NULL", s);
-  if (T == 0) return ok();
   AggArgs a{};
   for (int s = 0; s < S; ++s) a.src[s] = sources[s];
   a.n_stored = S;

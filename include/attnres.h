@@ -80,7 +80,7 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
  * sources     host array of S device pointers, each [T, d] of src_dtype
  *             (a [S, T, d] slab: sources[s] = base + s*T*d elements)
  * S           1 .. ATTNRES_MAX_SOURCES
- * T, d        T >= 0 (T = 0 launches nothing), d >= 1
+ * T, d        T >= 0 (T = 0 launches nothing and accepts NULL buffers), d >= 1
  * src_dtype   ATTNRES_F32 or ATTNRES_BF16
  * w_l         device [d] fp32 pseudo-query
  * eps         > 0 or 0 (1e-5 in K3)

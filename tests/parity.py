@@ -12,6 +12,20 @@ The bars (all written out here, used by every parity test):
 
 r_ref and a_ref are the fp64 oracle's results on the very bytes the GPU
 read.  Nothing here computes the method itself.
+
+Free-running bf16 stacks (many layers, each side feeding its own stored
+outputs forward) cannot meet the 1e-5 weight bar: wherever the GPU's fp32
+value and the oracle's fp64 value of a stored tensor straddle a bf16
+rounding boundary, the stored values differ by one ulp, and those flips
+spread to later layers (measured: ~30% of elements after a few blocks, while
+fp32 storage stays within 2e-7).  With one-ulp differences of independent
+sign in the sources, the logit difference w.(dh)/rms has standard deviation
+at most 2^-7 (ulp <= 2^-7 |h|, w ~ N(0, 1/d) so E[sum_c w_c^2 h_c^2/rms^2] = 1);
+the largest of ~10^5 logits is within ~4.7 sigma = 0.037, and a softmax weight
+moves by at most about half the largest logit change: 0.018.  So free-running
+bf16 stacks use STACK_BF16_A_ATOL = 2e-2 for the weights (a bookkeeping
+mistake moves weights by O(0.1-1)); their outputs keep the bf16 bar above.
+fp32-storage stacks use the fp32 bars unchanged.
 """
 from __future__ import annotations
 
@@ -23,6 +37,7 @@ import oracle as O
 A_ATOL = 1e-5
 R_F32_RTOL = 1e-5
 R_BF16_MABS = 1e-3
+STACK_BF16_A_ATOL = 2e-2
 
 
 def to64(t: torch.Tensor) -> np.ndarray:

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def native():
-    from depth_wise_attention_block_gb300 import build as B
+    import __graft_entry__
+    B = __graft_entry__._build_module()
     if not os.path.exists(B.LIB_PATH):
         B.build()
     from depth_wise_attention_block_gb300 import _native
@@ -146,5 +147,7 @@ def test_aggregate_rejects_bad_arguments_before_any_launch(native):
     assert call(src=(ctypes.c_void_p * 3)(0x1000, None, 0x3000)) == native.ATTNRES_EINVAL
     assert b"sources[1]" in native.lib.attnres_last_error()
     assert agg(None, 3, 4, 8, 1, 0x4000, 1e-5, 0x5000, 1, None, None, None) == native.ATTNRES_EINVAL
-    # T = 0 is a valid empty problem: nothing is launched
+    # T = 0 is a valid empty problem: nothing is launched, buffers may be NULL
     assert call(T=0) == 0
+    assert agg(None, 3, 0, 8, 1, None, 1e-5, None, 1, None, None, None) == native.ATTNRES_EINVAL  # sources list
+    assert agg(src, 3, 0, 8, 1, None, 1e-5, None, 1, None, None, None) == 0

@@ -51,8 +51,9 @@ constexpr int kRingBarrierId = 1;                        // named barrier of the
 struct RingShared {
   uint64_t full[kRingMaxSlots];   // slot holds a landed row
   uint64_t empty[kRingMaxSlots];  // every consumer warp has taken its part of the row
-  float red[kRingConsumerWarps][2 * kRingSmax];
-  float a[kRingSmax + 1];
+  // per-warp totals of dot(w, h_s) and sum(h_s^2), double-buffered by the
+  // token loop's iteration parity (one barrier per token suffices)
+  float red[2][kRingConsumerWarps][2 * kRingSmax];
   // set (never cleared) when a wait of the token loop's iteration i gave up;
   // indexed by i & 1 so a fast warp flagging iteration i+1 cannot be seen
   // by a slow warp still reading the flag of iteration i
@@ -95,6 +96,13 @@ struct Vec<bf16_t> {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                       pack_bf16x2(f[6], f[7]));
   }
+  // the 8 values as 4 packed fp32 pairs
+  static __device__ __forceinline__ void pairs(const uint4& v, uint64_t* p) {
+    p[0] = f2_pack(bf16lo(v.x), bf16hi(v.x));
+    p[1] = f2_pack(bf16lo(v.y), bf16hi(v.y));
+    p[2] = f2_pack(bf16lo(v.z), bf16hi(v.z));
+    p[3] = f2_pack(bf16lo(v.w), bf16hi(v.w));
+  }
 };
 template <>
 struct Vec<float> {
@@ -107,7 +115,47 @@ struct Vec<float> {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                       __float_as_uint(f[3]));
   }
+  static __device__ __forceinline__ void pairs(const uint4& v, uint64_t* p) {
+    p[0] = f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+    p[1] = f2_pack(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
 };
+
+// One level of a reduce-scatter over the warp: N values per lane; lanes
+// whose bit OFF is clear keep values [0, K), the others [K, N) (padded to
+// M values); each exchanges what it does not keep with lane ^ OFF.
+template <int N, int K, int OFF>
+__device__ __forceinline__ void rs_level(float* v, int lane) {
+  constexpr int M = K > N - K ? K : N - K;
+  const bool up = (lane & OFF) != 0;
+  float out[M];
+#pragma unroll
+  for (int i = 0; i < M; ++i) {
+    const float lo_part = i < K ? v[i] : 0.f;
+    const float hi_part = K + i < N ? v[K + i] : 0.f;
+    const float keep = up ? hi_part : lo_part;
+    const float send = up ? lo_part : hi_part;
+    out[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+  }
+#pragma unroll
+  for (int i = 0; i < M; ++i) v[i] = out[i];
+}
+
+// 18 partials (dot and sum of squares of 9 sources) summed over the warp in
+// 20 shuffles (18 -> 9 -> 5 -> 3 -> 2 -> 1 values per lane).  Afterwards the
+// lanes of kRsValidLanes hold, in v[0], the warp total of value rs_index(lane).
+constexpr uint32_t kRsValidLanes = 0x17371737u;
+__device__ __forceinline__ int rs_index(int lane) {
+  return 9 * ((lane >> 4) & 1) + 5 * ((lane >> 3) & 1) + 3 * ((lane >> 2) & 1) + 2 * ((lane >> 1) & 1) +
+         (lane & 1);
+}
+__device__ __forceinline__ void reduce_scatter18(float* v, int lane) {
+  rs_level<18, 9, 16>(v, lane);
+  rs_level<9, 5, 8>(v, lane);
+  rs_level<5, 3, 4>(v, lane);
+  rs_level<3, 2, 2>(v, lane);
+  rs_level<2, 1, 1>(v, lane);
+}
 
 // store EPV output values of vector `vec` of an output row
 template <typename Tout, int EPV>
@@ -191,12 +239,16 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
   }
 
   // ------------------------------------------------------------ consumers --
-  float wreg[VPT][EPV];
+  constexpr int NP = EPV / 2;  // packed fp32 pairs per 16-byte vector
+  uint64_t wp[VPT][NP];        // this thread's channels of w, as pairs
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = tid + k * kRingConsumers;
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) wreg[k][e] = (v < p.nvec) ? __ldg(p.w + v * EPV + e) : 0.f;
+    for (int j = 0; j < NP; ++j) {
+      const bool in = v < p.nvec;
+      wp[k][j] = f2_pack(in ? __ldg(p.w + v * EPV + 2 * j) : 0.f, in ? __ldg(p.w + v * EPV + 2 * j + 1) : 0.f);
+    }
   }
 
   const int S = p.S;
@@ -222,13 +274,14 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
 
   int iter = 0;
   for (long long t = blockIdx.x; t < T; t += gridDim.x, ++iter) {
-    volatile int* abort_flag = &sh.abort_flag[iter & 1];
+    const int buf = iter & 1;
+    volatile int* abort_flag = &sh.abort_flag[buf];
     uint4 x[kRingSmax][VPT];
-    float dot[kRingSmax], ss[kRingSmax];
+    float part[2 * kRingSmax];  // [2s] = dot(w, h_s), [2s+1] = sum(h_s^2), this thread's channels
 #pragma unroll
     for (int s = 0; s < kRingSmax; ++s) {
-      dot[s] = 0.f;
-      ss[s] = 0.f;
+      part[2 * s] = 0.f;
+      part[2 * s + 1] = 0.f;
       if (s < S) {
         if (!FUSED || s < p.n_stored) {
           consume(x[s]);
@@ -261,89 +314,81 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
             }
           }
         }
+        uint64_t dot2 = 0, ss2 = 0;  // two interleaved partial sums each
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-          float f[EPV];
-          Vec<Tin>::unpack(x[s][k], f);
+          uint64_t h[NP];
+          Vec<Tin>::pairs(x[s][k], h);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            dot[s] = fmaf(wreg[k][e], f[e], dot[s]);
-            ss[s] = fmaf(f[e], f[e], ss[s]);
+          for (int j = 0; j < NP; ++j) {
+            dot2 = f2_fma(wp[k][j], h[j], dot2);
+            ss2 = f2_fma(h[j], h[j], ss2);
           }
         }
+        part[2 * s] = f2_hsum(dot2);
+        part[2 * s + 1] = f2_hsum(ss2);
       }
     }
 
-    // ---- reduce dot / sum of squares of every source over the CTA
-#pragma unroll
-    for (int s = 0; s < kRingSmax; ++s) {
-      if (s < S) {
-        dot[s] = warp_sum(dot[s]);
-        ss[s] = warp_sum(ss[s]);
-      }
+    // ---- warp totals (reduce-scatter), then one CTA-wide step through smem
+    reduce_scatter18(part, lane);
+    if ((kRsValidLanes >> lane) & 1u) {
+      const int idx = rs_index(lane);
+      if (idx < 2 * S) sh.red[buf][warp][idx] = part[0];
     }
     const bool warp_failed = __any_sync(0xffffffffu, !ok);
-    if (lane == 0) {
-#pragma unroll
-      for (int s = 0; s < kRingSmax; ++s) {
-        if (s < S) {
-          sh.red[warp][2 * s] = dot[s];
-          sh.red[warp][2 * s + 1] = ss[s];
-        }
-      }
-      if (warp_failed) *abort_flag = 1;
-    }
+    if (lane == 0 && warp_failed) *abort_flag = 1;
     named_barrier_sync(kRingBarrierId, kRingConsumers);
 
-    // ---- logits and the depth softmax (warp 0; lane 2s holds source s)
-    if (warp == 0) {
-      float v = 0.f;
-      if (lane < 2 * S) {
+    // ---- logits and the depth softmax, computed by every warp (lane 2s
+    // holds source s); all warps sum in the same order, so agree bit for bit
+    const bool abort = *abort_flag != 0;
+    float tot = 0.f;
+    if (lane < 2 * S) {
 #pragma unroll
-        for (int w = 0; w < kRingConsumerWarps; ++w) v += sh.red[w][lane];
-      }
-      const float sumsq = __shfl_down_sync(0xffffffffu, v, 1);
-      const bool is_src = lane < 2 * S && (lane & 1) == 0;
-      const float z = is_src ? v / sqrtf(sumsq / (float)p.d + p.eps) : -INFINITY;
-      const float m = warp_max(z);
-      const float e = is_src ? expf(z - m) : 0.f;
-      const float tot = warp_sum(e);
-      if (is_src) {
-        float a = e / tot;
-        if (*abort_flag) a = __int_as_float(0x7fc00000);
-        sh.a[lane >> 1] = a;
-        if (p.out_a) p.out_a[t * S + (lane >> 1)] = a;
-      }
+      for (int w = 0; w < kRingConsumerWarps; ++w) tot += sh.red[buf][w][lane];
     }
-    named_barrier_sync(kRingBarrierId, kRingConsumers);
+    const float sumsq = __shfl_down_sync(0xffffffffu, tot, 1);
+    const bool is_src = lane < 2 * S && (lane & 1) == 0;
+    const float z = is_src ? tot / sqrtf(sumsq / (float)p.d + p.eps) : -INFINITY;
+    const float m = warp_max(z);
+    const float e = is_src ? expf(z - m) : 0.f;
+    const float esum = warp_sum(e);
+    float a = abort ? __int_as_float(0x7fc00000) : e / esum;
+    if (warp == 0 && is_src && p.out_a) p.out_a[t * S + (lane >> 1)] = a;
+    uint64_t a2[kRingSmax];
+#pragma unroll
+    for (int s = 0; s < kRingSmax; ++s) {
+      const float as = __shfl_sync(0xffffffffu, a, 2 * s);
+      a2[s] = f2_pack(as, as);
+    }
 
     // ---- r = sum_s a_s h_s from the registers
-    const bool abort = *abort_flag != 0;
-    float as[kRingSmax];
-#pragma unroll
-    for (int s = 0; s < kRingSmax; ++s) as[s] = (s < S) ? sh.a[s] : 0.f;
     char* orow = p.out_r + t * (long long)p.out_row_bytes;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * kRingConsumers;
       if (v < p.nvec) {
-        float acc[EPV];
+        uint64_t acc[NP];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+        for (int j = 0; j < NP; ++j) acc[j] = 0;
 #pragma unroll
         for (int s = 0; s < kRingSmax; ++s) {
           if (s < S) {
-            float f[EPV];
-            Vec<Tin>::unpack(x[s][k], f);
+            uint64_t h[NP];
+            Vec<Tin>::pairs(x[s][k], h);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) acc[e] = fmaf(as[s], f[e], acc[e]);
+            for (int j = 0; j < NP; ++j) acc[j] = f2_fma(a2[s], h[j], acc[j]);
           }
         }
+        float r[EPV];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) f2_unpack(acc[j], r[2 * j], r[2 * j + 1]);
         if (abort) {
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) acc[e] = __int_as_float(0x7fc00000);
+          for (int e2 = 0; e2 < EPV; ++e2) r[e2] = __int_as_float(0x7fc00000);
         }
-        store_out<Tout, EPV>(orow, v, acc);
+        store_out<Tout, EPV>(orow, v, r);
       }
     }
     if (abort) {

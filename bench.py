@@ -432,7 +432,7 @@ def run_gpu(args):
                        "parallelism": f"token-sharded x{ws}, no data exchange"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "agg_ring_kernel<bf16,bf16,2,false>",
+                         "kernel": "agg_ring_kernel<bf16,bf16,VPT=2,unfused,exact>",
                          "algorithmic_bytes_per_launch": bytes_launch, "peak_source": peak_src,
                          "launch_ms_mean": launch_ms, "launch_ms_median": m["launch_ms_median"]},
             "hbm_gbs_achieved": achieved,

@@ -79,6 +79,7 @@ struct RingParams {
   int out_row_bytes;
   int nslots;
   float eps;
+  float inv_d;    // 1/d rounded to fp32
 };
 
 template <typename Tin>
@@ -174,8 +175,10 @@ __device__ __forceinline__ void store_out(char* row, int vec, const float* acc) 
   }
 }
 
-template <typename Tin, typename Tout, int VPT, bool FUSED>
+template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT>
 __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_constant__ RingParams p) {
+  // EXACT: the row holds exactly VPT * kRingConsumers vectors, so every
+  // consumer thread owns VPT of them and no bounds test is needed
   constexpr int EPV = Vec<Tin>::kElems;
   extern __shared__ __align__(128) unsigned char smem[];
   RingShared& sh = *reinterpret_cast<RingShared*>(smem);
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     const int v = tid + k * kRingConsumers;
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
-      const bool in = v < p.nvec;
+      const bool in = EXACT || v < p.nvec;
       wp[k][j] = f2_pack(in ? __ldg(p.w + v * EPV + 2 * j) : 0.f, in ? __ldg(p.w + v * EPV + 2 * j + 1) : 0.f);
     }
   }
@@ -262,7 +265,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * kRingConsumers;
-      dst[k] = (ok && v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
+      // after a failed wait the slot holds stale data: harmless, the token is abandoned
+      dst[k] = (EXACT || v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&sh.empty[slot]));
@@ -294,7 +298,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
 #pragma unroll
           for (int k = 0; k < VPT; ++k) {
             const int v = tid + k * kRingConsumers;
-            if (v < p.nvec) {
+            if (EXACT || v < p.nvec) {
               float f[EPV];
               Vec<Tin>::unpack(fv[k], f);
               if (p.fuse_prev) {
@@ -314,19 +318,21 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
             }
           }
         }
-        uint64_t dot2 = 0, ss2 = 0;  // two interleaved partial sums each
+        // two packed accumulators each (four partial sums) to keep the
+        // dependent FMA chains short
+        uint64_t dot2[2] = {0, 0}, ss2[2] = {0, 0};
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           uint64_t h[NP];
           Vec<Tin>::pairs(x[s][k], h);
 #pragma unroll
           for (int j = 0; j < NP; ++j) {
-            dot2 = f2_fma(wp[k][j], h[j], dot2);
-            ss2 = f2_fma(h[j], h[j], ss2);
+            dot2[j & 1] = f2_fma(wp[k][j], h[j], dot2[j & 1]);
+            ss2[j & 1] = f2_fma(h[j], h[j], ss2[j & 1]);
           }
         }
-        part[2 * s] = f2_hsum(dot2);
-        part[2 * s + 1] = f2_hsum(ss2);
+        part[2 * s] = f2_hsum(dot2[0]) + f2_hsum(dot2[1]);
+        part[2 * s + 1] = f2_hsum(ss2[0]) + f2_hsum(ss2[1]);
       }
     }
 
@@ -350,11 +356,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     }
     const float sumsq = __shfl_down_sync(0xffffffffu, tot, 1);
     const bool is_src = lane < 2 * S && (lane & 1) == 0;
-    const float z = is_src ? tot / sqrtf(sumsq / (float)p.d + p.eps) : -INFINITY;
+    // fast reciprocal square root, exponential and division: each within a
+    // few fp32 ulps, far inside the 1e-5 weight tolerance
+    const float z = is_src ? tot * rsqrtf(fmaf(sumsq, p.inv_d, p.eps)) : -INFINITY;
     const float m = warp_max(z);
-    const float e = is_src ? expf(z - m) : 0.f;
+    const float e = is_src ? __expf(z - m) : 0.f;
     const float esum = warp_sum(e);
-    float a = abort ? __int_as_float(0x7fc00000) : e / esum;
+    float a = abort ? __int_as_float(0x7fc00000) : __fdividef(e, esum);
     if (warp == 0 && is_src && p.out_a) p.out_a[t * S + (lane >> 1)] = a;
     uint64_t a2[kRingSmax];
 #pragma unroll
@@ -368,7 +376,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * kRingConsumers;
-      if (v < p.nvec) {
+      if (EXACT || v < p.nvec) {
         uint64_t acc[NP];
 #pragma unroll
         for (int j = 0; j < NP; ++j) acc[j] = 0;
@@ -520,14 +528,14 @@ cudaError_t device_info(DeviceInfo* info) {
   return cudaSuccess;
 }
 
-template <typename Tin, typename Tout, int VPT, bool FUSED>
+template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT>
 static cudaError_t launch_ring_t(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
   static bool configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  auto kern = agg_ring_kernel<Tin, Tout, VPT, FUSED>;
+  auto kern = agg_ring_kernel<Tin, Tout, VPT, FUSED, EXACT>;
   if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
     DeviceInfo di;
     e = device_info(&di);
@@ -543,12 +551,17 @@ static cudaError_t launch_ring_t(const RingParams& rp, int grid, int smem, cudaS
 template <typename Tin, typename Tout>
 static cudaError_t launch_ring_vpt(const RingParams& rp, int vpt, bool fused, int grid, int smem,
                                    cudaStream_t stream) {
+  const bool exact = rp.nvec == vpt * kRingConsumers;
   if (vpt == 1) {
-    return fused ? launch_ring_t<Tin, Tout, 1, true>(rp, grid, smem, stream)
-                 : launch_ring_t<Tin, Tout, 1, false>(rp, grid, smem, stream);
+    return fused ? launch_ring_t<Tin, Tout, 1, true, false>(rp, grid, smem, stream)
+                 : launch_ring_t<Tin, Tout, 1, false, false>(rp, grid, smem, stream);
   }
-  return fused ? launch_ring_t<Tin, Tout, 2, true>(rp, grid, smem, stream)
-               : launch_ring_t<Tin, Tout, 2, false>(rp, grid, smem, stream);
+  if (exact) {
+    return fused ? launch_ring_t<Tin, Tout, 2, true, true>(rp, grid, smem, stream)
+                 : launch_ring_t<Tin, Tout, 2, false, true>(rp, grid, smem, stream);
+  }
+  return fused ? launch_ring_t<Tin, Tout, 2, true, false>(rp, grid, smem, stream)
+               : launch_ring_t<Tin, Tout, 2, false, false>(rp, grid, smem, stream);
 }
 
 template <typename Tin, typename Tout>
@@ -611,6 +624,7 @@ cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
     rp.out_row_bytes = (int)((long long)a.d * osz);
     rp.nslots = nslots;
     rp.eps = a.eps;
+    rp.inv_d = 1.0f / (float)a.d;
     const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
     const int smem = kRingHeaderBytes + nslots * (int)row_bytes;
     *path = kPathRing;

@@ -112,8 +112,8 @@ def test_unaligned_pointers_take_the_generic_path(lib):
     r, a = _run(lib, H, inp.w)
     _compare(H, inp.w, r, a, torch.bfloat16)
     r2, a2 = _run(lib, inp.H, inp.w)
-    # same values from the other kernel, within fp32 rounding
-    assert (a - a2).abs().max().item() < 1e-6
+    # same values from the other kernel, within a few fp32 ulps
+    assert (a - a2).abs().max().item() < 5e-6
 
 
 def test_empty_T_writes_nothing(lib):

@@ -382,6 +382,17 @@ def bench_long(A, W, dev, peak, reps=8):
         "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}}
 
 
+def run_only(args):
+    """One secondary workload alone (for profiling); prints its numbers."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import depth_wise_attention_block_gb300 as A
+    import workloads as W
+    peak, _ = hbm_peak()
+    res = bench_stacks(A, W, dev, peak) if args.only == "stacks" else bench_long(A, W, dev, peak)
+    print(json.dumps(res), flush=True)
+
+
 def run_gpu(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -458,11 +469,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true", help="skip the stack and long-context workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["stacks", "long"], help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_gpu(args)
 

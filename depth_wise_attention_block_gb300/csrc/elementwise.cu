@@ -21,7 +21,7 @@
 namespace attnres {
 
 constexpr int kEwThreads = 256;
-constexpr int kEwCtasPerSm = 4;
+constexpr int kEwCtasPerSm = 8;  // 2048 threads per SM
 
 template <typename T>
 struct Vec16;
@@ -94,18 +94,39 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, con
   const long long n = T_ * (long long)d;
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
+    // kUnroll independent 16-byte loads in flight per thread before any math
     constexpr int E = Vec16<T>::kElems;
+    constexpr int kUnroll = 4;
     const int vrow = d / E;  // vectors per row (d % E == 0 here)
     const long long nv = n / E;
     const uint4* X4 = reinterpret_cast<const uint4*>(x);
     uint4* O4 = reinterpret_cast<uint4*>(out);
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
-      const int c0 = (int)(i % vrow) * E;
-      float f[E];
-      Vec16<T>::unpack(X4[i], f);
+    for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < nv; i0 += kUnroll * stride) {
+      uint4 v[kUnroll];
 #pragma unroll
-      for (int e = 0; e < E; ++e) f[e] = tanhf(f[e] * __ldg(g + c0 + e)) * __ldg(s + c0 + e);
-      O4[i] = Vec16<T>::pack(f);
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long i = i0 + u * stride;
+        if (i < nv) v[u] = X4[i];
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long i = i0 + u * stride;
+        if (i < nv) {
+          const int c0 = (int)(i % vrow) * E;
+          float f[E], gg[E], ss[E];
+          Vec16<T>::unpack(v[u], f);
+#pragma unroll
+          for (int e = 0; e < E; e += 4) {
+            const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + c0 + e));
+            const float4 s4 = __ldg(reinterpret_cast<const float4*>(s + c0 + e));
+            gg[e] = g4.x; gg[e + 1] = g4.y; gg[e + 2] = g4.z; gg[e + 3] = g4.w;
+            ss[e] = s4.x; ss[e + 1] = s4.y; ss[e + 2] = s4.z; ss[e + 3] = s4.w;
+          }
+#pragma unroll
+          for (int e = 0; e < E; ++e) f[e] = tanhf(f[e] * gg[e]) * ss[e];
+          O4[i] = Vec16<T>::pack(f);
+        }
+      }
     }
   } else {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -152,7 +173,8 @@ static cudaError_t launch_synth_t(const void* x, const float* g, const float* s,
                                   cudaStream_t st) {
   constexpr int E = 16 / (int)sizeof(T);
   const long long n = T_ * (long long)d;
-  const bool vec = d % E == 0 && al16(x) && al16(out);
+  // the vector path also reads g and s as float4: they must be 16-byte aligned
+  const bool vec = d % E == 0 && al16(x) && al16(out) && al16(g) && al16(s);
   const T* X = static_cast<const T*>(x);
   T* O = static_cast<T*>(out);
   if (vec) synth_layer_kernel<T, true><<<ew_grid(n / E), kEwThreads, 0, st>>>(X, g, s, O, T_, d);

@@ -31,6 +31,7 @@
 // as round(prev + F) (or F), written out as the new partial sum / block
 // representation, and used, already rounded, as a source.
 #include <math.h>
+#include <stdlib.h>
 
 #include "attnres.h"
 #include "device_common.cuh"
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
   const int lane = tid & 31;
   const int nslots = p.nslots;
   const long long T = p.T;
+  pdl_trigger();
 
   if (tid == 0) {
     for (int k = 0; k < nslots; ++k) {
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // everything below may read what the previous kernel wrote
 
   if (warp == kRingConsumerWarps) {
     // ----------------------------------------------------------- producer --
@@ -431,6 +434,8 @@ __global__ void __launch_bounds__(kGenThreads) agg_generic_kernel(const __grid_c
   __shared__ float s_za[kMaxSources];  // logits, then weights
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d = p.d, S = p.S;
+  pdl_trigger();
+  pdl_wait();
   for (long long t = blockIdx.x; t < p.T; t += gridDim.x) {
     const long long row = t * (long long)d;
     // pass 1: logit of every source (forming the fused source on the way)
@@ -544,8 +549,8 @@ static cudaError_t launch_ring_t(const RingParams& rp, int grid, int smem, cudaS
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
-  kern<<<grid, kRingThreads, smem, stream>>>(rp);
-  return cudaGetLastError();
+  e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, rp);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
@@ -566,8 +571,16 @@ static cudaError_t launch_ring_vpt(const RingParams& rp, int vpt, bool fused, in
 
 template <typename Tin, typename Tout>
 static cudaError_t launch_generic_t(const GenericParams& gp, int grid, cudaStream_t stream) {
-  agg_generic_kernel<Tin, Tout><<<grid, kGenThreads, 0, stream>>>(gp);
-  return cudaGetLastError();
+  const cudaError_t e = launch_kernel(agg_generic_kernel<Tin, Tout>, dim3(grid), dim3(kGenThreads), 0, stream, gp);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("ATTNRES_NO_PDL");
+    return !(v && v[0] && v[0] != '0');
+  }();
+  return on;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

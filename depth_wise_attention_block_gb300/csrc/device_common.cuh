@@ -191,6 +191,14 @@ __device__ __forceinline__ float f2_hsum(uint64_t v) {
   return lo + hi;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Every kernel here lets the next kernel on its stream be launched early
+// (pdl_trigger, first thing) and waits for the previous grid to complete and
+// its memory to be visible (pdl_wait) before its first global-memory access.
+// Both are no-ops when the launch did not opt in.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report_error(int* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }

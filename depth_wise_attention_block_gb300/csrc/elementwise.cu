@@ -58,6 +58,8 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kEwThreads) fold_kernel(const T* prev, const T* F, T* dst,
                                                           long long n) {
   // dst may alias prev (the partial sum is updated in place)
+  pdl_trigger();
+  pdl_wait();
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
     constexpr int E = Vec16<T>::kElems;
@@ -91,6 +93,8 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, const float* __restrict__ g,
                                                                  const float* __restrict__ s, T* out,
                                                                  long long T_, int d) {
+  pdl_trigger();
+  pdl_wait();
   const long long n = T_ * (long long)d;
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
@@ -157,9 +161,9 @@ static cudaError_t launch_fold_t(const void* prev, const void* F, void* dst, lon
   const T* P = static_cast<const T*>(prev);
   const T* Fp = static_cast<const T*>(F);
   T* D = static_cast<T*>(dst);
-  if (vec) fold_kernel<T, true><<<ew_grid(n / E), kEwThreads, 0, st>>>(P, Fp, D, n);
-  else fold_kernel<T, false><<<ew_grid(n), kEwThreads, 0, st>>>(P, Fp, D, n);
-  return cudaGetLastError();
+  const cudaError_t e = vec ? launch_kernel(fold_kernel<T, true>, dim3(ew_grid(n / E)), dim3(kEwThreads), 0, st, P, Fp, D, n)
+                           : launch_kernel(fold_kernel<T, false>, dim3(ew_grid(n)), dim3(kEwThreads), 0, st, P, Fp, D, n);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_fold(const void* prev, const void* F, void* dst, int64_t n, int dtype, cudaStream_t stream) {
@@ -177,9 +181,10 @@ static cudaError_t launch_synth_t(const void* x, const float* g, const float* s,
   const bool vec = d % E == 0 && al16(x) && al16(out) && al16(g) && al16(s);
   const T* X = static_cast<const T*>(x);
   T* O = static_cast<T*>(out);
-  if (vec) synth_layer_kernel<T, true><<<ew_grid(n / E), kEwThreads, 0, st>>>(X, g, s, O, T_, d);
-  else synth_layer_kernel<T, false><<<ew_grid(n), kEwThreads, 0, st>>>(X, g, s, O, T_, d);
-  return cudaGetLastError();
+  const cudaError_t e =
+      vec ? launch_kernel(synth_layer_kernel<T, true>, dim3(ew_grid(n / E)), dim3(kEwThreads), 0, st, X, g, s, O, T_, d)
+          : launch_kernel(synth_layer_kernel<T, false>, dim3(ew_grid(n)), dim3(kEwThreads), 0, st, X, g, s, O, T_, d);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_synthetic_layer(const void* x, const float* g, const float* s, void* out, int64_t T, int d,

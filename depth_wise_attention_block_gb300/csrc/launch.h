@@ -48,6 +48,28 @@ cudaError_t launch_fold(const void* prev, const void* F, void* dst, int64_t n, i
 cudaError_t launch_synthetic_layer(const void* x, const float* g, const float* s, void* out,
                                    int64_t T, int d, int dtype, cudaStream_t stream);
 
+// Launch `kern` with programmatic stream serialization allowed (the kernel
+// may start while the previous kernel on the stream finishes; every kernel
+// here waits for it with griddepcontrol.wait before touching global memory).
+// Set ATTNRES_NO_PDL=1 in the environment to launch plainly.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Per-device properties, cached.
 struct DeviceInfo {
   int sm_count;

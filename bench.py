@@ -301,7 +301,8 @@ def bench_main(args, A, W, dev, ws):
 
 def bench_e2e(args, A, dev, sets):
     """Through the public API with host buffers: pinned H2D of the sources
-    and the query, the aggregation, D2H of r and the weights, every step."""
+    and the query, the aggregation, D2H of r and the weights, every step
+    (aggregate_host pipelines them over 4 token chunks)."""
     s = sets[0]
     H_host = torch.empty(s.H.shape, dtype=s.H.dtype, pin_memory=True)
     H_host.copy_(s.H)

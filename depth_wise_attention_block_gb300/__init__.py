@@ -185,18 +185,58 @@ def attnres_synthetic_layer(x: torch.Tensor, g: torch.Tensor, s: torch.Tensor, o
     _N.check(rc, "attnres_synthetic_layer")
 
 
+_HOST_STREAMS: dict = {}
+
+
+def _host_streams(device):
+    key = torch.device(device).index
+    if key not in _HOST_STREAMS:
+        _HOST_STREAMS[key] = (torch.cuda.Stream(device), torch.cuda.Stream(device))
+    return _HOST_STREAMS[key]
+
+
 def aggregate_host(H_host: torch.Tensor, w_host: torch.Tensor, r_host: torch.Tensor, a_host: torch.Tensor | None,
                    H_dev: torch.Tensor, w_dev: torch.Tensor, r_dev: torch.Tensor, a_dev: torch.Tensor | None,
-                   eps: float = ATTNRES_DEFAULT_EPS, stream=None) -> None:
-    """One aggregation from and to host memory: copy the [S, T, d] sources
-    and w in (pinned host -> device), aggregate, copy r (and the weights)
-    back.  The device buffers are the caller's; everything is asynchronous
-    on `stream` (synchronise before reading r_host)."""
-    st = stream if stream is not None else torch.cuda.current_stream()
-    with torch.cuda.stream(st):
-        H_dev.copy_(H_host, non_blocking=True)
+                   eps: float = ATTNRES_DEFAULT_EPS, stream=None, chunks: int = 4) -> None:
+    """One aggregation from and to host memory, pipelined over token chunks.
+
+    The [S, T, d] sources and w are copied in from pinned host memory, each
+    chunk of tokens is aggregated as soon as its rows have arrived, and its r
+    (and weights) are copied back while later chunks are still coming in: the
+    host link (the limit of this path) carries both directions at once.  The
+    device buffers are the caller's.  Asynchronous: `stream` (default: the
+    current stream) is complete, and r_host valid, once it is synchronised.
+    """
+    from .shard import token_range
+    S, T, d = H_host.shape
+    cur = stream if stream is not None else torch.cuda.current_stream()
+    copy_in, copy_out = _host_streams(H_dev.device)
+    start = torch.cuda.Event()
+    start.record(cur)
+    copy_in.wait_event(start)
+    copy_out.wait_event(start)
+    chunks = max(1, min(chunks, T))
+    with torch.cuda.stream(copy_in):
         w_dev.copy_(w_host, non_blocking=True)
-        attnres_aggregate(H_dev, w_dev, r_dev, a_dev, eps=eps, stream=st)
-        r_host.copy_(r_dev, non_blocking=True)
-        if a_host is not None and a_dev is not None:
-            a_host.copy_(a_dev, non_blocking=True)
+    for c in range(chunks):
+        t0, t1 = token_range(T, c, chunks)
+        if t1 == t0:
+            continue
+        with torch.cuda.stream(copy_in):
+            for s in range(S):
+                H_dev[s, t0:t1].copy_(H_host[s, t0:t1], non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(copy_in)
+        cur.wait_event(arrived)
+        with torch.cuda.stream(cur):
+            attnres_aggregate([H_dev[s, t0:t1] for s in range(S)], w_dev, r_dev[t0:t1],
+                              a_dev[t0:t1] if a_dev is not None else None, eps=eps, stream=cur)
+            done = torch.cuda.Event()
+            done.record(cur)
+        copy_out.wait_event(done)
+        with torch.cuda.stream(copy_out):
+            r_host[t0:t1].copy_(r_dev[t0:t1], non_blocking=True)
+            if a_host is not None and a_dev is not None:
+                a_host[t0:t1].copy_(a_dev[t0:t1], non_blocking=True)
+    cur.wait_stream(copy_in)
+    cur.wait_stream(copy_out)

@@ -144,3 +144,23 @@ def test_deterministic_across_runs(lib):
     r1, a1 = _run(lib, inp.H, inp.w)
     r2, a2 = _run(lib, inp.H, inp.w)
     assert torch.equal(r1, r2) and torch.equal(a1, a2)
+
+
+def test_aggregate_host_pipeline_matches_device_path(lib):
+    # host buffers in and out, chunked over tokens: every token is computed by
+    # the same arithmetic as in one launch over all tokens, so bit for bit
+    T, d, S = 1000, 7168, 9
+    inp = W.block_bf16(T=T, d=d, seed=9, device="cuda")
+    H_host = torch.empty(inp.H.shape, dtype=inp.H.dtype, pin_memory=True)
+    H_host.copy_(inp.H)
+    w_host = inp.w.cpu().pin_memory()
+    r_host = torch.full((T, d), float("nan"), dtype=torch.bfloat16, pin_memory=True)
+    a_host = torch.full((T, S), float("nan"), dtype=torch.float32, pin_memory=True)
+    H_dev, w_dev = torch.empty_like(inp.H), torch.empty_like(inp.w)
+    r_dev = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    a_dev = torch.empty((T, S), dtype=torch.float32, device="cuda")
+    for chunks in (1, 3, 7):
+        lib.aggregate_host(H_host, w_host, r_host, a_host, H_dev, w_dev, r_dev, a_dev, chunks=chunks)
+        torch.cuda.synchronize()
+        r_ref, a_ref = _run(lib, inp.H, inp.w)
+        assert torch.equal(r_host.cuda(), r_ref) and torch.equal(a_host.cuda(), a_ref)

@@ -1,0 +1,216 @@
+// Pieces shared by the two ring kernels of libattnres (aggregate.cu: one
+// group of at most 9 sources per token; aggregate_multi.cu: any number of
+// sources in groups of 9 with an online softmax): the shared-memory layout,
+// the kernel parameters, 16-byte vector packing, the warp reduce-scatter of
+// the per-source partial sums, output stores, and the TMA producer.
+#pragma once
+
+#include "attnres.h"
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace attnres {
+
+// ------------------------------------------------------------ ring kernel --
+
+constexpr int kRingConsumerWarps = 14;
+constexpr int kRingConsumers = kRingConsumerWarps * 32;  // 448
+constexpr int kRingThreads = kRingConsumers + 32;        // + one producer warp
+constexpr int kRingSmax = 9;                             // K3: embedding + 7 blocks + partial
+constexpr int kRingMaxVpt = 2;                           // 16-byte vectors per thread per row
+constexpr int kRingMaxSlots = 16;
+constexpr int kRingBarrierId = 1;                        // named barrier of the consumers
+
+struct RingShared {
+  uint64_t full[kRingMaxSlots];   // slot holds a landed row
+  uint64_t empty[kRingMaxSlots];  // every consumer warp has taken its part of the row
+  // per-warp totals of dot(w, h_s) and sum(h_s^2), double-buffered by the
+  // token loop's iteration parity (one barrier per token suffices)
+  float red[2][kRingConsumerWarps][2 * kRingSmax];
+  // set (never cleared) when a wait of the token loop's iteration i gave up;
+  // indexed by i & 1 so a fast warp flagging iteration i+1 cannot be seen
+  // by a slow warp still reading the flag of iteration i
+  int abort_flag[2];
+  float zbuf[kMaxSources];  // logits of the token in flight (multi-group kernel)
+};
+constexpr int kRingHeaderBytes = (int)((sizeof(RingShared) + 127) / 128 * 128);
+
+struct RingParams {
+  const char* src[kMaxSources];
+  const char* fuse_prev;
+  const char* fuse_F;
+  char* fuse_dst;
+  const float* w;
+  char* out_r;
+  float* out_a;
+  int* dev_err;
+  long long T;
+  int d;
+  int n_stored;
+  int S;
+  int nvec;       // 16-byte vectors per source row
+  int row_bytes;  // bytes per source row
+  int out_row_bytes;
+  int nslots;
+  float eps;
+  float inv_d;    // 1/d rounded to fp32
+};
+
+template <typename Tin>
+struct Vec;
+template <>
+struct Vec<bf16_t> {
+  static constexpr int kElems = 8;
+  static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+  // the 8 values as 4 packed fp32 pairs
+  static __device__ __forceinline__ void pairs(const uint4& v, uint64_t* p) {
+    p[0] = f2_pack(bf16lo(v.x), bf16hi(v.x));
+    p[1] = f2_pack(bf16lo(v.y), bf16hi(v.y));
+    p[2] = f2_pack(bf16lo(v.z), bf16hi(v.z));
+    p[3] = f2_pack(bf16lo(v.w), bf16hi(v.w));
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int kElems = 4;
+  static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  static __device__ __forceinline__ void pairs(const uint4& v, uint64_t* p) {
+    p[0] = f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+    p[1] = f2_pack(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+};
+
+// One level of a reduce-scatter over the warp: N values per lane; lanes
+// whose bit OFF is clear keep values [0, K), the others [K, N) (padded to
+// M values); each exchanges what it does not keep with lane ^ OFF.
+template <int N, int K, int OFF>
+__device__ __forceinline__ void rs_level(float* v, int lane) {
+  constexpr int M = K > N - K ? K : N - K;
+  const bool up = (lane & OFF) != 0;
+  float out[M];
+#pragma unroll
+  for (int i = 0; i < M; ++i) {
+    const float lo_part = i < K ? v[i] : 0.f;
+    const float hi_part = K + i < N ? v[K + i] : 0.f;
+    const float keep = up ? hi_part : lo_part;
+    const float send = up ? lo_part : hi_part;
+    out[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+  }
+#pragma unroll
+  for (int i = 0; i < M; ++i) v[i] = out[i];
+}
+
+// 18 partials (dot and sum of squares of 9 sources) summed over the warp in
+// 20 shuffles (18 -> 9 -> 5 -> 3 -> 2 -> 1 values per lane).  Afterwards the
+// lanes of kRsValidLanes hold, in v[0], the warp total of value rs_index(lane).
+constexpr uint32_t kRsValidLanes = 0x17371737u;
+__device__ __forceinline__ int rs_index(int lane) {
+  return 9 * ((lane >> 4) & 1) + 5 * ((lane >> 3) & 1) + 3 * ((lane >> 2) & 1) + 2 * ((lane >> 1) & 1) +
+         (lane & 1);
+}
+__device__ __forceinline__ void reduce_scatter18(float* v, int lane) {
+  rs_level<18, 9, 16>(v, lane);
+  rs_level<9, 5, 8>(v, lane);
+  rs_level<5, 3, 4>(v, lane);
+  rs_level<3, 2, 2>(v, lane);
+  rs_level<2, 1, 1>(v, lane);
+}
+
+// store EPV output values of vector `vec` of an output row
+template <typename Tout, int EPV>
+__device__ __forceinline__ void store_out(char* row, int vec, const float* acc) {
+  if constexpr (sizeof(Tout) == 2 && EPV == 8) {
+    *reinterpret_cast<uint4*>(row + (size_t)vec * 16) = Vec<bf16_t>::pack(acc);
+  } else if constexpr (sizeof(Tout) == 2 && EPV == 4) {
+    *reinterpret_cast<uint2*>(row + (size_t)vec * 8) =
+        make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+  } else if constexpr (sizeof(Tout) == 4 && EPV == 8) {
+    uint4* o = reinterpret_cast<uint4*>(row + (size_t)vec * 32);
+    o[0] = Vec<float>::pack(acc);
+    o[1] = Vec<float>::pack(acc + 4);
+  } else {
+    *reinterpret_cast<uint4*>(row + (size_t)vec * 16) = Vec<float>::pack(acc);
+  }
+}
+
+
+// The producer: one thread streams every source row of this CTA's tokens
+// (t = blockIdx.x, blockIdx.x + gridDim.x, ...) into the ring, in order,
+// each row one TMA bulk copy completing on its slot's `full` barrier, after
+// the slot's previous row was released by all consumer warps.  On a wait
+// that runs out it stops issuing; in every case it waits (bounded) for its
+// copies in flight before returning, so the CTA never exits under a copy.
+__device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh, uint32_t ring) {
+  const int nslots = p.nslots;
+  const long long T = p.T;
+  const bool fused = p.fuse_F != nullptr;
+  const int rows = p.n_stored + (fused ? (p.fuse_prev ? 2 : 1) : 0);
+  uint32_t slot = 0, lap = 0;
+  long long issued = 0;
+  bool ok = true;
+  for (long long t = blockIdx.x; t < T && ok; t += gridDim.x) {
+    const long long off = t * (long long)p.row_bytes;
+    for (int j = 0; j < rows; ++j) {
+      const char* g;
+      if (j < p.n_stored) g = p.src[j] + off;
+      else if (p.fuse_prev && j == p.n_stored) g = p.fuse_prev + off;
+      else g = p.fuse_F + off;
+      // first lap: parity 1 of a fresh barrier counts as complete
+      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u)) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = smem_addr(&sh.full[slot]);
+      mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
+      bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+      ++issued;
+      if (++slot == (uint32_t)nslots) {
+        slot = 0;
+        ++lap;
+      }
+    }
+  }
+  if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+  // Every issued copy must have landed before this CTA exits: wait on the
+  // latest armed phase of each slot (already-consumed phases pass at once).
+  const long long armed_slots = issued < nslots ? issued : nslots;
+  for (int k = 0; k < armed_slots; ++k) {
+    const long long uses = (issued - 1 - k) / nslots + 1;
+    mbar_wait_bounded(smem_addr(&sh.full[k]), (uint32_t)((uses - 1) & 1));
+  }
+}
+
+// Launch of the multi-group kernel (aggregate_multi.cu).
+cudaError_t launch_ring_multi(const RingParams& rp, int vpt, bool fused, bool exact, bool in_bf16, bool out_bf16,
+                              int grid, int smem, cudaStream_t stream);
+
+// Barrier set-up by thread 0 (the caller synchronises the CTA afterwards).
+__device__ __forceinline__ void ring_init(const RingParams& p, RingShared& sh) {
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < p.nslots; ++k) {
+      mbar_init(smem_addr(&sh.full[k]), 1);
+      mbar_init(smem_addr(&sh.empty[k]), kRingConsumerWarps);
+    }
+    sh.abort_flag[0] = 0;
+    sh.abort_flag[1] = 0;
+    mbar_fence_init();
+  }
+}
+
+}  // namespace attnres

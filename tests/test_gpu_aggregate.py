@@ -83,7 +83,11 @@ SHAPES = [
     (129, 1000, 7, torch.float32, torch.bfloat16),     # ring, fp32 in, bf16 out (8-byte stores)
     (300, 3584, 9, torch.float32, torch.float32),      # ring, fp32, 2 vectors/thread
     (50, 7176, 9, torch.bfloat16, torch.bfloat16),     # generic: 897 vectors > 2 per thread
-    (40, 7168, 12, torch.bfloat16, torch.bfloat16),    # generic: S > 9
+    (40, 7168, 12, torch.bfloat16, torch.bfloat16),    # multi-group ring: S > 9 (groups of 6)
+    (300, 7168, 94, torch.bfloat16, torch.bfloat16),   # multi-group ring: Full AttnRes top layer, 94 sources
+    (200, 3584, 17, torch.float32, torch.float32),     # multi-group ring, fp32 (groups of 9)
+    (129, 7160, 10, torch.bfloat16, torch.float32),    # multi-group ring, ragged last vector pass
+    (50, 1000, 128, torch.float32, torch.bfloat16),    # multi-group ring, S = 128, one vector per thread
     (31, 7, 3, torch.float32, torch.float32),          # generic: row not a 16-byte multiple
     (31, 100, 128, torch.bfloat16, torch.float32),     # generic: S = 128
     (3, 7168, 1, torch.bfloat16, torch.bfloat16),      # S = 1

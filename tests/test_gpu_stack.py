@@ -106,6 +106,27 @@ def test_k3_layout_fp32_storage_93_layers(A, d):
     print(f"fp32 93-layer stack d={d}: worst weight error {wa:.3g}, worst output error {wr:.3g} x bound")
 
 
+@pytest.mark.parametrize("d", [3584, 7168])
+def test_full_attnres_fp32_storage_93_layers(A, d):
+    # block size 1 = Full AttnRes: layer l aggregates all l earlier outputs
+    # (up to 94 sources: the multi-group ring kernel at d=3584, the generic
+    # kernel at d=7168 fp32), at the fp32 bars over all 93 layers
+    stk = W.stack(T=16, d=d, num_layers=93, block_size=1, seed=43, device="cuda", dtype=torch.float32)
+    fwd = _gpu_stack(A, stk)
+    assert fwd.S[-1] == 94
+    tr = _oracle_stack(stk, store=O.round_fp32)
+    wa, wr = _check_stack(fwd, tr, slice(None), torch.float32, A_ATOL)
+    print(f"Full AttnRes fp32 93 layers d={d}: worst weight error {wa:.3g}, worst output error {wr:.3g} x bound")
+
+
+def test_full_attnres_bf16_93_layers(A):
+    stk = W.stack(T=16, d=7168, num_layers=93, block_size=1, seed=44, device="cuda")
+    fwd = _gpu_stack(A, stk, graph=True)
+    tr = _oracle_stack(stk)
+    wa, wr = _check_stack(fwd, tr, slice(None), torch.bfloat16, STACK_BF16_A_ATOL, check_blocks=False)
+    print(f"Full AttnRes bf16 93 layers: worst weight error {wa:.3g}, worst output error {wr:.3g} x bound")
+
+
 def test_fused_equals_unfused_bit_for_bit(A):
     L, B, T, d = 14, 4, 33, 7168
     stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=77, device="cuda")

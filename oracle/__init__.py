@@ -19,6 +19,7 @@ from .attnres_oracle import (  # noqa: F401
     rms,
     rmsnorm,
     depth_attention,
+    depth_attention_backward,
     block_index,
     position_in_block,
     block_layers,

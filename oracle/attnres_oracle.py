@@ -85,6 +85,42 @@ def depth_attention(H: Sequence[np.ndarray] | np.ndarray, w: np.ndarray,
     return r, a
 
 
+def depth_attention_backward(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
+                             eps: float = EPS) -> tuple[np.ndarray, np.ndarray]:
+    """Gradients of one depth-wise attention layer, recomputing its forward.
+
+    H [S, T, d] sources, w [d] pseudo-query, dr [T, d] gradient of the loss
+    with respect to r.  Returns (dH [S, T, d], dw [d]) in float64.  The
+    forward is recomputed here from H and w, as under the activation
+    checkpointing that wraps AttnRes in training ([Tutorial] ch. 4.6).
+
+    With rho_s = rms(h_s), z_s = (w . h_s) / rho_s, a = softmax(z),
+    r = sum_s a_s h_s, the chain rule gives, per token:
+        g_s   = dr . h_s,             gbar = sum_s a_s g_s
+        dz_s  = a_s (g_s - gbar)                       (softmax)
+        dh_s  = a_s dr                                 (through the values)
+              + dz_s (w - z_s rho_s h_s / (d rho_s^2)) / rho_s
+                                                       (through the logit;
+                                                        d rho_s / d h_s = h_s / (d rho_s))
+        dw   += sum_s dz_s h_s / rho_s
+    """
+    H = np.asarray(H, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    dr = np.asarray(dr, dtype=np.float64)
+    S, T, d = H.shape
+    rho = rms(H, eps)                                        # [S, T]
+    z = np.einsum("std,d->st", H, w) / rho                   # [S, T] logits
+    e = np.exp(z - z.max(axis=0, keepdims=True))
+    a = e / e.sum(axis=0, keepdims=True)                     # [S, T]
+    g = np.einsum("std,td->st", H, dr)                       # [S, T]
+    gbar = (a * g).sum(axis=0, keepdims=True)
+    dz = a * (g - gbar)                                      # [S, T]
+    dH = a[:, :, None] * dr[None]
+    dH = dH + (dz / rho)[:, :, None] * (w[None, None, :] - (z / (d * rho))[:, :, None] * H)
+    dw = np.einsum("st,std->d", dz / rho, H)
+    return dH, dw
+
+
 # --------------------------------------------------------------------------
 # Block bookkeeping: which sources layer l sees   [Tutorial ch. 4.3 Eq. 10]
 # --------------------------------------------------------------------------

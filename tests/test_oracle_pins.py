@@ -361,3 +361,59 @@ def test_block_stack_matches_brute_force(L, B):
         for t in range(T):
             np.testing.assert_allclose(tr.r[l][t], br[t][l], rtol=1e-12, atol=1e-13)
             np.testing.assert_allclose(tr.a[l][t], ba[t][l], rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------- backward -----
+
+def _loss(H, w, dr, eps):
+    r, _ = O.depth_attention(H, w, eps)
+    return float((r * dr).sum())
+
+
+@pytest.mark.parametrize("S,eps", [(1, 1e-5), (3, 1e-5), (9, 1e-5), (4, 0.0), (5, 0.3)])
+def test_backward_matches_central_differences(S, eps):
+    # the gradient of L = sum(dr * r) by central differences in fp64, entry by
+    # entry on a sample of coordinates (independent of the analytic formulas)
+    rng = np.random.default_rng(S * 7 + 1)
+    T, d = 3, 24
+    H = rng.standard_normal((S, T, d)) * rng.uniform(0.2, 3, size=(S, 1, 1))
+    w = rng.standard_normal(d) / math.sqrt(d) * 3
+    dr = rng.standard_normal((T, d))
+    dH, dw = O.depth_attention_backward(H, w, dr, eps)
+    step = 1e-6
+    for _ in range(40):
+        s, t, c = rng.integers(S), rng.integers(T), rng.integers(d)
+        Hp, Hm = H.copy(), H.copy()
+        Hp[s, t, c] += step
+        Hm[s, t, c] -= step
+        fd = (_loss(Hp, w, dr, eps) - _loss(Hm, w, dr, eps)) / (2 * step)
+        assert abs(fd - dH[s, t, c]) <= 1e-7 * (1 + abs(fd)), (s, t, c, fd, dH[s, t, c])
+    for c in range(d):
+        wp, wm = w.copy(), w.copy()
+        wp[c] += step
+        wm[c] -= step
+        fd = (_loss(H, wp, dr, eps) - _loss(H, wm, dr, eps)) / (2 * step)
+        assert abs(fd - dw[c]) <= 1e-7 * (1 + abs(fd)), (c, fd, dw[c])
+
+
+def test_backward_closed_forms():
+    rng = np.random.default_rng(5)
+    T, d = 4, 16
+    # one source: r = h_0, so dh_0 = dr and w has no influence
+    H = rng.standard_normal((1, T, d))
+    dr = rng.standard_normal((T, d))
+    dH, dw = O.depth_attention_backward(H, rng.standard_normal(d), dr)
+    assert np.array_equal(dH[0], dr) and np.array_equal(dw, np.zeros(d))
+    # zero query: uniform weights, dh_s = dr / S exactly in exact arithmetic
+    S = 5
+    H = rng.standard_normal((S, T, d)) * rng.uniform(0.1, 10, size=(S, 1, 1))
+    dH, dw = O.depth_attention_backward(H, np.zeros(d), dr)
+    np.testing.assert_allclose(dH, np.broadcast_to(dr / S, dH.shape), rtol=1e-14, atol=1e-15)
+    # eps = 0: the logit is invariant to scaling h_s, so its gradient is
+    # orthogonal to h_s and dh_s . h_s = a_s (dr . h_s)
+    w = rng.standard_normal(d) / math.sqrt(d)
+    dH, _ = O.depth_attention_backward(H, w, dr, eps=0.0)
+    _, a = O.depth_attention(H, w, eps=0.0)
+    lhs = np.einsum("std,std->st", dH, H)
+    rhs = a.T * np.einsum("std,td->st", H, dr)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-12)

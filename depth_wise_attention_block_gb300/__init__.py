@@ -31,7 +31,8 @@ from ._native import (  # noqa: F401
 )
 
 __all__ = [
-    "attnres_aggregate", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
+    "attnres_aggregate", "attnres_aggregate_backward", "attnres_aggregate_backward_workspace_size",
+    "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
     "attnres_layer_step", "attnres_synthetic_layer", "attnres_version", "AttnResState",
     "aggregate_host", "dtype_code", "AttnresError",
 ]
@@ -107,6 +108,44 @@ def attnres_aggregate(sources: Sequence[torch.Tensor] | torch.Tensor, w_l: torch
         _dev_ptr(out_r, "out_r"), dtype_code(out_r.dtype), _dev_ptr(out_weights, "out_weights", torch.float32),
         _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
     _N.check(rc, "attnres_aggregate")
+
+
+def attnres_aggregate_backward_workspace_size(T: int, d: int) -> int:
+    """Bytes of device workspace attnres_aggregate_backward needs."""
+    return _N.check(_N.lib.attnres_aggregate_backward_workspace_size(T, d), "attnres_aggregate_backward_workspace_size")
+
+
+def attnres_aggregate_backward(sources: Sequence[torch.Tensor] | torch.Tensor, w_l: torch.Tensor,
+                               grad_r: torch.Tensor, grad_sources: Sequence[torch.Tensor] | torch.Tensor,
+                               grad_w: torch.Tensor, workspace: torch.Tensor | None = None,
+                               eps: float = ATTNRES_DEFAULT_EPS, accumulate: bool = False,
+                               dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Gradients of attnres_aggregate with respect to its sources and w_l
+    (the forward is recomputed).  grad_sources: S tensors [T, d] (or one
+    [S, T, d]) of the sources' dtype, overwritten or (accumulate) added to;
+    grad_w: [d] float32, overwritten.  workspace: a device buffer of at least
+    attnres_aggregate_backward_workspace_size(T, d) bytes (allocated here
+    through torch when None)."""
+    srcs = list(sources.unbind(0)) if isinstance(sources, torch.Tensor) else list(sources)
+    grads = list(grad_sources.unbind(0)) if isinstance(grad_sources, torch.Tensor) else list(grad_sources)
+    if len(grads) != len(srcs):
+        raise ValueError("need one gradient buffer per source")
+    T, d = srcs[0].shape
+    dt = srcs[0].dtype
+    for i, t in enumerate(srcs + grads + [grad_r]):
+        if t.shape != (T, d) or t.dtype != dt:
+            raise ValueError(f"tensor {i}: expected [{T}, {d}] {dt}")
+    if workspace is None:
+        nbytes = attnres_aggregate_backward_workspace_size(T, d)
+        workspace = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device=srcs[0].device)
+    S = len(srcs)
+    sp = (ctypes.c_void_p * S)(*[_dev_ptr(t, f"sources[{i}]") for i, t in enumerate(srcs)])
+    gp = (ctypes.c_void_p * S)(*[_dev_ptr(t, f"grad_sources[{i}]") for i, t in enumerate(grads)])
+    rc = _N.lib.attnres_aggregate_backward(
+        sp, S, T, d, dtype_code(dt), _dev_ptr(w_l, "w_l", torch.float32), float(eps), _dev_ptr(grad_r, "grad_r"),
+        gp, int(bool(accumulate)), _dev_ptr(grad_w, "grad_w", torch.float32), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
+    _N.check(rc, "attnres_aggregate_backward")
 
 
 class AttnResState:

@@ -127,6 +127,64 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
   return ok();
 }
 
+int64_t attnres_aggregate_backward_workspace_size(int64_t T, int d) {
+  if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
+  const int64_t nb = backward_blocks(T);
+  if (nb < 0) return fail(ATTNRES_ECUDA, "no CUDA device");
+  ok();
+  return nb * (int64_t)d * (int64_t)sizeof(float);
+}
+
+int attnres_aggregate_backward(const void* const* sources, int S, int64_t T, int d, int dtype, const float* w_l,
+                               float eps, const void* grad_r, void* const* grad_sources, int accumulate,
+                               float* grad_w, void* workspace, int64_t workspace_bytes, int* dev_err, void* stream) {
+  if (!sources || !grad_sources) return fail(ATTNRES_EINVAL, "sources/grad_sources is NULL");
+  if (S < 1) return fail(ATTNRES_EINVAL, "S=%d < 1", S);
+  if (S > ATTNRES_MAX_SOURCES) return fail(ATTNRES_ERANGE, "S=%d > %d", S, ATTNRES_MAX_SOURCES);
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  if (!grad_w) return fail(ATTNRES_EINVAL, "grad_w is NULL");
+  if (accumulate != 0 && accumulate != 1) return fail(ATTNRES_EINVAL, "accumulate must be 0 or 1");
+  if (T > 0) {
+    if (!w_l || !grad_r || !workspace) return fail(ATTNRES_EINVAL, "w_l/grad_r/workspace is NULL");
+    for (int s = 0; s < S; ++s) {
+      if (!sources[s] || !grad_sources[s]) return fail(ATTNRES_EINVAL, "sources[%d]/grad_sources[%d] is NULL", s, s);
+      for (int j = 0; j < S; ++j)
+        if (grad_sources[s] == sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] aliases sources[%d]", s, j);
+      for (int j = 0; j < s; ++j)
+        if (grad_sources[s] == grad_sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] == grad_sources[%d]", s, j);
+    }
+    if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return fail(ATTNRES_EINVAL, "workspace not 4-byte aligned");
+    const int64_t need = attnres_aggregate_backward_workspace_size(T, d);
+    if (need < 0) return (int)need;
+    if (workspace_bytes < need)
+      return fail(ATTNRES_ERANGE, "workspace %lld bytes < %lld needed", (long long)workspace_bytes, (long long)need);
+  }
+  BwdArgs a{};
+  for (int s = 0; s < S && T > 0; ++s) {
+    a.src[s] = sources[s];
+    a.grad_src[s] = grad_sources[s];
+  }
+  a.S = S;
+  a.T = T;
+  a.d = d;
+  a.dtype = dtype;
+  a.w = w_l;
+  a.eps = eps;
+  a.grad_r = grad_r;
+  a.accumulate = accumulate != 0;
+  a.grad_w = grad_w;
+  a.workspace = static_cast<float*>(workspace);
+  a.dev_err = dev_err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_aggregate_backward(a);
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate_backward launch");
+  return ok();
+}
+
 int attnres_state_init(attnres_state* st, const void* h0, void* const* block_reps, int n_block_reps, void* partial,
                        int64_t T, int d, int dtype, int num_layers, int block_size, float eps) {
   if (!st || !h0 || !partial || !block_reps) return fail(ATTNRES_EINVAL, "NULL argument");

@@ -40,6 +40,27 @@ enum AggPath { kPathNone = 0, kPathRing = 1, kPathGeneric = 2, kPathRingMulti = 
 // Launch; returns cudaSuccess or the launch error.  *path gets the kernel.
 cudaError_t launch_aggregate(const AggArgs& a, AggPath* path);
 
+// Backward of one aggregation (see backward.cu).
+struct BwdArgs {
+  const void* src[kMaxSources];
+  void* grad_src[kMaxSources];
+  int S;
+  int64_t T;
+  int d;
+  int dtype;  // of sources, grad_r and grad_src
+  const float* w;
+  float eps;
+  const void* grad_r;
+  bool accumulate;
+  float* grad_w;
+  float* workspace;  // [backward_blocks(T), d] fp32
+  int* dev_err;
+  cudaStream_t stream;
+};
+cudaError_t launch_aggregate_backward(const BwdArgs& a);
+// CTAs (= fp32 workspace rows of d floats) the backward uses for T tokens
+int64_t backward_blocks(int64_t T);
+
 // dst = prev ? round(prev + F) : F over n = T*d elements of dtype.
 cudaError_t launch_fold(const void* prev, const void* F, void* dst, int64_t n, int dtype,
                         cudaStream_t stream);

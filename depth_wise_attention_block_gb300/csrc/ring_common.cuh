@@ -132,6 +132,46 @@ __device__ __forceinline__ void reduce_scatter18(float* v, int lane) {
   rs_level<2, 1, 1>(v, lane);
 }
 
+// Generic reduce-scatter of N <= 32 per-lane values over the warp, halving
+// the kept range at each of the offsets 16, 8, 4, 2, 1 (lower lanes keep the
+// first ceil(n/2) values).  Afterwards lane `lane` holds in v[0] the warp
+// total of value rs_lane_index<N>(lane), if rs_lane_valid<N>(lane).
+template <int N, int OFF>
+__device__ __forceinline__ void rs_levels(float* v, int lane) {
+  if constexpr (OFF >= 1) {
+    if constexpr (N > 1) {
+      constexpr int K = (N + 1) / 2;
+      rs_level<N, K, OFF>(v, lane);
+      rs_levels<K, OFF / 2>(v, lane);
+    } else {
+      // one value left per lane: the remaining levels sum it pairwise
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
+      rs_levels<1, OFF / 2>(v, lane);
+    }
+  }
+}
+template <int N>
+__device__ __forceinline__ void reduce_scatter(float* v, int lane) {
+  rs_levels<N, 16>(v, lane);
+}
+// index held by a lane after reduce_scatter<N>, or -1 if it holds padding
+template <int N>
+__device__ __forceinline__ int rs_lane_index(int lane) {
+  int n = N, base = 0, len = N;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const int K = (n + 1) / 2;
+    if (lane & off) {
+      base += K;
+      len = len > K ? len - K : 0;
+    } else {
+      len = len < K ? len : K;
+    }
+    n = K;
+  }
+  return len >= 1 ? base : -1;
+}
+
 // store EPV output values of vector `vec` of an output row
 template <typename Tout, int EPV>
 __device__ __forceinline__ void store_out(char* row, int vec, const float* acc) {

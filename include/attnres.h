@@ -94,6 +94,43 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
                       float* out_weights, int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * attnres_aggregate_backward -- gradients of attnres_aggregate.  In training
+ * AttnRes runs under activation checkpointing ([Tutorial] ch. 4.6): nothing
+ * is kept from the forward; the logits and weights are recomputed here from
+ * the sources.  Per token, with rho_s = rms(h_s), z_s = w.h_s / rho_s,
+ * a = softmax(z) and dr the gradient of the loss with respect to r:
+ *   g_s = dr.h_s,  gbar = sum_s a_s g_s,  dz_s = a_s (g_s - gbar),
+ *   alpha_s = dz_s / rho_s,  beta_s = alpha_s z_s / (d rho_s)
+ *   grad_sources[s][t,:]  =  (or +=)  a_s dr + alpha_s w - beta_s h_s
+ *   grad_w[c]             =  sum_t sum_s alpha_s h_s[t,c]
+ *
+ * sources, S, T, d, w_l, eps  as in attnres_aggregate; dtype is that of the
+ *             sources, of grad_r and of grad_sources
+ * grad_r      device [T, d] of dtype
+ * grad_sources host array of S device pointers [T, d] of dtype, none of them
+ *             aliasing a source or each other; overwritten (accumulate = 0)
+ *             or added to (accumulate = 1: a source read by several layers
+ *             collects the gradient of each)
+ * grad_w      device [d] fp32, overwritten (fp32 sums in a fixed order:
+ *             bit-reproducible)
+ * workspace   device scratch, 4-byte aligned, at least
+ *             attnres_aggregate_backward_workspace_size(T, d) bytes, owned
+ *             by the caller; its contents on entry do not matter
+ * Reads (S + 1) rows and writes S rows per token (S more read with
+ * accumulate).  T = 0 only zeroes grad_w.
+ * ---------------------------------------------------------------------- */
+int attnres_aggregate_backward(const void* const* sources, int S, int64_t T, int d, int dtype,
+                               const float* w_l, float eps, const void* grad_r,
+                               void* const* grad_sources, int accumulate, float* grad_w,
+                               void* workspace, int64_t workspace_bytes, int* dev_err,
+                               void* stream);
+
+/* Bytes of workspace attnres_aggregate_backward needs for T tokens of d
+ * channels on the current device (one fp32 row of d per CTA it runs, at most
+ * one CTA per SM).  Negative attnres_status on error. */
+int64_t attnres_aggregate_backward_workspace_size(int64_t T, int d);
+
+/* ------------------------------------------------------------------------
  * Stack state: the resident depth sources of one batch of T tokens.
  * ([Tutorial] ch. 4.3-4.6: b_0 = embedding, b_1 .. b_N completed block sums
  * kept resident, one running partial sum of the current block.)

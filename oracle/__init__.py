@@ -20,6 +20,7 @@ from .attnres_oracle import (  # noqa: F401
     rmsnorm,
     depth_attention,
     depth_attention_backward,
+    depth_attention_backward_scales,
     block_index,
     position_in_block,
     block_layers,

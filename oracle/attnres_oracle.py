@@ -121,6 +121,37 @@ def depth_attention_backward(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
     return dH, dw
 
 
+def depth_attention_backward_scales(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
+                                    eps: float = EPS) -> tuple[np.ndarray, np.ndarray]:
+    """Condition scales of the two gradients, for tolerances: the size of the
+    terms a forward-stable evaluation rounds.  Dot products count with their
+    absolute products (gabs_s = sum_c |dr_c h_sc|, zabs_s = sum_c |w_c h_sc|
+    / rho_s), and a rounding u in the logits moves a weight by about
+    a_s * 2 u max_j zabs_j.  Returns (dH_scale [S,T,d], dw_scale [d]):
+        adz_s  = a_s (gabs_s + sum_j a_j gabs_j + 2 |g_s - gbar| zmax) / rho_s
+        dH_s  ~ a_s |dr| (1 + 2 zmax) + adz_s (|w| + zabs_s |h_s| / (d rho_s))
+        dw    ~ sum_t sum_s adz_s |h_s|
+    """
+    H = np.asarray(H, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    dr = np.asarray(dr, dtype=np.float64)
+    S, T, d = H.shape
+    rho = rms(H, eps)
+    z = np.einsum("std,d->st", H, w) / rho
+    e = np.exp(z - z.max(axis=0, keepdims=True))
+    a = e / e.sum(axis=0, keepdims=True)
+    g = np.einsum("std,td->st", H, dr)
+    gbar = (a * g).sum(axis=0, keepdims=True)
+    gabs = np.einsum("std,td->st", np.abs(H), np.abs(dr))
+    zabs = np.einsum("std,d->st", np.abs(H), np.abs(w)) / rho
+    zmax = zabs.max(axis=0, keepdims=True)
+    adz = a * (gabs + (a * gabs).sum(axis=0, keepdims=True) + 2 * np.abs(g - gbar) * zmax) / rho
+    dHs = (a * (1 + 2 * zmax))[:, :, None] * np.abs(dr)[None] + adz[:, :, None] * (
+        np.abs(w)[None, None, :] + (zabs / (d * rho))[:, :, None] * np.abs(H))
+    dws = np.einsum("st,std->d", adz, np.abs(H))
+    return dHs, dws
+
+
 # --------------------------------------------------------------------------
 # Block bookkeeping: which sources layer l sees   [Tutorial ch. 4.3 Eq. 10]
 # --------------------------------------------------------------------------

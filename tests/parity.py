@@ -71,6 +71,24 @@ def oracle_aggregate(H: torch.Tensor, w: torch.Tensor, eps: float, chunk: int = 
     return r, a, cond, M
 
 
+def oracle_backward(H: torch.Tensor, w: torch.Tensor, dr: torch.Tensor, eps: float, chunk: int = 256):
+    """Oracle gradients and their condition scales, token chunk by chunk."""
+    S, T, d = H.shape
+    dH = np.empty((S, T, d))
+    dHs = np.empty((S, T, d))
+    dw = np.zeros(d)
+    dws = np.zeros(d)
+    w64 = to64(w)
+    for t0 in range(0, T, chunk):
+        h, g = to64(H[:, t0:t0 + chunk]), to64(dr[t0:t0 + chunk])
+        a, b = O.depth_attention_backward(h, w64, g, eps)
+        sa, sb = O.depth_attention_backward_scales(h, w64, g, eps)
+        dH[:, t0:t0 + chunk], dHs[:, t0:t0 + chunk] = a, sa
+        dw += b
+        dws += sb
+    return dH, dw, dHs, dws
+
+
 def check_weights(a_gpu: np.ndarray, a_ref: np.ndarray) -> float:
     err = np.abs(a_gpu - a_ref)
     worst = float(err.max()) if err.size else 0.0

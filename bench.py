@@ -387,6 +387,34 @@ def bench_long(A, W, dev, peak, reps=8):
         "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}}
 
 
+def bench_backward(A, W, dev, peak, reps=20):
+    """Backward of the single-layer workload (gradients of all 9 sources and
+    of w, forward recomputed): (S+1) rows read and S rows written per token."""
+    inp = W.block_bf16(T=T_MAIN, d=D_MAIN, seed=1, device=dev)
+    g = torch.Generator(device=dev).manual_seed(11)
+    dr = torch.randn((T_MAIN, D_MAIN), generator=g, device=dev).to(torch.bfloat16)
+    gH = torch.empty_like(inp.H)
+    gw = torch.empty(D_MAIN, device=dev)
+    ws = torch.empty(A.attnres_aggregate_backward_workspace_size(T_MAIN, D_MAIN) // 4, device=dev)
+    run = lambda: A.attnres_aggregate_backward(inp.H, inp.w, dr, gH, gw, workspace=ws)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    by = T_MAIN * (2 * S_MAIN + 1) * D_MAIN * 2 + D_MAIN * 4
+    gbs = by / (ms * 1e-3) / 1e9
+    del inp, dr, gH, ws
+    torch.cuda.empty_cache()
+    return {"backward_T4096_d7168_S9": {"ms_per_step": ms, "tokens_per_s": T_MAIN / (ms * 1e-3),
+                                        "algorithmic_bytes": by, "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}}
+
+
 def run_only(args):
     """One secondary workload alone (for profiling); prints its numbers."""
     dev = torch.device("cuda", 0)
@@ -394,7 +422,7 @@ def run_only(args):
     import depth_wise_attention_block_gb300 as A
     import workloads as W
     peak, _ = hbm_peak()
-    res = bench_stacks(A, W, dev, peak) if args.only == "stacks" else bench_long(A, W, dev, peak)
+    res = {"stacks": bench_stacks, "long": bench_long, "backward": bench_backward}[args.only](A, W, dev, peak)
     print(json.dumps(res), flush=True)
 
 
@@ -428,6 +456,7 @@ def run_gpu(args):
     if not args.no_extras:
         extras.update(bench_stacks(A, W, dev, peak))
         extras.update(bench_long(A, W, dev, peak))
+        extras.update(bench_backward(A, W, dev, peak))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -474,7 +503,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true", help="skip the stack and long-context workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["stacks", "long"], help="run one secondary workload alone")
+    ap.add_argument("--only", choices=["stacks", "long", "backward"], help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -185,6 +185,61 @@ int attnres_aggregate_backward(const void* const* sources, int S, int64_t T, int
   return ok();
 }
 
+int attnres_aggregate_backward_noalloc(const void* const* sources, int S, int64_t T, int d, int dtype,
+                                       const float* w_l, float eps, const void* grad_r, void* const* grad_sources,
+                                       int accumulate, float* grad_w, int* dev_err, void* stream) {
+  if (!sources || !grad_sources) return fail(ATTNRES_EINVAL, "sources/grad_sources is NULL");
+  if (S < 1) return fail(ATTNRES_EINVAL, "S=%d < 1", S);
+  if (S > ATTNRES_MAX_SOURCES) return fail(ATTNRES_ERANGE, "S=%d > %d", S, ATTNRES_MAX_SOURCES);
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  if (!grad_w) return fail(ATTNRES_EINVAL, "grad_w is NULL");
+  if (accumulate != 0 && accumulate != 1) return fail(ATTNRES_EINVAL, "accumulate must be 0 or 1");
+  float* scratch = nullptr;
+  int64_t capacity = 0;
+  if (T > 0) {
+    if (!w_l || !grad_r) return fail(ATTNRES_EINVAL, "w_l/grad_r is NULL");
+    for (int s = 0; s < S; ++s) {
+      if (!sources[s] || !grad_sources[s]) return fail(ATTNRES_EINVAL, "sources[%d]/grad_sources[%d] is NULL", s, s);
+      for (int j = 0; j < S; ++j)
+        if (grad_sources[s] == sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] aliases sources[%d]", s, j);
+      for (int j = 0; j < s; ++j)
+        if (grad_sources[s] == grad_sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] == grad_sources[%d]", s, j);
+    }
+    const int64_t rows = backward_blocks(T);
+    if (rows < 0) return fail(ATTNRES_ECUDA, "no CUDA device");
+    cudaError_t e = noalloc_backward_scratch(&scratch, &capacity);
+    if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate_backward_noalloc scratch lookup");
+    if (rows * (int64_t)d > capacity)
+      return fail(ATTNRES_ERANGE,
+                  "attnres_aggregate_backward_noalloc: needs %lld fp32 scratch values (%lld rows x d=%d), the "
+                  "built-in scratch holds %lld; use attnres_aggregate_backward with a workspace",
+                  (long long)(rows * (int64_t)d), (long long)rows, d, (long long)capacity);
+  }
+  BwdArgs a{};
+  for (int s = 0; s < S && T > 0; ++s) {
+    a.src[s] = sources[s];
+    a.grad_src[s] = grad_sources[s];
+  }
+  a.S = S;
+  a.T = T;
+  a.d = d;
+  a.dtype = dtype;
+  a.w = w_l;
+  a.eps = eps;
+  a.grad_r = grad_r;
+  a.accumulate = accumulate != 0;
+  a.grad_w = grad_w;
+  a.workspace = scratch;
+  a.dev_err = dev_err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_aggregate_backward(a);
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate_backward_noalloc launch");
+  return ok();
+}
+
 int attnres_state_init(attnres_state* st, const void* h0, void* const* block_reps, int n_block_reps, void* partial,
                        int64_t T, int d, int dtype, int num_layers, int block_size, float eps) {
   if (!st || !h0 || !partial || !block_reps) return fail(ATTNRES_EINVAL, "NULL argument");

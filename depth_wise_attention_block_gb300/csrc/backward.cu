@@ -26,6 +26,8 @@
 // rows in a fixed order.
 #include <math.h>
 
+#include <mutex>
+
 #include "ring_common.cuh"
 
 namespace attnres {
@@ -497,6 +499,42 @@ cudaError_t launch_aggregate_backward(const BwdArgs& a) {
   e = launch_kernel(dw_reduce_kernel, dim3(rgrid), dim3(256), 0, a.stream, (const float*)a.workspace, grid, a.d,
                     a.grad_w);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// ------------------------------------------- backward without allocation --
+//
+// For callers that cannot allocate device memory (for instance code running
+// inside a graph-replay or real-time serving loop with a fixed memory budget,
+// or a host that forbids cudaMalloc after start-up): the backward's fp32
+// workspace lives in this file-scope array instead of a caller buffer.  It is
+// part of the library's module, so every GPU that loads the library holds it
+// until the process exits.  Every call shares it and it keeps the previous
+// call's contents; the backward writes every element it later reads, so
+// nothing has to be cleared.  Calls whose kernels overlap on a GPU race on it.
+constexpr int64_t kNoAllocScratchFloats = 160 * 8192;  // 5 MiB: 160 CTA rows of d <= 8192
+static __device__ __align__(256) float g_noalloc_bwd_scratch[kNoAllocScratchFloats];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (a host-side name of a __device__ array is not a device
+// address).  The first call on a device performs the lookup.
+cudaError_t noalloc_backward_scratch(float** ptr, int64_t* capacity_floats) {
+  constexpr int kMaxDevices = 64;
+  static float* addr[kMaxDevices] = {};
+  static std::mutex lock;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> guard(lock);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_bwd_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float*>(p);
+  }
+  *ptr = addr[dev];
+  *capacity_floats = kNoAllocScratchFloats;
+  return cudaSuccess;
 }
 
 }  // namespace attnres

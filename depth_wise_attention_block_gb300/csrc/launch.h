@@ -60,6 +60,9 @@ struct BwdArgs {
 cudaError_t launch_aggregate_backward(const BwdArgs& a);
 // CTAs (= fp32 workspace rows of d floats) the backward uses for T tokens
 int64_t backward_blocks(int64_t T);
+// Device address and size (floats) of the library's own backward scratch
+// array on the current device (backward.cu).
+cudaError_t noalloc_backward_scratch(float** ptr, int64_t* capacity_floats);
 
 // dst = prev ? round(prev + F) : F over n = T*d elements of dtype.
 cudaError_t launch_fold(const void* prev, const void* F, void* dst, int64_t n, int dtype,

@@ -131,6 +131,34 @@ int attnres_aggregate_backward(const void* const* sources, int S, int64_t T, int
 int64_t attnres_aggregate_backward_workspace_size(int64_t T, int d);
 
 /* ------------------------------------------------------------------------
+ * attnres_aggregate_backward_noalloc -- attnres_aggregate_backward without
+ * a caller workspace, for callers that cannot allocate device memory (code
+ * that runs under a fixed device-memory budget or must not call cudaMalloc
+ * once it is running, e.g. inside a serving or replay loop).  The pages
+ * have no counterpart: this is a library convenience.
+ *
+ * The workspace is a scratch array built into the library (1,310,720 fp32
+ * values, 5 MiB, held by every GPU that loads the library until the process
+ * exits).  Calls needing more (CTAs x d fp32 values, CTAs = min(T, SMs); on
+ * a 152-SM GB300 any T with d <= 8192 fits) return ATTNRES_ERANGE with a
+ * message naming the sizes; use attnres_aggregate_backward then.  Nothing
+ * is allocated and no allocating library routine is called.
+ *
+ * The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress, with that device current) and caches it: make that
+ * first call before any stream capture.  All calls share the array and it
+ * keeps the previous call's contents (every value a call reads it has
+ * written first, so nothing needs clearing); calls whose kernels overlap on
+ * a GPU (other streams or host threads) race on it and must be serialised.
+ * Arguments, results and errors otherwise as attnres_aggregate_backward.
+ * ---------------------------------------------------------------------- */
+int attnres_aggregate_backward_noalloc(const void* const* sources, int S, int64_t T, int d,
+                                       int dtype, const float* w_l, float eps,
+                                       const void* grad_r, void* const* grad_sources,
+                                       int accumulate, float* grad_w, int* dev_err,
+                                       void* stream);
+
+/* ------------------------------------------------------------------------
  * Stack state: the resident depth sources of one batch of T tokens.
  * ([Tutorial] ch. 4.3-4.6: b_0 = embedding, b_1 .. b_N completed block sums
  * kept resident, one running partial sum of the current block.)

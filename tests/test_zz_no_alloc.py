@@ -1,0 +1,79 @@
+"""attnres_aggregate_backward_noalloc: the backward for callers that cannot
+allocate device memory (a fixed memory budget, or no cudaMalloc once the
+process is serving).  Its scratch workspace is an array built into the
+library instead of a caller buffer.
+
+Checked through the C ABI: two calls in a row (different shapes and dtypes,
+so the second starts on the first one's leftover scratch) give the same
+gradients as attnres_aggregate_backward with a caller workspace, within the
+backward parity bar; a request larger than the built-in scratch is refused.
+This file is collected last so that a run stopping at the first failure
+has run every other test before it.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.parity import oracle_backward, to64, ulp_bf16
+
+pytestmark = pytest.mark.gpu
+EPS = 1e-5
+
+
+def _inputs(T, d, S, dtype, seed):
+    inp = W.block_bf16(T=T, d=d, seed=seed, device="cuda", num_blocks=max(S - 2, 0), src_dtype=dtype)
+    H = inp.H[:S].contiguous()
+    g = torch.Generator(device="cuda").manual_seed(seed + 1)
+    dr = torch.randn((T, d), generator=g, device="cuda").to(dtype)
+    return H, inp.w, dr
+
+
+def _call_noalloc(A, H, w, dr, gH, gw):
+    S, T, d = H.shape
+    sp = (ctypes.c_void_p * S)(*[H[s].data_ptr() for s in range(S)])
+    gp = (ctypes.c_void_p * S)(*[gH[s].data_ptr() for s in range(S)])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = A._N.lib.attnres_aggregate_backward_noalloc(
+        sp, S, T, d, A.dtype_code(H.dtype), w.data_ptr(), EPS, dr.data_ptr(), gp, 0, gw.data_ptr(),
+        err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    return rc, err
+
+
+def test_noalloc_backward_matches_workspace_backward_twice():
+    import depth_wise_attention_block_gb300 as A
+    for T, d, S, dtype, seed in [(2048, 7168, 9, torch.bfloat16, 21), (700, 3584, 4, torch.float32, 22)]:
+        H, w, dr = _inputs(T, d, S, dtype, seed)
+        ref_gH = torch.empty_like(H)
+        ref_gw = torch.empty(d, device="cuda")
+        A.attnres_aggregate_backward(H, w, dr, ref_gH, ref_gw, eps=EPS)
+        gH = torch.full_like(H, float("nan"))
+        gw = torch.full((d,), float("nan"), device="cuda")
+        rc, err = _call_noalloc(A, H, w, dr, gH, gw)
+        torch.cuda.synchronize()
+        assert rc == 0, A._N.lib.attnres_last_error()
+        assert int(err.item()) == 0
+        # the parity bar of the backward tests, around the workspace entry point's result
+        _, _, dHs, dws = oracle_backward(H, w, dr, EPS)
+        assert (np.abs(to64(gw) - to64(ref_gw)) <= 1e-5 * dws + 1e-30).all()
+        ref = to64(ref_gH)
+        bound = 1e-5 * dHs if dtype == torch.float32 else ulp_bf16(ref) + 1e-3 * dHs.max(axis=2, keepdims=True)
+        assert (np.abs(to64(gH) - ref) <= bound).all()
+        print(f"no-alloc backward T={T} d={d} S={S} {dtype}: bitwise equal = "
+              f"{torch.equal(gH, ref_gH) and torch.equal(gw, ref_gw)}")
+
+
+def test_noalloc_backward_refuses_oversize():
+    import depth_wise_attention_block_gb300 as A
+    # one fp32 row of d per CTA, min(T, SMs) CTAs: pick d just past the
+    # built-in 1,310,720 values
+    T, S = 200, 2
+    rows = min(T, torch.cuda.get_device_properties(0).multi_processor_count)
+    d = 8 * (1310720 // (8 * rows) + 1)
+    H, w, dr = _inputs(T, d, S, torch.float32, 5)
+    gH, gw = torch.zeros_like(H), torch.zeros(d, device="cuda")
+    rc, _ = _call_noalloc(A, H, w, dr, gH, gw)
+    assert rc == A._N.ATTNRES_ERANGE
+    assert b"built-in scratch" in A._N.lib.attnres_last_error()

@@ -49,7 +49,7 @@ WORKLOAD = "block_attnres_single_layer_T4096_d7168_S9"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "aggregate_ring_T4096_d7168_S9.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "depth_wise_attention_block_gb300", "csrc", f)
-                  for f in ("aggregate.cu", "device_common.cuh")]
+                  for f in ("aggregate.cu", "ring_common.cuh", "device_common.cuh")]
 
 
 def algorithmic_bytes(T: int, d: int, S: int, esz: int = 2) -> int:

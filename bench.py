@@ -345,22 +345,27 @@ def _time_forward(fwd, reps):
 
 def bench_stacks(A, W, dev, peak):
     """The 93-layer stack forwards, replayed from a CUDA graph (the eager
-    Python launch loop is also timed for the prefill stack)."""
+    Python launch loop is also timed), with the single-pass schedule and the
+    two-phase one (one inter-block pass per block, one merge per layer)."""
     from depth_wise_attention_block_gb300.stack import StackForward
     out = {}
     for name, T, seed, reps in (("stack_prefill_T2048", 2048, 2, 10), ("stack_decode_T64", 64, 3, 50)):
         stk = W.stack(T=T, seed=seed, device=dev)
-        fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size)
-        eager_ms = _time_forward(fwd, reps)
-        fwd.capture()
-        ms = _time_forward(fwd, reps)
-        gbs = fwd.bytes_moved() / (ms * 1e-3) / 1e9
-        out[name] = {"ms_per_forward": ms, "tokens_per_s": T / (ms * 1e-3), "layers": stk.num_layers,
-                     "us_per_layer": 1e3 * ms / (stk.num_layers + 1), "launches_per_forward": fwd.launches_per_forward(),
-                     "cuda_graph": True, "eager_ms_per_forward": eager_ms, "bytes_per_forward": fwd.bytes_moved(),
-                     "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}
-        del fwd, stk
-        torch.cuda.empty_cache()
+        for schedule in ("single", "two_phase"):
+            fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, schedule=schedule)
+            eager_ms = _time_forward(fwd, reps)
+            fwd.capture()
+            ms = _time_forward(fwd, reps)
+            gbs = fwd.bytes_moved() / (ms * 1e-3) / 1e9
+            key = name if schedule == "single" else name + "_two_phase"
+            out[key] = {"ms_per_forward": ms, "tokens_per_s": T / (ms * 1e-3), "layers": stk.num_layers,
+                        "us_per_layer": 1e3 * ms / (stk.num_layers + 1), "schedule": schedule,
+                        "launches_per_forward": fwd.launches_per_forward(), "cuda_graph": True,
+                        "eager_ms_per_forward": eager_ms, "bytes_per_forward_single_pass_model": fwd.bytes_moved(),
+                        "achieved_gbs_single_pass_model": gbs, "frac_of_hbm_peak": gbs / peak}
+            del fwd
+            torch.cuda.empty_cache()
+        del stk
     return out
 
 

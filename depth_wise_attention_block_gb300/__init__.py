@@ -32,7 +32,7 @@ from ._native import (  # noqa: F401
 
 __all__ = [
     "attnres_aggregate", "attnres_aggregate_backward", "attnres_aggregate_backward_workspace_size",
-    "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
+    "attnres_interblock", "attnres_intrablock_step", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
     "attnres_layer_step", "attnres_synthetic_layer", "attnres_version", "AttnResState",
     "aggregate_host", "dtype_code", "AttnresError",
 ]
@@ -146,6 +146,39 @@ def attnres_aggregate_backward(sources: Sequence[torch.Tensor] | torch.Tensor, w
         gp, int(bool(accumulate)), _dev_ptr(grad_w, "grad_w", torch.float32), _dev_ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
     _N.check(rc, "attnres_aggregate_backward")
+
+
+def attnres_interblock(sources: Sequence[torch.Tensor], w_queries: Sequence[torch.Tensor] | torch.Tensor,
+                       out_r: torch.Tensor, out_lse: torch.Tensor, out_weights: torch.Tensor | None = None,
+                       eps: float = ATTNRES_DEFAULT_EPS, dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Phase 1 of the two-phase schedule: the n cached sources aggregated for
+    Q queries at once.  out_r [Q, T, d] fp32, out_lse [Q, T] fp32,
+    out_weights [Q, T, n] fp32 or None."""
+    srcs = list(sources)
+    qs = list(w_queries.unbind(0)) if isinstance(w_queries, torch.Tensor) else list(w_queries)
+    T, d = srcs[0].shape
+    dt = srcs[0].dtype
+    sp = (ctypes.c_void_p * len(srcs))(*[_dev_ptr(t, f"sources[{i}]") for i, t in enumerate(srcs)])
+    qp = (ctypes.c_void_p * len(qs))(*[_dev_ptr(q, f"w_queries[{i}]", torch.float32) for i, q in enumerate(qs)])
+    rc = _N.lib.attnres_interblock(sp, len(srcs), T, d, dtype_code(dt), qp, len(qs), float(eps),
+                                   _dev_ptr(out_r, "out_r", torch.float32), _dev_ptr(out_lse, "out_lse", torch.float32),
+                                   _dev_ptr(out_weights, "out_weights", torch.float32),
+                                   _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
+    _N.check(rc, "attnres_interblock")
+
+
+def attnres_intrablock_step(state: "AttnResState", F_prev: torch.Tensor | None, w_l: torch.Tensor, layer_idx: int,
+                            r_inter: torch.Tensor, lse_inter: torch.Tensor, a_inter: torch.Tensor | None,
+                            out_r: torch.Tensor, out_weights: torch.Tensor | None = None,
+                            dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Phase 2 of the two-phase schedule for one layer (see include/attnres.h)."""
+    rc = _N.lib.attnres_intrablock_step(
+        ctypes.byref(state.struct), _dev_ptr(F_prev, "F_prev", state.h0.dtype), _dev_ptr(w_l, "w_l", torch.float32),
+        layer_idx, _dev_ptr(r_inter, "r_inter", torch.float32), _dev_ptr(lse_inter, "lse_inter", torch.float32),
+        _dev_ptr(a_inter, "a_inter", torch.float32), _dev_ptr(out_r, "out_r", state.h0.dtype),
+        _dev_ptr(out_weights, "out_weights", torch.float32), _dev_ptr(dev_err, "dev_err", torch.int32),
+        _stream_ptr(stream))
+    _N.check(rc, "attnres_intrablock_step")
 
 
 class AttnResState:

@@ -33,6 +33,8 @@ EXPORTED = (
     "attnres_aggregate_backward",
     "attnres_aggregate_backward_workspace_size",
     "attnres_aggregate_backward_noalloc",
+    "attnres_interblock",
+    "attnres_intrablock_step",
     "attnres_state_init",
     "attnres_state_reset",
     "attnres_num_sources",
@@ -77,6 +79,9 @@ def _load() -> ctypes.CDLL:
         "attnres_aggregate_backward_workspace_size": (i64, [i64, i32]),
         "attnres_aggregate_backward_noalloc": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, vp, f32, vp,
                                                       ctypes.POINTER(vp), i32, vp, vp, vp]),
+        "attnres_interblock": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, ctypes.POINTER(vp), i32, f32, vp, vp,
+                                      vp, vp, vp]),
+        "attnres_intrablock_step": (i32, [sp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "attnres_state_init": (i32, [sp, vp, ctypes.POINTER(vp), i32, vp, i64, i32, i32, i32, i32, f32]),
         "attnres_state_reset": (i32, [sp]),
         "attnres_num_sources": (i32, [i32, i32, i32]),

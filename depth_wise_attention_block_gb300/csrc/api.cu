@@ -240,6 +240,98 @@ int attnres_aggregate_backward_noalloc(const void* const* sources, int S, int64_
   return ok();
 }
 
+int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int dtype,
+                       const float* const* w_queries, int Q, float eps, float* out_r, float* out_lse,
+                       float* out_weights, int* dev_err, void* stream) {
+  if (!sources || !w_queries) return fail(ATTNRES_EINVAL, "sources/w_queries is NULL");
+  if (n < 1 || n > 9) return fail(ATTNRES_ERANGE, "n=%d cached sources: 1..9", n);
+  if (Q < 1 || Q > kMaxQueries) return fail(ATTNRES_ERANGE, "Q=%d queries: 1..%d", Q, kMaxQueries);
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  if (!twophase_supported(d, dtype))
+    return fail(ATTNRES_ERANGE, "two-phase schedule needs rows of a 16-byte multiple, at most 2 x 448 vectors");
+  if (T == 0) return ok();
+  if (!out_r || !out_lse) return fail(ATTNRES_EINVAL, "out_r/out_lse is NULL");
+  InterArgs a{};
+  for (int s = 0; s < n; ++s) {
+    if (!sources[s]) return fail(ATTNRES_EINVAL, "sources[%d] is NULL", s);
+    if (!twophase_pointers_ok(sources[s])) return fail(ATTNRES_EINVAL, "sources[%d] not 16-byte aligned", s);
+    a.src[s] = sources[s];
+  }
+  for (int q = 0; q < Q; ++q) {
+    if (!w_queries[q]) return fail(ATTNRES_EINVAL, "w_queries[%d] is NULL", q);
+    a.wq[q] = w_queries[q];
+  }
+  if (!twophase_pointers_ok(out_r)) return fail(ATTNRES_EINVAL, "out_r not 16-byte aligned");
+  a.n = n;
+  a.T = T;
+  a.d = d;
+  a.dtype = dtype;
+  a.Q = Q;
+  a.eps = eps;
+  a.out_r = out_r;
+  a.out_lse = out_lse;
+  a.out_a = out_weights;
+  a.dev_err = dev_err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_interblock(a);
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_interblock launch");
+  return ok();
+}
+
+int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* w_l, int layer_idx,
+                            const float* r_inter, const float* lse_inter, const float* a_inter, void* out_r,
+                            float* out_weights, int* dev_err, void* stream) {
+  (void)dev_err;  // the merge kernel has no waits
+  int rc = check_state(st);
+  if (rc) return rc;
+  const int L = st->num_layers, B = st->block_size;
+  if (layer_idx < 1 || layer_idx > L) return fail(ATTNRES_EINVAL, "layer_idx %d outside 1..L", layer_idx);
+  if (!w_l || !r_inter || !lse_inter || !out_r) return fail(ATTNRES_EINVAL, "w_l/r_inter/lse_inter/out_r is NULL");
+  if (!twophase_supported(st->d, st->dtype))
+    return fail(ATTNRES_ERANGE, "two-phase schedule needs rows of a 16-byte multiple, at most 2 x 448 vectors");
+  const int n = (layer_idx - 1) / B + 1;
+  const int i = (layer_idx - 1) % B + 1;
+  MergeArgs a{};
+  if (i == 1) {
+    if (F_prev) return fail(ATTNRES_EINVAL, "first layer of a block: fold the previous block first, F_prev NULL");
+    if (st->folded != layer_idx - 1)
+      return fail(ATTNRES_ESTATE, "intrablock_step(%d) needs folded == %d, state has %d", layer_idx, layer_idx - 1,
+                  st->folded);
+  } else {
+    if (!F_prev) return fail(ATTNRES_EINVAL, "F_prev is NULL");
+    if (st->folded != layer_idx - 2)
+      return fail(ATTNRES_ESTATE, "intrablock_step(%d) needs folded == %d, state has %d", layer_idx, layer_idx - 2,
+                  st->folded);
+    a.prev = i >= 3 ? st->partial : nullptr;
+    a.F = F_prev;
+    a.dst = st->partial;
+  }
+  for (const void* q : {a.prev, a.F, (const void*)a.dst, (const void*)r_inter, (const void*)out_r})
+    if (!twophase_pointers_ok(q)) return fail(ATTNRES_EINVAL, "two-phase buffers must be 16-byte aligned");
+  if (out_r == st->partial || out_r == st->h0) return fail(ATTNRES_EINVAL, "out_r aliases the state");
+  a.w = w_l;
+  a.r_inter = r_inter;
+  a.lse_inter = lse_inter;
+  a.a_inter = a_inter;
+  a.out_r = out_r;
+  a.out_a = out_weights;
+  a.T = st->T;
+  a.d = st->d;
+  a.dtype = st->dtype;
+  a.n = n;
+  a.eps = st->eps;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (st->T > 0) {
+    cudaError_t e = launch_merge(a);
+    if (e != cudaSuccess) return cuda_fail(e, "attnres_intrablock_step launch");
+  }
+  if (i >= 2) st->folded = layer_idx - 1;
+  return ok();
+}
+
 int attnres_state_init(attnres_state* st, const void* h0, void* const* block_reps, int n_block_reps, void* partial,
                        int64_t T, int d, int dtype, int num_layers, int block_size, float eps) {
   if (!st || !h0 || !partial || !block_reps) return fail(ATTNRES_EINVAL, "NULL argument");

@@ -40,6 +40,45 @@ enum AggPath { kPathNone = 0, kPathRing = 1, kPathGeneric = 2, kPathRingMulti = 
 // Launch; returns cudaSuccess or the launch error.  *path gets the kernel.
 cudaError_t launch_aggregate(const AggArgs& a, AggPath* path);
 
+// Two-phase schedule (twophase.cu).
+constexpr int kMaxQueries = 16;
+struct InterArgs {
+  const void* src[kMaxSources];
+  int n;  // cached sources, <= 9
+  int64_t T;
+  int d;
+  int dtype;
+  const float* wq[kMaxQueries];
+  int Q;
+  float eps;
+  float* out_r;    // [Q, T, d]
+  float* out_lse;  // [Q, T]
+  float* out_a;    // [Q, T, n] or null
+  int* dev_err;
+  cudaStream_t stream;
+};
+struct MergeArgs {
+  const void* prev;
+  const void* F;
+  void* dst;
+  const float* w;
+  const float* r_inter;
+  const float* lse_inter;
+  const float* a_inter;
+  void* out_r;
+  float* out_a;
+  int64_t T;
+  int d;
+  int dtype;
+  int n;
+  float eps;
+  cudaStream_t stream;
+};
+bool twophase_supported(int d, int dtype);
+bool twophase_pointers_ok(const void* p);
+cudaError_t launch_interblock(const InterArgs& a);
+cudaError_t launch_merge(const MergeArgs& a);
+
 // Backward of one aggregation (see backward.cu).
 struct BwdArgs {
   const void* src[kMaxSources];

@@ -1,0 +1,437 @@
+// Two-phase schedule of Block AttnRes inference (Kimi K3 chaptered tutorial,
+// ch. 4.4 and 4.6): the cached block sums [h_0, b_1 .. b_{n-1}] are fixed for
+// the whole of block n, so one batched inter-block pass reads each of them
+// once and aggregates them for every layer query of the block; each layer
+// then folds in its own partial sum with an online-softmax merge.
+//
+//  agg_interblock_kernel (phase 1): the TMA ring of the aggregation kernels
+//      (ring_common.cuh); a token's n <= 9 cached rows are taken into
+//      registers once, then for each of the Q queries w_q: logits, softmax,
+//      the normalised weighted sum (fp32 row), its log-sum-exp and weights.
+//      One cross-warp reduction step per query.
+//
+//  agg_merge_kernel (phase 2, one layer): p = round(prev + F) (or F) is
+//      stored as the new partial sum / block sum, its logit z_p = w.p/rms(p)
+//      is reduced over the CTA, and with m = max(lse, z_p)
+//          r = (e^{lse - m} r_inter + e^{z_p - m} p) / (e^{lse - m} + e^{z_p - m})
+//      weights: the inter-block ones scaled by e^{lse - m}/den, e^{z_p - m}/den
+//      for the partial.  Without a partial (first layer of a block) r is
+//      r_inter itself.
+#include <math.h>
+
+#include "ring_common.cuh"
+
+namespace attnres {
+
+struct InterParams {
+  RingParams rp;  // the cached sources (n_stored = S = n), geometry, ring
+  const float* wq[kMaxQueries];
+  int Q;
+  float* out_r;    // [Q, T, d] fp32
+  float* out_lse;  // [Q, T]
+  float* out_a;    // [Q, T, n] or null
+};
+
+template <typename Tin, int VPT, bool EXACT>
+__global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const __grid_constant__ InterParams ip) {
+  const RingParams& p = ip.rp;
+  constexpr int EPV = Vec<Tin>::kElems;
+  constexpr int NP = EPV / 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  RingShared& sh = *reinterpret_cast<RingShared*>(smem);
+  const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int nslots = p.nslots;
+  pdl_trigger();
+  ring_init(p, sh);
+  __syncthreads();
+  pdl_wait();
+
+  if (warp == kRingConsumerWarps) {
+    if (lane == 0) ring_produce(p, sh, ring);
+    return;
+  }
+
+  const int S = p.S;
+  const long long T = p.T;
+  uint32_t slot = 0, lap = 0;
+  bool ok = true;
+  int iter = 0;
+  bool abort = false;
+  for (long long t = blockIdx.x; t < T && !abort; t += gridDim.x) {
+    uint4 x[kRingSmax][VPT];
+#pragma unroll
+    for (int s = 0; s < kRingSmax; ++s) {
+      if (s < S) {
+        if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u)) ok = false;
+        const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          const int v = tid + k * kRingConsumers;
+          x[s][k] = (EXACT || v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sh.empty[slot]));
+        if (++slot == (uint32_t)nslots) {
+          slot = 0;
+          ++lap;
+        }
+      }
+    }
+    float inv_rho = 0.f;  // lane 2s: 1 / rms(h_s), from the first query's reduction
+    for (int q = 0; q < ip.Q && !abort; ++q, ++iter) {
+      const int buf = iter & 1;
+      volatile int* abort_flag = &sh.abort_flag[buf];
+      uint64_t wp[VPT][NP];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * kRingConsumers;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+          const bool in = EXACT || v < p.nvec;
+          wp[k][j] = f2_pack(in ? __ldg(ip.wq[q] + v * EPV + 2 * j) : 0.f,
+                             in ? __ldg(ip.wq[q] + v * EPV + 2 * j + 1) : 0.f);
+        }
+      }
+      float part[2 * kRingSmax];
+#pragma unroll
+      for (int s = 0; s < kRingSmax; ++s) {
+        uint64_t dot2 = 0, ss2 = 0;
+        if (s < S) {
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            uint64_t h[NP];
+            Vec<Tin>::pairs(x[s][k], h);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+              dot2 = f2_fma(wp[k][j], h[j], dot2);
+              if (q == 0) ss2 = f2_fma(h[j], h[j], ss2);
+            }
+          }
+        }
+        part[2 * s] = f2_hsum(dot2);
+        part[2 * s + 1] = f2_hsum(ss2);
+      }
+      reduce_scatter18(part, lane);
+      if ((kRsValidLanes >> lane) & 1u) {
+        const int idx = rs_index(lane);
+        if (idx < 2 * S) sh.red[buf][warp][idx] = part[0];
+      }
+      const bool warp_failed = __any_sync(0xffffffffu, !ok);
+      if (lane == 0 && warp_failed) *abort_flag = 1;
+      named_barrier_sync(kRingBarrierId, kRingConsumers);
+
+      abort = *abort_flag != 0;
+      float tot = 0.f;
+      if (lane < 2 * S) {
+#pragma unroll
+        for (int w = 0; w < kRingConsumerWarps; ++w) tot += sh.red[buf][w][lane];
+      }
+      const float sumsq = __shfl_down_sync(0xffffffffu, tot, 1);
+      const bool is_src = lane < 2 * S && (lane & 1) == 0;
+      // fast reciprocal square root, exponential, logarithm and division:
+      // a few fp32 ulps, far inside the parity tolerances
+      if (q == 0) inv_rho = rsqrtf(fmaf(sumsq, p.inv_d, p.eps));
+      const float z = is_src ? tot * inv_rho : -INFINITY;
+      const float m = warp_max(z);
+      const float e = is_src ? __expf(z - m) : 0.f;
+      const float esum = warp_sum(e);
+      const float nan = __int_as_float(0x7fc00000);
+      const float a = abort ? nan : __fdividef(e, esum);
+      if (warp == 0) {
+        if (is_src && ip.out_a) ip.out_a[((long long)q * T + t) * S + (lane >> 1)] = a;
+        if (lane == 0) ip.out_lse[(long long)q * T + t] = abort ? nan : m + __logf(esum);
+      }
+      uint64_t a2[kRingSmax];
+#pragma unroll
+      for (int s = 0; s < kRingSmax; ++s) {
+        const float as = __shfl_sync(0xffffffffu, a, 2 * s);
+        a2[s] = f2_pack(as, as);
+      }
+      char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)q * T + t) * (long long)p.d * 4;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * kRingConsumers;
+        if (EXACT || v < p.nvec) {
+          uint64_t acc[NP];
+#pragma unroll
+          for (int j = 0; j < NP; ++j) acc[j] = 0;
+#pragma unroll
+          for (int s = 0; s < kRingSmax; ++s) {
+            if (s < S) {
+              uint64_t h[NP];
+              Vec<Tin>::pairs(x[s][k], h);
+#pragma unroll
+              for (int j = 0; j < NP; ++j) acc[j] = f2_fma(a2[s], h[j], acc[j]);
+            }
+          }
+          float r[EPV];
+#pragma unroll
+          for (int j = 0; j < NP; ++j) f2_unpack(acc[j], r[2 * j], r[2 * j + 1]);
+          store_out<float, EPV>(orow, v, r);
+        }
+      }
+    }
+    if (abort && tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+  }
+}
+
+// ------------------------------------------------------------- phase 2 ---
+
+constexpr int kMergeThreads = kRingConsumers;  // 448: two 16-byte vectors each at d = 7168 bf16
+
+struct MergeParams {
+  const char* prev;  // partial sum before this layer, or null
+  const char* F;     // output of the previous layer, or null (first layer of a block)
+  char* dst;         // new partial sum / block sum (when F)
+  const float* w;
+  const float* r_inter;  // [T, d]
+  const float* lse_inter;  // [T]
+  const float* a_inter;  // [T, n] or null
+  char* out_r;
+  float* out_a;  // [T, n + (F ? 1 : 0)] or null
+  long long T;
+  int d;
+  int n;  // cached sources
+  int nvec;
+  float eps;
+  float inv_d;
+};
+
+template <typename Tin, int VPT>
+__global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_constant__ MergeParams p) {
+  constexpr int EPV = Vec<Tin>::kElems;
+  constexpr int NP = EPV / 2;
+  __shared__ float s_red[kMergeThreads / 32][2];
+  __shared__ float s_c[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();
+  const bool has_p = p.F != nullptr;
+  uint64_t wp[VPT][NP];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * kMergeThreads;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      const bool in = has_p && v < p.nvec;
+      wp[k][j] = f2_pack(in ? __ldg(p.w + v * EPV + 2 * j) : 0.f, in ? __ldg(p.w + v * EPV + 2 * j + 1) : 0.f);
+    }
+  }
+  const long long row_bytes = (long long)p.d * (long long)sizeof(Tin);
+  for (long long t = blockIdx.x; t < p.T; t += gridDim.x) {
+    uint4 x[VPT];
+    float c1 = 1.f, c2 = 0.f;
+    if (has_p) {
+      uint64_t dot2 = 0, ss2 = 0;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * kMergeThreads;
+        x[k] = make_uint4(0, 0, 0, 0);
+        if (v < p.nvec) {
+          float f[EPV];
+          Vec<Tin>::unpack(*reinterpret_cast<const uint4*>(p.F + t * row_bytes + (size_t)v * 16), f);
+          if (p.prev) {
+            float q[EPV];
+            Vec<Tin>::unpack(*reinterpret_cast<const uint4*>(p.prev + t * row_bytes + (size_t)v * 16), q);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) f[e] = q[e] + f[e];
+          }
+          x[k] = Vec<Tin>::pack(f);  // one rounding to the storage type
+          *reinterpret_cast<uint4*>(p.dst + t * row_bytes + (size_t)v * 16) = x[k];
+          uint64_t h[NP];
+          Vec<Tin>::pairs(x[k], h);
+#pragma unroll
+          for (int j = 0; j < NP; ++j) {
+            dot2 = f2_fma(wp[k][j], h[j], dot2);
+            ss2 = f2_fma(h[j], h[j], ss2);
+          }
+        }
+      }
+      float dot = warp_sum(f2_hsum(dot2));
+      float ss = warp_sum(f2_hsum(ss2));
+      if (lane == 0) {
+        s_red[warp][0] = dot;
+        s_red[warp][1] = ss;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float dd = 0.f, qq = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeThreads / 32; ++w) {
+          dd += s_red[w][0];
+          qq += s_red[w][1];
+        }
+        const float zp = dd * rsqrtf(fmaf(qq, p.inv_d, p.eps));
+        const float lse = p.lse_inter[t];
+        const float m = fmaxf(lse, zp);
+        const float e1 = __expf(lse - m), e2 = __expf(zp - m);
+        const float inv = __fdividef(1.0f, e1 + e2);
+        s_c[0] = e1 * inv;
+        s_c[1] = e2 * inv;
+      }
+      __syncthreads();
+      c1 = s_c[0];
+      c2 = s_c[1];
+    }
+    const uint64_t c1p = f2_pack(c1, c1), c2p = f2_pack(c2, c2);
+    char* orow = p.out_r + t * row_bytes;
+    const float* rrow = p.r_inter + t * (long long)p.d;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * kMergeThreads;
+      if (v < p.nvec) {
+        uint64_t ri[NP];
+#pragma unroll
+        for (int j = 0; j < NP; j += 2) {
+          const float4 f4 = *reinterpret_cast<const float4*>(rrow + v * EPV + 2 * j);
+          ri[j] = f2_pack(f4.x, f4.y);
+          ri[j + 1] = f2_pack(f4.z, f4.w);
+        }
+        uint64_t h[NP];
+        if (has_p) Vec<Tin>::pairs(x[k], h);
+        float out[EPV];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+          uint64_t r = f2_fma(c1p, ri[j], 0);
+          if (has_p) r = f2_fma(c2p, h[j], r);
+          f2_unpack(r, out[2 * j], out[2 * j + 1]);
+        }
+        store_out<Tin, EPV>(orow, v, out);
+      }
+    }
+    if (p.out_a && warp == 0) {
+      const int na = p.n + (has_p ? 1 : 0);
+      for (int s = lane; s < p.n; s += 32)
+        p.out_a[t * na + s] = (p.a_inter ? p.a_inter[t * p.n + s] : 0.f) * c1;
+      if (has_p && lane == 0) p.out_a[t * na + p.n] = c2;
+    }
+    __syncthreads();  // s_red / s_c are reused by the next token
+  }
+}
+
+// ---------------------------------------------------------------- launch --
+
+template <typename Tin, int VPT, bool EXACT>
+static cudaError_t launch_inter_t(const InterParams& ip, int grid, int smem, cudaStream_t stream) {
+  constexpr int kMaxDevices = 64;
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto kern = agg_interblock_kernel<Tin, VPT, EXACT>;
+  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+    DeviceInfo di;
+    e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+  }
+  e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, ip);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Geometry both phases need: 16-byte rows of at most 2 x 448 vectors.
+static bool twophase_geometry(int d, int dtype, int* nvec, int* vpt) {
+  const int esz = dtype == ATTNRES_BF16 ? 2 : 4;
+  const long long row_bytes = (long long)d * esz;
+  if (row_bytes % 16 != 0) return false;
+  *nvec = (int)(row_bytes / 16);
+  *vpt = (*nvec + kRingConsumers - 1) / kRingConsumers;
+  return *vpt >= 1 && *vpt <= kRingMaxVpt;
+}
+
+bool twophase_supported(int d, int dtype) {
+  int nvec, vpt;
+  return twophase_geometry(d, dtype, &nvec, &vpt);
+}
+
+cudaError_t launch_interblock(const InterArgs& a) {
+  if (a.T <= 0) return cudaSuccess;
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  int nvec = 0, vpt = 0;
+  if (!twophase_geometry(a.d, a.dtype, &nvec, &vpt)) return cudaErrorInvalidValue;
+  const bool bf16 = a.dtype == ATTNRES_BF16;
+  const int row_bytes = nvec * 16;
+  InterParams ip{};
+  RingParams& rp = ip.rp;
+  for (int s = 0; s < a.n; ++s) rp.src[s] = static_cast<const char*>(a.src[s]);
+  rp.w = a.wq[0];
+  rp.dev_err = a.dev_err;
+  rp.T = a.T;
+  rp.d = a.d;
+  rp.n_stored = a.n;
+  rp.S = a.n;
+  rp.nvec = nvec;
+  rp.row_bytes = row_bytes;
+  rp.out_row_bytes = a.d * 4;
+  rp.eps = a.eps;
+  rp.inv_d = 1.0f / (float)a.d;
+  int nslots = (di.max_smem_optin - kRingHeaderBytes) / row_bytes;
+  if (nslots > kRingMaxSlots) nslots = kRingMaxSlots;
+  if (nslots < 1) return cudaErrorInvalidValue;
+  rp.nslots = nslots;
+  for (int q = 0; q < a.Q; ++q) ip.wq[q] = a.wq[q];
+  ip.Q = a.Q;
+  ip.out_r = a.out_r;
+  ip.out_lse = a.out_lse;
+  ip.out_a = a.out_a;
+  const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
+  const int smem = kRingHeaderBytes + nslots * row_bytes;
+  const bool exact = nvec == vpt * kRingConsumers;
+  if (bf16) {
+    if (vpt == 1) return launch_inter_t<bf16_t, 1, false>(ip, grid, smem, a.stream);
+    return exact ? launch_inter_t<bf16_t, 2, true>(ip, grid, smem, a.stream)
+                 : launch_inter_t<bf16_t, 2, false>(ip, grid, smem, a.stream);
+  }
+  if (vpt == 1) return launch_inter_t<float, 1, false>(ip, grid, smem, a.stream);
+  return exact ? launch_inter_t<float, 2, true>(ip, grid, smem, a.stream)
+               : launch_inter_t<float, 2, false>(ip, grid, smem, a.stream);
+}
+
+cudaError_t launch_merge(const MergeArgs& a) {
+  if (a.T <= 0) return cudaSuccess;
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  int nvec = 0, vpt = 0;
+  if (!twophase_geometry(a.d, a.dtype, &nvec, &vpt)) return cudaErrorInvalidValue;
+  MergeParams mp{};
+  mp.prev = static_cast<const char*>(a.prev);
+  mp.F = static_cast<const char*>(a.F);
+  mp.dst = static_cast<char*>(a.dst);
+  mp.w = a.w;
+  mp.r_inter = a.r_inter;
+  mp.lse_inter = a.lse_inter;
+  mp.a_inter = a.a_inter;
+  mp.out_r = static_cast<char*>(a.out_r);
+  mp.out_a = a.out_a;
+  mp.T = a.T;
+  mp.d = a.d;
+  mp.n = a.n;
+  mp.nvec = nvec;
+  mp.eps = a.eps;
+  mp.inv_d = 1.0f / (float)a.d;
+  const long long cap = (long long)di.sm_count * 4;
+  const int grid = (int)(a.T < cap ? a.T : cap);
+  const bool bf16 = a.dtype == ATTNRES_BF16;
+  if (bf16) {
+    e = vpt == 1 ? launch_kernel(agg_merge_kernel<bf16_t, 1>, dim3(grid), dim3(kMergeThreads), 0, a.stream, mp)
+                 : launch_kernel(agg_merge_kernel<bf16_t, 2>, dim3(grid), dim3(kMergeThreads), 0, a.stream, mp);
+  } else {
+    e = vpt == 1 ? launch_kernel(agg_merge_kernel<float, 1>, dim3(grid), dim3(kMergeThreads), 0, a.stream, mp)
+                 : launch_kernel(agg_merge_kernel<float, 2>, dim3(grid), dim3(kMergeThreads), 0, a.stream, mp);
+  }
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+bool twophase_pointers_ok(const void* p) { return p == nullptr || al16(p); }
+
+}  // namespace attnres

@@ -8,6 +8,13 @@ aggregates [h_0, b_1 .. b_N] (Kimi K3 chaptered tutorial, ch. 4.3: the final
 output layer aggregates all block representations).  2L+1 launches per
 forward; `capture()` records them into one CUDA graph so a decode-sized
 forward is not bound by launch latency.
+
+schedule="two_phase" runs the same forward as the tutorial's two-phase
+inference schedule (ch. 4.4, 4.6): at the start of block n the previous
+block is closed (attnres_block_step), one inter-block pass aggregates the
+cached [h_0, b_1 .. b_{n-1}] for all of the block's layer queries
+(attnres_interblock), and each layer merges its partial sum in
+(attnres_intrablock_step).
 """
 from __future__ import annotations
 
@@ -15,6 +22,10 @@ import torch
 
 from . import (
     AttnResState,
+    attnres_block_step,
+    attnres_interblock,
+    attnres_intrablock_step,
+    attnres_layer_sources,
     attnres_layer_step,
     attnres_num_sources,
     attnres_synthetic_layer,
@@ -31,7 +42,7 @@ class StackForward:
     """
 
     def __init__(self, h0, W, G, Sc, num_layers: int, block_size: int, eps: float = 1e-5,
-                 keep_weights: bool = True, dev_err: torch.Tensor | None = None):
+                 keep_weights: bool = True, dev_err: torch.Tensor | None = None, schedule: str = "single"):
         self.L, self.B = num_layers, block_size
         T, d = h0.shape
         self.T, self.d = T, d
@@ -49,11 +60,50 @@ class StackForward:
                 off += T * s
         self.dev_err = dev_err
         self.graph = None
+        if schedule not in ("single", "two_phase"):
+            raise ValueError("schedule must be 'single' or 'two_phase'")
+        self.schedule = schedule
+        if schedule == "two_phase":
+            q = min(block_size, num_layers)
+            n_max = -(-num_layers // block_size)          # cached sources of the last block
+            self.R_inter = torch.empty((q, T, d), dtype=torch.float32, device=h0.device)
+            self.lse_inter = torch.empty((q, T), dtype=torch.float32, device=h0.device)
+            self.A_flat = torch.empty(q * T * n_max, dtype=torch.float32, device=h0.device)
 
     def launches_per_forward(self) -> int:
+        if self.schedule == "two_phase":
+            N = -(-self.L // self.B)
+            return N + (N - 1) + 2 * self.L + 1
         return 2 * self.L + 1
 
+    def _issue_two_phase(self, stream=None) -> None:
+        st, L, B = self.state, self.L, self.B
+        st.reset()
+        bufs = {t.data_ptr(): t for t in [st.h0] + st.block_reps}
+        T = self.T
+        for n in range(1, -(-L // B) + 1):
+            first, last = (n - 1) * B + 1, min(n * B, L)
+            if n >= 2:
+                attnres_block_step(st, self.F, first - 1, dev_err=self.dev_err, stream=stream)
+            cached = [bufs[p] for p in attnres_layer_sources(st, first)]
+            Q = last - first + 1
+            A = self.A_flat[: Q * T * n].view(Q, T, n)
+            attnres_interblock(cached, self.W[first - 1:last], self.R_inter[:Q], self.lse_inter[:Q], A,
+                               dev_err=self.dev_err, stream=stream)
+            for layer in range(first, last + 1):
+                q = layer - first
+                attnres_intrablock_step(st, self.F if layer > first else None, self.W[layer - 1], layer,
+                                        self.R_inter[q], self.lse_inter[q], A[q], self.r,
+                                        self.weights[layer - 1] if self.weights is not None else None,
+                                        dev_err=self.dev_err, stream=stream)
+                attnres_synthetic_layer(self.r, self.G[layer - 1], self.Sc[layer - 1], self.F, stream=stream)
+        attnres_layer_step(st, self.F, self.W[L], L + 1, self.r,
+                           self.weights[L] if self.weights is not None else None, dev_err=self.dev_err, stream=stream)
+
     def _issue(self, stream=None) -> None:
+        if self.schedule == "two_phase":
+            self._issue_two_phase(stream)
+            return
         self.state.reset()
         for l in range(1, self.L + 2):
             attnres_layer_step(self.state, self.F if l > 1 else None, self.W[l - 1], l, self.r,

@@ -239,6 +239,49 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
                        void* out_r, float* out_weights, int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Two-phase schedule of inference ([Tutorial] ch. 4.4 and 4.6): the cached
+ * sources [h_0, b_1 .. b_{n-1}] do not change inside block n, so one
+ * batched inter-block pass reads each of them once and aggregates them for
+ * every layer query of the block; each layer then folds in its own partial
+ * sum with an online-softmax merge.  Same results as attnres_layer_step up
+ * to fp32 rounding.  Both calls need rows of a 16-byte multiple with at
+ * most 2 x 448 16-byte vectors (d <= 7168 bf16 / 3584 fp32) and 16-byte
+ * aligned buffers (ATTNRES_ERANGE / ATTNRES_EINVAL otherwise).
+ *
+ * attnres_interblock -- phase 1 for one block.
+ *   sources    host array of n (1..9) device pointers [T, d] of dtype
+ *   w_queries  host array of Q (1..16) device pointers [d] fp32 (the
+ *              block's layer queries in order)
+ *   out_r      device [Q, T, d] fp32: per query, the softmax-weighted sum
+ *              over the n sources (normalised)
+ *   out_lse    device [Q, T] fp32: log sum_s exp(z_qs) of those logits
+ *   out_weights device [Q, T, n] fp32 (softmax over the n sources) or NULL
+ *   Every source row is read once for all Q queries.
+ * ---------------------------------------------------------------------- */
+int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int dtype,
+                       const float* const* w_queries, int Q, float eps, float* out_r,
+                       float* out_lse, float* out_weights, int* dev_err, void* stream);
+
+/* attnres_intrablock_step -- phase 2 for layer l (1..L) of block n:
+ *   first layer of its block (i = 1): F_prev NULL and the previous block
+ *     already closed (attnres_block_step); r = r_inter.
+ *   later layers (i >= 2): F_prev = v_{l-1} is folded into the partial sum
+ *     exactly as attnres_layer_step folds it, p = the new partial sum,
+ *     z_p = w_l . RMSNorm(p), m = max(lse, z_p) and
+ *       r = (e^{lse-m} r_inter + e^{z_p-m} p) / (e^{lse-m} + e^{z_p-m}).
+ *   r_inter, lse_inter, a_inter: this layer's rows of attnres_interblock's
+ *     outputs ([T, d], [T], [T, n] or NULL).
+ *   out_r: device [T, d] of st->dtype; out_weights: [T, S_l] fp32 or NULL
+ *     (the cached sources' weights scaled into the merged softmax, then the
+ *     partial sum's).
+ * Needs folded == l-1 (i = 1) or l-2 (i >= 2); advances folded like
+ * attnres_layer_step.  The final aggregation (L+1) uses attnres_layer_step. */
+int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* w_l,
+                            int layer_idx, const float* r_inter, const float* lse_inter,
+                            const float* a_inter, void* out_r, float* out_weights,
+                            int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * attnres_synthetic_layer -- the stand-in layer body used to drive a stack
  * forward without trained weights (not part of the method):
  *   out[t,c] = tanh(x[t,c] * g[c]) * s[c], fp32 math, rounded to `dtype`.

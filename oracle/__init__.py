@@ -19,6 +19,8 @@ from .attnres_oracle import (  # noqa: F401
     rms,
     rmsnorm,
     depth_attention,
+    depth_attention_lse,
+    merge_partial_softmax,
     depth_attention_backward,
     depth_attention_backward_scales,
     block_index,

@@ -85,6 +85,29 @@ def depth_attention(H: Sequence[np.ndarray] | np.ndarray, w: np.ndarray,
     return r, a
 
 
+def depth_attention_lse(H: np.ndarray, w: np.ndarray, eps: float = EPS):
+    """depth_attention plus the log-sum-exp of the logits (lse [T]): the
+    summary of a set of sources that a later online-softmax merge needs."""
+    H = np.asarray(H, dtype=np.float64)
+    r, a = depth_attention(H, w, eps)
+    z = np.einsum("std,d->ts", rmsnorm(H, eps), np.asarray(w, np.float64))
+    m = z.max(axis=1)
+    return r, a, m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+
+
+def merge_partial_softmax(r1, lse1, r2, lse2):
+    """Online-softmax merge of two disjoint source sets ([Tutorial] ch. 4.4):
+    given each set's normalised weighted sum r_i and log-sum-exp lse_i, the
+    aggregation over the union is  (e^{lse1} r1 + e^{lse2} r2) /
+    (e^{lse1} + e^{lse2}),  evaluated with the larger lse subtracted."""
+    lse1, lse2 = np.asarray(lse1, np.float64), np.asarray(lse2, np.float64)
+    m = np.maximum(lse1, lse2)
+    c1, c2 = np.exp(lse1 - m), np.exp(lse2 - m)
+    den = c1 + c2
+    r = (c1[:, None] * np.asarray(r1, np.float64) + c2[:, None] * np.asarray(r2, np.float64)) / den[:, None]
+    return r, c1 / den, c2 / den
+
+
 def depth_attention_backward(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
                              eps: float = EPS) -> tuple[np.ndarray, np.ndarray]:
     """Gradients of one depth-wise attention layer, recomputing its forward.

@@ -31,10 +31,11 @@ def _oracle_stack(stk: W.Stack, tokens=None, store=O.round_bf16):
     return O.block_stack_forward(h0, Wq, fn, stk.num_layers, stk.block_size, store=store)
 
 
-def _gpu_stack(A, stk: W.Stack, graph=False):
+def _gpu_stack(A, stk: W.Stack, graph=False, schedule="single"):
     from depth_wise_attention_block_gb300.stack import StackForward
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, dev_err=err)
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, dev_err=err,
+                       schedule=schedule)
     if graph:
         fwd.capture()
     fwd.run()
@@ -186,3 +187,50 @@ def test_bytes_model_counts_k3_sources(A):
     fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, 93, 12)
     assert sum(fwd.S[:93]) == 493 and fwd.S[-1] == 9
     assert fwd.bytes_moved() > 0
+
+
+# ------------------------------------------------- two-phase schedule -------
+
+@pytest.mark.parametrize("n,Q,dtype,d", [(1, 12, torch.bfloat16, 7168), (5, 3, torch.bfloat16, 7168),
+                                         (9, 12, torch.float32, 3584), (8, 9, torch.bfloat16, 7160)])
+def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d):
+    from tests.parity import oracle_aggregate
+    T = 150
+    inp = W.block_bf16(T=T, d=d, seed=60 + n + Q, device="cuda", num_blocks=max(n - 2, 0), src_dtype=dtype)
+    H = inp.H[:n].contiguous()
+    g = torch.Generator(device="cuda").manual_seed(n)
+    Wq = torch.randn((Q, d), generator=g, device="cuda") / d ** 0.5
+    R = torch.empty((Q, T, d), device="cuda")
+    lse = torch.empty((Q, T), device="cuda")
+    Aw = torch.empty((Q, T, n), device="cuda")
+    A.attnres_interblock(list(H.unbind(0)), Wq, R, lse, Aw)
+    torch.cuda.synchronize()
+    for q in range(Q):
+        r_ref, a_ref, l_ref = O.depth_attention_lse(to64(H), to64(Wq[q]))
+        _, _, cond, M = oracle_aggregate(H, Wq[q], 1e-5)
+        assert np.abs(to64(Aw[q]) - a_ref).max() <= A_ATOL
+        assert (np.abs(to64(R[q]) - r_ref) <= R_F32_RTOL * (np.abs(r_ref) + cond)).all()
+        assert (np.abs(to64(lse[q]) - l_ref) <= 1e-5 * (1 + np.abs(l_ref))).all()
+
+
+@pytest.mark.parametrize("L,B,T,d,dtype", [
+    (7, 3, 6, 64, torch.bfloat16),
+    (9, 4, 7, 7168, torch.bfloat16),
+    (93, 12, 16, 3584, torch.float32),     # the K3 layout at the fp32 bars
+])
+def test_two_phase_stack_matches_the_oracle(A, L, B, T, d, dtype):
+    stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=71 + L, device="cuda", dtype=dtype)
+    fwd = _gpu_stack(A, stk, schedule="two_phase")
+    store = O.round_bf16 if dtype == torch.bfloat16 else O.round_fp32
+    tr = _oracle_stack(stk, store=store)
+    tol = A_ATOL if dtype == torch.float32 else STACK_BF16_A_ATOL
+    wa, wr = _check_stack(fwd, tr, slice(None), dtype, tol, check_blocks=(L < 20 or dtype == torch.float32))
+    print(f"two-phase stack L={L} B={B} d={d} {dtype}: worst weight error {wa:.3g}, output {wr:.3g} x bound")
+
+
+def test_two_phase_decode_T64_graph(A):
+    stk = W.stack_T64(device="cuda")
+    fwd = _gpu_stack(A, stk, graph=True, schedule="two_phase")
+    tr = _oracle_stack(stk)
+    wa, wr = _check_stack(fwd, tr, slice(None), torch.bfloat16, STACK_BF16_A_ATOL, check_blocks=False)
+    print(f"two-phase decode stack T=64: worst weight error {wa:.3g}, output {wr:.3g} x bound")

@@ -417,3 +417,26 @@ def test_backward_closed_forms():
     lhs = np.einsum("std,std->st", dH, H)
     rhs = a.T * np.einsum("std,td->st", H, dr)
     np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------- two-phase merge pin ----
+
+@pytest.mark.parametrize("split", [1, 3, 8])
+def test_merge_of_partial_softmaxes_equals_the_union(split):
+    # aggregating cached sources first and merging the partial sum in later
+    # (the two-phase schedule) must equal one softmax over all sources
+    rng = np.random.default_rng(split)
+    S, T, d = 9, 5, 32
+    H = rng.standard_normal((S, T, d)) * rng.uniform(0.3, 3, size=(S, 1, 1))
+    w = rng.standard_normal(d) / math.sqrt(d) * 2
+    r_all, a_all = O.depth_attention(H, w)
+    r1, a1, l1 = O.depth_attention_lse(H[:split], w)
+    r2, a2, l2 = O.depth_attention_lse(H[split:], w)
+    r, c1, c2 = O.merge_partial_softmax(r1, l1, r2, l2)
+    np.testing.assert_allclose(r, r_all, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(np.concatenate([a1 * c1[:, None], a2 * c2[:, None]], axis=1), a_all,
+                               rtol=1e-12, atol=1e-15)
+    # lse of a single source is its logit
+    _, _, l0 = O.depth_attention_lse(H[:1], w)
+    z0 = (O.rmsnorm(H[0]) @ w)
+    np.testing.assert_allclose(l0, z0, rtol=1e-13, atol=1e-14)

@@ -426,15 +426,17 @@ cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
   const int epv = 16 / esz;
 
   // ---- can a ring kernel take it?  (S <= 9: one group per token; up to
-  // 128: groups of 9 with an online softmax)
-  bool ring = S <= kMaxSources && row_bytes % 16 == 0;
+  // 128: groups of 9 with an online softmax; few tokens: a cluster per token)
+  bool aligned = S <= kMaxSources && row_bytes % 16 == 0;
   const long long nvec = row_bytes / 16;
-  const int vpt = (int)((nvec + kRingConsumers - 1) / kRingConsumers);
-  ring = ring && vpt >= 1 && vpt <= kRingMaxVpt;
-  for (int s = 0; ring && s < a.n_stored; ++s) ring = aligned16(a.src[s]);
-  if (ring && fused) ring = aligned16(a.fuse_F) && aligned16(a.fuse_dst) && (!a.fuse_prev || aligned16(a.fuse_prev));
+  for (int s = 0; aligned && s < a.n_stored; ++s) aligned = aligned16(a.src[s]);
+  if (aligned && fused)
+    aligned = aligned16(a.fuse_F) && aligned16(a.fuse_dst) && (!a.fuse_prev || aligned16(a.fuse_prev));
   const int out_store = epv * osz > 16 ? 16 : epv * osz;  // widest single store of an output vector
-  if (ring) ring = (reinterpret_cast<uintptr_t>(a.out_r) % out_store) == 0;
+  if (aligned) aligned = (reinterpret_cast<uintptr_t>(a.out_r) % out_store) == 0;
+  const int split_c = aligned && S <= kRingSmax ? split_cluster_size(a.T, di.sm_count, nvec) : 0;
+  const int vpt = (int)((nvec + kRingConsumers - 1) / kRingConsumers);
+  bool ring = aligned && vpt >= 1 && vpt <= kRingMaxVpt;
   int nslots = 0;
   if (ring) {
     const long long avail = (long long)di.max_smem_optin - kRingHeaderBytes;
@@ -443,7 +445,7 @@ cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
     ring = nslots >= 1;
   }
 
-  if (ring) {
+  if (ring || split_c > 0) {
     RingParams rp{};
     for (int s = 0; s < a.n_stored; ++s) rp.src[s] = static_cast<const char*>(a.src[s]);
     rp.fuse_prev = static_cast<const char*>(a.fuse_prev);
@@ -463,6 +465,10 @@ cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
     rp.nslots = nslots;
     rp.eps = a.eps;
     rp.inv_d = 1.0f / (float)a.d;
+    if (split_c > 0) {
+      *path = kPathRingSplit;
+      return launch_ring_split(rp, split_c, fused, in_bf16, out_bf16, di.sm_count, di.max_smem_optin, a.stream);
+    }
     const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
     const int smem = kRingHeaderBytes + nslots * (int)row_bytes;
     if (S > kRingSmax) {

@@ -35,7 +35,7 @@ struct AggArgs {
 };
 
 // Which kernel a launch took (for tests and the bench).
-enum AggPath { kPathNone = 0, kPathRing = 1, kPathGeneric = 2, kPathRingMulti = 3 };
+enum AggPath { kPathNone = 0, kPathRing = 1, kPathGeneric = 2, kPathRingMulti = 3, kPathRingSplit = 4 };
 
 // Launch; returns cudaSuccess or the launch error.  *path gets the kernel.
 cudaError_t launch_aggregate(const AggArgs& a, AggPath* path);

@@ -240,6 +240,14 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
 cudaError_t launch_ring_multi(const RingParams& rp, int vpt, bool fused, bool exact, bool in_bf16, bool out_bf16,
                               int grid, int smem, cudaStream_t stream);
 
+// Split-d cluster variant for few tokens (aggregate_split.cu): the cluster
+// size to use for T tokens (0 = none) and its launch.  Off unless the
+// environment sets ATTNRES_SPLIT=1.
+bool split_enabled();
+int split_cluster_size(long long T, int sm_count, long long nvec);
+cudaError_t launch_ring_split(const RingParams& rp_full, int C, bool fused, bool in_bf16, bool out_bf16,
+                              int sm_count, int max_smem, cudaStream_t stream);
+
 // Barrier set-up by thread 0 (the caller synchronises the CTA afterwards).
 __device__ __forceinline__ void ring_init(const RingParams& p, RingShared& sh) {
   if (threadIdx.x == 0) {

@@ -41,6 +41,11 @@
  *  - Any pointer alignment and any d >= 1 is accepted; rows that start on a
  *    16-byte boundary with 16-byte-multiple row length take the bulk-copy
  *    (TMA) path, others a plain-load kernel (still on the GPU).
+ *  - Environment, read once per process: ATTNRES_NO_PDL=1 launches without
+ *    programmatic dependent launch; ATTNRES_SPLIT=1 lets a launch of at most
+ *    9 sources over few tokens (T times the cluster size within the SM
+ *    count) share each token across a thread-block cluster of 2, 4 or 8
+ *    CTAs.  Results agree with the default path to the order of fp32 sums.
  */
 #ifndef ATTNRES_H
 #define ATTNRES_H

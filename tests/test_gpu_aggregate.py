@@ -4,10 +4,14 @@ Covers the two named single-layer workloads at full size (T=64/d=256/S=4
 fp32; T=4096/d=7168/S=9 bf16, every token), the long-context workload
 (T=131072, on all outlier tokens plus a random sample), and shapes that
 span several tiles with ragged tails: ragged token counts per CTA, rows
-whose 16-byte vectors do not fill the last pass, both kernels (bulk-copy
-ring and plain-load generic), every dtype pairing, S = 1..128, T = 0 and 1,
-unaligned pointers.
+whose 16-byte vectors do not fill the last pass, every kernel (bulk-copy
+ring, its multi-group and cluster-split variants, plain-load generic),
+every dtype pairing, S = 1..128, T = 0 and 1, unaligned pointers.
 """
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -18,6 +22,9 @@ from tests.parity import check_r, check_weights, oracle_aggregate, to64
 pytestmark = pytest.mark.gpu
 
 EPS = 1e-5
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+# the opt-in cluster-split variant for few tokens (read once per process)
+SPLIT = os.environ.get("ATTNRES_SPLIT", "0") not in ("", "0")
 
 
 @pytest.fixture(scope="module")
@@ -93,6 +100,14 @@ SHAPES = [
     (3, 7168, 1, torch.bfloat16, torch.bfloat16),      # S = 1
     (1, 7168, 9, torch.bfloat16, torch.bfloat16),      # T = 1
     (5, 64, 2, torch.bfloat16, torch.bfloat16),        # tiny row: 8 vectors
+    # few tokens: a cluster of C CTAs per token, each a channel slice
+    (64, 7168, 9, torch.bfloat16, torch.bfloat16),     # split C=2, 448 vectors per CTA (decode size)
+    (19, 7168, 9, torch.bfloat16, torch.bfloat16),     # split C=8, 112 vectors: partial last warp
+    (38, 7168, 5, torch.float32, torch.float32),       # split C=4, fp32
+    (17, 4096, 9, torch.float32, torch.bfloat16),      # split C=8, fp32 in, bf16 out (8-byte stores)
+    (70, 2048, 7, torch.bfloat16, torch.float32),      # split C=2, 128 vectors, fp32 out
+    (76, 1024, 9, torch.bfloat16, torch.bfloat16),     # split C=2, 64 vectors, C*T = 152 exactly
+    (2, 7168, 2, torch.bfloat16, torch.bfloat16),      # split C=8, S = 2
 ]
 
 
@@ -105,6 +120,65 @@ def test_shapes(lib, T, d, S, sdt, odt):
     _compare(H, inp.w, r, a, odt)
     if S == 1:
         assert torch.equal(r.float(), H[0].float()) and torch.equal(a, torch.ones_like(a))
+
+
+def test_split_matches_one_cta_per_token(lib):
+    # the first 64 tokens alone take the cluster kernel, all 4096 the
+    # one-CTA-per-token ring: same values up to the order of fp32 sums
+    inp = W.block_T4096_d7168(device="cuda")
+    r_ring, a_ring = _run(lib, inp.H, inp.w, torch.float32)
+    H64 = inp.H[:, :64].contiguous()
+    r_split, a_split = _run(lib, H64, inp.w, torch.float32)
+    assert (a_split - a_ring[:64]).abs().max().item() < 5e-6
+    scale = inp.H[:, :64].float().abs().amax(0)
+    # |a_s| differ by < 5e-6 each over 9 sources, plus fp32 rounding of r
+    assert ((r_split - r_ring[:64]).abs() <= 6e-5 * scale + 1e-30).all()
+
+
+def _kernel_names(fn):
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    return [e.name for e in prof.events() if "agg_" in e.name]
+
+
+def test_dispatch_picks_the_expected_kernel(lib):
+    inp = W.block_bf16(T=4096, d=7168, seed=3, device="cuda")
+    cases = [  # (sources, tokens, expected kernel)
+        (inp.H, 4096, "agg_ring_kernel"),
+        (inp.H[:, :64].contiguous(), 64, "agg_split_kernel" if SPLIT else "agg_ring_kernel"),
+        (inp.H[:, :64, :7160].contiguous(), 64, "agg_ring_kernel"),  # 895 vectors: no even split
+        (torch.cat([inp.H[:, :40]] * 2)[:12].contiguous(), 40, "agg_ring_multi_kernel"),
+    ]
+    seen_any = False
+    for H, T, want in cases:
+        r = torch.empty((T, H.shape[2]), dtype=torch.bfloat16, device="cuda")
+        names = _kernel_names(lambda: lib.attnres_aggregate(H, inp.w[: H.shape[2]], r))
+        if not names:
+            continue
+        seen_any = True
+        assert len(names) == 1 and names[0].split("<")[0].split("(")[0].split()[-1].endswith(want), (want, names)
+    if not seen_any:
+        pytest.skip("the profiler recorded no kernels")
+
+
+def test_split_variant_parity_in_a_child_process():
+    # the cluster-split variant is opt-in per process: run the few-token
+    # parity tests again in a child with it switched on
+    if SPLIT:
+        pytest.skip("this is the child")
+    env = dict(os.environ, ATTNRES_SPLIT="1")
+    tests = ["tests/test_gpu_aggregate.py::test_shapes",
+             "tests/test_gpu_aggregate.py::test_split_matches_one_cta_per_token",
+             "tests/test_gpu_aggregate.py::test_dispatch_picks_the_expected_kernel",
+             "tests/test_gpu_stack.py::test_fused_equals_unfused_bit_for_bit",
+             "tests/test_gpu_stack.py::test_decode_stack_T64_every_token",
+             "tests/test_gpu_stack.py::test_full_attnres_fp32_storage_93_layers"]
+    res = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider"] + tests,
+                         env=env, cwd=ROOT, capture_output=True, text=True, timeout=1200)
+    assert res.returncode == 0, res.stdout[-4000:] + res.stderr[-2000:]
+    print(res.stdout.strip().splitlines()[-1])
 
 
 def test_unaligned_pointers_take_the_generic_path(lib):

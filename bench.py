@@ -49,7 +49,7 @@ WORKLOAD = "block_attnres_single_layer_T4096_d7168_S9"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "aggregate_ring_T4096_d7168_S9.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "depth_wise_attention_block_gb300", "csrc", f)
-                  for f in ("aggregate.cu", "ring_common.cuh", "device_common.cuh")]
+                  for f in ("ring_kernel.cuh", "ring_fixed_s.cu", "ring_common.cuh", "device_common.cuh")]
 
 
 def algorithmic_bytes(T: int, d: int, S: int, esz: int = 2) -> int:
@@ -482,7 +482,7 @@ def run_gpu(args):
                        "parallelism": f"token-sharded x{ws}, no data exchange"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "agg_ring_kernel<bf16,bf16,VPT=2,unfused,exact>",
+                         "kernel": "agg_ring_kernel<bf16,bf16,VPT=2,unfused,exact,S=9>",
                          "algorithmic_bytes_per_launch": bytes_launch, "peak_source": peak_src,
                          "launch_ms_mean": launch_ms, "launch_ms_median": m["launch_ms_median"]},
             "hbm_gbs_achieved": achieved,

@@ -41,197 +41,9 @@
 #include "device_common.cuh"
 #include "launch.h"
 #include "ring_common.cuh"
+#include "ring_kernel.cuh"
 
 namespace attnres {
-
-template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT>
-__global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_constant__ RingParams p) {
-  // EXACT: the row holds exactly VPT * kRingConsumers vectors, so every
-  // consumer thread owns VPT of them and no bounds test is needed
-  constexpr int EPV = Vec<Tin>::kElems;
-  extern __shared__ __align__(128) unsigned char smem[];
-  RingShared& sh = *reinterpret_cast<RingShared*>(smem);
-  const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int nslots = p.nslots;
-  const long long T = p.T;
-  pdl_trigger();
-
-  ring_init(p, sh);
-  __syncthreads();
-  pdl_wait();  // everything below may read what the previous kernel wrote
-
-  if (warp == kRingConsumerWarps) {
-    if (lane == 0) ring_produce(p, sh, ring);
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers --
-  constexpr int NP = EPV / 2;  // packed fp32 pairs per 16-byte vector
-  uint64_t wp[VPT][NP];        // this thread's channels of w, as pairs
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = tid + k * kRingConsumers;
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-      const bool in = EXACT || v < p.nvec;
-      wp[k][j] = f2_pack(in ? __ldg(p.w + v * EPV + 2 * j) : 0.f, in ? __ldg(p.w + v * EPV + 2 * j + 1) : 0.f);
-    }
-  }
-
-  const int S = p.S;
-  uint32_t slot = 0, lap = 0;
-  bool ok = true;
-
-  // take this thread's vectors of the next landed row, then release the slot
-  auto consume = [&](uint4* dst) {
-    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u)) ok = false;
-    const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = tid + k * kRingConsumers;
-      // after a failed wait the slot holds stale data: harmless, the token is abandoned
-      dst[k] = (EXACT || v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&sh.empty[slot]));
-    if (++slot == (uint32_t)nslots) {
-      slot = 0;
-      ++lap;
-    }
-  };
-
-  int iter = 0;
-  for (long long t = blockIdx.x; t < T; t += gridDim.x, ++iter) {
-    const int buf = iter & 1;
-    volatile int* abort_flag = &sh.abort_flag[buf];
-    uint4 x[kRingSmax][VPT];
-    float part[2 * kRingSmax];  // [2s] = dot(w, h_s), [2s+1] = sum(h_s^2), this thread's channels
-#pragma unroll
-    for (int s = 0; s < kRingSmax; ++s) {
-      part[2 * s] = 0.f;
-      part[2 * s + 1] = 0.f;
-      if (s < S) {
-        if (!FUSED || s < p.n_stored) {
-          consume(x[s]);
-        } else {
-          // the fused source: round(prev + F), stored as the new partial / b_n
-          uint4 pv[VPT], fv[VPT];
-          if (p.fuse_prev) consume(pv);
-          consume(fv);
-          char* drow = p.fuse_dst + t * (long long)p.row_bytes;
-#pragma unroll
-          for (int k = 0; k < VPT; ++k) {
-            const int v = tid + k * kRingConsumers;
-            if (EXACT || v < p.nvec) {
-              float f[EPV];
-              Vec<Tin>::unpack(fv[k], f);
-              if (p.fuse_prev) {
-                float q[EPV];
-                Vec<Tin>::unpack(pv[k], q);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) f[e] = q[e] + f[e];
-              }
-              if (!ok) {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) f[e] = __int_as_float(0x7fc00000);
-              }
-              x[s][k] = Vec<Tin>::pack(f);  // one rounding to the storage type
-              *reinterpret_cast<uint4*>(drow + (size_t)v * 16) = x[s][k];
-            } else {
-              x[s][k] = make_uint4(0, 0, 0, 0);
-            }
-          }
-        }
-        // two packed accumulators each (four partial sums) to keep the
-        // dependent FMA chains short
-        uint64_t dot2[2] = {0, 0}, ss2[2] = {0, 0};
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          uint64_t h[NP];
-          Vec<Tin>::pairs(x[s][k], h);
-#pragma unroll
-          for (int j = 0; j < NP; ++j) {
-            dot2[j & 1] = f2_fma(wp[k][j], h[j], dot2[j & 1]);
-            ss2[j & 1] = f2_fma(h[j], h[j], ss2[j & 1]);
-          }
-        }
-        part[2 * s] = f2_hsum(dot2[0]) + f2_hsum(dot2[1]);
-        part[2 * s + 1] = f2_hsum(ss2[0]) + f2_hsum(ss2[1]);
-      }
-    }
-
-    // ---- warp totals (reduce-scatter), then one CTA-wide step through smem
-    reduce_scatter18(part, lane);
-    if ((kRsValidLanes >> lane) & 1u) {
-      const int idx = rs_index(lane);
-      if (idx < 2 * S) sh.red[buf][warp][idx] = part[0];
-    }
-    const bool warp_failed = __any_sync(0xffffffffu, !ok);
-    if (lane == 0 && warp_failed) *abort_flag = 1;
-    named_barrier_sync(kRingBarrierId, kRingConsumers);
-
-    // ---- logits and the depth softmax, computed by every warp (lane 2s
-    // holds source s); all warps sum in the same order, so agree bit for bit
-    const bool abort = *abort_flag != 0;
-    float tot = 0.f;
-    if (lane < 2 * S) {
-#pragma unroll
-      for (int w = 0; w < kRingConsumerWarps; ++w) tot += sh.red[buf][w][lane];
-    }
-    const float sumsq = __shfl_down_sync(0xffffffffu, tot, 1);
-    const bool is_src = lane < 2 * S && (lane & 1) == 0;
-    // fast reciprocal square root, exponential and division: each within a
-    // few fp32 ulps, far inside the 1e-5 weight tolerance
-    const float z = is_src ? tot * rsqrtf(fmaf(sumsq, p.inv_d, p.eps)) : -INFINITY;
-    const float m = warp_max(z);
-    const float e = is_src ? __expf(z - m) : 0.f;
-    const float esum = warp_sum(e);
-    float a = abort ? __int_as_float(0x7fc00000) : __fdividef(e, esum);
-    if (warp == 0 && is_src && p.out_a) p.out_a[t * S + (lane >> 1)] = a;
-    uint64_t a2[kRingSmax];
-#pragma unroll
-    for (int s = 0; s < kRingSmax; ++s) {
-      const float as = __shfl_sync(0xffffffffu, a, 2 * s);
-      a2[s] = f2_pack(as, as);
-    }
-
-    // ---- r = sum_s a_s h_s from the registers
-    char* orow = p.out_r + t * (long long)p.out_row_bytes;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = tid + k * kRingConsumers;
-      if (EXACT || v < p.nvec) {
-        uint64_t acc[NP];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) acc[j] = 0;
-#pragma unroll
-        for (int s = 0; s < kRingSmax; ++s) {
-          if (s < S) {
-            uint64_t h[NP];
-            Vec<Tin>::pairs(x[s][k], h);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) acc[j] = f2_fma(a2[s], h[j], acc[j]);
-          }
-        }
-        float r[EPV];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) f2_unpack(acc[j], r[2 * j], r[2 * j + 1]);
-        if (abort) {
-#pragma unroll
-          for (int e2 = 0; e2 < EPV; ++e2) r[e2] = __int_as_float(0x7fc00000);
-        }
-        store_out<Tout, EPV>(orow, v, r);
-      }
-    }
-    if (abort) {
-      if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
-      break;
-    }
-  }
-}
 
 // --------------------------------------------------------- generic kernel --
 
@@ -357,30 +169,16 @@ cudaError_t device_info(DeviceInfo* info) {
   return cudaSuccess;
 }
 
-template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT>
-static cudaError_t launch_ring_t(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  auto kern = agg_ring_kernel<Tin, Tout, VPT, FUSED, EXACT>;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
-    DeviceInfo di;
-    e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
-  }
-  e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, rp);
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
-
 template <typename Tin, typename Tout>
 static cudaError_t launch_ring_vpt(const RingParams& rp, int vpt, bool fused, int grid, int smem,
                                    cudaStream_t stream) {
   const bool exact = rp.nvec == vpt * kRingConsumers;
+  if constexpr (sizeof(Tin) == 2 && sizeof(Tout) == 2) {
+    // bf16 storage at d = 7168 (the K3 width): one kernel per source count
+    if (exact && vpt == 2 && rp.S >= 1 && rp.S <= kRingSmax)
+      return fused ? launch_ring_fixed_s_fused(rp, grid, smem, stream)
+                   : launch_ring_fixed_s(rp, grid, smem, stream);
+  }
   if (vpt == 1) {
     return fused ? launch_ring_t<Tin, Tout, 1, true, false>(rp, grid, smem, stream)
                  : launch_ring_t<Tin, Tout, 1, false, false>(rp, grid, smem, stream);

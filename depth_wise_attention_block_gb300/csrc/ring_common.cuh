@@ -240,6 +240,11 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
 cudaError_t launch_ring_multi(const RingParams& rp, int vpt, bool fused, bool exact, bool in_bf16, bool out_bf16,
                               int grid, int smem, cudaStream_t stream);
 
+// The ring kernel for bf16 rows of d = 7168 with the source count fixed at
+// compile time (ring_fixed_s.cu, ring_fixed_s_fused.cu); rp.S in 1..9.
+cudaError_t launch_ring_fixed_s(const RingParams& rp, int grid, int smem, cudaStream_t stream);
+cudaError_t launch_ring_fixed_s_fused(const RingParams& rp, int grid, int smem, cudaStream_t stream);
+
 // Split-d cluster variant for few tokens (aggregate_split.cu): the cluster
 // size to use for T tokens (0 = none) and its launch.  Off unless the
 // environment sets ATTNRES_SPLIT=1.

@@ -132,6 +132,16 @@ __device__ __forceinline__ void reduce_scatter18(float* v, int lane) {
   rs_level<2, 1, 1>(v, lane);
 }
 
+// The same after its first level (offset 16) was done by the caller: v holds
+// 9 values per lane, value i of the lanes with bit 4 clear and value 9 + i
+// of the others.
+__device__ __forceinline__ void reduce_scatter18_after_first(float* v, int lane) {
+  rs_level<9, 5, 8>(v, lane);
+  rs_level<5, 3, 4>(v, lane);
+  rs_level<3, 2, 2>(v, lane);
+  rs_level<2, 1, 1>(v, lane);
+}
+
 // Generic reduce-scatter of N <= 32 per-lane values over the warp, halving
 // the kept range at each of the offsets 16, 8, 4, 2, 1 (lower lanes keep the
 // first ceil(n/2) values).  Afterwards lane `lane` holds in v[0] the warp

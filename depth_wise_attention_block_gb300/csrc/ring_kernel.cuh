@@ -22,6 +22,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
   // with it the per-source guards fold away and the compiler schedules the
   // whole token as one block.
   constexpr int EPV = Vec<Tin>::kElems;
+  // kEarlyRs: the first reduce-scatter level is taken per source during the
+  // first pass (one partial live per source instead of two).  That keeps the
+  // fused kernels (more live state) from spilling; the unfused ones are
+  // faster without it at S = 9.
+  constexpr bool kEarlyRs = FUSED;
   extern __shared__ __align__(128) unsigned char smem[];
   RingShared& sh = *reinterpret_cast<RingShared*>(smem);
   const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
@@ -81,11 +86,17 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     const int buf = iter & 1;
     volatile int* abort_flag = &sh.abort_flag[buf];
     uint4 x[kRingSmax][VPT];
-    float part[2 * kRingSmax];  // [2s] = dot(w, h_s), [2s+1] = sum(h_s^2), this thread's channels
+    // Partials laid out as [dot(w, h_0..h_8), sum(h_0^2)..sum(h_8^2)].  With
+    // kEarlyRs, per source, this thread's dot and sum of squares enter the
+    // first level of the warp reduce-scatter at once: lanes with bit 4 clear
+    // keep the dot products, the others the sums of squares, each adding its
+    // partner's (lane ^ 16).
+    const bool upper16 = (lane & 16) != 0;
+    float part[kEarlyRs ? kRingSmax : 2 * kRingSmax];
+#pragma unroll
+    for (int s = 0; s < (kEarlyRs ? kRingSmax : 2 * kRingSmax); ++s) part[s] = 0.f;
 #pragma unroll
     for (int s = 0; s < kRingSmax; ++s) {
-      part[2 * s] = 0.f;
-      part[2 * s + 1] = 0.f;
       if (s < S) {
         if (!FUSED || s < p.n_stored) {
           consume(x[s]);
@@ -131,16 +142,26 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
             ss2[j & 1] = f2_fma(h[j], h[j], ss2[j & 1]);
           }
         }
-        part[2 * s] = f2_hsum(dot2[0]) + f2_hsum(dot2[1]);
-        part[2 * s + 1] = f2_hsum(ss2[0]) + f2_hsum(ss2[1]);
+        const float dot = f2_hsum(dot2[0]) + f2_hsum(dot2[1]);
+        const float ss = f2_hsum(ss2[0]) + f2_hsum(ss2[1]);
+        if constexpr (kEarlyRs) {
+          part[s] = (upper16 ? ss : dot) + __shfl_xor_sync(0xffffffffu, upper16 ? dot : ss, 16);
+        } else {
+          part[s] = dot;
+          part[kRingSmax + s] = ss;
+        }
       }
     }
 
     // ---- warp totals (reduce-scatter), then one CTA-wide step through smem
-    reduce_scatter18(part, lane);
+    // remaining levels (9 -> 5 -> 3 -> 2 -> 1 values per lane); value index
+    // i < 9 is dot(w, h_i), 9 + i is sum(h_i^2), stored at [2i] and [2i + 1]
+    if constexpr (kEarlyRs) reduce_scatter18_after_first(part, lane);
+    else reduce_scatter18(part, lane);
     if ((kRsValidLanes >> lane) & 1u) {
       const int idx = rs_index(lane);
-      if (idx < 2 * S) sh.red[buf][warp][idx] = part[0];
+      const int src = idx < kRingSmax ? idx : idx - kRingSmax;
+      if (src < S) sh.red[buf][warp][idx < kRingSmax ? 2 * idx : 2 * src + 1] = part[0];
     }
     const bool warp_failed = __any_sync(0xffffffffu, !ok);
     if (lane == 0 && warp_failed) *abort_flag = 1;
@@ -164,23 +185,43 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     const float esum = warp_sum(e);
     float a = abort ? __int_as_float(0x7fc00000) : __fdividef(e, esum);
     if (warp == 0 && is_src && p.out_a) p.out_a[t * S + (lane >> 1)] = a;
-    uint64_t a2[kRingSmax];
+    // ---- r = sum_s a_s h_s from the registers
+    uint64_t acc[VPT][NP];
 #pragma unroll
-    for (int s = 0; s < kRingSmax; ++s) {
-      const float as = __shfl_sync(0xffffffffu, a, 2 * s);
-      a2[s] = f2_pack(as, as);
+    for (int k = 0; k < VPT; ++k) {
+#pragma unroll
+      for (int j = 0; j < NP; ++j) acc[k][j] = 0;
     }
-
-    // ---- r = sum_s a_s h_s from the registers.  With a fixed source count
-    // the compiler would otherwise keep the first pass's unpacked fp32
-    // values alive across the barrier (twice the registers, spilled); the
-    // empty asm makes it unpack the packed registers again instead.
-    if constexpr (SC != 0) {
+    {
+      if constexpr (SC != 0) {
+        // With a fixed source count the compiler would otherwise keep the
+        // first pass's unpacked fp32 values alive across the barrier (twice
+        // the registers, spilled); the empty asm makes it unpack the packed
+        // registers again instead.
+#pragma unroll
+        for (int s = 0; s < kRingSmax; ++s) {
+#pragma unroll
+          for (int k = 0; k < VPT; ++k)
+            asm volatile("" : "+r"(x[s][k].x), "+r"(x[s][k].y), "+r"(x[s][k].z), "+r"(x[s][k].w));
+        }
+      }
+      uint64_t a2[kRingSmax];
 #pragma unroll
       for (int s = 0; s < kRingSmax; ++s) {
+        const float as = __shfl_sync(0xffffffffu, a, 2 * s);
+        a2[s] = f2_pack(as, as);
+      }
 #pragma unroll
-        for (int k = 0; k < VPT; ++k)
-          asm volatile("" : "+r"(x[s][k].x), "+r"(x[s][k].y), "+r"(x[s][k].z), "+r"(x[s][k].w));
+      for (int k = 0; k < VPT; ++k) {
+#pragma unroll
+        for (int s = 0; s < kRingSmax; ++s) {
+          if (s < S) {
+            uint64_t h[NP];
+            Vec<Tin>::pairs(x[s][k], h);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) acc[k][j] = f2_fma(a2[s], h[j], acc[k][j]);
+          }
+        }
       }
     }
     char* orow = p.out_r + t * (long long)p.out_row_bytes;
@@ -188,21 +229,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * kRingConsumers;
       if (EXACT || v < p.nvec) {
-        uint64_t acc[NP];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) acc[j] = 0;
-#pragma unroll
-        for (int s = 0; s < kRingSmax; ++s) {
-          if (s < S) {
-            uint64_t h[NP];
-            Vec<Tin>::pairs(x[s][k], h);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) acc[j] = f2_fma(a2[s], h[j], acc[j]);
-          }
-        }
         float r[EPV];
 #pragma unroll
-        for (int j = 0; j < NP; ++j) f2_unpack(acc[j], r[2 * j], r[2 * j + 1]);
+        for (int j = 0; j < NP; ++j) f2_unpack(acc[k][j], r[2 * j], r[2 * j + 1]);
         if (abort) {
 #pragma unroll
           for (int e2 = 0; e2 < EPV; ++e2) r[e2] = __int_as_float(0x7fc00000);

@@ -384,14 +384,33 @@ __global__ void __launch_bounds__(kBwdGenThreads) agg_bwd_generic_kernel(const _
   }
 }
 
-__global__ void __launch_bounds__(256) dw_reduce_kernel(const float* ws, int nb, int d, float* dw) {
+// dw[c] = sum over the nb workspace rows of ws[b, c], in a fixed order: the
+// kDwSplit threads of channel c each add rows b = part, part + kDwSplit, ...
+// in turn (all their loads independent, so in flight together), then the
+// kDwSplit partials are added in part order through shared memory.  A block
+// covers 32 consecutive channels (coalesced 128-byte row segments).
+constexpr int kDwSplit = 8;
+constexpr int kDwThreads = 32 * kDwSplit;
+
+__global__ void __launch_bounds__(kDwThreads) dw_reduce_kernel(const float* ws, int nb, int d, float* dw) {
+  __shared__ float part_sum[kDwSplit][32];
   pdl_trigger();
   pdl_wait();
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < d; c += gridDim.x * blockDim.x) {
-    float s = 0.f;
+  const int cl = threadIdx.x & 31;
+  const int part = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + cl;
+  float s = 0.f;
+  if (c < d) {
 #pragma unroll 8
-    for (int b = 0; b < nb; ++b) s += ws[(size_t)b * d + c];
-    dw[c] = s;
+    for (int b = part; b < nb; b += kDwSplit) s += ws[(size_t)b * d + c];
+  }
+  part_sum[part][cl] = s;
+  __syncthreads();
+  if (part == 0 && c < d) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < kDwSplit; ++k) t += part_sum[k][cl];
+    dw[c] = t;
   }
 }
 
@@ -495,8 +514,8 @@ cudaError_t launch_aggregate_backward(const BwdArgs& a) {
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int rgrid = (a.d + 255) / 256;
-  e = launch_kernel(dw_reduce_kernel, dim3(rgrid), dim3(256), 0, a.stream, (const float*)a.workspace, grid, a.d,
+  const int rgrid = (a.d + 31) / 32;
+  e = launch_kernel(dw_reduce_kernel, dim3(rgrid), dim3(kDwThreads), 0, a.stream, (const float*)a.workspace, grid, a.d,
                     a.grad_w);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

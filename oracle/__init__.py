@@ -32,7 +32,9 @@ from .attnres_oracle import (  # noqa: F401
     round_bf16,
     round_fp32,
     synthetic_layer,
+    synthetic_layer_backward,
     block_stack_forward,
+    block_stack_backward,
     full_stack_forward,
     StackTrace,
 )

@@ -277,6 +277,15 @@ def synthetic_layer(x: np.ndarray, g: np.ndarray, s: np.ndarray) -> np.ndarray:
     return np.tanh(x * np.asarray(g, np.float64)) * np.asarray(s, np.float64)
 
 
+def synthetic_layer_backward(x: np.ndarray, g: np.ndarray, s: np.ndarray, dv: np.ndarray) -> np.ndarray:
+    """Gradient through F_l: d/dx [tanh(x g) s] = (1 - tanh(x g)^2) g s, times
+    the incoming gradient dv (per channel; the stand-in body, not the method)."""
+    x = np.asarray(x, dtype=np.float64)
+    g = np.asarray(g, np.float64)
+    th = np.tanh(x * g)
+    return np.asarray(dv, np.float64) * (1.0 - th * th) * g * np.asarray(s, np.float64)
+
+
 # --------------------------------------------------------------------------
 # Stacks
 # --------------------------------------------------------------------------
@@ -371,3 +380,56 @@ def full_stack_forward(h0: np.ndarray, W: np.ndarray, layer_fn: Callable[[int, n
         else:
             tr.final_sources = list(history)
     return tr
+
+
+def block_stack_backward(h0: np.ndarray, W: np.ndarray, G: np.ndarray, Sc: np.ndarray,
+                         num_layers: int, block_size: int, dr_out: np.ndarray,
+                         eps: float = EPS) -> tuple[np.ndarray, np.ndarray]:
+    """Gradients of the loss sum(r_{L+1} * dr_out) of a Block AttnRes stack
+    whose layer bodies are synthetic_layer(., G[l-1], Sc[l-1]), with respect
+    to the embedding h_0 and the pseudo-queries W[0..L].  Exact fp64.
+
+    Reverse mode over the value lists ([Tutorial ch. 4.3] Eq. 10): every
+    source of layer l is h_0 or a sum of layer outputs v_first..v_last, so the
+    gradient layer l's aggregation sends to that source reaches each of those
+    outputs unchanged.  Layers are visited from the final aggregation down to
+    layer 1; when layer j is reached every layer that reads v_j (later layers
+    of its block through the partial sum, later blocks and the final
+    aggregation through b_n) has been visited, so dL/dv_j is complete and
+    goes through the layer body to r_j, dL/dr_j = dL/dv_j F_j'(r_j), and on
+    into layer j's own aggregation.  The forward is recomputed from h_0, W,
+    G, Sc (as under activation checkpointing, [Tutorial] ch. 4.6).
+    Returns (dh0 [T, d], dW [L+1, d]).
+    """
+    L, B = num_layers, block_size
+    G = np.asarray(G, np.float64)
+    Sc = np.asarray(Sc, np.float64)
+    fn = lambda l, x: synthetic_layer(x, G[l - 1], Sc[l - 1])
+    tr = block_stack_forward(h0, W, fn, L, B, eps)
+    v = {0: np.asarray(h0, np.float64)}
+    for j in range(1, L + 1):
+        v[j] = tr.v[j - 1]
+    dv = {j: np.zeros_like(v[0]) for j in range(0, L + 1)}
+    dW = np.zeros((L + 1, v[0].shape[1]))
+    for layer in range(L + 1, 0, -1):
+        if layer == L + 1:
+            dr = np.asarray(dr_out, np.float64)
+        else:
+            dr = synthetic_layer_backward(tr.r[layer - 1], G[layer - 1], Sc[layer - 1], dv[layer])
+        entries = value_list(layer, B, L)
+        srcs = []
+        for entry in entries:
+            if entry[0] == "embed":
+                srcs.append(v[0])
+            else:
+                _, _, first, last = entry
+                srcs.append(sum(v[j] for j in range(first, last + 1)))
+        dH, dW[layer - 1] = depth_attention_backward(np.stack(srcs), W[layer - 1], dr, eps)
+        for entry, dh in zip(entries, dH):
+            if entry[0] == "embed":
+                dv[0] += dh
+            else:
+                _, _, first, last = entry
+                for j in range(first, last + 1):
+                    dv[j] += dh
+    return dv[0], dW

@@ -440,3 +440,69 @@ def test_merge_of_partial_softmaxes_equals_the_union(split):
     _, _, l0 = O.depth_attention_lse(H[:1], w)
     z0 = (O.rmsnorm(H[0]) @ w)
     np.testing.assert_allclose(l0, z0, rtol=1e-13, atol=1e-14)
+
+
+# ------------------------------------------------------- stack backward -----
+
+def _tiny_grad_stack(L, B, T=2, d=6, seed=0):
+    rng = np.random.default_rng(100 + 10 * L + B + seed)
+    h0 = rng.standard_normal((T, d))
+    W = rng.standard_normal((L + 1, d)) / math.sqrt(d) * 2
+    G = rng.standard_normal((L, d))
+    Sc = rng.uniform(0.05, 0.2, size=(L, d)) * 5     # larger bodies: every layer matters
+    dr = rng.standard_normal((T, d))
+    return h0, W, G, Sc, dr
+
+
+def _stack_loss(h0, W, G, Sc, L, B, dr, full=False):
+    fn = lambda l, x: O.synthetic_layer(x, G[l - 1], Sc[l - 1])
+    tr = O.full_stack_forward(h0, W, fn, L) if full else O.block_stack_forward(h0, W, fn, L, B)
+    return float((tr.r[L] * dr).sum())
+
+
+@pytest.mark.parametrize("L,B", [(1, 1), (4, 2), (6, 3), (7, 12), (5, 4), (9, 3)])
+def test_stack_backward_matches_central_differences(L, B):
+    # every entry of dh0 and dW against central differences of the stack
+    # forward (a separate code path: explicit value lists and range sums)
+    h0, W, G, Sc, dr = _tiny_grad_stack(L, B)
+    dh0, dW = O.block_stack_backward(h0, W, G, Sc, L, B, dr)
+    step = 1e-6
+    for (arr, grad) in ((h0, dh0), (W, dW)):
+        for idx in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += step
+            m[idx] -= step
+            args_p = (p, W) if arr is h0 else (h0, p)
+            args_m = (m, W) if arr is h0 else (h0, m)
+            fd = (_stack_loss(*args_p, G, Sc, L, B, dr) - _stack_loss(*args_m, G, Sc, L, B, dr)) / (2 * step)
+            assert abs(fd - grad[idx]) <= 1e-7 * (1 + abs(fd)), (idx, fd, grad[idx])
+
+
+def test_stack_backward_block_size_one_is_full_attnres():
+    # block size 1 makes every layer output its own block: the gradients must
+    # be those of Full AttnRes, checked by differences of the Full forward
+    L = 5
+    h0, W, G, Sc, dr = _tiny_grad_stack(L, 1, seed=3)
+    dh0, dW = O.block_stack_backward(h0, W, G, Sc, L, 1, dr)
+    step = 1e-6
+    for idx in [(0, 0), (1, 3), (0, 5)]:
+        p, m = h0.copy(), h0.copy()
+        p[idx] += step
+        m[idx] -= step
+        fd = (_stack_loss(p, W, G, Sc, L, 1, dr, full=True) - _stack_loss(m, W, G, Sc, L, 1, dr, full=True)) / (2 * step)
+        assert abs(fd - dh0[idx]) <= 1e-7 * (1 + abs(fd))
+    for idx in [(0, 1), (3, 2), (5, 4)]:
+        p, m = W.copy(), W.copy()
+        p[idx] += step
+        m[idx] -= step
+        fd = (_stack_loss(h0, p, G, Sc, L, 1, dr, full=True) - _stack_loss(h0, m, G, Sc, L, 1, dr, full=True)) / (2 * step)
+        assert abs(fd - dW[idx]) <= 1e-7 * (1 + abs(fd))
+
+
+def test_synthetic_layer_backward_closed_form():
+    # d/dx tanh(x g) s at x = 0 is g s; far from zero it vanishes
+    g = np.array([0.5, -2.0, 3.0])
+    s = np.array([0.1, 0.2, 0.15])
+    one = np.ones(3)
+    np.testing.assert_allclose(O.synthetic_layer_backward(np.zeros(3), g, s, one), g * s, rtol=0, atol=0)
+    assert np.all(np.abs(O.synthetic_layer_backward(np.full(3, 40.0), g, s, one)) < 1e-20)

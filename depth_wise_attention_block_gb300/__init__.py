@@ -33,7 +33,8 @@ from ._native import (  # noqa: F401
 __all__ = [
     "attnres_aggregate", "attnres_aggregate_backward", "attnres_aggregate_backward_workspace_size",
     "attnres_interblock", "attnres_intrablock_step", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
-    "attnres_layer_step", "attnres_synthetic_layer", "attnres_version", "AttnResState",
+    "attnres_layer_step", "attnres_synthetic_layer", "attnres_synthetic_layer_backward", "attnres_fold",
+    "attnres_version", "AttnResState",
     "aggregate_host", "dtype_code", "AttnresError",
 ]
 
@@ -255,6 +256,30 @@ def attnres_synthetic_layer(x: torch.Tensor, g: torch.Tensor, s: torch.Tensor, o
                                         _dev_ptr(s, "s", torch.float32), _dev_ptr(out, "out", x.dtype), T, d,
                                         dtype_code(x.dtype), _stream_ptr(stream))
     _N.check(rc, "attnres_synthetic_layer")
+
+
+def attnres_synthetic_layer_backward(x: torch.Tensor, g: torch.Tensor, s: torch.Tensor, grad_out_a: torch.Tensor,
+                                     grad_out_b: torch.Tensor | None, grad_x: torch.Tensor, stream=None) -> None:
+    """Gradient of the stand-in body: grad_x = (grad_out_a + grad_out_b) * (1 - tanh(x g)^2) * g * s."""
+    T, d = x.shape
+    for name, t in (("grad_out_a", grad_out_a), ("grad_out_b", grad_out_b), ("grad_x", grad_x)):
+        if t is not None and t.shape != (T, d):
+            raise ValueError(f"{name} must be [T, d]")
+    rc = _N.lib.attnres_synthetic_layer_backward(
+        _dev_ptr(x, "x"), _dev_ptr(g, "g", torch.float32), _dev_ptr(s, "s", torch.float32),
+        _dev_ptr(grad_out_a, "grad_out_a", x.dtype), _dev_ptr(grad_out_b, "grad_out_b", x.dtype),
+        _dev_ptr(grad_x, "grad_x", x.dtype), T, d, dtype_code(x.dtype), _stream_ptr(stream))
+    _N.check(rc, "attnres_synthetic_layer_backward")
+
+
+def attnres_fold(prev: torch.Tensor | None, F: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """Block bookkeeping on plain buffers: dst = prev + F (one rounding), or F when prev is None."""
+    T, d = F.shape
+    if dst.shape != (T, d) or (prev is not None and prev.shape != (T, d)):
+        raise ValueError("prev, F and dst must all be [T, d]")
+    rc = _N.lib.attnres_fold(_dev_ptr(prev, "prev", F.dtype), _dev_ptr(F, "F"), _dev_ptr(dst, "dst", F.dtype), T, d,
+                             dtype_code(F.dtype), _stream_ptr(stream))
+    _N.check(rc, "attnres_fold")
 
 
 _HOST_STREAMS: dict = {}

@@ -42,6 +42,8 @@ EXPORTED = (
     "attnres_block_step",
     "attnres_layer_step",
     "attnres_synthetic_layer",
+    "attnres_synthetic_layer_backward",
+    "attnres_fold",
     "attnres_status_string",
     "attnres_last_error",
     "attnres_version",
@@ -89,6 +91,8 @@ def _load() -> ctypes.CDLL:
         "attnres_block_step": (i32, [sp, vp, i32, vp, vp]),
         "attnres_layer_step": (i32, [sp, vp, vp, i32, vp, vp, vp, vp]),
         "attnres_synthetic_layer": (i32, [vp, vp, vp, vp, i64, i32, i32, vp]),
+        "attnres_synthetic_layer_backward": (i32, [vp, vp, vp, vp, vp, vp, i64, i32, i32, vp]),
+        "attnres_fold": (i32, [vp, vp, vp, i64, i32, i32, vp]),
         "attnres_status_string": (ctypes.c_char_p, [i32]),
         "attnres_last_error": (ctypes.c_char_p, []),
         "attnres_version": (i32, []),

@@ -479,4 +479,26 @@ int attnres_synthetic_layer(const void* x, const float* g, const float* s, void*
   return ok();
 }
 
+int attnres_synthetic_layer_backward(const void* x, const float* g, const float* s, const void* grad_out_a,
+                                     const void* grad_out_b, void* grad_x, int64_t T, int d, int dtype, void* stream) {
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (!size_ok(T, d)) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (T == 0) return ok();
+  if (!x || !g || !s || !grad_out_a || !grad_x) return fail(ATTNRES_EINVAL, "NULL argument");
+  cudaError_t e = launch_synthetic_layer_backward(x, g, s, grad_out_a, grad_out_b, grad_x, T, d, dtype,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_synthetic_layer_backward launch");
+  return ok();
+}
+
+int attnres_fold(const void* prev, const void* F, void* dst, int64_t T, int d, int dtype, void* stream) {
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (!size_ok(T, d)) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (T == 0) return ok();
+  if (!F || !dst) return fail(ATTNRES_EINVAL, "NULL argument");
+  cudaError_t e = launch_fold(prev, F, dst, T * (int64_t)d, dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_fold launch");
+  return ok();
+}
+
 }  // extern "C"

@@ -8,6 +8,8 @@
 //                     does the same arithmetic inside the aggregation.
 //  synth_layer_kernel the stand-in layer body F(x) = tanh(x * g) * s used to
 //                     drive a stack without trained weights.
+//  synth_layer_backward_kernel  its gradient, dx = (dv_a + dv_b) *
+//                     (1 - tanh(x g)^2) * g * s (dv_b optional).
 //
 // Both are HBM-bound streams: 16-byte vector accesses when every pointer is
 // 16-byte aligned and rows hold whole vectors, scalar accesses otherwise;
@@ -140,6 +142,51 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, con
   }
 }
 
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kEwThreads) synth_layer_backward_kernel(const T* x, const float* __restrict__ g,
+                                                                          const float* __restrict__ s, const T* dva,
+                                                                          const T* dvb, T* dx, long long T_, int d) {
+  pdl_trigger();
+  pdl_wait();
+  const long long n = T_ * (long long)d;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if constexpr (VEC) {
+    constexpr int E = Vec16<T>::kElems;
+    const int vrow = d / E;
+    const long long nv = n / E;
+    const uint4* X4 = reinterpret_cast<const uint4*>(x);
+    const uint4* A4 = reinterpret_cast<const uint4*>(dva);
+    const uint4* B4 = reinterpret_cast<const uint4*>(dvb);
+    uint4* O4 = reinterpret_cast<uint4*>(dx);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+      const int c0 = (int)(i % vrow) * E;
+      float f[E], ga[E], gb[E];
+      Vec16<T>::unpack(X4[i], f);
+      Vec16<T>::unpack(A4[i], ga);
+      if (dvb) {
+        Vec16<T>::unpack(B4[i], gb);
+#pragma unroll
+        for (int e = 0; e < E; ++e) ga[e] += gb[e];
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float gg = __ldg(g + c0 + e), ss = __ldg(s + c0 + e);
+        const float th = tanhf(f[e] * gg);
+        f[e] = ga[e] * (1.f - th * th) * gg * ss;
+      }
+      O4[i] = Vec16<T>::pack(f);
+    }
+  } else {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+      const int c = (int)(i % d);
+      float dv = load_elem(dva + i);
+      if (dvb) dv += load_elem(dvb + i);
+      const float th = tanhf(load_elem(x + i) * g[c]);
+      store_elem(dx + i, dv * (1.f - th * th) * g[c] * s[c]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- launch --
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -192,6 +239,32 @@ cudaError_t launch_synthetic_layer(const void* x, const float* g, const float* s
   if (T <= 0) return cudaSuccess;
   return dtype == ATTNRES_BF16 ? launch_synth_t<bf16_t>(x, g, s, out, T, d, stream)
                                : launch_synth_t<float>(x, g, s, out, T, d, stream);
+}
+
+template <typename T>
+static cudaError_t launch_synth_bwd_t(const void* x, const float* g, const float* s, const void* dva,
+                                      const void* dvb, void* dx, long long T_, int d, cudaStream_t st) {
+  constexpr int E = 16 / (int)sizeof(T);
+  const long long n = T_ * (long long)d;
+  const bool vec = d % E == 0 && al16(x) && al16(dva) && (!dvb || al16(dvb)) && al16(dx);
+  const T* X = static_cast<const T*>(x);
+  const T* A = static_cast<const T*>(dva);
+  const T* B = static_cast<const T*>(dvb);
+  T* O = static_cast<T*>(dx);
+  const cudaError_t e =
+      vec ? launch_kernel(synth_layer_backward_kernel<T, true>, dim3(ew_grid(n / E)), dim3(kEwThreads), 0, st, X, g, s,
+                          A, B, O, T_, d)
+          : launch_kernel(synth_layer_backward_kernel<T, false>, dim3(ew_grid(n)), dim3(kEwThreads), 0, st, X, g, s, A,
+                          B, O, T_, d);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_synthetic_layer_backward(const void* x, const float* g, const float* s, const void* dva,
+                                            const void* dvb, void* dx, int64_t T, int d, int dtype,
+                                            cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  return dtype == ATTNRES_BF16 ? launch_synth_bwd_t<bf16_t>(x, g, s, dva, dvb, dx, T, d, stream)
+                               : launch_synth_bwd_t<float>(x, g, s, dva, dvb, dx, T, d, stream);
 }
 
 }  // namespace attnres

@@ -110,6 +110,9 @@ cudaError_t launch_fold(const void* prev, const void* F, void* dst, int64_t n, i
 // out = round(tanh(x * g[c]) * s[c]) over [T, d].
 cudaError_t launch_synthetic_layer(const void* x, const float* g, const float* s, void* out,
                                    int64_t T, int d, int dtype, cudaStream_t stream);
+cudaError_t launch_synthetic_layer_backward(const void* x, const float* g, const float* s, const void* dva,
+                                            const void* dvb, void* dx, int64_t T, int d, int dtype,
+                                            cudaStream_t stream);
 
 // Launch `kern` with programmatic stream serialization allowed (the kernel
 // may start while the previous kernel on the stream finishes; every kernel

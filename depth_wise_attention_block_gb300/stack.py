@@ -22,13 +22,18 @@ import torch
 
 from . import (
     AttnResState,
+    attnres_aggregate,
+    attnres_aggregate_backward,
+    attnres_aggregate_backward_workspace_size,
     attnres_block_step,
+    attnres_fold,
     attnres_interblock,
     attnres_intrablock_step,
     attnres_layer_sources,
     attnres_layer_step,
     attnres_num_sources,
     attnres_synthetic_layer,
+    attnres_synthetic_layer_backward,
 )
 
 
@@ -43,7 +48,7 @@ class StackForward:
 
     def __init__(self, h0, W, G, Sc, num_layers: int, block_size: int, eps: float = 1e-5,
                  keep_weights: bool = True, dev_err: torch.Tensor | None = None, schedule: str = "single"):
-        self.L, self.B = num_layers, block_size
+        self.L, self.B, self.eps = num_layers, block_size, eps
         T, d = h0.shape
         self.T, self.d = T, d
         self.W, self.G, self.Sc = W, G, Sc
@@ -151,3 +156,106 @@ class StackForward:
             if l <= self.L:
                 total += 2 * row + 2 * self.d * 4        # F_l: read r, write F (+ g, s)
         return total
+
+
+class StackBackward:
+    """Gradients of the loss sum(r_out * dr_out) of a StackForward's stack
+    with respect to h_0 and every pseudo-query W[0..L], with the forward
+    recomputed block by block from what the forward keeps (h_0 and the block
+    representations b_1 .. b_N: activation checkpointing at block
+    granularity, [Tutorial] ch. 4.6).
+
+    Per block n, from the last block down:
+      recompute: r_l = attnres_aggregate([h_0, b_1..b_{n-1}, P_l]) for the
+        block's layers, v_l = F_l(r_l), P_{l+1} = P_l + v_l (attnres_fold),
+        keeping every r_l and partial sum P_l;
+      backward, layer by layer from the block's last: dL/dv_l is the
+        gradient of b_n (from later blocks and the final aggregation) plus
+        that of the partial sums of the block's later layers, dL/dr_l =
+        dL/dv_l F_l'(r_l) (attnres_synthetic_layer_backward), and
+        attnres_aggregate_backward (accumulate) adds layer l's gradients into
+        those of h_0, b_1..b_{n-1} and the block's running partial-sum
+        gradient, and writes dW[l-1].
+    The final aggregation's backward (over [h_0, b_1..b_N]) starts it.
+    Gradients are kept in the stack's storage dtype.  Outputs: `dh0` [T, d],
+    `dW` [L+1, d] fp32.
+    """
+
+    def __init__(self, fwd: StackForward):
+        self.fwd = fwd
+        st, T, d, B = fwd.state, fwd.T, fwd.d, fwd.B
+        dt, dev = st.h0.dtype, st.h0.device
+        self.N = -(-fwd.L // B)
+        self.dh0 = torch.empty((T, d), dtype=dt, device=dev)
+        self.gb = [torch.empty((T, d), dtype=dt, device=dev) for _ in range(self.N)]
+        self.gpart = torch.empty((T, d), dtype=dt, device=dev)
+        self.gr = torch.empty((T, d), dtype=dt, device=dev)
+        self.v = torch.empty((T, d), dtype=dt, device=dev)
+        q = min(B, fwd.L)
+        self.R = torch.empty((q, T, d), dtype=dt, device=dev)       # r_l of the block being processed
+        self.P = torch.empty((q, T, d), dtype=dt, device=dev)       # P[i-1]: partial sum read by position i >= 2
+        self.dW = torch.empty((fwd.L + 1, d), dtype=torch.float32, device=dev)
+        nbytes = attnres_aggregate_backward_workspace_size(T, d)
+        self.ws = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=dev)
+        self.graph = None
+
+    def _issue(self, dr_out, stream=None) -> None:
+        f, st = self.fwd, self.fwd.state
+        L, B, eps = f.L, f.B, f.eps
+        b = st.block_reps[: self.N]
+        attnres_aggregate_backward([st.h0] + b, f.W[L], dr_out, [self.dh0] + self.gb, self.dW[L],
+                                   workspace=self.ws, eps=eps, accumulate=False, stream=stream)
+        for n in range(self.N, 0, -1):
+            first, last = (n - 1) * B + 1, min(n * B, L)
+            cached = [st.h0] + b[: n - 1]
+            for layer in range(first, last + 1):
+                i = layer - first + 1
+                srcs = cached + ([self.P[i - 1]] if i >= 2 else [])
+                attnres_aggregate(srcs, f.W[layer - 1], self.R[i - 1], eps=eps, stream=stream)
+                if layer < last:
+                    attnres_synthetic_layer(self.R[i - 1], f.G[layer - 1], f.Sc[layer - 1], self.v, stream=stream)
+                    attnres_fold(self.P[i - 1] if i >= 2 else None, self.v, self.P[i], stream=stream)
+            # the block's partial sums have no gradient yet (one memset)
+            if stream is None:
+                self.gpart.zero_()
+            else:
+                with torch.cuda.stream(stream):
+                    self.gpart.zero_()
+            for layer in range(last, first - 1, -1):
+                i = layer - first + 1
+                attnres_synthetic_layer_backward(self.R[i - 1], f.G[layer - 1], f.Sc[layer - 1], self.gb[n - 1],
+                                                 self.gpart if layer < last else None, self.gr, stream=stream)
+                srcs = cached + ([self.P[i - 1]] if i >= 2 else [])
+                grads = [self.dh0] + self.gb[: n - 1] + ([self.gpart] if i >= 2 else [])
+                attnres_aggregate_backward(srcs, f.W[layer - 1], self.gr, grads, self.dW[layer - 1],
+                                           workspace=self.ws, eps=eps, accumulate=True, stream=stream)
+
+    def run(self, dr_out=None, stream=None):
+        """One backward (replays the captured graph, recorded for the dr_out
+        given to capture(), if there is one); the forward must have run on
+        the same inputs."""
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self._issue(dr_out, stream)
+        return self.dh0, self.dW
+
+    def capture(self, dr_out) -> None:
+        """Record the whole backward for dr_out into a CUDA graph (after one
+        eager run)."""
+        self._issue(dr_out)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._issue(dr_out)
+        self.graph = g
+
+    def launches_per_backward(self) -> int:
+        """Kernel launches (plus one memset per block) of one backward."""
+        L, B, N = self.fwd.L, self.fwd.B, self.N
+        n = 2                                                  # final aggregation backward (+ its dw reduction)
+        for k in range(1, N + 1):
+            q = min(k * B, L) - (k - 1) * B
+            n += q + 2 * (q - 1)                               # recompute: aggregate, body, fold
+            n += q * (1 + 2)                                   # body backward, aggregation backward (+ dw reduction)
+        return n

@@ -295,6 +295,30 @@ int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* 
 int attnres_synthetic_layer(const void* x, const float* g, const float* s, void* out, int64_t T,
                             int d, int dtype, void* stream);
 
+/* ------------------------------------------------------------------------
+ * attnres_synthetic_layer_backward -- gradient of attnres_synthetic_layer
+ * (the stand-in body, not part of the method), for a stack backward:
+ *   grad_x[t,c] = (grad_out_a + grad_out_b)[t,c] * (1 - tanh(x g)^2) * g[c] * s[c]
+ * x: the layer's input [T, d] of dtype; grad_out_a: [T, d] of dtype, the
+ * gradient of the loss with respect to the layer's output; grad_out_b: a
+ * second such term added to it, or NULL; grad_x: [T, d] of dtype (may alias
+ * either gradient input); g, s: [d] fp32.  fp32 math, rounded to dtype.
+ * T = 0 launches nothing and accepts NULL buffers.
+ * ---------------------------------------------------------------------- */
+int attnres_synthetic_layer_backward(const void* x, const float* g, const float* s, const void* grad_out_a,
+                                     const void* grad_out_b, void* grad_x, int64_t T, int d, int dtype,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * attnres_fold -- the block bookkeeping of [Tutorial] ch. 4.3 (Eq. 10) on
+ * plain buffers, without a state: dst = prev + F (fp32 sum, one rounding to
+ * dtype), or dst = F when prev is NULL (a block's first layer output opens
+ * its partial sum).  prev, F, dst: device [T, d] of dtype; elementwise, so
+ * dst may alias prev or F.  Used where the partial sums of a block are kept
+ * per layer (the recomputed forward of a stack backward).
+ * ---------------------------------------------------------------------- */
+int attnres_fold(const void* prev, const void* F, void* dst, int64_t T, int d, int dtype, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* attnres_status_string(int status);
 

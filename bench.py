@@ -369,6 +369,40 @@ def bench_stacks(A, W, dev, peak):
     return out
 
 
+def bench_stack_backward(A, W, dev, peak, reps=5):
+    """The 93-layer prefill stack's backward (gradients of h0 and all 94
+    pseudo-queries, each block's forward recomputed from h0 and the stored
+    block sums), bf16 storage, replayed from a CUDA graph."""
+    from depth_wise_attention_block_gb300.stack import StackBackward, StackForward
+    T = 2048
+    stk = W.stack(T=T, seed=2, device=dev)
+    g = torch.Generator(device=dev).manual_seed(21)
+    dr = torch.randn((T, stk.h0.shape[1]), generator=g, device=dev).to(stk.h0.dtype)
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, keep_weights=False)
+    fwd.run()
+    bwd = StackBackward(fwd)
+    bwd.capture(dr)
+    for _ in range(2):
+        bwd.run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        bwd.run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    by = bwd.bytes_moved()
+    gbs = by / (ms * 1e-3) / 1e9
+    out = {"stack_backward_T2048": {"ms_per_backward": ms, "tokens_per_s": T / (ms * 1e-3), "layers": stk.num_layers,
+                                    "launches_per_backward": bwd.launches_per_backward(), "cuda_graph": True,
+                                    "bytes_per_backward_model": by, "achieved_gbs_model": gbs,
+                                    "frac_of_hbm_peak": gbs / peak}}
+    del bwd, fwd, stk, dr
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_long(A, W, dev, peak, reps=8):
     inp = W.block_T131072_d7168(device=dev)
     T = inp.H.shape[1]
@@ -427,7 +461,8 @@ def run_only(args):
     import depth_wise_attention_block_gb300 as A
     import workloads as W
     peak, _ = hbm_peak()
-    res = {"stacks": bench_stacks, "long": bench_long, "backward": bench_backward}[args.only](A, W, dev, peak)
+    res = {"stacks": bench_stacks, "long": bench_long, "backward": bench_backward,
+           "stack_backward": bench_stack_backward}[args.only](A, W, dev, peak)
     print(json.dumps(res), flush=True)
 
 
@@ -462,6 +497,7 @@ def run_gpu(args):
         extras.update(bench_stacks(A, W, dev, peak))
         extras.update(bench_long(A, W, dev, peak))
         extras.update(bench_backward(A, W, dev, peak))
+        extras.update(bench_stack_backward(A, W, dev, peak))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -508,7 +544,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true", help="skip the stack and long-context workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["stacks", "long", "backward"], help="run one secondary workload alone")
+    ap.add_argument("--only", choices=["stacks", "long", "backward", "stack_backward"],
+                    help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

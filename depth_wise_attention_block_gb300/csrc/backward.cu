@@ -61,16 +61,23 @@ struct BwdParams {
 };
 
 // Producer of the backward ring: rows [dr, h_0 .. h_{S-1}] of each token.
+// Rows per token, in ring order: grad_r, the S sources and, when the
+// gradients accumulate, the S old gradient rows (read back through the ring
+// like the rest, so pass 2 never waits on a plain load).  Pass 2 holds the
+// source slots while it takes the old gradients: with nslots >= S + 1 the
+// first old-gradient row always finds a free slot, and each later one a
+// slot released by an earlier step of pass 2 (slots are reused in order).
+template <bool ACC>
 __device__ __forceinline__ void bwd_produce(const BwdParams& p, BwdShared& sh, uint32_t ring) {
   const int nslots = p.nslots;
-  const int rows = p.S + 1;
+  const int rows = ACC ? 2 * p.S + 1 : p.S + 1;
   uint32_t slot = 0, lap = 0;
   long long issued = 0;
   bool ok = true;
   for (long long t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
     const long long off = t * (long long)p.row_bytes;
     for (int j = 0; j < rows; ++j) {
-      const char* g = (j == 0 ? p.grad_r : p.src[j - 1]) + off;
+      const char* g = (j == 0 ? p.grad_r : j <= p.S ? p.src[j - 1] : p.grad_src[j - 1 - p.S]) + off;
       if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u)) {
         ok = false;
         break;
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_bwd_ring_kernel(const __g
   pdl_wait();  // everything below may read what the previous kernel wrote
 
   if (warp == kRingConsumerWarps) {
-    if (lane == 0) bwd_produce(p, sh, ring);
+    if (lane == 0) bwd_produce<ACC>(p, sh, ring);
     return;
   }
 
@@ -242,8 +249,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_bwd_ring_kernel(const __g
         const float al = __shfl_sync(0xffffffffu, alpha, 3 * s);
         const float be = __shfl_sync(0xffffffffu, beta, 3 * s);
         const uint64_t a2 = f2_pack(as, as), al2 = f2_pack(al, al), nbe2 = f2_pack(-be, -be);
-        uint4 hv[VPT];
+        uint4 hv[VPT], gv[VPT];
         load_row(sl, hv);
+        if (ACC) {
+          // the old gradient row of source s, next in the ring
+          wait_slot(slot, lap & 1u);
+          load_row(slot, gv);
+        }
         char* grow = p.grad_src[s] + t * (long long)p.row_bytes;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_bwd_ring_kernel(const __g
             Vec<T>::pairs(hv[k], h);
             float out[EPV];
             uint64_t old[NP];
-            if (ACC) Vec<T>::pairs(*reinterpret_cast<const uint4*>(grow + (size_t)v * 16), old);
+            if (ACC) Vec<T>::pairs(gv[k], old);
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
               uint64_t dh = f2_fma(a2, drp[k][j], ACC ? old[j] : 0);
@@ -267,6 +279,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_bwd_ring_kernel(const __g
         }
         release(sl);
         if (++sl == (uint32_t)nslots) sl = 0;
+        if (ACC) {
+          release(slot);
+          if (++slot == (uint32_t)nslots) { slot = 0; ++lap; }
+        }
       }
     }
     if (abort) {

@@ -151,30 +151,54 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_backward_kernel(const 
   const long long n = T_ * (long long)d;
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
+    // kUnroll independent vectors of each input in flight per thread before any math
     constexpr int E = Vec16<T>::kElems;
+    constexpr int kUnroll = 4;
     const int vrow = d / E;
     const long long nv = n / E;
     const uint4* X4 = reinterpret_cast<const uint4*>(x);
     const uint4* A4 = reinterpret_cast<const uint4*>(dva);
     const uint4* B4 = reinterpret_cast<const uint4*>(dvb);
     uint4* O4 = reinterpret_cast<uint4*>(dx);
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
-      const int c0 = (int)(i % vrow) * E;
-      float f[E], ga[E], gb[E];
-      Vec16<T>::unpack(X4[i], f);
-      Vec16<T>::unpack(A4[i], ga);
-      if (dvb) {
-        Vec16<T>::unpack(B4[i], gb);
+    for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < nv; i0 += kUnroll * stride) {
+      uint4 xv[kUnroll], av[kUnroll], bv[kUnroll];
 #pragma unroll
-        for (int e = 0; e < E; ++e) ga[e] += gb[e];
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long i = i0 + u * stride;
+        if (i < nv) {
+          xv[u] = X4[i];
+          av[u] = A4[i];
+          if (dvb) bv[u] = B4[i];
+        }
       }
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float gg = __ldg(g + c0 + e), ss = __ldg(s + c0 + e);
-        const float th = tanhf(f[e] * gg);
-        f[e] = ga[e] * (1.f - th * th) * gg * ss;
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long i = i0 + u * stride;
+        if (i < nv) {
+          const int c0 = (int)(i % vrow) * E;
+          float f[E], ga[E];
+          Vec16<T>::unpack(xv[u], f);
+          Vec16<T>::unpack(av[u], ga);
+          if (dvb) {
+            float gb[E];
+            Vec16<T>::unpack(bv[u], gb);
+#pragma unroll
+            for (int e = 0; e < E; ++e) ga[e] += gb[e];
+          }
+#pragma unroll
+          for (int e = 0; e < E; e += 4) {
+            const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + c0 + e));
+            const float4 s4 = __ldg(reinterpret_cast<const float4*>(s + c0 + e));
+            const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float th = tanhf(f[e + k] * gg[k]);
+              f[e + k] = ga[e + k] * (1.f - th * th) * gg[k] * ss[k];
+            }
+          }
+          O4[i] = Vec16<T>::pack(f);
+        }
       }
-      O4[i] = Vec16<T>::pack(f);
     }
   } else {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -246,7 +270,8 @@ static cudaError_t launch_synth_bwd_t(const void* x, const float* g, const float
                                       const void* dvb, void* dx, long long T_, int d, cudaStream_t st) {
   constexpr int E = 16 / (int)sizeof(T);
   const long long n = T_ * (long long)d;
-  const bool vec = d % E == 0 && al16(x) && al16(dva) && (!dvb || al16(dvb)) && al16(dx);
+  // the vector path also reads g and s as float4: they must be 16-byte aligned
+  const bool vec = d % E == 0 && al16(x) && al16(dva) && (!dvb || al16(dvb)) && al16(dx) && al16(g) && al16(s);
   const T* X = static_cast<const T*>(x);
   const T* A = static_cast<const T*>(dva);
   const T* B = static_cast<const T*>(dvb);

@@ -250,6 +250,25 @@ class StackBackward:
             self._issue(dr_out)
         self.graph = g
 
+    def bytes_moved(self) -> int:
+        """Minimum HBM bytes one backward moves: every row each call reads or
+        writes, once (the model behind its achieved bandwidth)."""
+        f = self.fwd
+        L, B, N = f.L, f.B, self.N
+        row = f.T * f.d * f.state.h0.element_size()
+        rows = (N + 2) + (N + 1)                               # final: sources + dr read, grads written
+        for n in range(1, N + 1):
+            q = min(n * B, L) - (n - 1) * B
+            for i in range(1, q + 1):
+                S = n + (1 if i >= 2 else 0)
+                rows += S + 1                                  # recompute: aggregate reads S, writes r
+                if i < q:
+                    rows += 2 + (3 if i >= 2 else 2)           # body: r -> v; fold: (P +) v -> P'
+                rows += (3 if i < q else 2) + 1                # body backward: r, gb (+ gpart) -> gr
+                rows += (2 * S + 1) + S                        # aggregation backward, accumulating
+            rows += 1                                          # memset of the partial-sum gradient
+        return rows * row + (L + 1) * f.d * 4
+
     def launches_per_backward(self) -> int:
         """Kernel launches (plus one memset per block) of one backward."""
         L, B, N = self.fwd.L, self.fwd.B, self.N

@@ -282,6 +282,13 @@ def attnres_fold(prev: torch.Tensor | None, F: torch.Tensor, dst: torch.Tensor, 
     _N.check(rc, "attnres_fold")
 
 
+def attnres_debug_wait_test(wait_limit_ns: int, withhold_row: int) -> None:
+    """Diagnostic: make the ring kernels' bounded waits run out (withhold_row
+    0..7 of every CTA's first token is armed without a copy; waits limited to
+    wait_limit_ns).  (0, -1) restores normal operation."""
+    _N.check(_N.lib.attnres_debug_wait_test(int(wait_limit_ns), int(withhold_row)), "attnres_debug_wait_test")
+
+
 _HOST_STREAMS: dict = {}
 
 

@@ -44,6 +44,7 @@ EXPORTED = (
     "attnres_synthetic_layer",
     "attnres_synthetic_layer_backward",
     "attnres_fold",
+    "attnres_debug_wait_test",
     "attnres_status_string",
     "attnres_last_error",
     "attnres_version",
@@ -93,6 +94,7 @@ def _load() -> ctypes.CDLL:
         "attnres_synthetic_layer": (i32, [vp, vp, vp, vp, i64, i32, i32, vp]),
         "attnres_synthetic_layer_backward": (i32, [vp, vp, vp, vp, vp, vp, i64, i32, i32, vp]),
         "attnres_fold": (i32, [vp, vp, vp, i64, i32, i32, vp]),
+        "attnres_debug_wait_test": (i32, [ctypes.c_uint64, i32]),
         "attnres_status_string": (ctypes.c_char_p, [i32]),
         "attnres_last_error": (ctypes.c_char_p, []),
         "attnres_version": (i32, []),

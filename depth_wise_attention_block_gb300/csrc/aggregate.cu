@@ -37,6 +37,8 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <atomic>
+
 #include "attnres.h"
 #include "device_common.cuh"
 #include "launch.h"
@@ -197,6 +199,21 @@ static cudaError_t launch_generic_t(const GenericParams& gp, int grid, cudaStrea
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+static std::atomic<unsigned long long> g_wait_limit_ns{0};
+static std::atomic<int> g_withhold_row1{0};
+
+void set_debug_wait_test(unsigned long long ns, int withhold_row) {
+  g_wait_limit_ns.store(ns);
+  g_withhold_row1.store(withhold_row + 1);
+}
+
+int debug_withhold_row1() { return g_withhold_row1.load(); }
+
+unsigned long long wait_limit_ns() {
+  const unsigned long long v = g_wait_limit_ns.load();
+  return v ? v : kWaitLimitNs;
+}
+
 bool pdl_enabled() {
   static const bool on = [] {
     const char* v = getenv("ATTNRES_NO_PDL");
@@ -263,6 +280,8 @@ cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
     rp.nslots = nslots;
     rp.eps = a.eps;
     rp.inv_d = 1.0f / (float)a.d;
+    rp.wait_ns = wait_limit_ns();
+    rp.withhold_row1 = debug_withhold_row1();
     if (split_c > 0) {
       *path = kPathRingSplit;
       return launch_ring_split(rp, split_c, fused, in_bf16, out_bf16, di.sm_count, di.max_smem_optin, a.stream);

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
 
   // take this thread's vectors of the next landed row, then release the slot
   auto consume = [&](uint4* dst) {
-    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u)) ok = false;
+    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u, p.wait_ns)) ok = false;
     const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -78,8 +78,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       // after a failed wait the slot holds stale data: harmless, the token is abandoned
       dst[k] = (EXACT || v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
     }
+    // Lane 0 releases the slot only while its own waits have all succeeded:
+    // then this phase completed and its copy landed.  After a wait ran out
+    // the copy may still be in flight, and the slot must not be refilled
+    // under it (the producer then runs out of slots, stops and drains).
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&sh.empty[slot]));
+    if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
     if (++slot == (uint32_t)nslots) {
       slot = 0;
       ++lap;

@@ -56,7 +56,7 @@ __device__ __forceinline__ void split_produce(const SplitParams& sp, RingShared&
       if (j < p.n_stored) g = p.src[j] + off;
       else if (p.fuse_prev && j == p.n_stored) g = p.fuse_prev + off;
       else g = p.fuse_F + off;
-      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u)) {
+      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -132,11 +132,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_split_kernel(const __grid
   uint32_t slot = 0, lap = 0;
   bool ok = true;
   auto consume = [&](uint4& dst) {
-    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u)) ok = false;
+    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u, p.wait_ns)) ok = false;
     const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
     dst = mine ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
+    // Lane 0 releases the slot only while its own waits have all succeeded:
+    // then this phase completed and its copy landed.  After a wait ran out
+    // the copy may still be in flight, and the slot must not be refilled
+    // under it (the producer then runs out of slots, stops and drains).
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&sh.empty[slot]));
+    if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
     if (++slot == (uint32_t)nslots) {
       slot = 0;
       ++lap;

@@ -491,6 +491,12 @@ int attnres_synthetic_layer_backward(const void* x, const float* g, const float*
   return ok();
 }
 
+int attnres_debug_wait_test(uint64_t wait_limit_ns, int withhold_row) {
+  if (withhold_row < -1 || withhold_row > 7) return fail(ATTNRES_EINVAL, "withhold_row %d", withhold_row);
+  set_debug_wait_test((unsigned long long)wait_limit_ns, withhold_row);
+  return ok();
+}
+
 int attnres_fold(const void* prev, const void* F, void* dst, int64_t T, int d, int dtype, void* stream) {
   if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
   if (!size_ok(T, d)) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);

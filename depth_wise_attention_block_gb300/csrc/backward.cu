@@ -44,6 +44,8 @@ struct BwdShared {
 constexpr int kBwdHeaderBytes = (int)((sizeof(BwdShared) + 127) / 128 * 128);
 
 struct BwdParams {
+  unsigned long long wait_ns;  // limit of each main-loop wait (the final drain keeps the default)
+  int withhold_row1;           // bounded-wait test (as RingParams::withhold_row1)
   const char* src[kMaxSources];
   char* grad_src[kMaxSources];
   const char* grad_r;
@@ -78,13 +80,14 @@ __device__ __forceinline__ void bwd_produce(const BwdParams& p, BwdShared& sh, u
     const long long off = t * (long long)p.row_bytes;
     for (int j = 0; j < rows; ++j) {
       const char* g = (j == 0 ? p.grad_r : j <= p.S ? p.src[j - 1] : p.grad_src[j - 1 - p.S]) + off;
-      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u)) {
+      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u, p.wait_ns)) {
         ok = false;
         break;
       }
       const uint32_t full = smem_addr(&sh.full[slot]);
       mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
-      bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+      if (issued + 1 != p.withhold_row1)
+        bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
       ++issued;
       if (++slot == (uint32_t)nslots) {
         slot = 0;
@@ -93,11 +96,7 @@ __device__ __forceinline__ void bwd_produce(const BwdParams& p, BwdShared& sh, u
     }
   }
   if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
-  const long long armed_slots = issued < nslots ? issued : nslots;
-  for (int k = 0; k < armed_slots; ++k) {
-    const long long uses = (issued - 1 - k) / nslots + 1;
-    mbar_wait_bounded(smem_addr(&sh.full[k]), (uint32_t)((uses - 1) & 1));
-  }
+  ring_drain(sh.full, nslots, issued, p.withhold_row1);
 }
 
 template <typename T, int VPT, bool ACC>
@@ -146,11 +145,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_bwd_ring_kernel(const __g
   uint32_t slot = 0, lap = 0;
   bool ok = true;
   auto wait_slot = [&](uint32_t sl, uint32_t parity) {
-    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[sl]), parity)) ok = false;
+    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[sl]), parity, p.wait_ns)) ok = false;
   };
   auto release = [&](uint32_t sl) {
+    // Lane 0 releases the slot only while its own waits have all succeeded:
+    // then this phase completed and its copy landed.  After a wait ran out
+    // the copy may still be in flight, and the slot must not be refilled
+    // under it (the producer then runs out of slots, stops and drains).
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&sh.empty[sl]));
+    if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[sl]));
   };
   auto load_row = [&](uint32_t sl, uint4* dst) {
     const uint32_t base = ring + sl * (uint32_t)p.row_bytes;
@@ -495,6 +498,8 @@ cudaError_t launch_aggregate_backward(const BwdArgs& a) {
   bp.S = a.S;
   bp.eps = a.eps;
   bp.inv_d = 1.0f / (float)a.d;
+  bp.wait_ns = wait_limit_ns();
+  bp.withhold_row1 = debug_withhold_row1();
   bp.row_bytes = (int)row_bytes;
 
   bool ring = a.S <= kBwdSmax && row_bytes % 16 == 0 && al16(a.grad_r);

@@ -116,17 +116,23 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kWaitMaxPolls = 1u << 26;
 
-// Wait until the phase with the given parity of `bar` has completed.
-// Returns false (and stops waiting) once the limit is reached.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Polling after a first try found the phase incomplete (kept out of line:
+// the hot path is the single try in mbar_wait_bounded).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < kWaitMaxPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 31u && global_timer_ns() - t0 > limit_ns) return false;
   }
   return false;
+}
+
+// Wait until the phase with the given parity of `bar` has completed.
+// Returns false (and stops waiting) once the limit is reached.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, limit_ns);
 }
 
 // --------------------------------------------------------- bulk copies ----

@@ -120,6 +120,14 @@ cudaError_t launch_synthetic_layer_backward(const void* x, const float* g, const
 // Set ATTNRES_NO_PDL=1 in the environment to launch plainly.
 bool pdl_enabled();
 
+// The bounded-wait test (attnres_debug_wait_test): the limit of each
+// main-loop wait in the ring kernels (2 s by default; the final drain always
+// keeps 2 s) and 1 + the row each CTA's producer arms without a copy (0 =
+// none).
+unsigned long long wait_limit_ns();
+int debug_withhold_row1();
+void set_debug_wait_test(unsigned long long ns, int withhold_row);
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                           Args&&... args) {

@@ -36,6 +36,9 @@ struct RingShared {
 constexpr int kRingHeaderBytes = (int)((sizeof(RingShared) + 127) / 128 * 128);
 
 struct RingParams {
+  unsigned long long wait_ns;  // limit of each main-loop wait (the final drain keeps the default)
+  int withhold_row1;           // bounded-wait test: 1 + the row of each CTA's first token armed
+                               // without a copy (its waits must run out); 0 = none
   const char* src[kMaxSources];
   const char* fuse_prev;
   const char* fuse_F;
@@ -200,6 +203,19 @@ __device__ __forceinline__ void store_out(char* row, int vec, const float* acc) 
 }
 
 
+// Every issued copy must have landed before a CTA exits: wait on the latest
+// armed phase of each slot (already-consumed phases pass at once).  The
+// one row the bounded-wait test arms without a copy is skipped: its slot is
+// never released (its waits run out), so that phase is still its latest.
+__device__ __forceinline__ void ring_drain(uint64_t* full, int nslots, long long issued, int withhold_row1) {
+  const long long armed_slots = issued < nslots ? issued : nslots;
+  for (int k = 0; k < armed_slots; ++k) {
+    const long long uses = (issued - 1 - k) / nslots + 1;
+    if (uses == 1 && k + 1 == withhold_row1) continue;
+    mbar_wait_bounded(smem_addr(&full[k]), (uint32_t)((uses - 1) & 1));
+  }
+}
+
 // The producer: one thread streams every source row of this CTA's tokens
 // (t = blockIdx.x, blockIdx.x + gridDim.x, ...) into the ring, in order,
 // each row one TMA bulk copy completing on its slot's `full` barrier, after
@@ -222,13 +238,15 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
       else if (p.fuse_prev && j == p.n_stored) g = p.fuse_prev + off;
       else g = p.fuse_F + off;
       // first lap: parity 1 of a fresh barrier counts as complete
-      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u)) {
+      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u, p.wait_ns)) {
         ok = false;
         break;
       }
       const uint32_t full = smem_addr(&sh.full[slot]);
       mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
-      bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+      // the bounded-wait test arms one row of the first token without its copy
+      if (issued + 1 != p.withhold_row1)
+        bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
       ++issued;
       if (++slot == (uint32_t)nslots) {
         slot = 0;
@@ -237,13 +255,7 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
     }
   }
   if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
-  // Every issued copy must have landed before this CTA exits: wait on the
-  // latest armed phase of each slot (already-consumed phases pass at once).
-  const long long armed_slots = issued < nslots ? issued : nslots;
-  for (int k = 0; k < armed_slots; ++k) {
-    const long long uses = (issued - 1 - k) / nslots + 1;
-    mbar_wait_bounded(smem_addr(&sh.full[k]), (uint32_t)((uses - 1) & 1));
-  }
+  ring_drain(sh.full, nslots, issued, p.withhold_row1);
 }
 
 // Launch of the multi-group kernel (aggregate_multi.cu).

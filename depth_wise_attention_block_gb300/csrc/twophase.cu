@@ -65,15 +65,19 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
 #pragma unroll
     for (int s = 0; s < kRingSmax; ++s) {
       if (s < S) {
-        if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u)) ok = false;
+        if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u, p.wait_ns)) ok = false;
         const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           const int v = tid + k * kRingConsumers;
           x[s][k] = (EXACT || v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
         }
+        // Lane 0 releases the slot only while its own waits have all succeeded:
+        // then this phase completed and its copy landed.  After a wait ran out
+        // the copy may still be in flight, and the slot must not be refilled
+        // under it (the producer then runs out of slots, stops and drains).
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh.empty[slot]));
+        if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
         if (++slot == (uint32_t)nslots) {
           slot = 0;
           ++lap;
@@ -374,6 +378,8 @@ cudaError_t launch_interblock(const InterArgs& a) {
   rp.out_row_bytes = a.d * 4;
   rp.eps = a.eps;
   rp.inv_d = 1.0f / (float)a.d;
+  rp.wait_ns = wait_limit_ns();
+  rp.withhold_row1 = debug_withhold_row1();
   int nslots = (di.max_smem_optin - kRingHeaderBytes) / row_bytes;
   if (nslots > kRingMaxSlots) nslots = kRingMaxSlots;
   if (nslots < 1) return cudaErrorInvalidValue;

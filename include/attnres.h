@@ -319,6 +319,27 @@ int attnres_synthetic_layer_backward(const void* x, const float* g, const float*
  * ---------------------------------------------------------------------- */
 int attnres_fold(const void* prev, const void* F, void* dst, int64_t T, int d, int dtype, void* stream);
 
+/* ------------------------------------------------------------------------
+ * attnres_debug_wait_test -- a diagnostic with no counterpart in the pages:
+ * makes the bounded waits of the ring kernels launched afterwards from this
+ * process run out on a healthy GPU, so that their timeout path can be tested
+ * without a fault.
+ *   wait_limit_ns  limit of every main-loop wait (a ring slot's landing or
+ *                  release); 0 = the default, 2 s.  The drain at a kernel's
+ *                  exit always waits up to 2 s for the copies it issued.
+ *   withhold_row   0..7: every CTA's producer arms that row of its first
+ *                  token but issues no copy for it, so the consumers' wait
+ *                  on it runs out after wait_limit_ns; -1 = none.
+ * Expected effect: ATTNRES_DEVERR_WAIT_TIMEOUT in dev_err, NaN outputs for
+ * the abandoned token, the kernel returns (no slot is refilled under a copy
+ * in flight; its copies are drained), the context stays usable.  Outputs of
+ * kernels launched in this mode are not meaningful.  (0, -1) restores
+ * normal operation.  Process-wide; not for use while other threads launch.
+ * The cluster-split variant's producer ignores withhold_row.
+ * Returns ATTNRES_OK, or ATTNRES_EINVAL for withhold_row outside -1..7.
+ * ---------------------------------------------------------------------- */
+int attnres_debug_wait_test(uint64_t wait_limit_ns, int withhold_row);
+
 /* Human-readable name of a status code (static string). */
 const char* attnres_status_string(int status);
 

@@ -1,0 +1,116 @@
+"""The timeout path of the bounded waits, exercised on a healthy GPU.
+
+attnres_debug_wait_test(limit, row) makes every CTA's producer arm one row
+of its first token without issuing its copy, and limits the main-loop
+waits: the consumers' wait on that row runs out.  The kernel must then set
+ATTNRES_DEVERR_WAIT_TIMEOUT, write NaN for the token it abandons, leave the
+timed-out slot unreleased (no copy is ever issued into it again), stop its
+producer, drain every copy it did issue, and return; after (0, -1) restores
+normal operation the same call must give correct results.  Nothing here
+faults or hangs a GPU: every wait is bounded and every issued copy targets
+valid memory and is waited for before the CTA exits.
+"""
+import pytest
+import torch
+
+import workloads as W
+from tests.parity import check_weights, oracle_aggregate, to64
+
+pytestmark = pytest.mark.gpu
+
+LIMIT_NS = 1_000_000   # 1 ms: far above any healthy copy's latency
+
+
+@pytest.fixture(scope="module")
+def A():
+    import depth_wise_attention_block_gb300 as A
+    return A
+
+
+@pytest.fixture(scope="module")
+def TIMEOUT_BIT(A):
+    return A.ATTNRES_DEVERR_WAIT_TIMEOUT
+
+
+@pytest.fixture
+def withheld(A):
+    A.attnres_debug_wait_test(LIMIT_NS, 0)
+    try:
+        yield
+    finally:
+        A.attnres_debug_wait_test(0, -1)
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def test_aggregate_times_out_and_recovers(A, TIMEOUT_BIT):
+    inp = W.block_T4096_d7168(device="cuda")
+    r = torch.zeros((4096, 7168), dtype=torch.bfloat16, device="cuda")
+    a = torch.zeros((4096, 9), device="cuda")
+    err = _err()
+    A.attnres_debug_wait_test(LIMIT_NS, 0)
+    try:
+        A.attnres_aggregate(inp.H, inp.w, r, a, dev_err=err)
+        torch.cuda.synchronize()
+    finally:
+        A.attnres_debug_wait_test(0, -1)
+    assert int(err.item()) & TIMEOUT_BIT
+    # one CTA per SM; each abandons its first token (NaN) and writes nothing after it
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    assert torch.isnan(r[:n].float()).all() and torch.isnan(a[:n]).all()
+    assert (r[n:] == 0).all() and (a[n:] == 0).all()
+    # normal operation again: no error, correct weights
+    err2 = _err()
+    A.attnres_aggregate(inp.H, inp.w, r, a, dev_err=err2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == 0
+    idx = torch.arange(0, 4096, 97, device="cuda")
+    _, a_ref, _, _ = oracle_aggregate(inp.H[:, idx].contiguous(), inp.w, 1e-5)
+    check_weights(to64(a[idx]), a_ref)
+
+
+def test_multi_group_times_out(A, TIMEOUT_BIT, withheld):
+    inp = W.block_bf16(T=600, d=7168, seed=3, device="cuda", num_blocks=10)
+    H = inp.H[:12].contiguous()
+    r = torch.zeros((600, 7168), dtype=torch.bfloat16, device="cuda")
+    err = _err()
+    A.attnres_aggregate(H, inp.w, r, None, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & TIMEOUT_BIT
+    assert torch.isnan(r[0].float()).all()
+
+
+def test_fused_stack_times_out(A, TIMEOUT_BIT, withheld):
+    from depth_wise_attention_block_gb300.stack import StackForward
+    stk = W.stack(T=256, num_layers=14, block_size=12, seed=9, device="cuda")
+    err = _err()
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, 14, 12, dev_err=err, keep_weights=False)
+    fwd.run()
+    torch.cuda.synchronize()
+    assert int(err.item()) & TIMEOUT_BIT
+
+
+def test_backward_times_out_and_recovers(A, TIMEOUT_BIT):
+    inp = W.block_bf16(T=1024, d=7168, seed=4, device="cuda")
+    dr = torch.randn((1024, 7168), device="cuda").to(torch.bfloat16)
+    gH = torch.zeros_like(inp.H)
+    gw = torch.zeros(7168, device="cuda")
+    err = _err()
+    A.attnres_debug_wait_test(LIMIT_NS, 0)
+    try:
+        A.attnres_aggregate_backward(inp.H, inp.w, dr, gH, gw, dev_err=err)
+        torch.cuda.synchronize()
+    finally:
+        A.attnres_debug_wait_test(0, -1)
+    assert int(err.item()) & TIMEOUT_BIT
+    err2 = _err()
+    A.attnres_aggregate_backward(inp.H, inp.w, dr, gH, gw, dev_err=err2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == 0 and torch.isfinite(gw).all()
+
+
+def test_wait_test_rejects_bad_rows(A):
+    with pytest.raises(Exception):
+        A.attnres_debug_wait_test(LIMIT_NS, 8)

@@ -21,15 +21,22 @@
 //      in flight.  Dot products and sums of squares for all S sources are
 //      reduced with a warp reduce-scatter and one cross-warp step (one named
 //      barrier per token); the weighted sum is then formed from registers.
-//      Every source byte is read from HBM exactly once.  The shared layout,
-//      vector packing and producer live in ring_common.cuh.
+//      Every source byte is read from HBM exactly once.  The kernel template
+//      is in ring_kernel.cuh (bf16 rows of d = 7168 get one instantiation
+//      per source count, ring_fixed_s.cu / ring_fixed_s_fused.cu); the
+//      shared layout, vector packing and producer live in ring_common.cuh.
+//      This file holds the dispatch and the generic kernel.
 //
 //  agg_ring_multi_kernel (aggregate_multi.cu: 10 <= S <= 128, same rows):
-//      the same ring, sources taken in groups of 9 with an online softmax.
+//      the same ring, sources taken in groups of 6 or 9 with an online
+//      softmax.
+//
+//  agg_split_kernel (aggregate_split.cu, opt-in with ATTNRES_SPLIT=1): few
+//      tokens, each shared by a thread-block cluster of 2-8 CTAs.
 //
 //  agg_generic_kernel  (everything else: any d, any pointer alignment, fp32
-//      rows too wide for registers).  One CTA per token, plain loads, two passes over the
-//      token's rows (the second mostly from L2).
+//      rows too wide for registers).  One CTA per token, plain loads, two
+//      passes over the token's rows (the second mostly from L2).
 //
 // Both can fuse the block bookkeeping: the last source is formed on the fly
 // as round(prev + F) (or F), written out as the new partial sum / block

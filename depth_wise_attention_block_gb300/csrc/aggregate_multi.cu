@@ -1,7 +1,7 @@
 // Depth-wise attention over MORE than 9 sources per token (Full AttnRes:
 // block size 1 gives layer l its l sources, up to 94 for 93 layers; Kimi K3
 // chaptered tutorial, ch. 4.2 Eq. 8-9).  Same ring design as the 9-source
-// kernel in aggregate.cu (persistent CTA per SM, TMA bulk copies of source
+// kernel in ring_kernel.cuh (persistent CTA per SM, TMA bulk copies of source
 // rows into a shared-memory ring, consumer threads owning fixed 16-byte
 // vectors), but a token's sources are taken in groups of up to 9 and folded
 // into the output with an online softmax (tutorial, ch. 4.4: a running

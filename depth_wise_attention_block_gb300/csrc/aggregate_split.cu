@@ -1,19 +1,20 @@
 // Depth-wise attention for few tokens (decode: T = 64 leaves most SMs idle
 // with one CTA per token), an opt-in variant: a thread-block cluster of C
 // CTAs shares each token, every CTA streaming and owning one channel slice
-// of every source row.  The math is that of agg_ring_kernel (aggregate.cu); per token each
-// CTA reduces its slice's dot(w, h_s) and sum(h_s^2) partials as usual,
-// then the C slice totals are exchanged through distributed shared memory:
-// warp 0 stores its 2S totals into every CTA's exchange buffer of the
-// cluster and arrives (release, cluster scope) on each CTA's exchange
-// mbarrier (C arrivals complete it, its own included); every consumer warp
-// waits on its own CTA's mbarrier and sums the C contributions in rank
-// order, so all CTAs form bit-identical logits and weights, then writes its
-// slice of r.  The exchange buffers and mbarriers are double-buffered: a
-// peer overwrites buffer b only after this CTA's arrival for the next token,
-// which comes after all of its warps have read buffer b.  A cluster barrier
-// after the set-up and another before exit keep every CTA alive while a peer
-// may still write into it.  No multicast.
+// of every source row.  The math is that of agg_ring_kernel
+// (ring_kernel.cuh); per token each CTA reduces its slice's dot(w, h_s) and
+// sum(h_s^2) partials as usual, then the C slice totals are exchanged
+// through distributed shared memory: lane 0 of warp 0 stores its CTA's 2S
+// totals into every CTA's exchange buffer of the cluster and arrives
+// (release, cluster scope) on each CTA's exchange mbarrier (C arrivals
+// complete it, its own included); every consumer warp waits on its own CTA's
+// mbarrier and sums the C contributions in rank order, so all CTAs form
+// bit-identical logits and weights, then writes its slice of r.  The
+// exchange buffers and mbarriers are double-buffered: a peer overwrites
+// buffer b only after this CTA's arrival for the next token, which comes
+// after all of its warps have read buffer b.  A cluster barrier after the
+// set-up and another before exit keep every CTA alive while a peer may still
+// write into it.  No multicast.
 #include <math.h>
 #include <stdlib.h>
 

@@ -4,7 +4,7 @@
 //                     tutorial, ch. 4.3 Eq. 10 and ch. 4.6): the output v of
 //                     a layer is added to the running partial sum of its
 //                     block, dst = round(prev + v), or copied when the
-//                     partial sum is empty.  The fused path in aggregate.cu
+//                     partial sum is empty.  The fused path of the ring kernel (ring_kernel.cuh)
 //                     does the same arithmetic inside the aggregation.
 //  synth_layer_kernel the stand-in layer body F(x) = tanh(x * g) * s used to
 //                     drive a stack without trained weights.

@@ -1,8 +1,9 @@
-// Pieces shared by the two ring kernels of libattnres (aggregate.cu: one
+// Pieces shared by the ring kernels of libattnres (ring_kernel.cuh: one
 // group of at most 9 sources per token; aggregate_multi.cu: any number of
-// sources in groups of 9 with an online softmax): the shared-memory layout,
-// the kernel parameters, 16-byte vector packing, the warp reduce-scatter of
-// the per-source partial sums, output stores, and the TMA producer.
+// sources in groups with an online softmax; aggregate_split.cu and
+// twophase.cu: variants): the shared-memory layout, the kernel parameters,
+// 16-byte vector packing, the warp reduce-scatter of the per-source partial
+// sums, output stores, the TMA producer and its drain.
 #pragma once
 
 #include "attnres.h"

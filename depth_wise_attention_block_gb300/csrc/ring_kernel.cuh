@@ -2,7 +2,7 @@
 // aggregate.cu (source count read at run time) and the translation units
 // that instantiate it once per fixed source count (ring_fixed_s.cu,
 // ring_fixed_s_fused.cu: bf16 rows of d = 7168, 1 <= S <= 9).  The
-// arithmetic and the ring protocol are described in aggregate.cu.
+// arithmetic and the ring protocol are described at the top of aggregate.cu.
 #pragma once
 
 #include <math.h>

@@ -122,6 +122,23 @@ def test_shapes(lib, T, d, S, sdt, odt):
         assert torch.equal(r.float(), H[0].float()) and torch.equal(a, torch.ones_like(a))
 
 
+def test_rows_beyond_2_gib_use_64_bit_offsets(lib):
+    # T = 160000 bf16 rows of d = 7168: a source spans 2.29 GB, so the later
+    # tokens' rows start beyond 2^31 bytes (64-bit offsets in every kernel
+    # address); the last tokens are checked against the oracle
+    T, d = 160000, 7168
+    g = torch.Generator(device="cuda").manual_seed(17)
+    H = torch.empty((2, T, d), dtype=torch.bfloat16, device="cuda")
+    for s in range(2):
+        H[s].normal_(generator=g).mul_(1.0 + s)
+    w = torch.randn(d, generator=g, device="cuda") / d ** 0.5
+    r, a = _run(lib, H, w, torch.bfloat16)
+    tail = torch.arange(T - 300, T, device="cuda")
+    _compare(H[:, tail].contiguous(), w, r[tail], a[tail], torch.bfloat16)
+    del H, r, a
+    torch.cuda.empty_cache()
+
+
 def test_split_matches_one_cta_per_token(lib):
     # the first 64 tokens alone take the cluster kernel, all 4096 the
     # one-CTA-per-token ring: same values up to the order of fp32 sums

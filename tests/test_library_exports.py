@@ -151,3 +151,50 @@ def test_aggregate_rejects_bad_arguments_before_any_launch(native):
     assert call(T=0) == 0
     assert agg(None, 3, 0, 8, 1, None, 1e-5, None, 1, None, None, None) == native.ATTNRES_EINVAL  # sources list
     assert agg(src, 3, 0, 8, 1, None, 1e-5, None, 1, None, None, None) == 0
+
+
+def test_backward_rejects_bad_arguments_before_any_launch(native):
+    bwd = native.lib.attnres_aggregate_backward
+    src = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    grads = (ctypes.c_void_p * 2)(0x3000, 0x4000)
+    ok_args = dict(src=src, S=2, T=4, d=8, dt=1, w=0x5000, eps=1e-5, dr=0x6000, g=grads, acc=0, gw=0x7000,
+                   ws=0x8000, wsb=1 << 20)
+
+    def call(**kw):
+        a = {**ok_args, **kw}
+        return bwd(a["src"], a["S"], a["T"], a["d"], a["dt"], a["w"], a["eps"], a["dr"], a["g"], a["acc"], a["gw"],
+                   a["ws"], a["wsb"], None, None)
+
+    assert call(S=0) == native.ATTNRES_EINVAL
+    assert call(S=129) == native.ATTNRES_ERANGE
+    assert call(dt=2) == native.ATTNRES_EDTYPE
+    assert call(d=0) == native.ATTNRES_EINVAL
+    assert call(gw=None) == native.ATTNRES_EINVAL
+    assert call(acc=2) == native.ATTNRES_EINVAL
+    assert call(dr=None) == native.ATTNRES_EINVAL
+    assert call(ws=None) == native.ATTNRES_EINVAL
+    assert call(ws=0x8002) == native.ATTNRES_EINVAL                        # workspace not 4-byte aligned
+    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x1000)) == native.ATTNRES_EINVAL   # grad aliases a source
+    assert b"aliases" in native.lib.attnres_last_error()
+    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x3000)) == native.ATTNRES_EINVAL   # two grads alias
+    assert call(src=None) == native.ATTNRES_EINVAL
+
+
+def test_fold_and_stand_in_backward_reject_bad_arguments(native):
+    fold = native.lib.attnres_fold
+    assert fold(0x1000, None, 0x2000, 4, 8, 1, None) == native.ATTNRES_EINVAL        # F is NULL
+    assert fold(0x1000, 0x3000, None, 4, 8, 1, None) == native.ATTNRES_EINVAL        # dst is NULL
+    assert fold(0x1000, 0x3000, 0x2000, 4, 8, 7, None) == native.ATTNRES_EDTYPE
+    assert fold(0x1000, 0x3000, 0x2000, -1, 8, 1, None) == native.ATTNRES_EINVAL
+    assert fold(None, None, None, 0, 8, 1, None) == 0                                # T = 0: nothing to do
+    sb = native.lib.attnres_synthetic_layer_backward
+    assert sb(0x1000, 0x2000, 0x3000, None, None, 0x4000, 4, 8, 1, None) == native.ATTNRES_EINVAL
+    assert sb(0x1000, None, 0x3000, 0x5000, None, 0x4000, 4, 8, 1, None) == native.ATTNRES_EINVAL
+    assert sb(0x1000, 0x2000, 0x3000, 0x5000, None, 0x4000, 4, 8, 3, None) == native.ATTNRES_EDTYPE
+    assert sb(0x1000, 0x2000, 0x3000, 0x5000, None, 0x4000, 4, 0, 1, None) == native.ATTNRES_EINVAL
+
+
+def test_debug_wait_test_checks_its_row(native):
+    assert native.lib.attnres_debug_wait_test(0, 8) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_debug_wait_test(0, -2) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_debug_wait_test(0, -1) == 0                           # normal operation

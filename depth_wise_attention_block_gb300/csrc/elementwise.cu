@@ -100,37 +100,42 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, con
   const long long n = T_ * (long long)d;
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
-    // kUnroll independent 16-byte loads in flight per thread before any math
+    // A thread owns one 16-byte channel vector (its g and s stay in
+    // registers) and walks down the tokens, kUnroll rows in flight at a
+    // time; consecutive threads take consecutive vectors of a row.
     constexpr int E = Vec16<T>::kElems;
     constexpr int kUnroll = 4;
     const int vrow = d / E;  // vectors per row (d % E == 0 here)
-    const long long nv = n / E;
-    const uint4* X4 = reinterpret_cast<const uint4*>(x);
-    uint4* O4 = reinterpret_cast<uint4*>(out);
-    for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < nv; i0 += kUnroll * stride) {
-      uint4 v[kUnroll];
+    const int cv = blockIdx.x * blockDim.x + threadIdx.x;
+    if (cv < vrow) {
+      float gg[E], ss[E];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const long long i = i0 + u * stride;
-        if (i < nv) v[u] = X4[i];
+      for (int e = 0; e < E; e += 4) {
+        const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + cv * E + e));
+        const float4 s4 = __ldg(reinterpret_cast<const float4*>(s + cv * E + e));
+        gg[e] = g4.x; gg[e + 1] = g4.y; gg[e + 2] = g4.z; gg[e + 3] = g4.w;
+        ss[e] = s4.x; ss[e + 1] = s4.y; ss[e + 2] = s4.z; ss[e + 3] = s4.w;
       }
+      const uint4* X4 = reinterpret_cast<const uint4*>(x) + cv;
+      uint4* O4 = reinterpret_cast<uint4*>(out) + cv;
+      const long long rstep = gridDim.y;
+      for (long long t0 = blockIdx.y; t0 < T_; t0 += kUnroll * rstep) {
+        uint4 v[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const long long i = i0 + u * stride;
-        if (i < nv) {
-          const int c0 = (int)(i % vrow) * E;
-          float f[E], gg[E], ss[E];
-          Vec16<T>::unpack(v[u], f);
+        for (int u = 0; u < kUnroll; ++u) {
+          const long long t = t0 + u * rstep;
+          if (t < T_) v[u] = X4[t * vrow];
+        }
 #pragma unroll
-          for (int e = 0; e < E; e += 4) {
-            const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + c0 + e));
-            const float4 s4 = __ldg(reinterpret_cast<const float4*>(s + c0 + e));
-            gg[e] = g4.x; gg[e + 1] = g4.y; gg[e + 2] = g4.z; gg[e + 3] = g4.w;
-            ss[e] = s4.x; ss[e + 1] = s4.y; ss[e + 2] = s4.z; ss[e + 3] = s4.w;
+        for (int u = 0; u < kUnroll; ++u) {
+          const long long t = t0 + u * rstep;
+          if (t < T_) {
+            float f[E];
+            Vec16<T>::unpack(v[u], f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[e] = tanhf(f[e] * gg[e]) * ss[e];
+            O4[t * vrow] = Vec16<T>::pack(f);
           }
-#pragma unroll
-          for (int e = 0; e < E; ++e) f[e] = tanhf(f[e] * gg[e]) * ss[e];
-          O4[i] = Vec16<T>::pack(f);
         }
       }
     }
@@ -151,52 +156,56 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_backward_kernel(const 
   const long long n = T_ * (long long)d;
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
-    // kUnroll independent vectors of each input in flight per thread before any math
+    // as synth_layer_kernel: one channel vector per thread, down the tokens
     constexpr int E = Vec16<T>::kElems;
     constexpr int kUnroll = 4;
     const int vrow = d / E;
-    const long long nv = n / E;
-    const uint4* X4 = reinterpret_cast<const uint4*>(x);
-    const uint4* A4 = reinterpret_cast<const uint4*>(dva);
-    const uint4* B4 = reinterpret_cast<const uint4*>(dvb);
-    uint4* O4 = reinterpret_cast<uint4*>(dx);
-    for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < nv; i0 += kUnroll * stride) {
-      uint4 xv[kUnroll], av[kUnroll], bv[kUnroll];
+    const int cv = blockIdx.x * blockDim.x + threadIdx.x;
+    if (cv < vrow) {
+      float gg[E], ss[E];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const long long i = i0 + u * stride;
-        if (i < nv) {
-          xv[u] = X4[i];
-          av[u] = A4[i];
-          if (dvb) bv[u] = B4[i];
-        }
+      for (int e = 0; e < E; e += 4) {
+        const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + cv * E + e));
+        const float4 s4 = __ldg(reinterpret_cast<const float4*>(s + cv * E + e));
+        gg[e] = g4.x; gg[e + 1] = g4.y; gg[e + 2] = g4.z; gg[e + 3] = g4.w;
+        ss[e] = s4.x; ss[e + 1] = s4.y; ss[e + 2] = s4.z; ss[e + 3] = s4.w;
       }
+      const uint4* X4 = reinterpret_cast<const uint4*>(x) + cv;
+      const uint4* A4 = reinterpret_cast<const uint4*>(dva) + cv;
+      const uint4* B4 = dvb ? reinterpret_cast<const uint4*>(dvb) + cv : nullptr;
+      uint4* O4 = reinterpret_cast<uint4*>(dx) + cv;
+      const long long rstep = gridDim.y;
+      for (long long t0 = blockIdx.y; t0 < T_; t0 += kUnroll * rstep) {
+        uint4 xv[kUnroll], av[kUnroll], bv[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const long long i = i0 + u * stride;
-        if (i < nv) {
-          const int c0 = (int)(i % vrow) * E;
-          float f[E], ga[E];
-          Vec16<T>::unpack(xv[u], f);
-          Vec16<T>::unpack(av[u], ga);
-          if (dvb) {
-            float gb[E];
-            Vec16<T>::unpack(bv[u], gb);
-#pragma unroll
-            for (int e = 0; e < E; ++e) ga[e] += gb[e];
+        for (int u = 0; u < kUnroll; ++u) {
+          const long long t = t0 + u * rstep;
+          if (t < T_) {
+            xv[u] = X4[t * vrow];
+            av[u] = A4[t * vrow];
+            if (B4) bv[u] = B4[t * vrow];
           }
+        }
 #pragma unroll
-          for (int e = 0; e < E; e += 4) {
-            const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + c0 + e));
-            const float4 s4 = __ldg(reinterpret_cast<const float4*>(s + c0 + e));
-            const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+        for (int u = 0; u < kUnroll; ++u) {
+          const long long t = t0 + u * rstep;
+          if (t < T_) {
+            float f[E], ga[E];
+            Vec16<T>::unpack(xv[u], f);
+            Vec16<T>::unpack(av[u], ga);
+            if (B4) {
+              float gb[E];
+              Vec16<T>::unpack(bv[u], gb);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float th = tanhf(f[e + k] * gg[k]);
-              f[e + k] = ga[e + k] * (1.f - th * th) * gg[k] * ss[k];
+              for (int e = 0; e < E; ++e) ga[e] += gb[e];
             }
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const float th = tanhf(f[e] * gg[e]);
+              f[e] = ga[e] * (1.f - th * th) * gg[e] * ss[e];
+            }
+            O4[t * vrow] = Vec16<T>::pack(f);
           }
-          O4[i] = Vec16<T>::pack(f);
         }
       }
     }
@@ -214,6 +223,22 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_backward_kernel(const 
 // ---------------------------------------------------------------- launch --
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Grid of the channel-vector kernels: x covers the vrow vectors of a row
+// with kColThreads threads per block, y strides over the tokens, sized to
+// fill every SM at full occupancy.
+constexpr int kColThreads = 128;
+
+static dim3 col_grid(int vrow, long long T_) {
+  DeviceInfo di;
+  if (device_info(&di) != cudaSuccess) di.sm_count = 1;
+  const int gx = (vrow + kColThreads - 1) / kColThreads;
+  long long gy = (long long)di.sm_count * (2048 / kColThreads) / gx;
+  if (gy > T_) gy = T_;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  return dim3(gx, (unsigned)gy);
+}
 
 static int ew_grid(long long work_items) {
   DeviceInfo di;
@@ -253,7 +278,7 @@ static cudaError_t launch_synth_t(const void* x, const float* g, const float* s,
   const T* X = static_cast<const T*>(x);
   T* O = static_cast<T*>(out);
   const cudaError_t e =
-      vec ? launch_kernel(synth_layer_kernel<T, true>, dim3(ew_grid(n / E)), dim3(kEwThreads), 0, st, X, g, s, O, T_, d)
+      vec ? launch_kernel(synth_layer_kernel<T, true>, col_grid(d / E, T_), dim3(kColThreads), 0, st, X, g, s, O, T_, d)
           : launch_kernel(synth_layer_kernel<T, false>, dim3(ew_grid(n)), dim3(kEwThreads), 0, st, X, g, s, O, T_, d);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -277,7 +302,7 @@ static cudaError_t launch_synth_bwd_t(const void* x, const float* g, const float
   const T* B = static_cast<const T*>(dvb);
   T* O = static_cast<T*>(dx);
   const cudaError_t e =
-      vec ? launch_kernel(synth_layer_backward_kernel<T, true>, dim3(ew_grid(n / E)), dim3(kEwThreads), 0, st, X, g, s,
+      vec ? launch_kernel(synth_layer_backward_kernel<T, true>, col_grid(d / E, T_), dim3(kColThreads), 0, st, X, g, s,
                           A, B, O, T_, d)
           : launch_kernel(synth_layer_backward_kernel<T, false>, dim3(ew_grid(n)), dim3(kEwThreads), 0, st, X, g, s, A,
                           B, O, T_, d);

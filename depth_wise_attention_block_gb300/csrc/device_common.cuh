@@ -116,9 +116,8 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kWaitMaxPolls = 1u << 26;
 
-// Polling after a first try found the phase incomplete (kept out of line:
-// the hot path is the single try in mbar_wait_bounded).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+// Polling after a first try found the phase incomplete.
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < kWaitMaxPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -133,6 +132,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, limit_ns);
+}
+
+// As mbar_wait_bounded, with the limit read from shared memory (written once
+// at set-up) only when the first try finds the phase incomplete: no register
+// holds it through the caller's loop.
+__device__ __forceinline__ bool mbar_wait_bounded_sh(uint32_t bar, uint32_t parity, const uint64_t* limit_smem) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, *reinterpret_cast<const volatile uint64_t*>(limit_smem));
 }
 
 // --------------------------------------------------------- bulk copies ----

@@ -32,6 +32,7 @@ struct RingShared {
   // indexed by i & 1 so a fast warp flagging iteration i+1 cannot be seen
   // by a slow warp still reading the flag of iteration i
   int abort_flag[2];
+  uint64_t wait_ns;  // copy of RingParams::wait_ns (read by the consumers' slow waits)
   float zbuf[kMaxSources];  // logits of the token in flight (multi-group kernel)
 };
 constexpr int kRingHeaderBytes = (int)((sizeof(RingShared) + 127) / 128 * 128);
@@ -285,6 +286,7 @@ __device__ __forceinline__ void ring_init(const RingParams& p, RingShared& sh) {
     }
     sh.abort_flag[0] = 0;
     sh.abort_flag[1] = 0;
+    sh.wait_ns = p.wait_ns;
     mbar_fence_init();
   }
 }

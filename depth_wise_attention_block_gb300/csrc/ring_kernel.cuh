@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
 
   // take this thread's vectors of the next landed row, then release the slot
   auto consume = [&](uint4* dst) {
-    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u, p.wait_ns)) ok = false;
+    if (ok && !mbar_wait_bounded_sh(smem_addr(&sh.full[slot]), lap & 1u, &sh.wait_ns)) ok = false;
     const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {

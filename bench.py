@@ -31,6 +31,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -166,6 +167,20 @@ class ClockSampler:
                 "source": "nvml" if self._nvml is not None else "nvidia-smi"}
 
 
+def host_info() -> dict:
+    """Host cores, machine and NVIDIA driver version (read-only NVML query)."""
+    info = {"cores": os.cpu_count(), "machine": platform.machine(), "driver": None}
+    try:
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() == 0:
+            buf = ctypes.create_string_buffer(96)
+            if nv.nvmlSystemGetDriverVersion(buf, 96) == 0:
+                info["driver"] = buf.value.decode()
+    except Exception:
+        pass
+    return info
+
+
 # ------------------------------------------------------------------ peaks ---
 
 def hbm_peak():
@@ -201,22 +216,45 @@ def profiled_traffic():
 
 # ------------------------------------------------------------- CPU oracle ---
 
-def time_oracle(H_cpu: torch.Tensor, w_cpu: torch.Tensor, budget_s: float, chunk: int = 64):
+def time_oracle(H_cpu: torch.Tensor, w_cpu: torch.Tensor, budget_s: float, chunk: int = 64, keep: int = 0):
     """Run the fp64 oracle over consecutive token chunks of the workload for
-    about `budget_s` seconds; returns (tokens, seconds)."""
+    about `budget_s` seconds; returns (tokens, seconds, outputs), outputs
+    holding the oracle's (r, a) of the first `keep` tokens (for the parity
+    figures of the bench line)."""
     import oracle as O
     w64 = w_cpu.double().numpy()
     T = H_cpu.shape[1]
     tokens, t0 = 0, time.perf_counter()
     start = 0
+    kept_r, kept_a = [], []
     while True:
         h = H_cpu[:, start:start + chunk].double().numpy()
-        O.depth_attention(h, w64)
+        r, a = O.depth_attention(h, w64)
+        if tokens < keep:
+            kept_r.append(r)
+            kept_a.append(a)
         tokens += h.shape[1]
         start = (start + chunk) % T
         el = time.perf_counter() - t0
         if el >= budget_s:
-            return tokens, el
+            out = (np.concatenate(kept_r)[:keep], np.concatenate(kept_a)[:keep]) if kept_r else None
+            return tokens, el, out
+
+
+def parity_figures(H_cpu, r_gpu, a_gpu, ref):
+    """Worst errors of the GPU's first tokens against the oracle's: weights
+    (absolute, bound 1e-5) and r (relative to the bf16 bar: one bf16 ulp of
+    r_ref plus 1e-3 max_s,c |h_s| per token; bound 1)."""
+    r_ref, a_ref = ref
+    n = r_ref.shape[0]
+    h = H_cpu[:, :n].double().numpy()
+    M = np.abs(h).max(axis=(0, 2))
+    _, e = np.frexp(np.abs(r_ref))
+    ulp = np.ldexp(1.0, np.maximum(e - 8, -133))
+    dr = np.abs(r_gpu[:n].double().numpy() - r_ref)
+    return {"tokens": int(n), "max_weight_abs_err": float(np.abs(a_gpu[:n].double().numpy() - a_ref).max()),
+            "weight_bound": 1e-5, "max_r_err_over_bf16_bar": float((dr / (ulp + 1e-3 * M[:, None])).max()),
+            "r_bound": 1.0, "against": "fp64 oracle (the CPU-baseline leg's own outputs)"}
 
 
 def run_reference(args):
@@ -226,7 +264,7 @@ def run_reference(args):
     import workloads as W
     inp = W.block_bf16(T=T_MAIN, d=D_MAIN, seed=1, device="cpu")
     # calibrate the per-step sample so warm-up + steps end within ~2 minutes
-    tok, el = time_oracle(inp.H, inp.w, 2.0, chunk=16)
+    tok, el, _ = time_oracle(inp.H, inp.w, 2.0, chunk=16)
     rate = tok / el
     per_step = max(1, int(rate * 110.0 / max(1, args.steps + args.warmup)))
     per_step = min(per_step, T_MAIN)
@@ -500,6 +538,16 @@ def run_gpu(args):
     achieved = bytes_launch / (launch_ms * 1e-3) / 1e9
     traffic, digest = profiled_traffic()
 
+    # the first tokens of set 0 as computed here, for the parity figures
+    probe = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        s0 = m["sets"][0]
+        r0 = torch.empty((T_MAIN, D_MAIN), dtype=torch.bfloat16, device=dev)
+        a0 = torch.empty((T_MAIN, S_MAIN), dtype=torch.float32, device=dev)
+        A.attnres_aggregate(s0.H, s0.w, r0, a0)
+        torch.cuda.synchronize()
+        probe = {"H": s0.H.cpu(), "w": s0.w.cpu(), "r": r0[:256].cpu(), "a": a0[:256].cpu()}
+        del r0, a0
     e2e = bench_e2e(args, A, dev, m["sets"])
     e2e_ms = max_over_ranks(e2e["ms_per_step"], ws, dev)
     e2e["value"] = ws * T_MAIN / (e2e_ms * 1e-3)
@@ -513,13 +561,14 @@ def run_gpu(args):
         extras.update(bench_backward(A, W, dev, peak))
         extras.update(bench_stack_backward(A, W, dev, peak))
 
-    cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        inp = W.block_bf16(T=T_MAIN, d=D_MAIN, seed=1, device="cpu")
-        tok, el = time_oracle(inp.H, inp.w, args.cpu_seconds)
+    cpu, parity = None, None
+    if probe is not None:
+        tok, el, ref = time_oracle(probe["H"], probe["w"], args.cpu_seconds, keep=256)
         cpu = {"value": tok / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{tok} tokens of the {T_MAIN}-token workload in 64-token chunks "
                          f"(single-threaded numpy fp64, {el:.1f} s)"}
+        if ref is not None:
+            parity = parity_figures(probe["H"], probe["r"], probe["a"], ref)
 
     if rank == 0:
         line = {
@@ -543,6 +592,8 @@ def run_gpu(args):
             "gpu_launches": m["launches"],
             "clocks": m["clocks"],
             "cpu_baseline": cpu,
+            "parity": parity,
+            "host": host_info(),
             "secondary": extras,
             "gpu": torch.cuda.get_device_name(dev),
         }

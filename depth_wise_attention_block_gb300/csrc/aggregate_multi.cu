@@ -15,7 +15,10 @@
 //   r = acc / l;   a_s = exp(z_s - m) / l   (logits kept in shared memory)
 //
 // Every source byte is still read from HBM once; each group costs one
-// cross-warp reduction step (one named barrier).
+// cross-warp reduction step (one named barrier).  A token's source list is
+// padded to a whole number of groups with re-reads of its source 0 row
+// (L2-resident by then) whose logits are -inf (weight exactly 0), so every
+// group has the compile-time size and the per-source guards fold away.
 #include <math.h>
 
 #include "ring_common.cuh"
@@ -65,6 +68,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
   }
 
   const int S = p.S;
+  const int S_pad = S + p.pad_rows;  // a whole number of groups of GS (padding rows weigh 0)
   uint32_t slot = 0, lap = 0;
   bool ok = true;
 
@@ -100,8 +104,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
 #pragma unroll
       for (int j = 0; j < NP; ++j) acc[k][j] = 0;
 
-    for (int g0 = 0; g0 < S; g0 += GS, ++iter) {
-      const int G = S - g0 < GS ? S - g0 : GS;
+    for (int g0 = 0; g0 < S_pad; g0 += GS, ++iter) {
       const int buf = iter & 1;
       volatile int* abort_flag = &sh.abort_flag[buf];
       uint4 x[GS][VPT];
@@ -113,8 +116,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       }
 #pragma unroll
       for (int s = 0; s < GS; ++s) {
-        if (s < G) {
-          if (!FUSED || g0 + s < p.n_stored) {
+        {
+          // stored sources and padding rows are single rows; the fused
+          // source (index n_stored = S - 1) is formed from prev and F
+          if (!FUSED || g0 + s != p.n_stored) {
             consume(x[s]);
           } else {
             // the fused source (the token's last): round(prev + F), stored as
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       reduce_scatter18(part, lane);
       if ((kRsValidLanes >> lane) & 1u) {
         const int idx = rs_index(lane);
-        if (idx < 2 * G) sh.red[buf][warp][idx] = part[0];
+        if (idx < 2 * GS) sh.red[buf][warp][idx] = part[0];
       }
       const bool warp_failed = __any_sync(0xffffffffu, !ok);
       if (lane == 0 && warp_failed) *abort_flag = 1;
@@ -176,12 +181,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       // holds source g0+s; all warps agree bit for bit)
       abort = *abort_flag != 0;
       float tot = 0.f;
-      if (lane < 2 * G) {
+      if (lane < 2 * GS) {
 #pragma unroll
         for (int w = 0; w < kRingConsumerWarps; ++w) tot += sh.red[buf][w][lane];
       }
       const float sumsq = __shfl_down_sync(0xffffffffu, tot, 1);
-      const bool is_src = lane < 2 * G && (lane & 1) == 0;
+      // padding sources (index >= S) get a logit of -inf: weight exactly 0
+      const bool is_src = lane < 2 * GS && (lane & 1) == 0 && g0 + (lane >> 1) < S;
       // fast reciprocal square root and exponential: a few fp32 ulps, far
       // inside the 1e-5 weight tolerance
       const float z = is_src ? tot * rsqrtf(fmaf(sumsq, p.inv_d, p.eps)) : -INFINITY;
@@ -191,6 +197,14 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       l = l * c + warp_sum(e);
       if (warp == 0 && is_src) sh.zbuf[g0 + (lane >> 1)] = z;
       m = m_new;
+      // re-materialise the packed sources so the compiler does not keep the
+      // first pass's unpacked values across the barrier (that spills)
+#pragma unroll
+      for (int s = 0; s < GS; ++s) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+          asm volatile("" : "+r"(x[s][k].x), "+r"(x[s][k].y), "+r"(x[s][k].z), "+r"(x[s][k].w));
+      }
       const uint64_t c2 = f2_pack(c, c);
       uint64_t e2[GS];
 #pragma unroll
@@ -206,12 +220,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
           for (int j = 0; j < NP; ++j) acc[k][j] = f2_fma(acc[k][j], c2, 0);
 #pragma unroll
           for (int s = 0; s < GS; ++s) {
-            if (s < G) {
-              uint64_t h[NP];
-              Vec<Tin>::pairs(x[s][k], h);
+            uint64_t h[NP];
+            Vec<Tin>::pairs(x[s][k], h);
 #pragma unroll
-              for (int j = 0; j < NP; ++j) acc[k][j] = f2_fma(e2[s], h[j], acc[k][j]);
-            }
+            for (int j = 0; j < NP; ++j) acc[k][j] = f2_fma(e2[s], h[j], acc[k][j]);
           }
         }
       }
@@ -262,7 +274,11 @@ static cudaError_t launch_multi_t(const RingParams& rp, int grid, int smem, cuda
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
-  e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, rp);
+  // pad every token's source list to a whole number of groups
+  constexpr int GS = MultiGroup<Tin, VPT>::kSize;
+  RingParams padded = rp;
+  padded.pad_rows = (GS - rp.S % GS) % GS;
+  e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, padded);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

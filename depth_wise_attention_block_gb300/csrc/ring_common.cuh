@@ -39,6 +39,7 @@ constexpr int kRingHeaderBytes = (int)((sizeof(RingShared) + 127) / 128 * 128);
 
 struct RingParams {
   unsigned long long wait_ns;  // limit of each main-loop wait (the final drain keeps the default)
+  int pad_rows;                // rows appended to each token (re-reads of src[0]'s row; multi-group kernel)
   int withhold_row1;           // bounded-wait test: 1 + the row of each CTA's first token armed
                                // without a copy (its waits must run out); 0 = none
   const char* src[kMaxSources];
@@ -228,7 +229,8 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
   const int nslots = p.nslots;
   const long long T = p.T;
   const bool fused = p.fuse_F != nullptr;
-  const int rows = p.n_stored + (fused ? (p.fuse_prev ? 2 : 1) : 0);
+  const int real_rows = p.n_stored + (fused ? (p.fuse_prev ? 2 : 1) : 0);
+  const int rows = real_rows + p.pad_rows;
   uint32_t slot = 0, lap = 0;
   long long issued = 0;
   bool ok = true;
@@ -237,6 +239,7 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
     for (int j = 0; j < rows; ++j) {
       const char* g;
       if (j < p.n_stored) g = p.src[j] + off;
+      else if (j >= real_rows) g = p.src[0] + off;  // padding: source 0's row again
       else if (p.fuse_prev && j == p.n_stored) g = p.fuse_prev + off;
       else g = p.fuse_F + off;
       // first lap: parity 1 of a fresh barrier counts as complete

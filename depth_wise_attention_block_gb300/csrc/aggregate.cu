@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kGenThreads) agg_generic_kernel(const __grid_c
 cudaError_t device_info(DeviceInfo* info) {
   constexpr int kMaxDevices = 64;
   static DeviceInfo cache[kMaxDevices];
-  static bool have[kMaxDevices] = {};
+  static std::atomic<bool> have[kMaxDevices];  // set after cache[dev] is filled
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

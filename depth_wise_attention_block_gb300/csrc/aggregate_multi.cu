@@ -19,6 +19,7 @@
 // padded to a whole number of groups with re-reads of its source 0 row
 // (L2-resident by then) whose logits are -inf (weight exactly 0), so every
 // group has the compile-time size and the per-source guards fold away.
+#include <atomic>
 #include <math.h>
 
 #include "ring_common.cuh"
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
 template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT>
 static cudaError_t launch_multi_t(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
-  static bool configured[kMaxDevices] = {};
+  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -15,6 +15,7 @@
 // after all of its warps have read buffer b.  A cluster barrier after the
 // set-up and another before exit keep every CTA alive while a peer may still
 // write into it.  No multicast.
+#include <atomic>
 #include <math.h>
 #include <stdlib.h>
 
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_split_kernel(const __grid
 template <typename Tin, typename Tout, bool FUSED>
 static cudaError_t launch_split_t(const SplitParams& sp, int grid, int smem, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
-  static bool configured[kMaxDevices] = {};
+  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -24,6 +24,7 @@
 // dw is deterministic: every CTA writes its partial sums to its own row of a
 // caller-provided fp32 workspace [grid, d]; dw_reduce_kernel then adds the
 // rows in a fixed order.
+#include <atomic>
 #include <math.h>
 
 #include <mutex>
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kDwThreads) dw_reduce_kernel(const float* ws, 
 template <typename T, int VPT, bool ACC>
 static cudaError_t launch_bwd_ring_t(const BwdParams& bp, int grid, int smem, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
-  static bool configured[kMaxDevices] = {};
+  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -5,6 +5,7 @@
 // arithmetic and the ring protocol are described at the top of aggregate.cu.
 #pragma once
 
+#include <atomic>
 #include <math.h>
 
 #include "attnres.h"
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
 template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT, int SC = 0>
 static cudaError_t launch_ring_t(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
-  static bool configured[kMaxDevices] = {};
+  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

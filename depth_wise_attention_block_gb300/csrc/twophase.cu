@@ -17,6 +17,7 @@
 //      weights: the inter-block ones scaled by e^{lse - m}/den, e^{z_p - m}/den
 //      for the partial.  Without a partial (first layer of a block) r is
 //      r_inter itself.
+#include <atomic>
 #include <math.h>
 
 #include "ring_common.cuh"
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_c
 template <typename Tin, int VPT, bool EXACT>
 static cudaError_t launch_inter_t(const InterParams& ip, int grid, int smem, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
-  static bool configured[kMaxDevices] = {};
+  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

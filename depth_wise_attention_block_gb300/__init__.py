@@ -53,6 +53,11 @@ def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None, contiguous=True) -> 
         return None
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    # the library launches on the current device: another device's memory
+    # must never reach its kernels
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device} but the current device is cuda:{cur}")
     if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:

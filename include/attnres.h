@@ -25,7 +25,8 @@
  *
  * Conventions for every call:
  *  - Tensors are row-major [T, d] (token-major, channel contiguous) in device
- *    memory; `sources` / `block_reps` are HOST arrays of DEVICE pointers.
+ *    memory of the CURRENT device (cudaGetDevice), on which every call
+ *    launches; `sources` / `block_reps` are HOST arrays of DEVICE pointers.
  *  - The caller owns and allocates every buffer.  The library allocates no
  *    device memory and keeps no device-side global state.
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;

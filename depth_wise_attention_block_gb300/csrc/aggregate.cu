@@ -185,8 +185,9 @@ static cudaError_t launch_ring_vpt(const RingParams& rp, int vpt, bool fused, in
   if constexpr (sizeof(Tin) == 2 && sizeof(Tout) == 2) {
     // bf16 storage at d = 7168 (the K3 width): one kernel per source count
     if (exact && vpt == 2 && rp.S >= 1 && rp.S <= kRingSmax)
-      return fused ? launch_ring_fixed_s_fused(rp, grid, smem, stream)
-                   : launch_ring_fixed_s(rp, grid, smem, stream);
+      return !fused ? launch_ring_fixed_s(rp, grid, smem, stream)
+             : rp.fuse_prev ? launch_ring_fixed_s_fused_prev(rp, grid, smem, stream)
+                            : launch_ring_fixed_s_fused_noprev(rp, grid, smem, stream);
   }
   if (vpt == 1) {
     return fused ? launch_ring_t<Tin, Tout, 1, true, false>(rp, grid, smem, stream)

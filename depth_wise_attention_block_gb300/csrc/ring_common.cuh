@@ -268,9 +268,11 @@ cudaError_t launch_ring_multi(const RingParams& rp, int vpt, bool fused, bool ex
                               int grid, int smem, cudaStream_t stream);
 
 // The ring kernel for bf16 rows of d = 7168 with the source count fixed at
-// compile time (ring_fixed_s.cu, ring_fixed_s_fused.cu); rp.S in 1..9.
+// compile time (ring_fixed_s.cu; fused: ring_fixed_s_fused.cu with a
+// previous partial sum, ring_fixed_s_fused_noprev.cu without); rp.S in 1..9.
 cudaError_t launch_ring_fixed_s(const RingParams& rp, int grid, int smem, cudaStream_t stream);
-cudaError_t launch_ring_fixed_s_fused(const RingParams& rp, int grid, int smem, cudaStream_t stream);
+cudaError_t launch_ring_fixed_s_fused_prev(const RingParams& rp, int grid, int smem, cudaStream_t stream);
+cudaError_t launch_ring_fixed_s_fused_noprev(const RingParams& rp, int grid, int smem, cudaStream_t stream);
 
 // Split-d cluster variant for few tokens (aggregate_split.cu): the cluster
 // size to use for T tokens (0 = none) and its launch.  Off unless the

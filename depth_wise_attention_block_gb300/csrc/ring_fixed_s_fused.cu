@@ -1,21 +1,22 @@
 // agg_ring_kernel for bf16 rows of exactly 2 x 448 16-byte vectors
-// (d = 7168) and a source count fixed at compile time, with the block bookkeeping fused (the last source formed as round(prev + F)).  One
-// instantiation per S = 1..9.
+// (d = 7168), a source count fixed at compile time and the block
+// bookkeeping fused, its fused source adding a previous partial sum (round(prev + F)).  One instantiation per
+// S = 1..9.
 #include "ring_kernel.cuh"
 
 namespace attnres {
 
-cudaError_t launch_ring_fixed_s_fused(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
+cudaError_t launch_ring_fixed_s_fused_prev(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
   switch (rp.S) {
-    case 1: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 1>(rp, grid, smem, stream);
-    case 2: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 2>(rp, grid, smem, stream);
-    case 3: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 3>(rp, grid, smem, stream);
-    case 4: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 4>(rp, grid, smem, stream);
-    case 5: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 5>(rp, grid, smem, stream);
-    case 6: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 6>(rp, grid, smem, stream);
-    case 7: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 7>(rp, grid, smem, stream);
-    case 8: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 8>(rp, grid, smem, stream);
-    case 9: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 9>(rp, grid, smem, stream);
+    case 1: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 1, 2>(rp, grid, smem, stream);
+    case 2: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 2, 2>(rp, grid, smem, stream);
+    case 3: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 3, 2>(rp, grid, smem, stream);
+    case 4: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 4, 2>(rp, grid, smem, stream);
+    case 5: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 5, 2>(rp, grid, smem, stream);
+    case 6: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 6, 2>(rp, grid, smem, stream);
+    case 7: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 7, 2>(rp, grid, smem, stream);
+    case 8: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 8, 2>(rp, grid, smem, stream);
+    case 9: return launch_ring_t<bf16_t, bf16_t, 2, true, true, 9, 2>(rp, grid, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

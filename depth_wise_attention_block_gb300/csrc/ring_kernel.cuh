@@ -15,19 +15,23 @@
 
 namespace attnres {
 
-template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT, int SC>
+template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT, int SC, int PREV = 0>
 __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_constant__ RingParams p) {
   // EXACT: the row holds exactly VPT * kRingConsumers vectors, so every
   // consumer thread owns VPT of them and no bounds test is needed.
   // SC: the source count when fixed at compile time (0: p.S at run time);
   // with it the per-source guards fold away and the compiler schedules the
   // whole token as one block.
+  // PREV (fused kernels): whether the fused source adds a previous partial
+  // sum, fixed at compile time (1: no, 2: yes) or read from p (0).  Fixed, it
+  // keeps the fused S = 9 kernel from spilling.
   constexpr int EPV = Vec<Tin>::kElems;
   // kEarlyRs: the first reduce-scatter level is taken per source during the
   // first pass (one partial live per source instead of two).  That keeps the
   // fused kernels (more live state) from spilling; the unfused ones are
   // faster without it at S = 9.
   constexpr bool kEarlyRs = FUSED;
+  const bool has_prev = PREV == 0 ? p.fuse_prev != nullptr : PREV == 2;
   extern __shared__ __align__(128) unsigned char smem[];
   RingShared& sh = *reinterpret_cast<RingShared*>(smem);
   const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
         } else {
           // the fused source: round(prev + F), stored as the new partial / b_n
           uint4 pv[VPT], fv[VPT];
-          if (p.fuse_prev) consume(pv);
+          if (has_prev) consume(pv);
           consume(fv);
           char* drow = p.fuse_dst + t * (long long)p.row_bytes;
 #pragma unroll
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
             if (EXACT || v < p.nvec) {
               float f[EPV];
               Vec<Tin>::unpack(fv[k], f);
-              if (p.fuse_prev) {
+              if (has_prev) {
                 float q[EPV];
                 Vec<Tin>::unpack(pv[k], q);
 #pragma unroll
@@ -251,14 +255,14 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
   }
 }
 
-template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT, int SC = 0>
+template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT, int SC = 0, int PREV = 0>
 static cudaError_t launch_ring_t(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  auto kern = agg_ring_kernel<Tin, Tout, VPT, FUSED, EXACT, SC>;
+  auto kern = agg_ring_kernel<Tin, Tout, VPT, FUSED, EXACT, SC, PREV>;
   if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
     DeviceInfo di;
     e = device_info(&di);

@@ -356,35 +356,47 @@ def bench_main(args, A, W, dev, ws):
             "launches": K, "sets": sets}
 
 
+E2E_CHUNK_TOKENS = 1024  # tokens per staging chunk of the host-buffer call
+E2E_SLOTS = 2             # staging slots: copy in, compute and copy out overlap
+
+
 def bench_e2e(args, A, dev, sets):
-    """Through the public API with host buffers: pinned H2D of the sources
-    and the query, the aggregation, D2H of r and the weights, every step
-    (aggregate_host pipelines them over 4 token chunks)."""
+    """Through the C-ABI call with host buffers (attnres_aggregate_host): the
+    sources and the query copied in from pinned host memory, the aggregation,
+    r and the weights copied back, every step; the library streams
+    1024-token chunks through two device staging slots."""
     s = sets[0]
     H_host = torch.empty(s.H.shape, dtype=s.H.dtype, pin_memory=True)
     H_host.copy_(s.H)
     w_host = s.w.cpu().pin_memory()
     r_host = torch.empty((T_MAIN, D_MAIN), dtype=torch.bfloat16, pin_memory=True)
     a_host = torch.empty((T_MAIN, S_MAIN), dtype=torch.float32, pin_memory=True)
-    H_dev, w_dev = torch.empty_like(s.H), torch.empty_like(s.w)
-    r_dev = torch.empty((T_MAIN, D_MAIN), dtype=torch.bfloat16, device=dev)
-    a_dev = torch.empty((T_MAIN, S_MAIN), dtype=torch.float32, device=dev)
+    nbytes = A.attnres_aggregate_host_workspace_size(S_MAIN, E2E_CHUNK_TOKENS, D_MAIN, torch.bfloat16,
+                                                     torch.bfloat16, True, E2E_SLOTS)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+
+    def step():
+        A.attnres_aggregate_host(H_host, w_host, r_host, a_host, workspace=ws, chunk_tokens=E2E_CHUNK_TOKENS,
+                                 stream=stream)
+
     K = max(3, min(args.steps, 30))
     for _ in range(3):
-        A.aggregate_host(H_host, w_host, r_host, a_host, H_dev, w_dev, r_dev, a_dev, stream=stream)
+        step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        A.aggregate_host(H_host, w_host, r_host, a_host, H_dev, w_dev, r_dev, a_dev, stream=stream)
+        step()
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / K
     h2d = H_host.numel() * H_host.element_size() + w_host.numel() * 4
     d2h = r_host.numel() * 2 + a_host.numel() * 4
     return {"value": T_MAIN / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K, "call": "attnres_aggregate_host",
+            "chunk_tokens": E2E_CHUNK_TOKENS, "staging_slots": E2E_SLOTS,
+            "workspace_bytes": nbytes, "host_link_gbs": (h2d + d2h) / (ms * 1e-3) / 1e9}
 
 
 def _time_forward(fwd, reps):

@@ -35,7 +35,7 @@ __all__ = [
     "attnres_interblock", "attnres_intrablock_step", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
     "attnres_layer_step", "attnres_synthetic_layer", "attnres_synthetic_layer_backward", "attnres_fold",
     "attnres_version", "AttnResState",
-    "aggregate_host", "dtype_code", "AttnresError",
+    "attnres_aggregate_host", "attnres_aggregate_host_workspace_size", "dtype_code", "AttnresError",
 ]
 
 _DT = {torch.float32: ATTNRES_F32, torch.bfloat16: ATTNRES_BF16}
@@ -294,58 +294,69 @@ def attnres_debug_wait_test(wait_limit_ns: int, withhold_row: int) -> None:
     _N.check(_N.lib.attnres_debug_wait_test(int(wait_limit_ns), int(withhold_row)), "attnres_debug_wait_test")
 
 
-_HOST_STREAMS: dict = {}
+def _host_ptr(t: torch.Tensor | None, name: str, dtype=None) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
 
 
-def _host_streams(device):
-    key = torch.device(device).index
-    if key not in _HOST_STREAMS:
-        _HOST_STREAMS[key] = (torch.cuda.Stream(device), torch.cuda.Stream(device))
-    return _HOST_STREAMS[key]
+def attnres_aggregate_host_workspace_size(S: int, chunk_tokens: int, d: int, src_dtype: torch.dtype,
+                                          out_dtype: torch.dtype, with_weights: bool = True, slots: int = 2) -> int:
+    """Bytes of device workspace attnres_aggregate_host needs for `slots`
+    staging slots of chunk_tokens tokens."""
+    return _N.check(_N.lib.attnres_aggregate_host_workspace_size(
+        int(S), int(chunk_tokens), int(d), dtype_code(src_dtype), dtype_code(out_dtype), int(bool(with_weights)),
+        int(slots)), "attnres_aggregate_host_workspace_size")
 
 
-def aggregate_host(H_host: torch.Tensor, w_host: torch.Tensor, r_host: torch.Tensor, a_host: torch.Tensor | None,
-                   H_dev: torch.Tensor, w_dev: torch.Tensor, r_dev: torch.Tensor, a_dev: torch.Tensor | None,
-                   eps: float = ATTNRES_DEFAULT_EPS, stream=None, chunks: int = 4) -> None:
-    """One aggregation from and to host memory, pipelined over token chunks.
+def attnres_aggregate_host(sources_host: Sequence[torch.Tensor] | torch.Tensor, w_host: torch.Tensor,
+                           r_host: torch.Tensor, weights_host: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, chunk_tokens: int = 1024,
+                           eps: float = ATTNRES_DEFAULT_EPS, dev_err: torch.Tensor | None = None,
+                           stream=None) -> None:
+    """attnres_aggregate with sources, query and outputs in host memory.
 
-    The [S, T, d] sources and w are copied in from pinned host memory, each
-    chunk of tokens is aggregated as soon as its rows have arrived, and its r
-    (and weights) are copied back while later chunks are still coming in: the
-    host link (the limit of this path) carries both directions at once.  The
-    device buffers are the caller's.  Asynchronous: `stream` (default: the
-    current stream) is complete, and r_host valid, once it is synchronised.
+    sources_host: S CPU tensors [T, d] (float32 or bfloat16, one dtype,
+    pinned for full speed) or one [S, T, d] CPU tensor; w_host: [d] float32;
+    r_host: [T, d] float32/bfloat16; weights_host: [T, S] float32 or None;
+    workspace: a CUDA tensor of at least attnres_aggregate_host_workspace_size
+    bytes (None: two slots are allocated through torch).  The library streams
+    token chunks through the workspace's staging slots; synchronise `stream`
+    (default: the current stream) before reading r_host.
     """
-    from .shard import token_range
-    S, T, d = H_host.shape
-    cur = stream if stream is not None else torch.cuda.current_stream()
-    copy_in, copy_out = _host_streams(H_dev.device)
-    start = torch.cuda.Event()
-    start.record(cur)
-    copy_in.wait_event(start)
-    copy_out.wait_event(start)
-    chunks = max(1, min(chunks, T))
-    with torch.cuda.stream(copy_in):
-        w_dev.copy_(w_host, non_blocking=True)
-    for c in range(chunks):
-        t0, t1 = token_range(T, c, chunks)
-        if t1 == t0:
-            continue
-        with torch.cuda.stream(copy_in):
-            for s in range(S):
-                H_dev[s, t0:t1].copy_(H_host[s, t0:t1], non_blocking=True)
-            arrived = torch.cuda.Event()
-            arrived.record(copy_in)
-        cur.wait_event(arrived)
-        with torch.cuda.stream(cur):
-            attnres_aggregate([H_dev[s, t0:t1] for s in range(S)], w_dev, r_dev[t0:t1],
-                              a_dev[t0:t1] if a_dev is not None else None, eps=eps, stream=cur)
-            done = torch.cuda.Event()
-            done.record(cur)
-        copy_out.wait_event(done)
-        with torch.cuda.stream(copy_out):
-            r_host[t0:t1].copy_(r_dev[t0:t1], non_blocking=True)
-            if a_host is not None and a_dev is not None:
-                a_host[t0:t1].copy_(a_dev[t0:t1], non_blocking=True)
-    cur.wait_stream(copy_in)
-    cur.wait_stream(copy_out)
+    if isinstance(sources_host, torch.Tensor):
+        if sources_host.dim() != 3:
+            raise ValueError("a stacked sources tensor must be [S, T, d]")
+        srcs = list(sources_host.unbind(0))
+    else:
+        srcs = list(sources_host)
+    if not srcs:
+        raise ValueError("need at least one source")
+    T, d = srcs[0].shape
+    dt = srcs[0].dtype
+    for i, s in enumerate(srcs):
+        if s.shape != (T, d) or s.dtype != dt:
+            raise ValueError(f"source {i}: expected [{T}, {d}] {dt}, got {list(s.shape)} {s.dtype}")
+    ptrs = (ctypes.c_void_p * len(srcs))(*[_host_ptr(s, f"sources_host[{i}]") for i, s in enumerate(srcs)])
+    if r_host.shape != (T, d):
+        raise ValueError("r_host must be [T, d]")
+    if weights_host is not None and weights_host.shape != (T, len(srcs)):
+        raise ValueError("weights_host must be [T, S]")
+    if w_host.shape != (d,):
+        raise ValueError("w_host must be [d]")
+    if workspace is None:
+        nbytes = attnres_aggregate_host_workspace_size(len(srcs), max(1, min(int(chunk_tokens), T)), d, dt,
+                                                       r_host.dtype, weights_host is not None, 2)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=torch.cuda.current_device())
+    rc = _N.lib.attnres_aggregate_host(
+        ptrs, len(srcs), T, d, dtype_code(dt), _host_ptr(w_host, "w_host", torch.float32), float(eps),
+        _host_ptr(r_host, "r_host"), dtype_code(r_host.dtype), _host_ptr(weights_host, "weights_host", torch.float32),
+        int(chunk_tokens), _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
+    _N.check(rc, "attnres_aggregate_host")

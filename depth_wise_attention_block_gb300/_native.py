@@ -30,6 +30,8 @@ ATTNRES_DEFAULT_EPS = 1e-5
 # every function declared in include/attnres.h
 EXPORTED = (
     "attnres_aggregate",
+    "attnres_aggregate_host",
+    "attnres_aggregate_host_workspace_size",
     "attnres_aggregate_backward",
     "attnres_aggregate_backward_workspace_size",
     "attnres_aggregate_backward_noalloc",
@@ -77,6 +79,9 @@ def _load() -> ctypes.CDLL:
     sp = ctypes.POINTER(AttnresState)
     sig = {
         "attnres_aggregate": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, vp, f32, vp, i32, vp, vp, vp]),
+        "attnres_aggregate_host": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, vp, f32, vp, i32, vp, i64, vp,
+                                          i64, vp, vp]),
+        "attnres_aggregate_host_workspace_size": (i64, [i32, i64, i32, i32, i32, i32, i32]),
         "attnres_aggregate_backward": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, vp, f32, vp,
                                               ctypes.POINTER(vp), i32, vp, vp, i64, vp, vp]),
         "attnres_aggregate_backward_workspace_size": (i64, [i64, i32]),

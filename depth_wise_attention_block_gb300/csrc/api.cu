@@ -75,6 +75,61 @@ int check_state(const attnres_state* st) {
   return ATTNRES_OK;
 }
 
+
+// ---- host-buffer aggregation: staging-slot layout and the copy pipeline ----
+
+constexpr int kMaxHostSlots = 8;  // more than 3 slots gains nothing; bounds the events made per call
+
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+int64_t dtype_bytes(int dt) { return dt == ATTNRES_BF16 ? 2 : 4; }
+
+// Workspace: the query (d fp32), then per slot the [S, n, d] sources of a
+// chunk of n <= chunk_tokens tokens, its r and (optionally) its weights.
+struct HostLayout {
+  int64_t w_bytes, src_bytes, r_bytes, a_bytes, slot_bytes;
+};
+
+HostLayout host_layout(int S, int64_t Tc, int d, int src_dtype, int out_dtype, bool with_weights) {
+  HostLayout L;
+  L.w_bytes = align256(int64_t(d) * 4);
+  L.src_bytes = align256(int64_t(S) * Tc * d * dtype_bytes(src_dtype));
+  L.r_bytes = align256(Tc * d * dtype_bytes(out_dtype));
+  L.a_bytes = with_weights ? align256(Tc * S * 4) : 0;
+  L.slot_bytes = L.src_bytes + L.r_bytes + L.a_bytes;
+  return L;
+}
+
+// The two copy streams and the per-slot events of one call; released when
+// the call returns (CUDA defers the release until queued work is done).
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t arrived[kMaxHostSlots] = {}, computed[kMaxHostSlots] = {}, drained[kMaxHostSlots] = {};
+
+  cudaError_t create(int nslots) {
+    cudaError_t e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+    for (int k = 0; k < nslots && e == cudaSuccess; ++k) {
+      e = cudaEventCreateWithFlags(&arrived[k], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&computed[k], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&drained[k], cudaEventDisableTiming);
+    }
+    return e;
+  }
+
+  ~HostPipe() {
+    for (int k = 0; k < kMaxHostSlots; ++k) {
+      if (arrived[k]) cudaEventDestroy(arrived[k]);
+      if (computed[k]) cudaEventDestroy(computed[k]);
+      if (drained[k]) cudaEventDestroy(drained[k]);
+    }
+    if (start) cudaEventDestroy(start);
+    if (in) cudaStreamDestroy(in);
+    if (out) cudaStreamDestroy(out);
+  }
+};
+
 }  // namespace
 
 extern "C" {
@@ -124,6 +179,107 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
   AggPath path;
   cudaError_t e = launch_aggregate(a, &path);
   if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate launch");
+  return ok();
+}
+
+int64_t attnres_aggregate_host_workspace_size(int S, int64_t chunk_tokens, int d, int src_dtype, int out_dtype,
+                                              int with_weights, int slots) {
+  if (S < 1) return fail(ATTNRES_EINVAL, "S=%d < 1", S);
+  if (S > ATTNRES_MAX_SOURCES) return fail(ATTNRES_ERANGE, "S=%d > %d", S, ATTNRES_MAX_SOURCES);
+  if (!valid_dtype(src_dtype) || !valid_dtype(out_dtype)) return fail(ATTNRES_EDTYPE, "dtype %d/%d", src_dtype, out_dtype);
+  if (chunk_tokens < 1 || d < 1) return fail(ATTNRES_EINVAL, "chunk_tokens=%lld d=%d", (long long)chunk_tokens, d);
+  if (!size_ok(chunk_tokens, d)) return fail(ATTNRES_ERANGE, "chunk_tokens*d too large");
+  if (with_weights != 0 && with_weights != 1) return fail(ATTNRES_EINVAL, "with_weights must be 0 or 1");
+  if (slots < 1 || slots > kMaxHostSlots) return fail(ATTNRES_EINVAL, "slots=%d not in 1..%d", slots, kMaxHostSlots);
+  const HostLayout L = host_layout(S, chunk_tokens, d, src_dtype, out_dtype, with_weights != 0);
+  ok();
+  return L.w_bytes + int64_t(slots) * L.slot_bytes;
+}
+
+int attnres_aggregate_host(const void* const* sources_host, int S, int64_t T, int d, int src_dtype,
+                           const float* w_host, float eps, void* r_host, int out_dtype, float* weights_host,
+                           int64_t chunk_tokens, void* workspace, int64_t workspace_bytes, int* dev_err,
+                           void* stream) {
+  if (!sources_host) return fail(ATTNRES_EINVAL, "sources_host is NULL");
+  if (S < 1) return fail(ATTNRES_EINVAL, "S=%d < 1", S);
+  if (S > ATTNRES_MAX_SOURCES) return fail(ATTNRES_ERANGE, "S=%d > %d", S, ATTNRES_MAX_SOURCES);
+  if (!valid_dtype(src_dtype) || !valid_dtype(out_dtype)) return fail(ATTNRES_EDTYPE, "dtype %d/%d", src_dtype, out_dtype);
+  if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  if (chunk_tokens < 1) return fail(ATTNRES_EINVAL, "chunk_tokens=%lld < 1", (long long)chunk_tokens);
+  if (T == 0) return ok();
+  if (!w_host || !r_host || !workspace) return fail(ATTNRES_EINVAL, "w_host/r_host/workspace is NULL");
+  for (int s = 0; s < S; ++s)
+    if (!sources_host[s]) return fail(ATTNRES_EINVAL, "sources_host[%d] is NULL", s);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(ATTNRES_EINVAL, "workspace not 256-byte aligned");
+  const int64_t Tc = chunk_tokens < T ? chunk_tokens : T;
+  const int64_t nchunks = (T + Tc - 1) / Tc;
+  const HostLayout L = host_layout(S, Tc, d, src_dtype, out_dtype, weights_host != nullptr);
+  if (workspace_bytes < L.w_bytes + L.slot_bytes)
+    return fail(ATTNRES_ERANGE, "workspace %lld bytes < %lld needed for one slot of %lld tokens",
+                (long long)workspace_bytes, (long long)(L.w_bytes + L.slot_bytes), (long long)Tc);
+  int64_t fit = (workspace_bytes - L.w_bytes) / L.slot_bytes;
+  if (fit > nchunks) fit = nchunks;
+  const int nslots = fit > kMaxHostSlots ? kMaxHostSlots : int(fit);
+
+  const int64_t es = dtype_bytes(src_dtype), os = dtype_bytes(out_dtype);
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  HostPipe pipe;
+  cudaError_t e = pipe.create(nslots);
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate_host: creating copy streams/events");
+#define HOST_CK(call)                                           \
+  do {                                                          \
+    cudaError_t e_ = (call);                                    \
+    if (e_ != cudaSuccess) return cuda_fail(e_, "attnres_aggregate_host: " #call); \
+  } while (0)
+
+  char* ws = static_cast<char*>(workspace);
+  float* w_dev = reinterpret_cast<float*>(ws);
+  HOST_CK(cudaEventRecord(pipe.start, user));  // after the work already on `stream`
+  HOST_CK(cudaStreamWaitEvent(pipe.in, pipe.start, 0));
+  HOST_CK(cudaMemcpyAsync(w_dev, w_host, size_t(d) * 4, cudaMemcpyHostToDevice, pipe.in));
+  for (int64_t c = 0; c < nchunks; ++c) {
+    const int k = int(c % nslots);
+    const int64_t t0 = c * Tc, n = (T - t0) < Tc ? (T - t0) : Tc;
+    char* slot = ws + L.w_bytes + int64_t(k) * L.slot_bytes;
+    char* r_dev = slot + L.src_bytes;
+    float* a_dev = weights_host ? reinterpret_cast<float*>(slot + L.src_bytes + L.r_bytes) : nullptr;
+    // The slot is free again once the chunk that used it last has been copied out.
+    if (c >= nslots) HOST_CK(cudaStreamWaitEvent(pipe.in, pipe.drained[k], 0));
+    AggArgs a{};
+    for (int s = 0; s < S; ++s) {
+      char* dst = slot + int64_t(s) * n * d * es;  // [S, n, d] in the slot
+      HOST_CK(cudaMemcpyAsync(dst, static_cast<const char*>(sources_host[s]) + t0 * d * es, size_t(n * d * es),
+                              cudaMemcpyHostToDevice, pipe.in));
+      a.src[s] = dst;
+    }
+    HOST_CK(cudaEventRecord(pipe.arrived[k], pipe.in));
+    HOST_CK(cudaStreamWaitEvent(user, pipe.arrived[k], 0));
+    a.n_stored = S;
+    a.T = n;
+    a.d = d;
+    a.src_dtype = src_dtype;
+    a.w = w_dev;
+    a.eps = eps;
+    a.out_r = r_dev;
+    a.out_dtype = out_dtype;
+    a.out_a = a_dev;
+    a.dev_err = dev_err;
+    a.stream = user;
+    AggPath path;
+    HOST_CK(launch_aggregate(a, &path));
+    HOST_CK(cudaEventRecord(pipe.computed[k], user));
+    HOST_CK(cudaStreamWaitEvent(pipe.out, pipe.computed[k], 0));
+    HOST_CK(cudaMemcpyAsync(static_cast<char*>(r_host) + t0 * d * os, r_dev, size_t(n * d * os),
+                            cudaMemcpyDeviceToHost, pipe.out));
+    if (weights_host)
+      HOST_CK(cudaMemcpyAsync(weights_host + t0 * S, a_dev, size_t(n * S * 4), cudaMemcpyDeviceToHost, pipe.out));
+    HOST_CK(cudaEventRecord(pipe.drained[k], pipe.out));
+  }
+  // The copy-out stream is in order: its last event covers every chunk.
+  HOST_CK(cudaStreamWaitEvent(user, pipe.drained[(nchunks - 1) % nslots], 0));
+#undef HOST_CK
   return ok();
 }
 

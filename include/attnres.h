@@ -100,6 +100,54 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
                       float* out_weights, int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * attnres_aggregate_host -- attnres_aggregate on sources, query and outputs
+ * that live in HOST memory.  The pages have no counterpart: this is the
+ * library's way in for data that starts on the CPU.
+ *
+ * The tokens are cut into chunks of chunk_tokens (the last may be shorter).
+ * Chunk c goes to staging slot c mod nslots of `workspace`: its S source
+ * rows are copied in, aggregated as soon as they have arrived, and its r
+ * (and weights) copied out while later chunks are still coming in, so the
+ * host link carries both directions at once.  Results are those of
+ * attnres_aggregate on the same data (each token is computed alone).
+ *
+ * sources_host host array of S HOST pointers, each [T, d] of src_dtype.
+ *             Page-locked memory (cudaHostAlloc, cudaHostRegister) lets the
+ *             copies run at the link's rate, asynchronously; pageable memory
+ *             works, but the driver then stages each copy and the call
+ *             returns only once the sources have been read.
+ * w_host      host [d] fp32 pseudo-query
+ * r_host      host [T, d] of out_dtype; weights_host host [T, S] fp32 or NULL
+ * chunk_tokens >= 1 (values above T act as T)
+ * workspace   device buffer owned by the caller, 256-byte aligned, of
+ *             workspace_bytes >= attnres_aggregate_host_workspace_size(...,
+ *             1); the call uses as many slots as fit, at most 8 and at most
+ *             the number of chunks (2 to 3 slots let copies and compute
+ *             overlap).  Its contents on entry do not matter.
+ * stream      work already on `stream` comes first; work issued on `stream`
+ *             after the call waits until r_host / weights_host hold the
+ *             results, so synchronise `stream` before reading them or
+ *             writing the inputs again.  The copies run on two streams that
+ *             the call creates and destroys (CUDA defers their release until
+ *             their work is done); not for use under stream capture.
+ * Other arguments, bounds and errors as attnres_aggregate; nothing is
+ * copied or launched when an argument is rejected.
+ * ---------------------------------------------------------------------- */
+int attnres_aggregate_host(const void* const* sources_host, int S, int64_t T, int d,
+                           int src_dtype, const float* w_host, float eps, void* r_host,
+                           int out_dtype, float* weights_host, int64_t chunk_tokens,
+                           void* workspace, int64_t workspace_bytes, int* dev_err,
+                           void* stream);
+
+/* Bytes of workspace attnres_aggregate_host needs for `slots` staging slots
+ * of chunk_tokens tokens (the query, then per slot the [S, chunk_tokens, d]
+ * sources, r and, if with_weights, the weights, each part 256-byte
+ * aligned); slots 1..8.  Host only.  Negative attnres_status on bad
+ * arguments. */
+int64_t attnres_aggregate_host_workspace_size(int S, int64_t chunk_tokens, int d, int src_dtype,
+                                              int out_dtype, int with_weights, int slots);
+
+/* ------------------------------------------------------------------------
  * attnres_aggregate_backward -- gradients of attnres_aggregate.  In training
  * AttnRes runs under activation checkpointing ([Tutorial] ch. 4.6): nothing
  * is kept from the forward; the logits and weights are recomputed here from

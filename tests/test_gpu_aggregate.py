@@ -241,21 +241,69 @@ def test_deterministic_across_runs(lib):
     assert torch.equal(r1, r2) and torch.equal(a1, a2)
 
 
-def test_aggregate_host_pipeline_matches_device_path(lib):
-    # host buffers in and out, chunked over tokens: every token is computed by
-    # the same arithmetic as in one launch over all tokens, so bit for bit
+def _host_copy(t: torch.Tensor, pinned: bool) -> torch.Tensor:
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=pinned)
+    h.copy_(t)
+    return h
+
+
+@pytest.mark.parametrize("chunk,slots", [(1000, 1), (256, 2), (333, 3), (256, 1), (7, 2)])
+def test_aggregate_host_matches_device_path(lib, chunk, slots):
+    # host buffers in and out through the C ABI, chunked over tokens through
+    # a ring of staging slots: every token is computed by the same arithmetic
+    # as in one launch over all tokens, so bit for bit
     T, d, S = 1000, 7168, 9
     inp = W.block_bf16(T=T, d=d, seed=9, device="cuda")
-    H_host = torch.empty(inp.H.shape, dtype=inp.H.dtype, pin_memory=True)
-    H_host.copy_(inp.H)
-    w_host = inp.w.cpu().pin_memory()
+    H_host, w_host = _host_copy(inp.H, True), _host_copy(inp.w, True)
     r_host = torch.full((T, d), float("nan"), dtype=torch.bfloat16, pin_memory=True)
     a_host = torch.full((T, S), float("nan"), dtype=torch.float32, pin_memory=True)
-    H_dev, w_dev = torch.empty_like(inp.H), torch.empty_like(inp.w)
-    r_dev = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
-    a_dev = torch.empty((T, S), dtype=torch.float32, device="cuda")
-    for chunks in (1, 3, 7):
-        lib.aggregate_host(H_host, w_host, r_host, a_host, H_dev, w_dev, r_dev, a_dev, chunks=chunks)
+    nbytes = lib.attnres_aggregate_host_workspace_size(S, min(chunk, T), d, torch.bfloat16, torch.bfloat16, True, slots)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r_ref, a_ref = _run(lib, inp.H, inp.w)
+    for _ in range(2):  # a second call reuses the slots with stale contents
+        lib.attnres_aggregate_host(H_host, w_host, r_host, a_host, workspace=ws, chunk_tokens=chunk, dev_err=err)
         torch.cuda.synchronize()
-        r_ref, a_ref = _run(lib, inp.H, inp.w)
+        assert int(err.item()) == 0
         assert torch.equal(r_host.cuda(), r_ref) and torch.equal(a_host.cuda(), a_ref)
+        r_host.fill_(float("nan"))
+        a_host.fill_(float("nan"))
+
+
+def test_aggregate_host_pageable_fp32_ragged_rows_against_oracle(lib):
+    # pageable (not page-locked) host memory, fp32, rows of 100 channels (not
+    # a whole number of 16-byte vectors: the plain-load kernel), a ragged last
+    # chunk, no weights; checked against the oracle and the device path
+    g = torch.Generator().manual_seed(31)
+    S, T, d = 4, 37, 100
+    H = torch.randn(S, T, d, generator=g) * torch.tensor([0.5, 1.0, 2.0, 4.0]).view(S, 1, 1)
+    w = torch.randn(d, generator=g) / d ** 0.5
+    r_host = torch.full((T, d), float("nan"), dtype=torch.float32)
+    lib.attnres_aggregate_host(list(H.unbind(0)), w, r_host, None, chunk_tokens=5)
+    torch.cuda.synchronize()
+    assert not torch.isnan(r_host).any()
+    _compare(H, w, r_host, None, torch.float32)
+    r_dev, _ = _run(lib, H.cuda(), w.cuda(), torch.float32, with_weights=False)
+    assert torch.equal(r_host, r_dev.cpu())
+
+
+def test_aggregate_host_orders_after_stream_work(lib):
+    # the call is ordered after work already queued on its stream (a long
+    # kernel here), and an event recorded on the stream after the call
+    # completes only once the host outputs are final
+    S, T, d = 3, 64, 256
+    g = torch.Generator().manual_seed(32)
+    H = torch.randn(S, T, d, generator=g)
+    w = torch.randn(d, generator=g) / 16
+    stream = torch.cuda.Stream()
+    r_host = torch.full((T, d), float("nan"), dtype=torch.float32, pin_memory=True)
+    a_host = torch.full((T, S), float("nan"), dtype=torch.float32, pin_memory=True)
+    H_host, w_host = _host_copy(H, True), _host_copy(w, True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)  # a long kernel ahead of the call on its stream
+        lib.attnres_aggregate_host(H_host, w_host, r_host, a_host, chunk_tokens=16, stream=stream)
+        done = torch.cuda.Event()
+        done.record(stream)
+    done.synchronize()
+    r_dev, a_dev = _run(lib, H.cuda(), w.cuda(), torch.float32)
+    assert torch.equal(r_host, r_dev.cpu()) and torch.equal(a_host, a_dev.cpu())

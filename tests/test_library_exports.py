@@ -153,6 +153,60 @@ def test_aggregate_rejects_bad_arguments_before_any_launch(native):
     assert agg(src, 3, 0, 8, 1, None, 1e-5, None, 1, None, None, None) == 0
 
 
+def test_host_workspace_size_is_the_slot_layout(native):
+    # query row, then per slot the [S, chunk, d] sources, r and the weights,
+    # each part rounded up to 256 bytes; written out for the K3 block layout
+    size = native.lib.attnres_aggregate_host_workspace_size
+    q = 7168 * 4                               # 28,672 = 112 x 256
+    src = 9 * 256 * 7168 * 2                   # 33,030,144
+    r = 256 * 7168 * 2                         # 3,670,016
+    a = 256 * 9 * 4                            # 9,216
+    assert size(9, 256, 7168, 1, 1, 1, 2) == q + 2 * (src + r + a)
+    assert size(9, 256, 7168, 1, 1, 0, 1) == q + src + r
+    # fp32 out, ragged sizes: every part padded to 256 bytes on its own
+    assert size(3, 5, 10, 0, 0, 1, 3) == 256 + 3 * (768 + 256 + 256)
+    assert size(1, 100, 7, 1, 0, 0, 1) == 256 + 1536 + 2816
+    assert size(0, 256, 7168, 1, 1, 1, 2) == native.ATTNRES_EINVAL
+    assert size(129, 256, 7168, 1, 1, 1, 2) == native.ATTNRES_ERANGE
+    assert size(9, 0, 7168, 1, 1, 1, 2) == native.ATTNRES_EINVAL
+    assert size(9, 256, 7168, 2, 1, 1, 2) == native.ATTNRES_EDTYPE
+    assert size(9, 256, 7168, 1, 1, 2, 2) == native.ATTNRES_EINVAL
+    assert size(9, 256, 7168, 1, 1, 1, 0) == native.ATTNRES_EINVAL
+    assert size(9, 256, 7168, 1, 1, 1, 9) == native.ATTNRES_EINVAL
+
+
+def test_aggregate_host_rejects_bad_arguments_before_any_copy(native):
+    agg = native.lib.attnres_aggregate_host
+    src = (ctypes.c_void_p * 3)(0x1000, 0x2000, 0x3000)
+    need = native.lib.attnres_aggregate_host_workspace_size(3, 4, 8, 1, 1, 0, 1)
+    ok_args = dict(S=3, T=4, d=8, sdt=1, w=0x4000, eps=1e-5, r=0x5000, odt=1, chunk=4, ws=0x10000, wsb=need)
+
+    def call(**kw):
+        a = {**ok_args, **kw}
+        return agg(kw.get("src", src), a["S"], a["T"], a["d"], a["sdt"], a["w"], a["eps"], a["r"], a["odt"],
+                   None, a["chunk"], a["ws"], a["wsb"], None, None)
+
+    assert call(S=0) == native.ATTNRES_EINVAL
+    assert call(S=129) == native.ATTNRES_ERANGE
+    assert call(sdt=5) == native.ATTNRES_EDTYPE
+    assert call(T=-1) == native.ATTNRES_EINVAL
+    assert call(d=0) == native.ATTNRES_EINVAL
+    assert call(eps=float("inf")) == native.ATTNRES_EINVAL
+    assert call(chunk=0) == native.ATTNRES_EINVAL
+    assert call(w=None) == native.ATTNRES_EINVAL
+    assert call(r=None) == native.ATTNRES_EINVAL
+    assert call(ws=None) == native.ATTNRES_EINVAL
+    assert call(ws=0x10010) == native.ATTNRES_EINVAL
+    assert b"256-byte" in native.lib.attnres_last_error()
+    assert call(wsb=need - 1) == native.ATTNRES_ERANGE
+    assert b"one slot" in native.lib.attnres_last_error()
+    assert call(src=(ctypes.c_void_p * 3)(0x1000, 0x2000, None)) == native.ATTNRES_EINVAL
+    assert b"sources_host[2]" in native.lib.attnres_last_error()
+    assert call(T=1 << 40, d=7168) == native.ATTNRES_ERANGE
+    # T = 0: nothing copied or launched, buffers may be NULL
+    assert agg(src, 3, 0, 8, 1, None, 1e-5, None, 1, None, 4, None, 0, None, None) == 0
+
+
 def test_backward_rejects_bad_arguments_before_any_launch(native):
     bwd = native.lib.attnres_aggregate_backward
     src = (ctypes.c_void_p * 2)(0x1000, 0x2000)

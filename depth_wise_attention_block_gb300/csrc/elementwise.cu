@@ -91,6 +91,26 @@ __global__ void __launch_bounds__(kEwThreads) fold_kernel(const T* prev, const T
 
 // ------------------------------------------------------- synthetic layer --
 
+// tanh of the stand-in body.  With bf16 storage it is the hardware
+// approximation (tanh.approx.f32, relative error about 2^-11 by the PTX ISA):
+// below half a bf16 ulp (2^-9 relative), so a stored value moves by at most
+// one ulp, and only where the exact value lies next to a rounding boundary;
+// tanhf costs enough instructions to hold an L2-warm layer body to ~60 % of
+// the copy rate.  fp32 storage keeps tanhf.  The gradient kernel keeps tanhf
+// for both: 1 - tanh^2 would magnify the approximation's error near |tanh| = 1.
+template <typename T>
+__device__ __forceinline__ float body_tanh(float x);
+template <>
+__device__ __forceinline__ float body_tanh<bf16_t>(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+template <>
+__device__ __forceinline__ float body_tanh<float>(float x) {
+  return tanhf(x);
+}
+
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, const float* __restrict__ g,
                                                                  const float* __restrict__ s, T* out,
@@ -133,7 +153,7 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, con
             float f[E];
             Vec16<T>::unpack(v[u], f);
 #pragma unroll
-            for (int e = 0; e < E; ++e) f[e] = tanhf(f[e] * gg[e]) * ss[e];
+            for (int e = 0; e < E; ++e) f[e] = body_tanh<T>(f[e] * gg[e]) * ss[e];
             O4[t * vrow] = Vec16<T>::pack(f);
           }
         }
@@ -142,7 +162,7 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, con
   } else {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
       const int c = (int)(i % d);
-      store_elem(out + i, tanhf(load_elem(x + i) * g[c]) * s[c]);
+      store_elem(out + i, body_tanh<T>(load_elem(x + i) * g[c]) * s[c]);
     }
   }
 }
@@ -226,14 +246,16 @@ static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 
 // Grid of the channel-vector kernels: x covers the vrow vectors of a row
 // with kColThreads threads per block, y strides over the tokens, sized to
-// fill every SM at full occupancy.
+// threads_per_sm on every SM.  The forward body streams fastest with 1024
+// threads per SM (each walks more tokens, fewer blocks); its gradient reads
+// three rows per token and keeps 2048.
 constexpr int kColThreads = 128;
 
-static dim3 col_grid(int vrow, long long T_) {
+static dim3 col_grid(int vrow, long long T_, int threads_per_sm) {
   DeviceInfo di;
   if (device_info(&di) != cudaSuccess) di.sm_count = 1;
   const int gx = (vrow + kColThreads - 1) / kColThreads;
-  long long gy = (long long)di.sm_count * (2048 / kColThreads) / gx;
+  long long gy = (long long)di.sm_count * (threads_per_sm / kColThreads) / gx;
   if (gy > T_) gy = T_;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
@@ -278,7 +300,7 @@ static cudaError_t launch_synth_t(const void* x, const float* g, const float* s,
   const T* X = static_cast<const T*>(x);
   T* O = static_cast<T*>(out);
   const cudaError_t e =
-      vec ? launch_kernel(synth_layer_kernel<T, true>, col_grid(d / E, T_), dim3(kColThreads), 0, st, X, g, s, O, T_, d)
+      vec ? launch_kernel(synth_layer_kernel<T, true>, col_grid(d / E, T_, 1024), dim3(kColThreads), 0, st, X, g, s, O, T_, d)
           : launch_kernel(synth_layer_kernel<T, false>, dim3(ew_grid(n)), dim3(kEwThreads), 0, st, X, g, s, O, T_, d);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -302,7 +324,7 @@ static cudaError_t launch_synth_bwd_t(const void* x, const float* g, const float
   const T* B = static_cast<const T*>(dvb);
   T* O = static_cast<T*>(dx);
   const cudaError_t e =
-      vec ? launch_kernel(synth_layer_backward_kernel<T, true>, col_grid(d / E, T_), dim3(kColThreads), 0, st, X, g, s,
+      vec ? launch_kernel(synth_layer_backward_kernel<T, true>, col_grid(d / E, T_, 2048), dim3(kColThreads), 0, st, X, g, s,
                           A, B, O, T_, d)
           : launch_kernel(synth_layer_backward_kernel<T, false>, dim3(ew_grid(n)), dim3(kEwThreads), 0, st, X, g, s, A,
                           B, O, T_, d);

@@ -153,6 +153,33 @@ def test_fused_equals_unfused_bit_for_bit(A):
         assert torch.equal(b1, b2)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("T,d", [(300, 7168), (37, 100)])
+def test_synthetic_layer_against_oracle(A, dtype, T, d):
+    # The stand-in body F(x) = tanh(x g) s element by element against the
+    # oracle on the same stored inputs.  fp32 storage: a few fp32 ulps of the
+    # exact value.  bf16 storage (its tanh is the hardware approximation,
+    # well below half a bf16 ulp): within one bf16 ulp of the exact value,
+    # and nearly always its correctly rounded value.  d = 100 takes the
+    # plain-load kernel, d = 7168 the vector one.
+    gen = torch.Generator().manual_seed(41 + d)
+    x = (torch.randn(T, d, generator=gen) * 2.0).to(dtype)
+    G = torch.randn(d, generator=gen)
+    Sc = 0.05 + 0.15 * torch.rand(d, generator=gen)
+    out = torch.full((T, d), float("nan"), dtype=dtype, device="cuda")
+    A.attnres_synthetic_layer(x.cuda(), G.cuda(), Sc.cuda(), out)
+    torch.cuda.synchronize()
+    ref = O.synthetic_layer(to64(x), to64(G), to64(Sc))
+    got = to64(out)
+    err = np.abs(got - ref)
+    if dtype == torch.float32:
+        assert (err <= 1e-6 * np.abs(ref) + 1e-30).all(), f"worst {float((err / np.abs(ref)).max()):.3g} relative"
+    else:
+        assert (err <= ulp_bf16(ref)).all(), "a bf16 output is more than one ulp from the exact value"
+        off = float((got != O.round_bf16(ref)).mean())
+        assert off < 0.02, f"{off:.2%} of the outputs are not the correctly rounded value"
+
+
 def test_cuda_graph_replay_matches_eager(A):
     stk = W.stack(T=64, num_layers=20, block_size=12, seed=5, device="cuda")
     eager = _gpu_stack(A, stk)

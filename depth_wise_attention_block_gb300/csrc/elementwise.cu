@@ -9,7 +9,7 @@
 //  synth_layer_kernel the stand-in layer body F(x) = tanh(x * g) * s used to
 //                     drive a stack without trained weights.
 //  synth_layer_backward_kernel  its gradient, dx = (dv_a + dv_b) *
-//                     (1 - tanh(x g)^2) * g * s (dv_b optional).
+//                     sech(x g)^2 * g * s (dv_b optional).
 //
 // Both are HBM-bound streams: 16-byte vector accesses when every pointer is
 // 16-byte aligned and rows hold whole vectors, scalar accesses otherwise;
@@ -96,8 +96,7 @@ __global__ void __launch_bounds__(kEwThreads) fold_kernel(const T* prev, const T
 // below half a bf16 ulp (2^-9 relative), so a stored value moves by at most
 // one ulp, and only where the exact value lies next to a rounding boundary;
 // tanhf costs enough instructions to hold an L2-warm layer body to ~60 % of
-// the copy rate.  fp32 storage keeps tanhf.  The gradient kernel keeps tanhf
-// for both: 1 - tanh^2 would magnify the approximation's error near |tanh| = 1.
+// the copy rate.  fp32 storage keeps tanhf.
 template <typename T>
 __device__ __forceinline__ float body_tanh(float x);
 template <>
@@ -109,6 +108,18 @@ __device__ __forceinline__ float body_tanh<bf16_t>(float x) {
 template <>
 __device__ __forceinline__ float body_tanh<float>(float x) {
   return tanhf(x);
+}
+
+// sech^2(u) = 1 - tanh(u)^2, the derivative of tanh, for the gradient of the
+// stand-in body.  From one exponential: with E = exp(-2|u|) in (0, 1],
+// sech^2(u) = 4E / (1 + E)^2.  Every term is positive, so nothing cancels
+// (1 - tanh^2 loses the relative precision of its small values where |tanh|
+// nears 1); the fast exponential's relative error grows like |u| 2^-23,
+// a few fp32 ulps where sech^2 is not negligible.
+__device__ __forceinline__ float sech2(float u) {
+  const float E = __expf(-2.f * fabsf(u));
+  const float q = 1.f + E;
+  return __fdividef(4.f * E, q * q);
 }
 
 template <typename T, bool VEC>
@@ -220,10 +231,7 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_backward_kernel(const 
               for (int e = 0; e < E; ++e) ga[e] += gb[e];
             }
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-              const float th = tanhf(f[e] * gg[e]);
-              f[e] = ga[e] * (1.f - th * th) * gg[e] * ss[e];
-            }
+            for (int e = 0; e < E; ++e) f[e] = ga[e] * sech2(f[e] * gg[e]) * gg[e] * ss[e];
             O4[t * vrow] = Vec16<T>::pack(f);
           }
         }
@@ -234,8 +242,7 @@ __global__ void __launch_bounds__(kEwThreads) synth_layer_backward_kernel(const 
       const int c = (int)(i % d);
       float dv = load_elem(dva + i);
       if (dvb) dv += load_elem(dvb + i);
-      const float th = tanhf(load_elem(x + i) * g[c]);
-      store_elem(dx + i, dv * (1.f - th * th) * g[c] * s[c]);
+      store_elem(dx + i, dv * sech2(load_elem(x + i) * g[c]) * g[c] * s[c]);
     }
   }
 }

@@ -180,6 +180,36 @@ def test_synthetic_layer_against_oracle(A, dtype, T, d):
         assert off < 0.02, f"{off:.2%} of the outputs are not the correctly rounded value"
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("T,d,two", [(300, 7168, True), (300, 7168, False), (37, 100, True)])
+def test_synthetic_layer_backward_against_oracle(A, dtype, T, d, two):
+    # grad_x = (dv_a + dv_b) sech(x g)^2 g s element by element against the
+    # oracle on the same stored inputs (dv_a + dv_b summed in fp32 first, as
+    # the kernel does; exact for bf16 gradients).  fp32: within 1e-5 of the
+    # value plus 1e-6 of the scale |dv g s| (sech^2 <= 1); bf16: within one
+    # bf16 ulp of the exact value.
+    gen = torch.Generator().manual_seed(43 + d)
+    x = (torch.randn(T, d, generator=gen) * 2.0).to(dtype)
+    G = torch.randn(d, generator=gen)
+    Sc = 0.05 + 0.15 * torch.rand(d, generator=gen)
+    dva = torch.randn(T, d, generator=gen).to(dtype)
+    dvb = torch.randn(T, d, generator=gen).to(dtype) if two else None
+    gx = torch.full((T, d), float("nan"), dtype=dtype, device="cuda")
+    A.attnres_synthetic_layer_backward(x.cuda(), G.cuda(), Sc.cuda(), dva.cuda(),
+                                       dvb.cuda() if two else None, gx)
+    torch.cuda.synchronize()
+    dv = to64(dva) + (to64(dvb) if two else 0.0)
+    if dtype == torch.float32:
+        dv = dv.astype(np.float32).astype(np.float64)  # the kernel's fp32 sum
+    ref = O.synthetic_layer_backward(to64(x), to64(G), to64(Sc), dv)
+    scale = np.abs(dv * to64(G) * to64(Sc))
+    err = np.abs(to64(gx) - ref)
+    if dtype == torch.float32:
+        assert (err <= 1e-5 * np.abs(ref) + 1e-6 * scale).all(), f"worst {float((err / (scale + 1e-30)).max()):.3g}"
+    else:
+        assert (err <= ulp_bf16(ref) + 1e-6 * scale).all(), "a bf16 gradient is more than one ulp off"
+
+
 def test_cuda_graph_replay_matches_eager(A):
     stk = W.stack(T=64, num_layers=20, block_size=12, seed=5, device="cuda")
     eager = _gpu_stack(A, stk)

@@ -241,6 +241,44 @@ def time_oracle(H_cpu: torch.Tensor, w_cpu: torch.Tensor, budget_s: float, chunk
             return tokens, el, out
 
 
+def time_oracle_all_cores(H_cpu: torch.Tensor, w_cpu: torch.Tensor, budget_s: float, tokens_each: int = 256,
+                          chunk: int = 64):
+    """The oracle as it stands on every host core at once: one process per
+    core (`python -m oracle.cpu_rate`, numpy and the oracle only), each on
+    its own tokens_each-token slice of the workload, all timed from one
+    wall-clock instant.  Returns (tokens, seconds, processes): every
+    process's tokens over the union of their timed spans."""
+    import tempfile
+    procs_n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    T = H_cpu.shape[1]
+    with tempfile.TemporaryDirectory() as tmp:
+        bits_path, w_path = os.path.join(tmp, "bits.npy"), os.path.join(tmp, "w.npy")
+        np.save(bits_path, H_cpu.view(torch.int16).numpy().view(np.uint16))
+        np.save(w_path, w_cpu.float().numpy())
+        start_at = time.time() + 5.0
+        procs = []
+        for i in range(procs_n):
+            t0 = (i * tokens_each) % max(1, T - tokens_each + 1)
+            cmd = [sys.executable, "-m", "oracle.cpu_rate", bits_path, w_path, str(t0), str(tokens_each),
+                   repr(start_at), repr(budget_s), str(chunk)]
+            procs.append(subprocess.Popen(cmd, cwd=ROOT, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True))
+        got = []
+        try:
+            for p in procs:
+                out, err = p.communicate(timeout=budget_s + 300)
+                if p.returncode != 0:
+                    raise RuntimeError(f"oracle process exited {p.returncode}: {err.strip()[-200:]}")
+                got.append(json.loads(out.strip().splitlines()[-1]))
+        finally:
+            for p in procs:  # only the processes started above
+                if p.poll() is None:
+                    p.kill()
+                    p.wait()
+    tokens = sum(g["tokens"] for g in got)
+    span = max(g["end"] for g in got) - min(g["start"] for g in got)
+    return tokens, span, procs_n
+
+
 def parity_figures(H_cpu, r_gpu, a_gpu, ref):
     """Worst errors of the GPU's first tokens against the oracle's: weights
     (absolute, bound 1e-5) and r (relative to the bf16 bar: one bf16 ulp of
@@ -584,6 +622,15 @@ def run_gpu(args):
         cpu = {"value": tok / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{tok} tokens of the {T_MAIN}-token workload in 64-token chunks "
                          f"(single-threaded numpy fp64, {el:.1f} s)"}
+        if not args.no_cpu_all_cores:
+            try:
+                tok_n, el_n, procs_n = time_oracle_all_cores(probe["H"], probe["w"], args.cpu_seconds)
+                cpu["all_cores"] = {"value": tok_n / el_n if el_n > 0 else None, "unit": "tokens/s",
+                                    "cores": procs_n,
+                                    "sample": f"{procs_n} processes, each on its own 256 tokens of the workload "
+                                              f"in 64-token chunks, {tok_n} tokens in {el_n:.1f} s"}
+            except Exception as exc:  # the all-cores figure is an extra: report, do not fail the line
+                cpu["all_cores"] = {"error": str(exc)}
         if ref is not None:
             parity = parity_figures(probe["H"], probe["r"], probe["a"], ref)
 
@@ -629,6 +676,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true", help="skip the stack and long-context workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-all-cores", action="store_true", help="time the oracle on one core only")
     ap.add_argument("--only", choices=["stacks", "long", "backward", "stack_backward"],
                     help="run one secondary workload alone")
     args = ap.parse_args()

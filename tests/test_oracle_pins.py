@@ -506,3 +506,31 @@ def test_synthetic_layer_backward_closed_form():
     one = np.ones(3)
     np.testing.assert_allclose(O.synthetic_layer_backward(np.zeros(3), g, s, one), g * s, rtol=0, atol=0)
     assert np.all(np.abs(O.synthetic_layer_backward(np.full(3, 40.0), g, s, one)) < 1e-20)
+
+
+def test_cpu_rate_process_runs_the_oracle_on_its_slice(tmp_path):
+    # the bench's all-cores CPU baseline starts this module once per core;
+    # its widening of bf16 bit patterns must be exact and it must report
+    # whole chunks of its own tokens
+    import json
+    import subprocess
+    import sys
+    import time
+    rng = np.random.default_rng(5)
+    S, T, d = 3, 40, 16
+    x = rng.standard_normal((S, T, d)).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)  # truncated to bf16 patterns
+    w = (rng.standard_normal(d) / 4).astype(np.float32)
+    np.save(tmp_path / "bits.npy", bits)
+    np.save(tmp_path / "w.npy", w)
+    from oracle.cpu_rate import run
+    h = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(h, (x.view(np.uint32) & 0xFFFF0000).view(np.float32).astype(np.float64))
+    res = run(str(tmp_path / "bits.npy"), str(tmp_path / "w.npy"), 8, 24, 0.0, 0.05, 8)
+    assert res["tokens"] > 0 and res["tokens"] % 8 == 0 and res["end"] >= res["start"]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-m", "oracle.cpu_rate", str(tmp_path / "bits.npy"),
+                          str(tmp_path / "w.npy"), "0", "16", repr(time.time()), "0.05", "8"],
+                         cwd=root, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert json.loads(out.stdout.strip().splitlines()[-1])["tokens"] > 0

@@ -510,8 +510,12 @@ def bench_stack_backward(A, W, dev, peak, reps=5):
     return out
 
 
-def bench_long(A, W, dev, peak, reps=8):
-    inp = W.block_T131072_d7168(device=dev)
+def bench_long(A, W, dev, peak, reps=8, tokens=None):
+    """The long-context layer (T = 131072, x50 outliers on 1% of tokens);
+    `tokens` runs the same recipe at another length (a small case for
+    profiling)."""
+    inp = W.block_T131072_d7168(device=dev) if tokens is None else \
+        W.block_bf16(T=tokens, seed=4, device=dev, outlier_frac=0.01)
     T = inp.H.shape[1]
     r = torch.empty((T, D_MAIN), dtype=torch.bfloat16, device=dev)
     a = torch.empty((T, S_MAIN), dtype=torch.float32, device=dev)
@@ -528,9 +532,39 @@ def bench_long(A, W, dev, peak, reps=8):
     gbs = algorithmic_bytes(T, D_MAIN, S_MAIN) / (ms * 1e-3) / 1e9
     del inp, r, a
     torch.cuda.empty_cache()
-    return {"block_attnres_single_layer_T131072_d7168_S9": {
+    return {f"block_attnres_single_layer_T{T}_d7168_S9": {
         "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": algorithmic_bytes(T, D_MAIN, S_MAIN),
         "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}}
+
+
+def bench_full(A, W, dev, peak, reps=10, tokens=None, source_counts=(18, 47, 94)):
+    """Full AttnRes single layers (block size 1: every earlier layer output
+    is a source) at T = 2048 over S = 18, 47 and 94 bf16 sources: the
+    multi-group kernel.  Each source row read once, r (bf16) and the weights
+    (fp32) written once; launches back to back, CUDA events at the ends."""
+    T = tokens or 2048
+    out = {}
+    for S in source_counts:
+        inp = W.full_bf16(T=T, S=S, seed=5, device=dev)
+        r = torch.empty((T, D_MAIN), dtype=torch.bfloat16, device=dev)
+        a = torch.empty((T, S), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            A.attnres_aggregate(inp.H, inp.w, r, a)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            A.attnres_aggregate(inp.H, inp.w, r, a)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        by = algorithmic_bytes(T, D_MAIN, S)
+        out[f"full_attnres_single_layer_T{T}_d7168_S{S}"] = {
+            "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": by,
+            "achieved_gbs": by / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": by / (ms * 1e-3) / 1e9 / peak}
+        del inp, r, a
+        torch.cuda.empty_cache()
+    return out
 
 
 def bench_backward(A, W, dev, peak, reps=20):
@@ -568,8 +602,12 @@ def run_only(args):
     import depth_wise_attention_block_gb300 as A
     import workloads as W
     peak, _ = hbm_peak()
-    res = {"stacks": bench_stacks, "long": bench_long, "backward": bench_backward,
-           "stack_backward": bench_stack_backward}[args.only](A, W, dev, peak)
+    if args.only in ("long", "full"):
+        fn = bench_long if args.only == "long" else bench_full
+        res = fn(A, W, dev, peak, tokens=args.tokens)
+    else:
+        res = {"stacks": bench_stacks, "backward": bench_backward,
+               "stack_backward": bench_stack_backward}[args.only](A, W, dev, peak)
     print(json.dumps(res), flush=True)
 
 
@@ -613,6 +651,7 @@ def run_gpu(args):
     if not args.no_extras:
         extras.update(bench_stacks(A, W, dev, peak))
         extras.update(bench_long(A, W, dev, peak))
+        extras.update(bench_full(A, W, dev, peak))
         extras.update(bench_backward(A, W, dev, peak))
         extras.update(bench_stack_backward(A, W, dev, peak))
 
@@ -677,7 +716,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the stack and long-context workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cpu-all-cores", action="store_true", help="time the oracle on one core only")
-    ap.add_argument("--only", choices=["stacks", "long", "backward", "stack_backward"],
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="token count of the --only long / --only full workloads (small cases for profiling)")
+    ap.add_argument("--only", choices=["stacks", "long", "full", "backward", "stack_backward"],
                     help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:

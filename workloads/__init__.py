@@ -98,6 +98,24 @@ def block_bf16(T: int = 4096, d: int = D_MODEL, seed: int = 1, device="cpu",
     return SingleLayer(H=H, w=w, outlier_tokens=otok, outlier_sources=osrc)
 
 
+def full_bf16(T: int = 2048, d: int = D_MODEL, S: int = 94, seed: int = 5, device="cpu",
+              out_sigma: float = 0.1) -> SingleLayer:
+    """Full AttnRes single layer over S sources stored as one bf16 [S, T, d]
+    slab: the embedding h_0 ~ N(0, 1) and S - 1 earlier layer outputs
+    ~ N(0, out_sigma^2) (the stand-in body's outputs are bounded by its
+    scale s <= 0.2); w ~ N(0, 1/d)."""
+    g = _gen(seed, device)
+    H = torch.empty((S, T, d), dtype=torch.bfloat16, device=device)
+    for s in range(S):
+        x = torch.randn((T, d), generator=g, device=device, dtype=torch.float32)
+        if s > 0:
+            x.mul_(out_sigma)
+        H[s] = x.to(torch.bfloat16)
+        del x
+    w = torch.randn((d,), generator=g, device=device) / math.sqrt(d)
+    return SingleLayer(H=H, w=w)
+
+
 @dataclass
 class Stack:
     """Inputs of a synthetic L-layer Block AttnRes stack forward."""

@@ -225,6 +225,12 @@ int attnres_aggregate_host(const void* const* sources_host, int S, int64_t T, in
 
   const int64_t es = dtype_bytes(src_dtype), os = dtype_bytes(out_dtype);
   cudaStream_t user = static_cast<cudaStream_t>(stream);
+  // Copies on streams of its own cannot join a capture: refuse it up front
+  // rather than invalidate the caller's capture half way.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(user, &cap);
+  if (ce != cudaSuccess) return cuda_fail(ce, "attnres_aggregate_host: cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone) return fail(ATTNRES_EINVAL, "stream is being captured into a graph");
   HostPipe pipe;
   cudaError_t e = pipe.create(nslots);
   if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate_host: creating copy streams/events");

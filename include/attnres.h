@@ -129,7 +129,8 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
  *             results, so synchronise `stream` before reading them or
  *             writing the inputs again.  The copies run on two streams that
  *             the call creates and destroys (CUDA defers their release until
- *             their work is done); not for use under stream capture.
+ *             their work is done).  A stream being captured into a graph
+ *             is refused (ATTNRES_EINVAL).
  * Other arguments, bounds and errors as attnres_aggregate; nothing is
  * copied or launched when an argument is rejected.
  * ---------------------------------------------------------------------- */

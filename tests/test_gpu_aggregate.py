@@ -307,3 +307,20 @@ def test_aggregate_host_orders_after_stream_work(lib):
     done.synchronize()
     r_dev, a_dev = _run(lib, H.cuda(), w.cuda(), torch.float32)
     assert torch.equal(r_host, r_dev.cpu()) and torch.equal(a_host, a_dev.cpu())
+
+
+def test_aggregate_host_refuses_a_capturing_stream(lib):
+    # its copy streams cannot join a graph capture: the call is refused
+    # before it enqueues anything, and the capture itself stays valid
+    S, T, d = 2, 16, 256
+    H_host = torch.randn(S, T, d).pin_memory()
+    w_host = torch.randn(d).pin_memory()
+    r_host = torch.empty((T, d), dtype=torch.float32, pin_memory=True)
+    nbytes = lib.attnres_aggregate_host_workspace_size(S, 8, d, torch.float32, torch.float32, False, 2)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with pytest.raises(lib.AttnresError, match="captured"):
+        with torch.cuda.graph(graph, stream=side):
+            lib.attnres_aggregate_host(H_host, w_host, r_host, None, workspace=ws, chunk_tokens=8, stream=side)
+    torch.cuda.synchronize()

@@ -95,6 +95,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
     }
   };
 
+  // the value of a group's [dot_0, ss_0, dot_1, ss_1, ...] partials whose
+  // warp total this lane holds after the reduce-scatter (-1: none)
+  const int rs_idx = rs_lane_index<2 * GS>(lane);
   int iter = 0;  // groups processed by this CTA (selects the reduction buffer)
   bool abort = false;
   for (long long t = blockIdx.x; t < T && !abort; t += gridDim.x) {
@@ -109,12 +112,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       const int buf = iter & 1;
       volatile int* abort_flag = &sh.abort_flag[buf];
       uint4 x[GS][VPT];
-      float part[2 * kRingSmax];
-#pragma unroll
-      for (int s = 0; s < kRingSmax; ++s) {
-        part[2 * s] = 0.f;
-        part[2 * s + 1] = 0.f;
-      }
+      float part[2 * GS];  // every entry is set below
 #pragma unroll
       for (int s = 0; s < GS; ++s) {
         {
@@ -168,12 +166,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
         }
       }
 
-      // ---- warp totals (reduce-scatter), then one CTA-wide step
-      reduce_scatter18(part, lane);
-      if ((kRsValidLanes >> lane) & 1u) {
-        const int idx = rs_index(lane);
-        if (idx < 2 * GS) sh.red[buf][warp][idx] = part[0];
-      }
+      // ---- warp totals (a reduce-scatter over the group's 2 GS partials:
+      // 13 shuffles for GS = 6), then one CTA-wide step
+      reduce_scatter<2 * GS>(part, lane);
+      if (rs_idx >= 0) sh.red[buf][warp][rs_idx] = part[0];
       const bool warp_failed = __any_sync(0xffffffffu, !ok);
       if (lane == 0 && warp_failed) *abort_flag = 1;
       named_barrier_sync(kRingBarrierId, kRingConsumers);

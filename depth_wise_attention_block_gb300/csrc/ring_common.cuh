@@ -138,15 +138,6 @@ __device__ __forceinline__ void reduce_scatter18(float* v, int lane) {
   rs_level<2, 1, 1>(v, lane);
 }
 
-// The same after its first level (offset 16) was done by the caller: v holds
-// 9 values per lane, value i of the lanes with bit 4 clear and value 9 + i
-// of the others.
-__device__ __forceinline__ void reduce_scatter18_after_first(float* v, int lane) {
-  rs_level<9, 5, 8>(v, lane);
-  rs_level<5, 3, 4>(v, lane);
-  rs_level<3, 2, 2>(v, lane);
-  rs_level<2, 1, 1>(v, lane);
-}
 
 // Generic reduce-scatter of N <= 32 per-lane values over the warp, halving
 // the kept range at each of the offsets 16, 8, 4, 2, 1 (lower lanes keep the
@@ -170,23 +161,54 @@ template <int N>
 __device__ __forceinline__ void reduce_scatter(float* v, int lane) {
   rs_levels<N, 16>(v, lane);
 }
-// index held by a lane after reduce_scatter<N>, or -1 if it holds padding
+// The same after its first level (offset 16, lower lanes keeping values
+// [0, (N+1)/2)) was done by the caller: v holds (N+1)/2 values per lane.
 template <int N>
-__device__ __forceinline__ int rs_lane_index(int lane) {
-  int n = N, base = 0, len = N;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const int K = (n + 1) / 2;
-    if (lane & off) {
-      base += K;
-      len = len > K ? len - K : 0;
-    } else {
-      len = len < K ? len : K;
-    }
+__device__ __forceinline__ void reduce_scatter_after_first(float* v, int lane) {
+  rs_levels<(N + 1) / 2, 8>(v, lane);
+}
+// Size of the kept half at level `level` (0: offset 16 ... 4: offset 1) of
+// reduce_scatter<N>; it does not depend on which half a lane keeps.
+__host__ __device__ constexpr int rs_split(int N, int level) {
+  int n = N, K = 0;
+  for (int i = 0; i <= level; ++i) {
+    K = (n + 1) / 2;
     n = K;
   }
-  return len >= 1 ? base : -1;
+  return K;
 }
+// Lanes left holding a value after reduce_scatter<N> (the others hold
+// padding or a duplicate).
+__host__ __device__ constexpr uint32_t rs_valid_mask(int N) {
+  uint32_t m = 0;
+  for (int lane = 0; lane < 32; ++lane) {
+    int n = N, len = N;
+    for (int off = 16; off >= 1; off >>= 1) {
+      const int K = (n + 1) / 2;
+      if (lane & off) len = len > K ? len - K : 0;
+      else len = len < K ? len : K;
+      n = K;
+    }
+    if (len >= 1) m |= 1u << lane;
+  }
+  return m;
+}
+template <int N>
+struct RsMap {
+  static constexpr uint32_t kValid = rs_valid_mask(N);
+  static constexpr int K0 = rs_split(N, 0), K1 = rs_split(N, 1), K2 = rs_split(N, 2), K3 = rs_split(N, 3),
+                       K4 = rs_split(N, 4);
+};
+// index held by a lane after reduce_scatter<N>, or -1 if it holds padding:
+// the upper half taken at a level adds that level's kept size
+template <int N>
+__device__ __forceinline__ int rs_lane_index(int lane) {
+  using M = RsMap<N>;
+  const int idx = M::K0 * ((lane >> 4) & 1) + M::K1 * ((lane >> 3) & 1) + M::K2 * ((lane >> 2) & 1) +
+                  M::K3 * ((lane >> 1) & 1) + M::K4 * (lane & 1);
+  return ((M::kValid >> lane) & 1u) ? idx : -1;
+}
+static_assert(RsMap<18>::kValid == kRsValidLanes, "the 18-value map of the general form");
 
 // store EPV output values of vector `vec` of an output row
 template <typename Tout, int EPV>

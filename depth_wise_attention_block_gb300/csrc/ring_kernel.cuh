@@ -90,22 +90,26 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
     }
   };
 
+  // NR: the sources the reductions carry (the fixed count, else 9).  A
+  // token's partials are [dot(w, h_0..h_NR-1), sum(h_0^2)..sum(h_NR-1^2)],
+  // summed over the warp by a reduce-scatter of 2 NR values (20 shuffles at
+  // NR = 9, 6 at NR = 2).
+  constexpr int NR = SC ? SC : kRingSmax;
   int iter = 0;
   for (long long t = blockIdx.x; t < T; t += gridDim.x, ++iter) {
     const int buf = iter & 1;
     volatile int* abort_flag = &sh.abort_flag[buf];
     uint4 x[kRingSmax][VPT];
-    // Partials laid out as [dot(w, h_0..h_8), sum(h_0^2)..sum(h_8^2)].  With
-    // kEarlyRs, per source, this thread's dot and sum of squares enter the
-    // first level of the warp reduce-scatter at once: lanes with bit 4 clear
-    // keep the dot products, the others the sums of squares, each adding its
-    // partner's (lane ^ 16).
+    // With kEarlyRs, per source, this thread's dot and sum of squares enter
+    // the first level of the warp reduce-scatter at once: lanes with bit 4
+    // clear keep the dot products, the others the sums of squares, each
+    // adding its partner's (lane ^ 16).
     const bool upper16 = (lane & 16) != 0;
-    float part[kEarlyRs ? kRingSmax : 2 * kRingSmax];
+    float part[kEarlyRs ? NR : 2 * NR];
 #pragma unroll
-    for (int s = 0; s < (kEarlyRs ? kRingSmax : 2 * kRingSmax); ++s) part[s] = 0.f;
+    for (int s = 0; s < (kEarlyRs ? NR : 2 * NR); ++s) part[s] = 0.f;
 #pragma unroll
-    for (int s = 0; s < kRingSmax; ++s) {
+    for (int s = 0; s < NR; ++s) {
       if (s < S) {
         if (!FUSED || s < p.n_stored) {
           consume(x[s]);
@@ -157,20 +161,20 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
           part[s] = (upper16 ? ss : dot) + __shfl_xor_sync(0xffffffffu, upper16 ? dot : ss, 16);
         } else {
           part[s] = dot;
-          part[kRingSmax + s] = ss;
+          part[NR + s] = ss;
         }
       }
     }
 
-    // ---- warp totals (reduce-scatter), then one CTA-wide step through smem
-    // remaining levels (9 -> 5 -> 3 -> 2 -> 1 values per lane); value index
-    // i < 9 is dot(w, h_i), 9 + i is sum(h_i^2), stored at [2i] and [2i + 1]
-    if constexpr (kEarlyRs) reduce_scatter18_after_first(part, lane);
-    else reduce_scatter18(part, lane);
-    if ((kRsValidLanes >> lane) & 1u) {
-      const int idx = rs_index(lane);
-      const int src = idx < kRingSmax ? idx : idx - kRingSmax;
-      if (src < S) sh.red[buf][warp][idx < kRingSmax ? 2 * idx : 2 * src + 1] = part[0];
+    // ---- warp totals (reduce-scatter), then one CTA-wide step through smem;
+    // value index i < NR is dot(w, h_i), NR + i is sum(h_i^2), stored at [2i]
+    // and [2i + 1]
+    if constexpr (kEarlyRs) reduce_scatter_after_first<2 * NR>(part, lane);
+    else reduce_scatter<2 * NR>(part, lane);
+    const int rs_idx = rs_lane_index<2 * NR>(lane);  // value whose warp total this lane holds (-1: none)
+    if (rs_idx >= 0) {
+      const int src = rs_idx < NR ? rs_idx : rs_idx - NR;
+      if (src < S) sh.red[buf][warp][rs_idx < NR ? 2 * rs_idx : 2 * src + 1] = part[0];
     }
     const bool warp_failed = __any_sync(0xffffffffu, !ok);
     if (lane == 0 && warp_failed) *abort_flag = 1;
@@ -208,22 +212,22 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
         // the registers, spilled); the empty asm makes it unpack the packed
         // registers again instead.
 #pragma unroll
-        for (int s = 0; s < kRingSmax; ++s) {
+        for (int s = 0; s < NR; ++s) {
 #pragma unroll
           for (int k = 0; k < VPT; ++k)
             asm volatile("" : "+r"(x[s][k].x), "+r"(x[s][k].y), "+r"(x[s][k].z), "+r"(x[s][k].w));
         }
       }
-      uint64_t a2[kRingSmax];
+      uint64_t a2[NR];
 #pragma unroll
-      for (int s = 0; s < kRingSmax; ++s) {
+      for (int s = 0; s < NR; ++s) {
         const float as = __shfl_sync(0xffffffffu, a, 2 * s);
         a2[s] = f2_pack(as, as);
       }
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
 #pragma unroll
-        for (int s = 0; s < kRingSmax; ++s) {
+        for (int s = 0; s < NR; ++s) {
           if (s < S) {
             uint64_t h[NP];
             Vec<Tin>::pairs(x[s][k], h);

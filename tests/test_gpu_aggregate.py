@@ -100,6 +100,9 @@ SHAPES = [
     (3, 7168, 1, torch.bfloat16, torch.bfloat16),      # S = 1
     (1, 7168, 9, torch.bfloat16, torch.bfloat16),      # T = 1
     (5, 64, 2, torch.bfloat16, torch.bfloat16),        # tiny row: 8 vectors
+    (7, 8, 9, torch.bfloat16, torch.bfloat16),         # ring, one 16-byte vector per row
+    (13, 1, 4, torch.float32, torch.float32),          # d = 1: one channel (generic)
+    (9, 1, 9, torch.bfloat16, torch.bfloat16),         # d = 1, bf16 (generic)
     # few tokens: a cluster of C CTAs per token, each a channel slice
     (64, 7168, 9, torch.bfloat16, torch.bfloat16),     # split C=2, 448 vectors per CTA (decode size)
     (19, 7168, 9, torch.bfloat16, torch.bfloat16),     # split C=8, 112 vectors: partial last warp

@@ -85,6 +85,9 @@ def _check_stack(fwd, tr, tokens, dtype, weight_tol, check_blocks=True):
     (12, 1, 5, 40, torch.float32),      # block size 1 = Full AttnRes; S reaches 13 (generic kernel)
     (9, 4, 7, 7168, torch.bfloat16),    # K3 width, ring, 2 vectors per thread
     (5, 9, 3, 24, torch.float32),       # one block holds every layer
+    (1, 12, 4, 64, torch.float32),      # one layer: the final aggregation reads [h0, v1]
+    (12, 12, 5, 256, torch.bfloat16),   # the block ends exactly at the last layer
+    (2, 1, 3, 16, torch.bfloat16),      # block size 1, two layers
 ])
 def test_tiny_stacks_every_layer(A, L, B, T, d, dtype):
     stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=31 + L + B, device="cuda", dtype=dtype)

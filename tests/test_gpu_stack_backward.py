@@ -55,6 +55,8 @@ def _run(A, L, B, T, d, seed, dtype=torch.float32):
     (14, 4, 17, 1000),    # 250 vectors per row: ragged last warp
     (5, 1, 9, 256),       # block size 1: Full AttnRes
     (6, 12, 5, 7168),     # one block: every layer reads [h0, partial]; fp32 rows of d = 7168 (plain loads)
+    (1, 12, 4, 64),       # one layer: the final aggregation reads [h0, v1]
+    (8, 4, 6, 128),       # two whole blocks, the last layer ends the second
 ])
 def test_stack_backward_matches_the_oracle(A, L, B, T, d):
     stk, dr, dh0, dW, _ = _run(A, L, B, T, d, seed=50 + L + B)

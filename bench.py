@@ -537,6 +537,31 @@ def bench_long(A, W, dev, peak, reps=8, tokens=None):
         "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}}
 
 
+def bench_small_fp32(A, W, dev, peak, reps=2000):
+    """The small fp32 Full AttnRes layer (T = 64, d = 256, S = 4; 328,704
+    algorithmic bytes): far below any bandwidth bound, so its time is the
+    launch latency; reported, not graded against the roofline."""
+    inp = W.full_T64_d256()
+    H, w = inp.H.to(dev), inp.w.to(dev)
+    S, T, d = H.shape
+    r = torch.empty((T, d), dtype=torch.float32, device=dev)
+    a = torch.empty((T, S), dtype=torch.float32, device=dev)
+    for _ in range(10):
+        A.attnres_aggregate(H, w, r, a)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        A.attnres_aggregate(H, w, r, a)
+    e1.record()
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / reps
+    by = T * (S * d * 4 + d * 4 + S * 4)
+    return {"full_attnres_fp32_T64_d256_S4": {"us_per_launch": us, "launches": reps, "algorithmic_bytes": by,
+                                              "achieved_gbs": by / (us * 1e-6) / 1e9,
+                                              "bound": "launch latency (back-to-back launches, CUDA events at the ends)"}}
+
+
 def bench_full(A, W, dev, peak, reps=10, tokens=None, source_counts=(18, 47, 94)):
     """Full AttnRes single layers (block size 1: every earlier layer output
     is a source) at T = 2048 over S = 18, 47 and 94 bf16 sources: the
@@ -655,6 +680,7 @@ def run_gpu(args):
         extras.update(bench_stacks(A, W, dev, peak))
         extras.update(bench_long(A, W, dev, peak))
         extras.update(bench_full(A, W, dev, peak))
+        extras.update(bench_small_fp32(A, W, dev, peak))
         extras.update(bench_backward(A, W, dev, peak))
         extras.update(bench_stack_backward(A, W, dev, peak))
 

@@ -234,10 +234,21 @@ int attnres_aggregate_host(const void* const* sources_host, int S, int64_t T, in
   HostPipe pipe;
   cudaError_t e = pipe.create(nslots);
   if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate_host: creating copy streams/events");
+  // On a failure part way, work issued on `stream` afterwards must still
+  // wait for every copy already queued (the caller may free the buffers
+  // once it has synchronised): join both copy streams, best effort.
+  auto join_copies = [&]() {
+    if (cudaEventRecord(pipe.start, pipe.in) == cudaSuccess) cudaStreamWaitEvent(user, pipe.start, 0);
+    if (cudaEventRecord(pipe.arrived[0], pipe.out) == cudaSuccess) cudaStreamWaitEvent(user, pipe.arrived[0], 0);
+  };
 #define HOST_CK(call)                                           \
   do {                                                          \
     cudaError_t e_ = (call);                                    \
-    if (e_ != cudaSuccess) return cuda_fail(e_, "attnres_aggregate_host: " #call); \
+    if (e_ != cudaSuccess) {                                    \
+      const int rc_ = cuda_fail(e_, "attnres_aggregate_host: " #call); \
+      join_copies();                                            \
+      return rc_;                                               \
+    }                                                           \
   } while (0)
 
   char* ws = static_cast<char*>(workspace);

@@ -130,7 +130,9 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
  *             writing the inputs again.  The copies run on two streams that
  *             the call creates and destroys (CUDA defers their release until
  *             their work is done).  A stream being captured into a graph
- *             is refused (ATTNRES_EINVAL).
+ *             is refused (ATTNRES_EINVAL).  If a CUDA call fails part way
+ *             (ATTNRES_ECUDA), the copies already queued are still joined
+ *             into `stream` before the call returns.
  * Other arguments, bounds and errors as attnres_aggregate; nothing is
  * copied or launched when an argument is rejected.
  * ---------------------------------------------------------------------- */

@@ -556,10 +556,32 @@ def bench_small_fp32(A, W, dev, peak, reps=2000):
     e1.record()
     torch.cuda.synchronize()
     us = 1e3 * e0.elapsed_time(e1) / reps
+    # the same launches replayed from a CUDA graph: the device-side latency
+    # without the Python call
+    per_graph = 100
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        A.attnres_aggregate(H, w, r, a, stream=side)  # warm (outside the capture)
+        side.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(per_graph):
+                A.attnres_aggregate(H, w, r, a, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps // per_graph):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us_graph = 1e3 * e0.elapsed_time(e1) / (per_graph * (reps // per_graph))
     by = T * (S * d * 4 + d * 4 + S * 4)
-    return {"full_attnres_fp32_T64_d256_S4": {"us_per_launch": us, "launches": reps, "algorithmic_bytes": by,
-                                              "achieved_gbs": by / (us * 1e-6) / 1e9,
-                                              "bound": "launch latency (back-to-back launches, CUDA events at the ends)"}}
+    return {"full_attnres_fp32_T64_d256_S4": {
+        "us_per_launch": us, "us_per_launch_cuda_graph": us_graph, "launches": reps, "algorithmic_bytes": by,
+        "bound": "launch latency: eager = one Python call per launch; cuda_graph = the launches replayed"}}
 
 
 def bench_full(A, W, dev, peak, reps=10, tokens=None, source_counts=(18, 47, 94)):
@@ -631,7 +653,7 @@ def run_only(args):
         fn = bench_long if args.only == "long" else bench_full
         res = fn(A, W, dev, peak, tokens=args.tokens)
     else:
-        res = {"stacks": bench_stacks, "backward": bench_backward,
+        res = {"stacks": bench_stacks, "backward": bench_backward, "small": bench_small_fp32,
                "stack_backward": bench_stack_backward}[args.only](A, W, dev, peak)
     print(json.dumps(res), flush=True)
 
@@ -750,7 +772,7 @@ def main():
     ap.add_argument("--no-cpu-all-cores", action="store_true", help="time the oracle on one core only")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count of the --only long / --only full workloads (small cases for profiling)")
-    ap.add_argument("--only", choices=["stacks", "long", "full", "backward", "stack_backward"],
+    ap.add_argument("--only", choices=["stacks", "long", "full", "small", "backward", "stack_backward"],
                     help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -56,7 +56,7 @@ def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None, contiguous=True) -> 
     # the library launches on the current device: another device's memory
     # must never reach its kernels
     cur = torch.cuda.current_device()
-    if t.device.index != cur:
+    if t.get_device() != cur:
         raise ValueError(f"{name} is on {t.device} but the current device is cuda:{cur}")
     if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -65,8 +65,14 @@ def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None, contiguous=True) -> 
     return t.data_ptr()
 
 
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_ptr(stream) -> int:
     if stream is None:
+        # the current stream's handle without building a Stream object
+        if _RAW_STREAM is not None:
+            return _RAW_STREAM(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
@@ -91,26 +97,36 @@ def attnres_aggregate(sources: Sequence[torch.Tensor] | torch.Tensor, w_l: torch
     [S, T, d] tensor; w_l: [d] float32; out_r: [T, d] float32/bfloat16;
     out_weights: [T, S] float32 or None; dev_err: int32 [1] or None.
     """
+    if isinstance(sources, torch.Tensor) and sources.dim() == 3 and not sources.is_contiguous():
+        sources = list(sources.unbind(0))  # e.g. every other source: each slice checked below
     if isinstance(sources, torch.Tensor):
+        # one contiguous [S, T, d] tensor: checked once, source s at base + s * T * d
         if sources.dim() != 3:
             raise ValueError("a stacked sources tensor must be [S, T, d]")
-        srcs = list(sources.unbind(0))
+        S, T, d = sources.shape
+        dt = sources.dtype
+        base = _dev_ptr(sources, "sources")
+        step = T * d * sources.element_size()
+        ptrs = (ctypes.c_void_p * S)(*[base + i * step for i in range(S)]) if S else None
     else:
         srcs = list(sources)
-    if not srcs:
+        S = len(srcs)
+        if not srcs:
+            raise ValueError("need at least one source")
+        T, d = srcs[0].shape
+        dt = srcs[0].dtype
+        for i, s in enumerate(srcs):
+            if s.shape != (T, d) or s.dtype != dt:
+                raise ValueError(f"source {i}: expected [{T}, {d}] {dt}, got {list(s.shape)} {s.dtype}")
+        ptrs = (ctypes.c_void_p * S)(*[_dev_ptr(s, f"sources[{i}]") for i, s in enumerate(srcs)])
+    if S < 1:
         raise ValueError("need at least one source")
-    T, d = srcs[0].shape
-    dt = srcs[0].dtype
-    for i, s in enumerate(srcs):
-        if s.shape != (T, d) or s.dtype != dt:
-            raise ValueError(f"source {i}: expected [{T}, {d}] {dt}, got {list(s.shape)} {s.dtype}")
-    ptrs = (ctypes.c_void_p * len(srcs))(*[_dev_ptr(s, f"sources[{i}]") for i, s in enumerate(srcs)])
     if out_r.shape != (T, d):
         raise ValueError("out_r must be [T, d]")
-    if out_weights is not None and out_weights.shape != (T, len(srcs)):
+    if out_weights is not None and out_weights.shape != (T, S):
         raise ValueError("out_weights must be [T, S]")
     rc = _N.lib.attnres_aggregate(
-        ptrs, len(srcs), T, d, dtype_code(dt), _dev_ptr(w_l, "w_l", torch.float32), float(eps),
+        ptrs, S, T, d, dtype_code(dt), _dev_ptr(w_l, "w_l", torch.float32), float(eps),
         _dev_ptr(out_r, "out_r"), dtype_code(out_r.dtype), _dev_ptr(out_weights, "out_weights", torch.float32),
         _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
     _N.check(rc, "attnres_aggregate")

@@ -327,3 +327,25 @@ def test_aggregate_host_refuses_a_capturing_stream(lib):
         with torch.cuda.graph(graph, stream=side):
             lib.attnres_aggregate_host(H_host, w_host, r_host, None, workspace=ws, chunk_tokens=8, stream=side)
     torch.cuda.synchronize()
+
+
+def test_stacked_list_and_strided_sources_agree(lib):
+    # the binding takes a contiguous [S, T, d] stack by pointer arithmetic, a
+    # list one tensor at a time, and a strided stack (every other source of a
+    # larger one) slice by slice: the same sources give the same bits
+    inp = W.block_bf16(T=200, d=7168, seed=12, device="cuda")
+    S, T, d = inp.H.shape
+    r1, a1 = _run(lib, inp.H, inp.w)
+    r2 = torch.empty_like(r1)
+    a2 = torch.empty_like(a1)
+    lib.attnres_aggregate(list(inp.H.unbind(0)), inp.w, r2, a2)
+    wide = torch.zeros((2 * S, T, d), dtype=inp.H.dtype, device="cuda")
+    wide[::2] = inp.H
+    r3 = torch.empty_like(r1)
+    a3 = torch.empty_like(a1)
+    lib.attnres_aggregate(wide[::2], inp.w, r3, a3)
+    torch.cuda.synchronize()
+    assert torch.equal(r1, r2) and torch.equal(a1, a2)
+    assert torch.equal(r1, r3) and torch.equal(a1, a3)
+    with pytest.raises(ValueError):
+        lib.attnres_aggregate(inp.H[:0], inp.w, r1, None)

@@ -24,6 +24,12 @@
 
 namespace attnres {
 
+// Bring the cache line holding p into L1 ahead of its use (no register
+// holds the data; a later load of the line then hits).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 struct InterParams {
   RingParams rp;  // the cached sources (n_stored = S = n), geometry, ring
   const float* wq[kMaxQueries];
@@ -86,10 +92,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
       }
     }
     float inv_rho = 0.f;  // lane 2s: 1 / rms(h_s), from the first query's reduction
-    for (int q = 0; q < ip.Q && !abort; ++q, ++iter) {
-      const int buf = iter & 1;
-      volatile int* abort_flag = &sh.abort_flag[buf];
-      uint64_t wp[VPT][NP];
+    // this thread's channels of query q's w, as pairs; the next query's are
+    // loaded as soon as the current one's dot products are taken, so their
+    // latency hides behind its softmax and weighted sum
+    uint64_t wp[VPT][NP];
+    auto load_w = [&](int q) {
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int v = tid + k * kRingConsumers;
@@ -100,6 +107,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
                              in ? __ldg(ip.wq[q] + v * EPV + 2 * j + 1) : 0.f);
         }
       }
+    };
+    load_w(0);
+    for (int q = 0; q < ip.Q && !abort; ++q, ++iter) {
+      const int buf = iter & 1;
+      volatile int* abort_flag = &sh.abort_flag[buf];
       float part[2 * kRingSmax];
 #pragma unroll
       for (int s = 0; s < kRingSmax; ++s) {
@@ -126,6 +138,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
       }
       const bool warp_failed = __any_sync(0xffffffffu, !ok);
       if (lane == 0 && warp_failed) *abort_flag = 1;
+      if (q + 1 < ip.Q) load_w(q + 1);
       named_barrier_sync(kRingBarrierId, kRingConsumers);
 
       abort = *abort_flag != 0;
@@ -227,6 +240,15 @@ __global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_c
   }
   const long long row_bytes = (long long)p.d * (long long)sizeof(Tin);
   for (long long t = blockIdx.x; t < p.T; t += gridDim.x) {
+    // the inter-block row does not depend on this token's reduction: its
+    // lines are prefetched into L1 first (no registers held), so one DRAM
+    // round trip covers both inputs
+    const float* rrow = p.r_inter + t * (long long)p.d;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * kMergeThreads;
+      if (v < p.nvec) prefetch_l1(rrow + v * EPV);
+    }
     uint4 x[VPT];
     float c1 = 1.f, c2 = 0.f;
     if (has_p) {
@@ -283,7 +305,6 @@ __global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_c
     }
     const uint64_t c1p = f2_pack(c1, c1), c2p = f2_pack(c2, c2);
     char* orow = p.out_r + t * row_bytes;
-    const float* rrow = p.r_inter + t * (long long)p.d;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * kMergeThreads;

@@ -349,3 +349,18 @@ def test_stacked_list_and_strided_sources_agree(lib):
     assert torch.equal(r1, r3) and torch.equal(a1, a3)
     with pytest.raises(ValueError):
         lib.attnres_aggregate(inp.H[:0], inp.w, r1, None)
+
+
+def test_aggregate_host_multi_group_fp32_out(lib):
+    # more than 9 sources (the multi-group kernel) through the host-buffer
+    # call, fp32 output, a ragged last chunk: bit for bit the device path
+    T, d, S = 50, 7168, 20
+    inp = W.full_bf16(T=T, d=d, S=S, seed=13, device="cuda")
+    H_host, w_host = _host_copy(inp.H, True), _host_copy(inp.w, True)
+    r_host = torch.full((T, d), float("nan"), dtype=torch.float32, pin_memory=True)
+    a_host = torch.full((T, S), float("nan"), dtype=torch.float32, pin_memory=True)
+    lib.attnres_aggregate_host(H_host, w_host, r_host, a_host, chunk_tokens=16)
+    torch.cuda.synchronize()
+    r_ref, a_ref = _run(lib, inp.H, inp.w, torch.float32)
+    assert torch.equal(r_host.cuda(), r_ref) and torch.equal(a_host.cuda(), a_ref)
+    _compare(inp.H, inp.w, r_host, a_host, torch.float32)

@@ -746,7 +746,7 @@ def run_gpu(args):
                                           "pass after the timed region (each also pays the launch front end)"},
             "hbm_gbs_achieved": achieved,
             "e2e": e2e,
-            "gpu_launches": m["launches"],
+            "gpu_launches": ws * m["launches"],  # every rank launches the same K steps
             "clocks": m["clocks"],
             "cpu_baseline": cpu,
             "parity": parity,

@@ -43,6 +43,24 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 bool valid_dtype(int dt) { return dt == ATTNRES_F32 || dt == ATTNRES_BF16; }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return na > 0 && nb > 0 && pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
+}
+
+// The output r (and the weights) must not share memory with any source.
+int check_outputs_apart(const void* const* sources, int S, int64_t src_bytes, const void* out_r, int64_t r_bytes,
+                        const void* out_a, int64_t a_bytes) {
+  for (int s = 0; s < S; ++s) {
+    if (overlaps(out_r, r_bytes, sources[s], src_bytes)) return fail(ATTNRES_EINVAL, "r overlaps source %d", s);
+    if (out_a && overlaps(out_a, a_bytes, sources[s], src_bytes))
+      return fail(ATTNRES_EINVAL, "the weights overlap source %d", s);
+  }
+  if (out_a && overlaps(out_a, a_bytes, out_r, r_bytes)) return fail(ATTNRES_EINVAL, "the weights overlap r");
+  return ATTNRES_OK;
+}
+
 // T * d * 4 must stay well inside int64 (element offsets are 64-bit).
 bool size_ok(int64_t T, int d) { return T >= 0 && d >= 1 && T <= (((int64_t)1) << 40) / d; }
 
@@ -163,6 +181,11 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
   if (!w_l || !out_r) return fail(ATTNRES_EINVAL, "w_l/out_r is NULL");
   for (int s = 0; s < S; ++s)
     if (!sources[s]) return fail(ATTNRES_EINVAL, "sources[%d] is NULL", s);
+  {
+    const int64_t isz = src_dtype == ATTNRES_BF16 ? 2 : 4, osz = out_dtype == ATTNRES_BF16 ? 2 : 4;
+    const int rc = check_outputs_apart(sources, S, T * d * isz, out_r, T * d * osz, out_weights, T * S * 4);
+    if (rc != ATTNRES_OK) return rc;
+  }
   AggArgs a{};
   for (int s = 0; s < S; ++s) a.src[s] = sources[s];
   a.n_stored = S;
@@ -212,6 +235,11 @@ int attnres_aggregate_host(const void* const* sources_host, int S, int64_t T, in
   if (!w_host || !r_host || !workspace) return fail(ATTNRES_EINVAL, "w_host/r_host/workspace is NULL");
   for (int s = 0; s < S; ++s)
     if (!sources_host[s]) return fail(ATTNRES_EINVAL, "sources_host[%d] is NULL", s);
+  {
+    const int64_t isz = src_dtype == ATTNRES_BF16 ? 2 : 4, osz = out_dtype == ATTNRES_BF16 ? 2 : 4;
+    const int rc = check_outputs_apart(sources_host, S, T * d * isz, r_host, T * d * osz, weights_host, T * S * 4);
+    if (rc != ATTNRES_OK) return rc;
+  }
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(ATTNRES_EINVAL, "workspace not 256-byte aligned");
   const int64_t Tc = chunk_tokens < T ? chunk_tokens : T;
   const int64_t nchunks = (T + Tc - 1) / Tc;

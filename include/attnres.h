@@ -92,8 +92,9 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
  * eps         > 0 or 0 (1e-5 in K3)
  * out_r       device [T, d] of out_dtype; bf16 is rounded to nearest even
  * out_weights device [T, S] fp32, or NULL to skip
- * Each source row is read from device memory once.  out_r may not alias a
- * source.  Returns ATTNRES_OK or a negative attnres_status.
+ * Each source row is read from device memory once.  out_r and out_weights
+ * may not share a byte with a source or with each other (ATTNRES_EINVAL);
+ * sources may repeat.  Returns ATTNRES_OK or a negative attnres_status.
  * ---------------------------------------------------------------------- */
 int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int src_dtype,
                       const float* w_l, float eps, void* out_r, int out_dtype,

@@ -153,6 +153,30 @@ def test_aggregate_rejects_bad_arguments_before_any_launch(native):
     assert agg(src, 3, 0, 8, 1, None, 1e-5, None, 1, None, None, None) == 0
 
 
+def test_outputs_overlapping_a_source_are_refused(native):
+    # [T, d] bf16 sources of 4 x 8 x 2 = 64 bytes at 0x10000 and 0x20000;
+    # nothing is dereferenced: the ranges are compared before any launch
+    agg = native.lib.attnres_aggregate
+    src = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+
+    def call(r, a):
+        return agg(src, 2, 4, 8, 1, 0x40000, 1e-5, r, 1, a, None, None)
+
+    assert call(0x10000 + 32, None) == native.ATTNRES_EINVAL        # r inside source 0
+    assert b"r overlaps source 0" in native.lib.attnres_last_error()
+    assert call(0x20000 - 8, None) == native.ATTNRES_EINVAL         # r's tail reaches source 1
+    assert call(0x30000, 0x10000) == native.ATTNRES_EINVAL          # weights on source 0
+    assert call(0x30000, 0x30000 + 16) == native.ATTNRES_EINVAL     # weights inside r
+    assert b"weights overlap r" in native.lib.attnres_last_error()
+    # (every call here is refused before any CUDA call: no launch ever sees
+    # these made-up addresses)
+    # the host-buffer call checks its host ranges the same way
+    host = native.lib.attnres_aggregate_host
+    need = native.lib.attnres_aggregate_host_workspace_size(2, 4, 8, 1, 1, 0, 1)
+    assert host(src, 2, 4, 8, 1, 0x40000, 1e-5, 0x20000, 1, None, 4, 0x100000, need, None, None) == \
+        native.ATTNRES_EINVAL
+
+
 def test_host_workspace_size_is_the_slot_layout(native):
     # query row, then per slot the [S, chunk, d] sources, r and the weights,
     # each part rounded up to 256 bytes; written out for the K3 block layout

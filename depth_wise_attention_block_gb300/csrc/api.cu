@@ -512,7 +512,23 @@ int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* 
   }
   for (const void* q : {a.prev, a.F, (const void*)a.dst, (const void*)r_inter, (const void*)out_r})
     if (!twophase_pointers_ok(q)) return fail(ATTNRES_EINVAL, "two-phase buffers must be 16-byte aligned");
-  if (out_r == st->partial || out_r == st->h0) return fail(ATTNRES_EINVAL, "out_r aliases the state");
+  {
+    // r and the weights must not share memory with the state's rows or F
+    const int64_t row = st->T * st->d * (st->dtype == ATTNRES_BF16 ? 2 : 4);
+    const int64_t a_bytes = st->T * attnres_num_sources(layer_idx, B, L) * 4;
+    const void* rows[ATTNRES_MAX_BLOCKS + 3];
+    int nr = 0;
+    rows[nr++] = st->h0;
+    rows[nr++] = st->partial;
+    if (F_prev) rows[nr++] = F_prev;
+    for (int k = 0; k < num_blocks(L, B); ++k)
+      if (st->block_reps[k]) rows[nr++] = st->block_reps[k];
+    rc = check_outputs_apart(rows, nr, row, out_r, row, out_weights, a_bytes);
+    if (rc != ATTNRES_OK) return rc;
+    const int64_t inter_bytes = st->T * st->d * 4;  // the fp32 inter-block aggregate
+    if (overlaps(out_r, row, r_inter, inter_bytes) || (out_weights && overlaps(out_weights, a_bytes, r_inter, inter_bytes)))
+      return fail(ATTNRES_EINVAL, "an output overlaps r_inter");
+  }
   a.w = w_l;
   a.r_inter = r_inter;
   a.lse_inter = lse_inter;
@@ -634,7 +650,20 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
   const int need = layer_idx >= 2 ? layer_idx - 2 : 0;
   if (st->folded != need)
     return fail(ATTNRES_ESTATE, "layer_step(%d) needs folded == %d, state has %d", layer_idx, need, st->folded);
-  if (out_r == st->partial || out_r == st->h0) return fail(ATTNRES_EINVAL, "out_r aliases the state");
+  {
+    // r and the weights must not share memory with the state's rows or F
+    const int64_t row = st->T * st->d * (st->dtype == ATTNRES_BF16 ? 2 : 4);
+    const int64_t a_bytes = st->T * attnres_num_sources(layer_idx, B, L) * 4;
+    const void* rows[ATTNRES_MAX_BLOCKS + 3];
+    int nr = 0;
+    rows[nr++] = st->h0;
+    rows[nr++] = st->partial;
+    if (F_prev) rows[nr++] = F_prev;
+    for (int k = 0; k < num_blocks(L, B); ++k)
+      if (st->block_reps[k]) rows[nr++] = st->block_reps[k];
+    rc = check_outputs_apart(rows, nr, row, out_r, row, out_weights, a_bytes);
+    if (rc != ATTNRES_OK) return rc;
+  }
 
   AggArgs a{};
   a.T = st->T;
@@ -656,8 +685,6 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
     a.fuse_prev = fp.has_prev ? st->partial : nullptr;
     a.fuse_F = F_prev;
     a.fuse_dst = fp.ends_block ? st->block_reps[fp.block - 1] : st->partial;
-    for (int k = 0; k < num_blocks(L, B); ++k)
-      if (out_r == st->block_reps[k]) return fail(ATTNRES_EINVAL, "out_r aliases block_reps[%d]", k);
   }
   if (a.S() != attnres_num_sources(layer_idx, B, L))
     return fail(ATTNRES_ESTATE, "internal: source count mismatch at layer %d", layer_idx);

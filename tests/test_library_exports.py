@@ -101,10 +101,12 @@ def test_stack_calls_enforce_order(native):
     assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 2, 0x777, None, None, None) == native.ATTNRES_EINVAL
     assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, 3, 0x777, None, None, None) == native.ATTNRES_ESTATE
     assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, L + 2, 0x777, None, None, None) == native.ATTNRES_EINVAL
-    # out_r may not alias the state
+    # out_r may not share memory with the state (rows of 4 x 8 bf16 = 64 B)
     st.folded = 0
     assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 1, 0x20000, None, None, None) == native.ATTNRES_EINVAL
-    assert b"alias" in native.lib.attnres_last_error()
+    assert b"overlaps" in native.lib.attnres_last_error()
+    assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 1, 0x20000 + 48, None, None, None) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 1, 0x10000 - 32, None, None, None) == native.ATTNRES_EINVAL
     assert st.folded == 0
     assert native.lib.attnres_state_reset(ctypes.byref(st)) == 0
 

@@ -61,6 +61,21 @@ int check_outputs_apart(const void* const* sources, int S, int64_t src_bytes, co
   return ATTNRES_OK;
 }
 
+// Each source gradient must share no byte with a source, with grad_r or
+// with another gradient (row = bytes of one [T, d] row).
+int check_grads_apart(const void* const* sources, void* const* grads, int S, int64_t row, const void* grad_r) {
+  for (int s = 0; s < S; ++s) {
+    for (int j = 0; j < S; ++j)
+      if (overlaps(grads[s], row, sources[j], row))
+        return fail(ATTNRES_EINVAL, "grad_sources[%d] overlaps sources[%d]", s, j);
+    for (int j = 0; j < s; ++j)
+      if (overlaps(grads[s], row, grads[j], row))
+        return fail(ATTNRES_EINVAL, "grad_sources[%d] overlaps grad_sources[%d]", s, j);
+    if (overlaps(grads[s], row, grad_r, row)) return fail(ATTNRES_EINVAL, "grad_sources[%d] overlaps grad_r", s);
+  }
+  return ATTNRES_OK;
+}
+
 // T * d * 4 must stay well inside int64 (element offsets are 64-bit).
 bool size_ok(int64_t T, int d) { return T >= 0 && d >= 1 && T <= (((int64_t)1) << 40) / d; }
 
@@ -353,10 +368,10 @@ int attnres_aggregate_backward(const void* const* sources, int S, int64_t T, int
     if (!w_l || !grad_r || !workspace) return fail(ATTNRES_EINVAL, "w_l/grad_r/workspace is NULL");
     for (int s = 0; s < S; ++s) {
       if (!sources[s] || !grad_sources[s]) return fail(ATTNRES_EINVAL, "sources[%d]/grad_sources[%d] is NULL", s, s);
-      for (int j = 0; j < S; ++j)
-        if (grad_sources[s] == sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] aliases sources[%d]", s, j);
-      for (int j = 0; j < s; ++j)
-        if (grad_sources[s] == grad_sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] == grad_sources[%d]", s, j);
+    }
+    {
+      const int rc = check_grads_apart(sources, grad_sources, S, T * d * (dtype == ATTNRES_BF16 ? 2 : 4), grad_r);
+      if (rc != ATTNRES_OK) return rc;
     }
     if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return fail(ATTNRES_EINVAL, "workspace not 4-byte aligned");
     const int64_t need = attnres_aggregate_backward_workspace_size(T, d);
@@ -404,10 +419,10 @@ int attnres_aggregate_backward_noalloc(const void* const* sources, int S, int64_
     if (!w_l || !grad_r) return fail(ATTNRES_EINVAL, "w_l/grad_r is NULL");
     for (int s = 0; s < S; ++s) {
       if (!sources[s] || !grad_sources[s]) return fail(ATTNRES_EINVAL, "sources[%d]/grad_sources[%d] is NULL", s, s);
-      for (int j = 0; j < S; ++j)
-        if (grad_sources[s] == sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] aliases sources[%d]", s, j);
-      for (int j = 0; j < s; ++j)
-        if (grad_sources[s] == grad_sources[j]) return fail(ATTNRES_EINVAL, "grad_sources[%d] == grad_sources[%d]", s, j);
+    }
+    {
+      const int rc = check_grads_apart(sources, grad_sources, S, T * d * (dtype == ATTNRES_BF16 ? 2 : 4), grad_r);
+      if (rc != ATTNRES_OK) return rc;
     }
     const int64_t rows = backward_blocks(T);
     if (rows < 0) return fail(ATTNRES_ECUDA, "no CUDA device");
@@ -464,6 +479,18 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
   for (int q = 0; q < Q; ++q) {
     if (!w_queries[q]) return fail(ATTNRES_EINVAL, "w_queries[%d] is NULL", q);
     a.wq[q] = w_queries[q];
+  }
+  {
+    // the outputs ([Q, T, d] fp32 r, [Q, T] lse, [Q, T, n] weights) must not
+    // share memory with a source or with each other
+    const int64_t row = T * d * (dtype == ATTNRES_BF16 ? 2 : 4);
+    const int64_t r_bytes = (int64_t)Q * T * d * 4, lse_bytes = (int64_t)Q * T * 4, a_bytes = (int64_t)Q * T * n * 4;
+    const int rc = check_outputs_apart(sources, n, row, out_r, r_bytes, out_weights, a_bytes);
+    if (rc != ATTNRES_OK) return rc;
+    for (int s = 0; s < n; ++s)
+      if (overlaps(out_lse, lse_bytes, sources[s], row)) return fail(ATTNRES_EINVAL, "out_lse overlaps source %d", s);
+    if (overlaps(out_lse, lse_bytes, out_r, r_bytes) || (out_weights && overlaps(out_lse, lse_bytes, out_weights, a_bytes)))
+      return fail(ATTNRES_EINVAL, "out_lse overlaps another output");
   }
   if (!twophase_pointers_ok(out_r)) return fail(ATTNRES_EINVAL, "out_r not 16-byte aligned");
   a.n = n;
@@ -559,16 +586,21 @@ int attnres_state_init(attnres_state* st, const void* h0, void* const* block_rep
   const int N = num_blocks(num_layers, block_size);
   if (N > ATTNRES_MAX_BLOCKS) return fail(ATTNRES_ERANGE, "ceil(L/B)=%d > %d", N, ATTNRES_MAX_BLOCKS);
   if (n_block_reps < N) return fail(ATTNRES_EINVAL, "need %d block buffers, got %d", N, n_block_reps);
-  memset(st, 0, sizeof(*st));
-  st->h0 = h0;
+  // every buffer is one [T, d] row set; none may share memory with another
+  // (all checked before the struct is written)
+  const int64_t row = T * d * (dtype == ATTNRES_BF16 ? 2 : 4);
+  if (overlaps(partial, row, h0, row)) return fail(ATTNRES_EINVAL, "partial overlaps h0");
   for (int k = 0; k < N; ++k) {
     if (!block_reps[k]) return fail(ATTNRES_EINVAL, "block_reps[%d] is NULL", k);
-    if (block_reps[k] == partial || block_reps[k] == h0) return fail(ATTNRES_EINVAL, "block_reps[%d] aliases", k);
+    if (overlaps(block_reps[k], row, partial, row) || overlaps(block_reps[k], row, h0, row))
+      return fail(ATTNRES_EINVAL, "block_reps[%d] overlaps h0 or partial", k);
     for (int j = 0; j < k; ++j)
-      if (block_reps[j] == block_reps[k]) return fail(ATTNRES_EINVAL, "block_reps[%d] == block_reps[%d]", j, k);
-    st->block_reps[k] = block_reps[k];
+      if (overlaps(block_reps[j], row, block_reps[k], row))
+        return fail(ATTNRES_EINVAL, "block_reps[%d] overlaps block_reps[%d]", j, k);
   }
-  if (partial == h0) return fail(ATTNRES_EINVAL, "partial aliases h0");
+  memset(st, 0, sizeof(*st));
+  st->h0 = h0;
+  for (int k = 0; k < N; ++k) st->block_reps[k] = block_reps[k];
   st->partial = partial;
   st->T = T;
   st->d = d;

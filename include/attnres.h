@@ -166,7 +166,8 @@ int64_t attnres_aggregate_host_workspace_size(int S, int64_t chunk_tokens, int d
  *             sources, of grad_r and of grad_sources
  * grad_r      device [T, d] of dtype
  * grad_sources host array of S device pointers [T, d] of dtype, none of them
- *             aliasing a source or each other; overwritten (accumulate = 0)
+ *             sharing memory with a source, with grad_r or with each other
+ *             (ATTNRES_EINVAL); overwritten (accumulate = 0)
  *             or added to (accumulate = 1: a source read by several layers
  *             collects the gradient of each)
  * grad_w      device [d] fp32, overwritten (fp32 sums in a fixed order:
@@ -243,7 +244,8 @@ typedef struct attnres_state {
 } attnres_state;
 
 /* Fill *st.  n_block_reps must be >= ceil(L/B) (ATTNRES_ERANGE if
- * ceil(L/B) > ATTNRES_MAX_BLOCKS).  Buffers must not alias each other.
+ * ceil(L/B) > ATTNRES_MAX_BLOCKS).  The buffers may not share memory with
+ * each other (ATTNRES_EINVAL; *st is not written then).
  * Host only; sets folded = 0. */
 int attnres_state_init(attnres_state* st, const void* h0, void* const* block_reps,
                        int n_block_reps, void* partial, int64_t T, int d, int dtype,
@@ -288,7 +290,8 @@ int attnres_block_step(attnres_state* st, const void* F_out, int layer_idx, int*
  *   layer_idx  1..L+1 (L+1 = the final output aggregation over [h_0, b_1..b_N])
  *   F_prev     device [T, d] of st->dtype; NULL exactly when layer_idx == 1
  *   w_l        device [d] fp32 pseudo-query of this layer
- *   out_r      device [T, d] of st->dtype (must not alias the state's buffers)
+ *   out_r      device [T, d] of st->dtype; it and out_weights may not share
+ *              memory with the state's rows or F_prev (ATTNRES_EINVAL)
  *   out_weights device [T, S_l] fp32 or NULL
  * Needs folded == max(layer_idx - 2, 0); advances folded to layer_idx - 1.
  * Bit-identical to block_step(l-1) + aggregate(layer_sources(l)).
@@ -314,7 +317,8 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
  *              over the n sources (normalised)
  *   out_lse    device [Q, T] fp32: log sum_s exp(z_qs) of those logits
  *   out_weights device [Q, T, n] fp32 (softmax over the n sources) or NULL
- *   Every source row is read once for all Q queries.
+ *   Every source row is read once for all Q queries.  No output may share
+ *   memory with a source or with another output (ATTNRES_EINVAL).
  * ---------------------------------------------------------------------- */
 int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int dtype,
                        const float* const* w_queries, int Q, float eps, float* out_r,

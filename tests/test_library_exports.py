@@ -115,14 +115,25 @@ def test_state_init_rejects_bad_arguments(native):
     st = native.AttnresState()
     reps = (ctypes.c_void_p * 3)(0x1000, 0x2000, 0x3000)
     init = native.lib.attnres_state_init
-    assert init(ctypes.byref(st), None, reps, 3, 0x50, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
-    assert init(ctypes.byref(st), 0x40, reps, 2, 0x50, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL  # need 3
-    assert init(ctypes.byref(st), 0x40, reps, 3, 0x50, 4, 8, 7, 7, 3, 1e-5) == native.ATTNRES_EDTYPE
-    assert init(ctypes.byref(st), 0x40, reps, 3, 0x50, 4, 0, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
-    assert init(ctypes.byref(st), 0x40, reps, 3, 0x1000, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL  # alias
-    assert init(ctypes.byref(st), 0x40, reps, 3, 0x50, 4, 8, 1, 7, 3, -1.0) == native.ATTNRES_EINVAL
+    # rows of 4 x 8 bf16 = 64 bytes: h0 at 0x4000, partial at 0x5000
+    assert init(ctypes.byref(st), None, reps, 3, 0x5000, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
+    assert init(ctypes.byref(st), 0x4000, reps, 2, 0x5000, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL  # need 3
+    assert init(ctypes.byref(st), 0x4000, reps, 3, 0x5000, 4, 8, 7, 7, 3, 1e-5) == native.ATTNRES_EDTYPE
+    assert init(ctypes.byref(st), 0x4000, reps, 3, 0x5000, 4, 0, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
+    assert init(ctypes.byref(st), 0x4000, reps, 3, 0x5000, 4, 8, 1, 7, 3, -1.0) == native.ATTNRES_EINVAL
+    # buffers sharing memory: the same address, or overlapping ranges
+    assert init(ctypes.byref(st), 0x4000, reps, 3, 0x1000, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
+    assert init(ctypes.byref(st), 0x4000, reps, 3, 0x4000 + 32, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
+    assert b"partial overlaps h0" in native.lib.attnres_last_error()
+    near = (ctypes.c_void_p * 3)(0x1000, 0x1000 + 48, 0x3000)
+    assert init(ctypes.byref(st), 0x4000, near, 3, 0x5000, 4, 8, 1, 7, 3, 1e-5) == native.ATTNRES_EINVAL
+    assert b"block_reps[0] overlaps block_reps[1]" in native.lib.attnres_last_error()
+    assert st.T == 0 and not st.h0  # a refused call writes nothing
     many = (ctypes.c_void_p * 200)(*range(0x1000, 0x1000 + 200 * 16, 16))
-    assert init(ctypes.byref(st), 0x40, many, 200, 0x50, 4, 8, 1, 200, 1, 1e-5) == native.ATTNRES_ERANGE
+    assert init(ctypes.byref(st), 0x4000, many, 200, 0x5000, 4, 8, 1, 200, 1, 1e-5) == native.ATTNRES_ERANGE
+    # adjacent but disjoint buffers are fine
+    adj = (ctypes.c_void_p * 3)(0x1000, 0x1040, 0x1080)
+    assert init(ctypes.byref(st), 0x4000, adj, 3, 0x4040, 4, 8, 1, 7, 3, 1e-5) == 0
 
 
 def test_aggregate_rejects_bad_arguments_before_any_launch(native):
@@ -254,9 +265,12 @@ def test_backward_rejects_bad_arguments_before_any_launch(native):
     assert call(dr=None) == native.ATTNRES_EINVAL
     assert call(ws=None) == native.ATTNRES_EINVAL
     assert call(ws=0x8002) == native.ATTNRES_EINVAL                        # workspace not 4-byte aligned
-    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x1000)) == native.ATTNRES_EINVAL   # grad aliases a source
-    assert b"aliases" in native.lib.attnres_last_error()
-    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x3000)) == native.ATTNRES_EINVAL   # two grads alias
+    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x1000)) == native.ATTNRES_EINVAL   # grad on a source
+    assert b"overlaps sources" in native.lib.attnres_last_error()
+    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x1000 + 40)) == native.ATTNRES_EINVAL   # grad inside a source
+    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x3000)) == native.ATTNRES_EINVAL   # two grads share memory
+    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x3000 + 63)) == native.ATTNRES_EINVAL
+    assert call(g=(ctypes.c_void_p * 2)(0x3000, 0x6000 - 8)) == native.ATTNRES_EINVAL   # grad over grad_r
     assert call(src=None) == native.ATTNRES_EINVAL
 
 

@@ -662,6 +662,16 @@ int attnres_block_step(attnres_state* st, const void* F_out, int layer_idx, int*
   if (st->folded != layer_idx - 1)
     return fail(ATTNRES_ESTATE, "block_step(%d) needs folded == %d, state has %d", layer_idx, layer_idx - 1,
                 st->folded);
+  {
+    // F_out is read while the partial sum or a block sum is written: it may
+    // not share memory with any of the state's rows
+    const int64_t row = st->T * st->d * (st->dtype == ATTNRES_BF16 ? 2 : 4);
+    if (overlaps(F_out, row, st->h0, row) || overlaps(F_out, row, st->partial, row))
+      return fail(ATTNRES_EINVAL, "F_out overlaps h0 or partial");
+    for (int k = 0; k < num_blocks(L, B); ++k)
+      if (st->block_reps[k] && overlaps(F_out, row, st->block_reps[k], row))
+        return fail(ATTNRES_EINVAL, "F_out overlaps block_reps[%d]", k);
+  }
   const FoldPlan fp = fold_plan(layer_idx, B, L);
   void* dst = fp.ends_block ? st->block_reps[fp.block - 1] : st->partial;
   const void* prev = fp.has_prev ? st->partial : nullptr;

@@ -275,8 +275,9 @@ int attnres_layer_sources(const attnres_state* st, int layer_idx, const void** o
  *   if layer_idx ends its block (layer_idx % B == 0 or layer_idx == L):
  *        b_n = new, partial becomes empty
  *   else partial = new
- * F_out: device [T, d] of st->dtype.  Needs folded == layer_idx - 1;
- * advances folded.  One elementwise launch.
+ * F_out: device [T, d] of st->dtype, sharing no memory with the state's
+ * rows (ATTNRES_EINVAL).  Needs folded == layer_idx - 1; advances folded.
+ * One elementwise launch.
  * ---------------------------------------------------------------------- */
 int attnres_block_step(attnres_state* st, const void* F_out, int layer_idx, int* dev_err,
                        void* stream);

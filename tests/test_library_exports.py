@@ -96,6 +96,10 @@ def test_stack_calls_enforce_order(native):
     assert native.lib.attnres_layer_sources(ctypes.byref(st), 3, out, ctypes.byref(n)) == native.ATTNRES_ESTATE
     # block_step(2) before block_step(1)
     assert native.lib.attnres_block_step(ctypes.byref(st), 0x999, 2, None, None) == native.ATTNRES_ESTATE
+    # F_out may not share memory with the state's rows (h0 at 0x10000, partial at 0x20000)
+    assert native.lib.attnres_block_step(ctypes.byref(st), 0x20000 + 8, 1, None, None) == native.ATTNRES_EINVAL
+    assert b"F_out overlaps" in native.lib.attnres_last_error()
+    assert native.lib.attnres_block_step(ctypes.byref(st), 0x100000, 1, None, None) == native.ATTNRES_EINVAL
     # layer_step: F_prev must be NULL exactly at layer 1; layer 3 needs folded == 1
     assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, 1, 0x777, None, None, None) == native.ATTNRES_EINVAL
     assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 2, 0x777, None, None, None) == native.ATTNRES_EINVAL

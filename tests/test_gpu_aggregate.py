@@ -364,3 +364,30 @@ def test_aggregate_host_multi_group_fp32_out(lib):
     r_ref, a_ref = _run(lib, inp.H, inp.w, torch.float32)
     assert torch.equal(r_host.cuda(), r_ref) and torch.equal(a_host.cuda(), a_ref)
     _compare(inp.H, inp.w, r_host, a_host, torch.float32)
+
+
+def _random_cases(n=32, seed=2026):
+    # seeded shapes over every dispatch path: T 1..400, d 1..8192 (row
+    # lengths that are and are not whole 16-byte vectors), S 1..128, all
+    # dtype pairings; sized so the oracle finishes each in about a second
+    rng = np.random.default_rng(seed)
+    dts = [torch.bfloat16, torch.float32]
+    cases = []
+    while len(cases) < n:
+        S = int(rng.choice([1, 2, 3, 5, 8, 9, 10, 13, 24, 47, 94, 128]))
+        d = int(rng.choice([1, 7, 8, 64, 100, 256, 1000, 3584, 3592, 7160, 7168, 8192]))
+        T = int(rng.integers(1, 401))
+        if S * T * d > 12_000_000:
+            continue
+        cases.append((T, d, S, dts[int(rng.integers(2))], dts[int(rng.integers(2))]))
+    return cases
+
+
+@pytest.mark.parametrize("T,d,S,sdt,odt", _random_cases())
+def test_random_shapes_against_oracle(lib, T, d, S, sdt, odt):
+    g = torch.Generator(device="cuda").manual_seed(T * 131 + d * 7 + S)
+    sig = torch.exp(torch.randn(S, 1, 1, generator=g, device="cuda"))  # a scale per source
+    H = (torch.randn(S, T, d, generator=g, device="cuda") * sig).to(sdt)
+    w = torch.randn(d, generator=g, device="cuda") / max(d, 1) ** 0.5
+    r, a = _run(lib, H, w, odt)
+    _compare(H, w, r, a, odt)

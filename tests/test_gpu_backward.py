@@ -104,3 +104,38 @@ def test_backward_empty_T_zeroes_grad_w(A):
                                  torch.zeros_like(H), gw, workspace=torch.zeros(1, device="cuda"))
     torch.cuda.synchronize()
     assert torch.count_nonzero(gw) == 0
+
+
+def _random_cases(n=20, seed=77):
+    # seeded shapes for the backward: T 1..300, d from 8 to 8192, S 1..24
+    # (the ring backward up to 9 sources, the plain-load one beyond and for
+    # rows that are not whole 16-byte vectors), both dtypes, accumulate or
+    # not; small enough for the oracle backward to take about a second
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        S = int(rng.choice([1, 2, 3, 5, 8, 9, 12, 24]))
+        d = int(rng.choice([8, 64, 100, 1000, 3584, 3592, 7160, 7168, 8192]))
+        T = int(rng.integers(1, 301))
+        if S * T * d > 6_000_000:
+            continue
+        dtype = [torch.bfloat16, torch.float32][int(rng.integers(2))]
+        cases.append((T, d, S, dtype, bool(rng.integers(2))))
+    return cases
+
+
+@pytest.mark.parametrize("T,d,S,dtype,acc", _random_cases())
+def test_backward_random_shapes(A, T, d, S, dtype, acc):
+    g = torch.Generator(device="cuda").manual_seed(T * 17 + d + S)
+    sig = torch.exp(0.5 * torch.randn(S, 1, 1, generator=g, device="cuda"))
+    H = (torch.randn(S, T, d, generator=g, device="cuda") * sig).to(dtype)
+    w = torch.randn(d, generator=g, device="cuda") / d ** 0.5
+    dr = torch.randn((T, d), generator=g, device="cuda").to(dtype)
+    init = torch.randn(H.shape, generator=g, device="cuda").to(dtype) if acc else None
+    gH, gw = _run(A, H, w, dr, accumulate=acc, init=init)
+    dH, dw, dHs, dws = oracle_backward(H, w, dr, EPS)
+    if acc:
+        # the old gradients are added: the bar grows by their size
+        dH = dH + to64(init)
+        dHs = dHs + np.abs(to64(init))
+    _check(gH, gw, dH, dw, dHs, dws, dtype)

@@ -294,3 +294,27 @@ def test_two_phase_decode_T64_graph(A):
     tr = _oracle_stack(stk)
     wa, wr = _check_stack(fwd, tr, slice(None), torch.bfloat16, STACK_BF16_A_ATOL, check_blocks=False)
     print(f"two-phase decode stack T=64: worst weight error {wa:.3g}, output {wr:.3g} x bound")
+
+
+def _random_stacks(n=10, seed=93):
+    # seeded stack layouts: L 1..30, block size 1..12 (Full AttnRes to
+    # one block), T 1..20, widths on the ring and the plain-load paths
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        L = int(rng.integers(1, 31))
+        B = int(rng.integers(1, 13))
+        T = int(rng.integers(1, 21))
+        d = int(rng.choice([16, 64, 100, 256, 1000, 3584]))
+        out.append((L, B, T, d, [torch.bfloat16, torch.float32][int(rng.integers(2))]))
+    return out
+
+
+@pytest.mark.parametrize("L,B,T,d,dtype", _random_stacks())
+def test_random_stacks_against_oracle(A, L, B, T, d, dtype):
+    stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=7 * L + B + T, device="cuda", dtype=dtype)
+    fwd = _gpu_stack(A, stk)
+    store = O.round_bf16 if dtype == torch.bfloat16 else O.round_fp32
+    tr = _oracle_stack(stk, store=store)
+    tol = A_ATOL if dtype == torch.float32 else STACK_BF16_A_ATOL
+    _check_stack(fwd, tr, slice(None), dtype, tol, check_blocks=dtype == torch.float32 or L <= 12)

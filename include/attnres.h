@@ -27,8 +27,10 @@
  *  - Tensors are row-major [T, d] (token-major, channel contiguous) in device
  *    memory of the CURRENT device (cudaGetDevice), on which every call
  *    launches; `sources` / `block_reps` are HOST arrays of DEVICE pointers.
- *  - The caller owns and allocates every buffer.  The library allocates no
- *    device memory and keeps no device-side global state.
+ *  - The caller owns and allocates every buffer.  The library makes no
+ *    device allocation and keeps no device-side global state, with one
+ *    exception: the fixed scratch array built into it for
+ *    attnres_aggregate_backward_noalloc (see there).
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream) and never synchronise the device.
  *  - Argument errors are detected on the host before any launch and return

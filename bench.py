@@ -8,13 +8,18 @@ than the 129 MB L2) are rotated, so no step reads what the previous one left
 in L2.
 
 Printed (rank 0, one JSON line): tokens/s of the whole job, the roofline of
-the aggregation kernel (algorithmic bytes / CUDA-event launch time against
-the measured HBM copy bandwidth), an end-to-end figure through the public
-API with host buffers (pinned H2D of the sources, D2H of r and the weights
-inside the timed region), the fp64 oracle timed on the host cores on a
-bounded sample, the SM clocks sampled during the timed region, and the
-secondary workloads (93-layer prefill and decode stacks, 128K-token long
-context).
+the aggregation kernel (algorithmic bytes over the timed region's average
+launch time, against the measured HBM copy bandwidth; launches timed one by
+one beside it), an end-to-end figure through the C-ABI call with host
+buffers (attnres_aggregate_host: pinned H2D of the sources, D2H of r and the
+weights inside the timed region), the fp64 oracle timed on the host cores
+on a bounded sample (one core, and every core at once), parity of the GPU's
+first tokens against those oracle outputs, the SM clocks sampled during the
+timed region, and the secondary workloads (93-layer prefill and decode
+stacks in both schedules, 128K-token long context, Full AttnRes layers over
+18-94 sources, the small fp32 layer, the backward of one layer and of the
+prefill stack).  `--only <leg>` runs one secondary workload alone;
+`--tokens` shrinks the long and Full AttnRes legs for profiling.
 
 `--impl reference` times the fp64 CPU oracle instead (the only reference
 implementation of this method here), on the same workload and metric.

@@ -515,13 +515,22 @@ def bench_stack_backward(A, W, dev, peak, reps=5):
     return out
 
 
-def bench_long(A, W, dev, peak, reps=8, tokens=None):
+def bench_long(A, W, dev, peak, reps=8, tokens=None, oracle_seconds=0.0):
     """The long-context layer (T = 131072, x50 outliers on 1% of tokens);
     `tokens` runs the same recipe at another length (a small case for
-    profiling)."""
+    profiling).  With oracle_seconds > 0 the fp64 oracle is also timed on a
+    sample of the outlier tokens and its time for the whole layer
+    extrapolated linearly per token (reported as extrapolated)."""
     inp = W.block_T131072_d7168(device=dev) if tokens is None else \
         W.block_bf16(T=tokens, seed=4, device=dev, outlier_frac=0.01)
     T = inp.H.shape[1]
+    oracle = None
+    if oracle_seconds > 0 and inp.outlier_tokens is not None and inp.outlier_tokens.numel():
+        idx = inp.outlier_tokens[:256].sort().values
+        tok, el, _ = time_oracle(inp.H[:, idx].cpu(), inp.w.cpu(), oracle_seconds)
+        oracle = {"tokens_per_s": tok / el, "extrapolated_s_for_layer": T / (tok / el), "extrapolated": True,
+                  "sample": f"{tok} tokens in {el:.1f} s, drawn from the first {idx.numel()} outlier tokens "
+                            "(single-threaded numpy fp64)"}
     r = torch.empty((T, D_MAIN), dtype=torch.bfloat16, device=dev)
     a = torch.empty((T, S_MAIN), dtype=torch.float32, device=dev)
     for _ in range(2):
@@ -537,9 +546,11 @@ def bench_long(A, W, dev, peak, reps=8, tokens=None):
     gbs = algorithmic_bytes(T, D_MAIN, S_MAIN) / (ms * 1e-3) / 1e9
     del inp, r, a
     torch.cuda.empty_cache()
-    return {f"block_attnres_single_layer_T{T}_d7168_S9": {
-        "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": algorithmic_bytes(T, D_MAIN, S_MAIN),
-        "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}}
+    out = {"ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": algorithmic_bytes(T, D_MAIN, S_MAIN),
+           "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak}
+    if oracle is not None:
+        out["cpu_oracle"] = oracle
+    return {f"block_attnres_single_layer_T{T}_d7168_S9": out}
 
 
 def bench_small_fp32(A, W, dev, peak, reps=2000):
@@ -705,7 +716,8 @@ def run_gpu(args):
     extras = {}
     if not args.no_extras:
         extras.update(bench_stacks(A, W, dev, peak))
-        extras.update(bench_long(A, W, dev, peak))
+        extras.update(bench_long(A, W, dev, peak,
+                                 oracle_seconds=3.0 if rank == 0 and ws == 1 and not args.no_cpu_baseline else 0.0))
         extras.update(bench_full(A, W, dev, peak))
         extras.update(bench_small_fp32(A, W, dev, peak))
         extras.update(bench_backward(A, W, dev, peak))

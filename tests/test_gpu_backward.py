@@ -139,3 +139,25 @@ def test_backward_random_shapes(A, T, d, S, dtype, acc):
         dH = dH + to64(init)
         dHs = dHs + np.abs(to64(init))
     _check(gH, gw, dH, dw, dHs, dws, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_autograd_function_against_the_oracle(A, dtype):
+    # aggregate(H, w) in a torch graph: its forward equals attnres_aggregate
+    # bit for bit and the gradients of sum(r * dr) are the oracle's
+    from depth_wise_attention_block_gb300.autograd import aggregate
+    H0, w0, dr = _inputs(300, 3584, 9, dtype, seed=21)
+    H = H0.clone().requires_grad_(True)
+    w = w0.clone().requires_grad_(True)
+    r = aggregate(H, w)
+    r_ref = torch.empty_like(r)
+    A.attnres_aggregate(H0, w0, r_ref)
+    assert torch.equal(r.detach(), r_ref)
+    (r.float() * dr.float()).sum().backward()
+    dH, dw, dHs, dws = oracle_backward(H0, w0, dr, EPS)
+    assert H.grad.dtype == dtype and w.grad.dtype == torch.float32
+    _check(H.grad, w.grad, dH, dw, dHs, dws, dtype)
+    # only the query learns: no source gradient is formed
+    w2 = w0.clone().requires_grad_(True)
+    (aggregate(H0, w2).float() * dr.float()).sum().backward()
+    assert torch.equal(w2.grad, w.grad)

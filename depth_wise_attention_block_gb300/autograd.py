@@ -7,7 +7,9 @@ the backward attnres_aggregate_backward (the forward recomputed inside it,
 as under activation checkpointing: only H and w are kept).  Both run in the
 library's kernels; torch only allocates the outputs and the backward's
 workspace.  Gradients: dH in the sources' dtype, dw in fp32 (summed over
-tokens in a fixed order, so bit-reproducible).
+tokens in a fixed order, so bit-reproducible).  The incoming gradient of r
+is taken in the sources' dtype (the backward kernel reads it so): an fp32
+gradient for bf16 sources is rounded to bf16 first.
 """
 from __future__ import annotations
 

@@ -256,6 +256,12 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
   uint32_t slot = 0, lap = 0;
   long long issued = 0;
   bool ok = true;
+  // A fused layer step runs inside a stack, where source 0 (the embedding
+  // h_0) is read again by every layer: its rows are kept in L2 and every
+  // other row streams through once (evict first), which also spares the
+  // rows the previous kernels just wrote.  A single aggregation streams
+  // everything with the default policy.
+  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   for (long long t = blockIdx.x; t < T && ok; t += gridDim.x) {
     const long long off = t * (long long)p.row_bytes;
     for (int j = 0; j < rows; ++j) {
@@ -272,8 +278,13 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
       const uint32_t full = smem_addr(&sh.full[slot]);
       mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
       // the bounded-wait test arms one row of the first token without its copy
-      if (issued + 1 != p.withhold_row1)
-        bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+      if (issued + 1 != p.withhold_row1) {
+        if (fused)
+          bulk_copy_g2s_hint(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full,
+                             (j == 0 || j >= real_rows) ? keep : stream);
+        else
+          bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+      }
       ++issued;
       if (++slot == (uint32_t)nslots) {
         slot = 0;

@@ -9,7 +9,11 @@ tables or pre/post-processing.  Inputs reach it from the seeded generators in
 
 Every function is pinned by ``tests/test_oracle_pins.py`` to facts the pages
 and the mathematics fix (worked example, closed forms, invariants, special
-cases, an independent high-precision brute force).  No function here is
+cases, an independent high-precision brute force, central differences of the
+gradients).  The backward's tolerance scales are pinned by finite
+differences of every rounding sensitivity, a closed form at one source, a
+float32 evaluation and planted mistakes; the bf16 storage mode of the stack
+by a running-state restatement, bit for bit.  No function here is
 "parity unpinned"; the one free choice is the final aggregation's
 pseudo-query (the pages name the aggregation but not its query), and the
 final sources it acts on are pinned independently of that choice.
@@ -23,6 +27,8 @@ from .attnres_oracle import (  # noqa: F401
     merge_partial_softmax,
     depth_attention_backward,
     depth_attention_backward_scales,
+    backward_rounding_sites,
+    backward_scalar_sensitivities,
     block_index,
     position_in_block,
     block_layers,

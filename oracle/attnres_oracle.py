@@ -108,6 +108,42 @@ def merge_partial_softmax(r1, lse1, r2, lse2):
     return r, c1 / den, c2 / den
 
 
+def _backward_core(H: np.ndarray, w: np.ndarray, dr: np.ndarray, eps: float, bump: dict | None = None) -> dict:
+    """The backward of one layer, per token, step by step (float64).
+
+    With rho_s = rms(h_s), z_s = (w . h_s) / rho_s, a = softmax(z),
+    r = sum_s a_s h_s, the chain rule gives, per token:
+        g_s   = dr . h_s,             gbar = sum_s a_s g_s
+        dz_s  = a_s (g_s - gbar)                       (softmax)
+        alpha_s = dz_s / rho_s,       beta_s = alpha_s z_s / (d rho_s)
+        dh_s  = a_s dr + alpha_s w - beta_s h_s        (values; logit, with
+                                                        d rho_s / d h_s = h_s / (d rho_s))
+        dw   += sum_s alpha_s h_s
+    `bump` adds a given [S, T] (or [1, T] for gbar) array to one of the
+    intermediate quantities ss (= sum_c h_sc^2), g, z, a, gbar, dz, alpha,
+    beta as it is formed, so that the sensitivity of the gradients to each can be
+    taken by differences.  Returns the intermediates, dH [S, T, d] and the
+    per-token contributions to dw, dw_tok [T, d]."""
+    b = bump or {}
+    S, T, d = H.shape
+    ss = np.einsum("std,std->st", H, H) + b.get("ss", 0.0)
+    p = np.einsum("std,d->st", H, w)
+    g = np.einsum("std,td->st", H, dr) + b.get("g", 0.0)
+    rho = np.sqrt(ss / d + eps)
+    z = p / rho + b.get("z", 0.0)
+    m = z.max(axis=0, keepdims=True)
+    e = np.exp(z - m)
+    a = e / e.sum(axis=0, keepdims=True) + b.get("a", 0.0)   # [S, T]
+    gbar = (a * g).sum(axis=0, keepdims=True) + b.get("gbar", 0.0)
+    dz = a * (g - gbar) + b.get("dz", 0.0)
+    alpha = dz / rho + b.get("alpha", 0.0)
+    beta = alpha * z / (d * rho) + b.get("beta", 0.0)
+    dH = a[:, :, None] * dr[None] + alpha[:, :, None] * w[None, None, :] - beta[:, :, None] * H
+    dw_tok = np.einsum("st,std->td", alpha, H)
+    return dict(ss=ss, p=p, g=g, rho=rho, z=z, m=m, a=a, gbar=gbar, dz=dz, alpha=alpha, beta=beta,
+                dH=dH, dw_tok=dw_tok)
+
+
 def depth_attention_backward(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
                              eps: float = EPS) -> tuple[np.ndarray, np.ndarray]:
     """Gradients of one depth-wise attention layer, recomputing its forward.
@@ -116,62 +152,120 @@ def depth_attention_backward(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
     with respect to r.  Returns (dH [S, T, d], dw [d]) in float64.  The
     forward is recomputed here from H and w, as under the activation
     checkpointing that wraps AttnRes in training ([Tutorial] ch. 4.6).
+    The chain rule, step by step, is written out in _backward_core."""
+    H = np.asarray(H, dtype=np.float64)
+    c = _backward_core(H, np.asarray(w, np.float64), np.asarray(dr, np.float64), eps)
+    return c["dH"], c["dw_tok"].sum(axis=0)
 
-    With rho_s = rms(h_s), z_s = (w . h_s) / rho_s, a = softmax(z),
-    r = sum_s a_s h_s, the chain rule gives, per token:
-        g_s   = dr . h_s,             gbar = sum_s a_s g_s
-        dz_s  = a_s (g_s - gbar)                       (softmax)
-        dh_s  = a_s dr                                 (through the values)
-              + dz_s (w - z_s rho_s h_s / (d rho_s^2)) / rho_s
-                                                       (through the logit;
-                                                        d rho_s / d h_s = h_s / (d rho_s))
-        dw   += sum_s dz_s h_s / rho_s
-    """
+
+def backward_rounding_sites(H: np.ndarray, w: np.ndarray, dr: np.ndarray, eps: float = EPS) -> list:
+    """The rounding model behind depth_attention_backward_scales: every
+    quantity a straightforward evaluation of _backward_core rounds, as
+    (site, index, unit) triples -- a one-unit change of quantity `site`
+    [index] moves it by `unit` ([T]), one rounding's worth:
+        ss_j  : sum of squares (its roundings, then rho's: 4 d rho^2)   ss_j + 4 d rho_j^2
+        g_j   : dot product dr . h_j (its absolute terms)                 sum_c |dr_c h_jc|
+        z_j   : w . h_j / rho_j, then z - max and its exponential (the
+                dot's absolute terms mapped by 1/rho; one unit each of
+                z, z - max and the exponential's relative error)        sum_c|w_c h_jc|/rho_j + |z_j| + |z_j - m| + 1
+        a_j   : the sum of the exponentials and the division by it
+                (relative errors that do not keep sum_j a_j = 1)        2 a_j
+        gbar  : one unit per product a_k g_k                             sum_k a_k |g_k|
+        dz_j  : a subtraction and a product                              2 |dz_j|
+        alpha_j: a division                                              |alpha_j|
+        beta_j : three operations                                        3 |beta_j|
+    The final elementwise products and sums of dh and the sum of dw are
+    counted in depth_attention_backward_scales itself."""
     H = np.asarray(H, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)
     dr = np.asarray(dr, dtype=np.float64)
     S, T, d = H.shape
-    rho = rms(H, eps)                                        # [S, T]
-    z = np.einsum("std,d->st", H, w) / rho                   # [S, T] logits
-    e = np.exp(z - z.max(axis=0, keepdims=True))
-    a = e / e.sum(axis=0, keepdims=True)                     # [S, T]
-    g = np.einsum("std,td->st", H, dr)                       # [S, T]
-    gbar = (a * g).sum(axis=0, keepdims=True)
-    dz = a * (g - gbar)                                      # [S, T]
-    dH = a[:, :, None] * dr[None]
-    dH = dH + (dz / rho)[:, :, None] * (w[None, None, :] - (z / (d * rho))[:, :, None] * H)
-    dw = np.einsum("st,std->d", dz / rho, H)
-    return dH, dw
+    c = _backward_core(H, w, dr, eps)
+    absP = np.einsum("std,d->st", np.abs(H), np.abs(w))
+    absG = np.einsum("std,td->st", np.abs(H), np.abs(dr))
+    sites = []
+    for j in range(S):
+        sites.append(("ss", j, c["ss"][j] + 4 * d * c["rho"][j] ** 2))
+        sites.append(("g", j, absG[j]))
+        sites.append(("z", j, absP[j] / c["rho"][j] + np.abs(c["z"][j]) + np.abs(c["z"][j] - c["m"][0]) + 1))
+        sites.append(("a", j, 2 * c["a"][j]))
+        sites.append(("dz", j, 2 * np.abs(c["dz"][j])))
+        sites.append(("alpha", j, np.abs(c["alpha"][j])))
+        sites.append(("beta", j, 3 * np.abs(c["beta"][j])))
+    sites.append(("gbar", 0, (c["a"] * np.abs(c["g"])).sum(axis=0)))
+    return sites
+
+
+_RESPOND_ARG = {"ss": "dss", "g": "dg", "z": "dz_", "a": "da_", "gbar": "dgbar", "dz": "ddz", "alpha": "dalpha",
+                "beta": "dbeta"}
+
+
+def backward_scalar_sensitivities(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
+                                  eps: float = EPS) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """First-order rounding sensitivities of the per-token scalars a_s,
+    alpha_s, beta_s of _backward_core: for each,
+        sum over the sites of backward_rounding_sites |d x_s / d site| * unit(site),
+    the change of x_s when every rounded quantity moves by one unit of its
+    own size in the worst direction.  The derivatives follow
+    _backward_core step by step (chain rule, written out below).
+    Returns (sens_a, sens_alpha, sens_beta), each [S, T]."""
+    H = np.asarray(H, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    dr = np.asarray(dr, dtype=np.float64)
+    S, T, d = H.shape
+    c = _backward_core(H, w, dr, eps)
+    a, g, gbar, rho, z, alpha, beta = c["a"], c["g"], c["gbar"], c["rho"], c["z"], c["alpha"], c["beta"]
+
+    def respond(dss=0.0, dg=0.0, dz_=0.0, da_=0.0, dgbar=0.0, ddz=0.0, dalpha=0.0, dbeta=0.0):
+        # first-order changes of (a, alpha, beta) [S, T] for changes of the
+        # intermediates
+        drho = dss / (2 * d * rho)                            # rho^2 = ss/d + eps
+        dzt = dz_ - z * drho / rho                            # z = p / rho
+        da = a * (dzt - (a * dzt).sum(axis=0, keepdims=True)) + da_  # softmax, then its rounding
+        dgb = (da * g).sum(axis=0, keepdims=True) + (a * dg).sum(axis=0, keepdims=True) + dgbar
+        ddzt = da * (g - gbar) + a * (dg - dgb) + ddz
+        dal = ddzt / rho - alpha * drho / rho + dalpha
+        dbe = (dal * z + alpha * dzt) / (d * rho) - beta * drho / rho + dbeta
+        return da, dal, dbe
+
+    sa, sal, sbe = np.zeros((S, T)), np.zeros((S, T)), np.zeros((S, T))
+    for site, j, unit in backward_rounding_sites(H, w, dr, eps):
+        one = np.zeros((1 if site == "gbar" else S, T))
+        one[j] = 1.0
+        da, dal, dbe = respond(**{_RESPOND_ARG[site]: one})
+        sa += np.abs(da) * unit
+        sal += np.abs(dal) * unit
+        sbe += np.abs(dbe) * unit
+    return sa, sal, sbe
 
 
 def depth_attention_backward_scales(H: np.ndarray, w: np.ndarray, dr: np.ndarray,
                                     eps: float = EPS) -> tuple[np.ndarray, np.ndarray]:
-    """Condition scales of the two gradients, for tolerances: the size of the
-    terms a forward-stable evaluation rounds.  Dot products count with their
-    absolute products (gabs_s = sum_c |dr_c h_sc|, zabs_s = sum_c |w_c h_sc|
-    / rho_s), and a rounding u in the logits moves a weight by about
-    a_s * 2 u max_j zabs_j.  Returns (dH_scale [S,T,d], dw_scale [d]):
-        adz_s  = a_s (gabs_s + sum_j a_j gabs_j + 2 |g_s - gbar| zmax) / rho_s
-        dH_s  ~ a_s |dr| (1 + 2 zmax) + adz_s (|w| + zabs_s |h_s| / (d rho_s))
-        dw    ~ sum_t sum_s adz_s |h_s|
-    """
+    """Condition scales of the two gradients, for tolerances: how far an
+    evaluation moves each output when every rounded quantity moves by one
+    unit of its own size (backward_rounding_sites), to first order and all
+    in the worst direction.  With the scalar sensitivities of
+    backward_scalar_sensitivities (sens_*) and one unit each for the final
+    products and sums,
+        dH_scale[s, t, c] = (sens_a + 2|a_s|) |dr_c| + (sens_alpha + 2|alpha_s|) |w_c|
+                            + (sens_beta + 2|beta_s|) |h_sc|
+        dw_scale[c]       = sum_t sum_s (sens_alpha + 2|alpha_s|) |h_sc|
+    (every term of dh = a dr + alpha w - beta h and of dw = sum alpha h
+    counted with its absolute value).  Returns (dH_scale [S, T, d],
+    dw_scale [d]).  An evaluation with unit roundoff u errs by about u
+    times the scale or less: rounding errors of opposite sign cancel, and
+    the sum over tokens of dw is counted as if all its errors had one
+    sign."""
     H = np.asarray(H, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)
     dr = np.asarray(dr, dtype=np.float64)
-    S, T, d = H.shape
-    rho = rms(H, eps)
-    z = np.einsum("std,d->st", H, w) / rho
-    e = np.exp(z - z.max(axis=0, keepdims=True))
-    a = e / e.sum(axis=0, keepdims=True)
-    g = np.einsum("std,td->st", H, dr)
-    gbar = (a * g).sum(axis=0, keepdims=True)
-    gabs = np.einsum("std,td->st", np.abs(H), np.abs(dr))
-    zabs = np.einsum("std,d->st", np.abs(H), np.abs(w)) / rho
-    zmax = zabs.max(axis=0, keepdims=True)
-    adz = a * (gabs + (a * gabs).sum(axis=0, keepdims=True) + 2 * np.abs(g - gbar) * zmax) / rho
-    dHs = (a * (1 + 2 * zmax))[:, :, None] * np.abs(dr)[None] + adz[:, :, None] * (
-        np.abs(w)[None, None, :] + (zabs / (d * rho))[:, :, None] * np.abs(H))
-    dws = np.einsum("st,std->d", adz, np.abs(H))
+    c = _backward_core(H, w, dr, eps)
+    sa, sal, sbe = backward_scalar_sensitivities(H, w, dr, eps)
+    A = sa + 2 * np.abs(c["a"])
+    B = sal + 2 * np.abs(c["alpha"])
+    C = sbe + 2 * np.abs(c["beta"])
+    dHs = A[:, :, None] * np.abs(dr)[None] + B[:, :, None] * np.abs(w)[None, None, :] + C[:, :, None] * np.abs(H)
+    dws = np.einsum("st,std->d", B, np.abs(H))
     return dHs, dws
 
 

@@ -310,6 +310,84 @@ def test_stack_rounding_mode_stores_bf16_values():
     np.testing.assert_allclose(tr.r[-1], ex.r[-1], rtol=0.05, atol=0.05)
 
 
+def _running_state_stack(h0, W, G, Sc, L, B, store, slip=None):
+    """A second, independent statement of a stack with storage rounding,
+    written as the running state a stack keeps (Eq. 10's two cases): the
+    stored values are rounded exactly where they are written -- r_l, the
+    layer output v_l, and every new partial sum or block sum (the fp64 sum
+    of the stored partial sum and v_l, rounded once).  `slip` plants one of
+    three plausible misplacements of the rounding (to show the pin sees
+    them): "block_only" rounds a block sum only when it is finished,
+    "raw_r" feeds the layer body the unrounded r_l, "late_v" adds the
+    unrounded v_l and rounds it afterwards."""
+    blocks, partial, exact_partial = [], None, None
+    rs, as_, vs = [], [], []
+    for layer in range(1, L + 2):
+        srcs = [h0] + blocks + ([partial] if partial is not None else [])
+        r_raw, a = O.depth_attention(np.stack(srcs), W[layer - 1])
+        r = store(r_raw)
+        rs.append(r)
+        as_.append(a)
+        if layer == L + 1:
+            return rs, as_, vs, srcs
+        v_raw = O.synthetic_layer(r_raw if slip == "raw_r" else r, G[layer - 1], Sc[layer - 1])
+        v = store(v_raw)
+        vs.append(v)
+        add = v_raw if slip == "late_v" else v
+        if slip == "block_only":
+            exact_partial = add if exact_partial is None else exact_partial + add
+            partial = exact_partial
+        else:
+            partial = add if partial is None else store(partial + add)
+            if slip == "late_v":
+                partial = store(partial)
+        if layer % B == 0 or layer == L:      # the block ends here
+            blocks.append(store(partial))
+            partial, exact_partial = None, None
+
+
+@pytest.mark.parametrize("B", [1, 2, 3])
+@pytest.mark.parametrize("L", [1, 4, 7])
+def test_storage_rounding_is_placed_at_every_store(L, B):
+    # c12: with bf16 storage the oracle rounds r_l, v_l and each new partial
+    # or block sum once, where a stack stores them; checked bit for bit
+    # against the running-state statement above (fp64 between the stores)
+    h0, W, G, Sc, _ = _tiny_stack(L, 8, 3, 200 + 10 * L + B)
+    h0 = O.round_bf16(h0)
+    fn = lambda l, x: O.synthetic_layer(x, G[l - 1], Sc[l - 1])
+    tr = O.block_stack_forward(h0, W, fn, L, B, store=O.round_bf16)
+    rs, as_, vs, final = _running_state_stack(h0, W, G, Sc, L, B, O.round_bf16)
+    for l in range(L + 1):
+        assert np.array_equal(tr.r[l], rs[l]) and np.array_equal(tr.a[l], as_[l]), f"layer {l + 1}"
+    for l in range(L):
+        assert np.array_equal(tr.v[l], vs[l]), f"v_{l + 1}"
+    assert len(tr.final_sources) == len(final)
+    for x, y in zip(tr.final_sources, final):
+        assert np.array_equal(x, y)
+
+
+def test_storage_rounding_pin_sees_misplaced_roundings():
+    # the three slips of the running-state statement each change some stored
+    # value of a 7-layer stack with blocks of 3 (so the pin above would fail
+    # for an oracle that made one of them)
+    L, B = 7, 3
+    h0, W, G, Sc, _ = _tiny_stack(L, 8, 3, 290)
+    h0 = O.round_bf16(h0)
+    ref = _running_state_stack(h0, W, G, Sc, L, B, O.round_bf16)
+    for slip in ("block_only", "raw_r", "late_v"):
+        got = _running_state_stack(h0, W, G, Sc, L, B, O.round_bf16, slip=slip)
+        same = all(np.array_equal(x, y) for x, y in zip(ref[0] + ref[2] + ref[3], got[0] + got[2] + got[3]))
+        assert not same, slip
+
+
+def test_round_fp32_ties_to_even():
+    # 1 + 2^-24 is halfway between 1 and 1 + 2^-23: rounds to 1 (even);
+    # 1 + 3*2^-24 is halfway between 1 + 2^-23 and 1 + 2^-22: rounds up (even)
+    x = np.array([1 + 2 ** -24, 1 + 3 * 2 ** -24, -(1 + 3 * 2 ** -24), 1 + 2 ** -24 + 2 ** -50, 2.0 ** -149 * 0.5])
+    want = np.array([1.0, 1 + 2 ** -22, -(1 + 2 ** -22), 1 + 2 ** -23, 0.0])
+    assert np.array_equal(O.round_fp32(x), want)
+
+
 def _brute_force_stack(h0, W, G, Sc, L, B, eps=O.EPS):
     """Independent high-precision stack, written as a running-state machine
     from the two cases of Eq. 10 (the oracle instead rebuilds every source
@@ -417,6 +495,194 @@ def test_backward_closed_forms():
     lhs = np.einsum("std,std->st", dH, H)
     rhs = a.T * np.einsum("std,td->st", H, dr)
     np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------ backward tolerance scales -----
+#
+# depth_attention_backward_scales sets every backward parity bar.  It is the
+# first-order worst-case change of each gradient when each rounded quantity
+# of the evaluation moves by one unit of its own size.  Pinned here by
+# (1) the rounding model restated from its definition, (2) every scalar
+# sensitivity against central differences of the evaluation, (3) the closed
+# form at S = 1, (4) an actual fp32 evaluation erring within a few units of
+# it (and not far below), and (5) planted mistakes in the gradient formula
+# landing far outside 1e-5 of it.
+
+U32 = 2.0 ** -24
+
+
+def _bwd_case(S, T, d, eps, qscale, seed):
+    rng = np.random.default_rng(seed)
+    H = rng.standard_normal((S, T, d)) * rng.uniform(0.2, 3, size=(S, 1, 1))
+    w = rng.standard_normal(d) / math.sqrt(d) * qscale
+    dr = rng.standard_normal((T, d))
+    return H, w, dr
+
+
+def _model_units(H, w, dr, eps):
+    """The rounding model, restated: one unit per rounded quantity."""
+    S, T, d = H.shape
+    ss = (H * H).sum(axis=2)
+    rho = np.sqrt(ss / d + eps)
+    z = (H @ w) / rho
+    e = np.exp(z - z.max(axis=0))
+    a = e / e.sum(axis=0)
+    g = np.einsum("std,td->st", H, dr)
+    gbar = (a * g).sum(axis=0)
+    dz = a * (g - gbar)
+    alpha = dz / rho
+    beta = alpha * z / (d * rho)
+    P = np.abs(H) @ np.abs(w)
+    G = np.einsum("std,td->st", np.abs(H), np.abs(dr))
+    units = {}
+    for j in range(S):
+        units[("ss", j)] = ss[j] + 4 * d * rho[j] ** 2
+        units[("g", j)] = G[j]
+        units[("z", j)] = P[j] / rho[j] + np.abs(z[j]) + np.abs(z[j] - z.max(axis=0)) + 1
+        units[("a", j)] = 2 * a[j]
+        units[("dz", j)] = 2 * np.abs(dz[j])
+        units[("alpha", j)] = np.abs(alpha[j])
+        units[("beta", j)] = 3 * np.abs(beta[j])
+    units[("gbar", 0)] = (a * np.abs(g)).sum(axis=0)
+    return units, dict(g=g, rho=rho, z=z, a=a, alpha=alpha, beta=beta)
+
+
+@pytest.mark.parametrize("S,eps,qscale", [(1, 1e-5, 2.0), (2, 1e-5, 1.0), (4, 0.3, 3.0), (6, 1e-5, 0.0),
+                                          (9, 1e-5, 4.0)])
+def test_backward_scale_sensitivities_match_differences(S, eps, qscale):
+    from oracle.attnres_oracle import _backward_core
+    H, w, dr = _bwd_case(S, 4, 11, eps, qscale, seed=40 + S)
+    units, _ = _model_units(H, w, dr, eps)
+    sites = O.backward_rounding_sites(H, w, dr, eps)
+    assert {(site, j) for site, j, _ in sites} == set(units)
+    for site, j, unit in sites:
+        np.testing.assert_allclose(unit, units[(site, j)], rtol=1e-14, atol=0)
+    # every site's effect on (a, alpha, beta) by central differences of the
+    # evaluation, weighted by its unit, summed in absolute value
+    base = _backward_core(H, w, dr, eps)
+    want = {k: np.zeros((S, 4)) for k in ("a", "alpha", "beta")}
+    for (site, j), unit in units.items():
+        x = base[site][j]
+        step = 1e-6 * (np.abs(x) + 1e-3 * (1 + np.abs(x).max()))
+        bump = np.zeros((1 if site == "gbar" else S, 4))
+        bump[j] = step
+        up = _backward_core(H, w, dr, eps, bump={site: bump})
+        dn = _backward_core(H, w, dr, eps, bump={site: -bump})
+        for k in want:
+            want[k] += np.abs((up[k] - dn[k]) / (2 * step)) * unit
+    got = dict(zip(("a", "alpha", "beta"), O.backward_scalar_sensitivities(H, w, dr, eps)))
+    for k in want:
+        np.testing.assert_allclose(got[k], want[k], rtol=2e-6, atol=1e-9 * (want[k].max() + 1e-300))
+    # the scales are those sensitivities plus one unit per final product and sum
+    c = _backward_core(H, w, dr, eps)
+    Ak, Bk, Ck = (got[k] + 2 * np.abs(c[k]) for k in ("a", "alpha", "beta"))
+    dHs, dws = O.depth_attention_backward_scales(H, w, dr, eps)
+    np.testing.assert_allclose(dHs, Ak[:, :, None] * np.abs(dr) + Bk[:, :, None] * np.abs(w) +
+                               Ck[:, :, None] * np.abs(H), rtol=1e-14)
+    np.testing.assert_allclose(dws, np.einsum("st,std->d", Bk, np.abs(H)), rtol=1e-14)
+
+
+def test_backward_scale_closed_form_one_source():
+    # S = 1: a = 1 and alpha = beta = 0 exactly; only the rounding of the
+    # softmax normalisation (a unit of 2) and of gbar = a g (a unit of |g|)
+    # reach dz = a (g - gbar), which moves alpha by 1/rho and beta by
+    # z / (d rho^2) per unit of dz:
+    #   sens_a = 2, sens_alpha = 3|g|/rho, sens_beta = 3|g||z|/(d rho^2)
+    rng = np.random.default_rng(8)
+    T, d = 5, 24
+    H = rng.standard_normal((1, T, d)) * 1.7
+    w = rng.standard_normal(d) / 3
+    dr = rng.standard_normal((T, d))
+    rho = np.sqrt((H[0] ** 2).mean(axis=1) + O.EPS)
+    z = H[0] @ w / rho
+    g = (H[0] * dr).sum(axis=1)
+    sa, sal, sbe = O.backward_scalar_sensitivities(H, w, dr)
+    np.testing.assert_allclose(sa[0], 2.0, rtol=1e-14)
+    np.testing.assert_allclose(sal[0], 3 * np.abs(g) / rho, rtol=1e-12)
+    np.testing.assert_allclose(sbe[0], 3 * np.abs(g * z) / (d * rho ** 2), rtol=1e-12)
+    dHs, dws = O.depth_attention_backward_scales(H, w, dr)
+    np.testing.assert_allclose(dHs[0], 4 * np.abs(dr) + (3 * np.abs(g) / rho)[:, None] * np.abs(w)
+                               + (3 * np.abs(g * z) / (d * rho ** 2))[:, None] * np.abs(H[0]), rtol=1e-12)
+    np.testing.assert_allclose(dws, ((3 * np.abs(g) / rho)[:, None] * np.abs(H[0])).sum(axis=0), rtol=1e-12)
+
+
+def _backward_fp32(H, w, dr, eps):
+    """The backward evaluated in float32 (numpy casts only; sums by numpy's
+    pairwise float32 summation), as a kernel would."""
+    f = np.float32
+    h, wq, g_ = H.astype(f), w.astype(f), dr.astype(f)
+    S, T, d = H.shape
+    rho = np.sqrt(np.sum(h * h, axis=2, dtype=f) / f(d) + f(eps)).astype(f)
+    z = (np.sum(h * wq, axis=2, dtype=f) / rho).astype(f)
+    e = np.exp(z - z.max(axis=0)).astype(f)
+    a = (e / np.sum(e, axis=0, dtype=f)).astype(f)
+    g = np.sum(h * g_[None], axis=2, dtype=f)
+    gbar = np.sum(a * g, axis=0, dtype=f)
+    alpha = (a * (g - gbar) / rho).astype(f)
+    beta = (alpha * z / (f(d) * rho)).astype(f)
+    dH = a[:, :, None] * g_[None] + alpha[:, :, None] * wq - beta[:, :, None] * h
+    dw = np.sum(np.sum(alpha[:, :, None] * h, axis=0, dtype=f), axis=0, dtype=f)
+    return dH.astype(np.float64), dw.astype(np.float64)
+
+
+@pytest.mark.parametrize("d", [64, 1024, 7168])
+@pytest.mark.parametrize("S,qscale", [(2, 1.0), (5, 4.0), (9, 1.0), (9, 4.0)])
+def test_backward_scale_bounds_a_float32_evaluation(S, d, qscale):
+    # an fp32 evaluation errs by at most a few units of u times the scale
+    # everywhere (the GPU bars allow 1e-5, about 168 units), and by at least
+    # a sixteenth of one unit somewhere in the source gradients (the scale is
+    # not inflated); grad_w's scale counts its sum over tokens as if all
+    # errors had one sign, so it stays above the error by more
+    H, w, dr = _bwd_case(S, 32, d, 1e-5, qscale, seed=S * d)
+    H = H.astype(np.float32).astype(np.float64)
+    w = w.astype(np.float32).astype(np.float64)
+    dr = dr.astype(np.float32).astype(np.float64)
+    dH, dw = O.depth_attention_backward(H, w, dr)
+    dHs, dws = O.depth_attention_backward_scales(H, w, dr)
+    eH, ew = _backward_fp32(H, w, dr, 1e-5)
+    rH = np.abs(eH - dH) / (U32 * dHs)
+    rw = np.abs(ew - dw) / (U32 * dws)
+    assert rH.max() <= 4 and rw.max() <= 4, (rH.max(), rw.max())
+    assert rH.max() >= 1 / 16, rH.max()
+    assert rw.max() >= 1 / 512, rw.max()
+
+
+_BACKWARD_SLIPS = [
+    ("alpha = dz / rho + ", "alpha = dz + "),                            # missing 1/rho on the logit path
+    ("beta = alpha * z / (d * rho) + ", "beta = alpha * z / d + "),      # d rho / d h without 1/rho
+    ("- beta[:, :, None] * H", "+ 0 * H"),                               # the rms term dropped
+    ("dz = a * (g - gbar) + ", "dz = a * g + "),                         # softmax Jacobian without gbar
+    ("a[:, :, None] * dr[None] + alpha", "dr[None] + alpha"),           # value path without a
+    ("- beta[:, :, None] * H", "+ beta[:, :, None] * H"),                # wrong sign of the rms term
+    ("rho = np.sqrt(ss / d + eps)", "rho = np.sqrt(ss / d)"),            # eps dropped
+]
+
+
+@pytest.mark.parametrize("old,new", _BACKWARD_SLIPS)
+def test_backward_bar_rejects_planted_mistakes(old, new):
+    # each slip planted in a copy of the oracle's backward moves some
+    # gradient entry by more than 100 times the 1e-5 bar of the GPU tests
+    import types
+    import oracle.attnres_oracle as OA
+    src = open(OA.__file__).read()
+    assert src.count(old) == 1
+    import sys
+    mod = types.ModuleType("oracle_with_slip")
+    sys.modules[mod.__name__] = mod          # its dataclasses look their module up
+    try:
+        exec(compile(src.replace(old, new), "oracle_with_slip", "exec"), mod.__dict__)
+    finally:
+        del sys.modules[mod.__name__]
+    rng = np.random.default_rng(17)
+    S, T, d = 5, 6, 96
+    H = rng.standard_normal((S, T, d)) * np.array([1.0, 0.5, 2.0, 0.003, 1.3])[:, None, None]
+    w = rng.standard_normal(d) / math.sqrt(d) * 2
+    dr = rng.standard_normal((T, d))
+    dH, dw = O.depth_attention_backward(H, w, dr)
+    dHs, dws = O.depth_attention_backward_scales(H, w, dr)
+    bH, bw = mod.depth_attention_backward(H, w, dr)
+    worst = max((np.abs(bH - dH) / (1e-5 * dHs)).max(), (np.abs(bw - dw) / (1e-5 * dws)).max())
+    assert worst > 100, worst
 
 
 # --------------------------------------------------- two-phase merge pin ----

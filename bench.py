@@ -481,6 +481,30 @@ def bench_stacks(A, W, dev, peak):
     return out
 
 
+def bench_decode(A, W, dev, peak, reps=20):
+    """The 93-layer decode-shaped stack (T = 64, single pass) alone, replayed
+    from a CUDA graph: one eager forward inside capture(), 3 warm-up
+    replays, then `reps` timed replays (each forward is 2L + 1 = 187
+    launches; a launch-list profile skips the first 4 forwards)."""
+    from depth_wise_attention_block_gb300.stack import StackForward
+    stk = W.stack(T=64, seed=3, device=dev)
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size)
+    fwd.capture()
+    for _ in range(3):
+        fwd.run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fwd.run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    return {"stack_decode_T64": {"ms_per_forward": ms, "us_per_layer": 1e3 * ms / (stk.num_layers + 1),
+                                 "launches_per_forward": fwd.launches_per_forward(), "forwards_timed": reps,
+                                 "cuda_graph": True}}
+
+
 def bench_stack_backward(A, W, dev, peak, reps=5):
     """The 93-layer prefill stack's backward (gradients of h0 and all 94
     pseudo-queries, each block's forward recomputed from h0 and the stored
@@ -670,7 +694,7 @@ def run_only(args):
         res = fn(A, W, dev, peak, tokens=args.tokens)
     else:
         res = {"stacks": bench_stacks, "backward": bench_backward, "small": bench_small_fp32,
-               "stack_backward": bench_stack_backward}[args.only](A, W, dev, peak)
+               "stack_backward": bench_stack_backward, "decode": bench_decode}[args.only](A, W, dev, peak)
     print(json.dumps(res), flush=True)
 
 
@@ -789,7 +813,7 @@ def main():
     ap.add_argument("--no-cpu-all-cores", action="store_true", help="time the oracle on one core only")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count of the --only long / --only full workloads (small cases for profiling)")
-    ap.add_argument("--only", choices=["stacks", "long", "full", "small", "backward", "stack_backward"],
+    ap.add_argument("--only", choices=["stacks", "long", "full", "small", "backward", "stack_backward", "decode"],
                     help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -239,6 +239,12 @@ class AttnResState:
     def reset(self) -> None:
         _N.check(_N.lib.attnres_state_reset(ctypes.byref(self.struct)), "attnres_state_reset")
 
+    def resume(self, folded: int) -> None:
+        """Take up the stack after layer `folded` (v_1 .. v_folded already in
+        the buffers, e.g. received at a pipeline stage boundary); see
+        attnres_state_resume."""
+        _N.check(_N.lib.attnres_state_resume(ctypes.byref(self.struct), int(folded)), "attnres_state_resume")
+
 
 def attnres_layer_sources(state: AttnResState, layer_idx: int) -> list[int]:
     """Device pointers of layer `layer_idx`'s sources, in order."""
@@ -260,7 +266,8 @@ def attnres_block_step(state: AttnResState, F_out: torch.Tensor, layer_idx: int,
 def attnres_layer_step(state: AttnResState, F_prev: torch.Tensor | None, w_l: torch.Tensor, layer_idx: int,
                        out_r: torch.Tensor, out_weights: torch.Tensor | None = None,
                        dev_err: torch.Tensor | None = None, stream=None) -> None:
-    """Fused: fold F_prev = v_{l-1}, then aggregate layer `layer_idx`."""
+    """Fused: fold F_prev = v_{l-1}, then aggregate layer `layer_idx`.
+    F_prev None: nothing left to fold (layer 1, or a resumed state)."""
     rc = _N.lib.attnres_layer_step(
         ctypes.byref(state.struct), _dev_ptr(F_prev, "F_prev", state.h0.dtype),
         _dev_ptr(w_l, "w_l", torch.float32), layer_idx, _dev_ptr(out_r, "out_r", state.h0.dtype),

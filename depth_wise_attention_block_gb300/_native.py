@@ -39,6 +39,7 @@ EXPORTED = (
     "attnres_intrablock_step",
     "attnres_state_init",
     "attnres_state_reset",
+    "attnres_state_resume",
     "attnres_num_sources",
     "attnres_layer_sources",
     "attnres_block_step",
@@ -92,6 +93,7 @@ def _load() -> ctypes.CDLL:
         "attnres_intrablock_step": (i32, [sp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "attnres_state_init": (i32, [sp, vp, ctypes.POINTER(vp), i32, vp, i64, i32, i32, i32, i32, f32]),
         "attnres_state_reset": (i32, [sp]),
+        "attnres_state_resume": (i32, [sp, i32]),
         "attnres_num_sources": (i32, [i32, i32, i32]),
         "attnres_layer_sources": (i32, [sp, i32, ctypes.POINTER(vp), ctypes.POINTER(i32)]),
         "attnres_block_step": (i32, [sp, vp, i32, vp, vp]),

@@ -170,6 +170,8 @@ cudaError_t device_info(DeviceInfo* info) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev);
+  if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDevices) {
     cache[dev] = di;
     have[dev] = true;
@@ -290,6 +292,10 @@ cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
     rp.inv_d = 1.0f / (float)a.d;
     rp.wait_ns = wait_limit_ns();
     rp.withhold_row1 = debug_withhold_row1();
+    // a fused step keeps source 0 (h_0, read by every layer) in L2 only
+    // while all of its rows fit in half of L2; beyond that the marked lines
+    // would crowd out the rest, and every row takes the default policy
+    rp.keep_src0 = fused && a.T * (long long)row_bytes <= (long long)di.l2_bytes / 2;
     if (split_c > 0) {
       *path = kPathRingSplit;
       return launch_ring_split(rp, split_c, fused, in_bf16, out_bf16, di.sm_count, di.max_smem_optin, a.stream);

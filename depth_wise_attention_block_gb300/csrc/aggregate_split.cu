@@ -64,7 +64,9 @@ __device__ __forceinline__ void split_produce(const SplitParams& sp, RingShared&
       }
       const uint32_t full = smem_addr(&sh.full[slot]);
       mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
-      bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+      // the bounded-wait test arms one row of the first token without its copy
+      if (issued + 1 != p.withhold_row1)
+        bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
       ++issued;
       if (++slot == (uint32_t)nslots) {
         slot = 0;
@@ -73,11 +75,7 @@ __device__ __forceinline__ void split_produce(const SplitParams& sp, RingShared&
     }
   }
   if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
-  const long long armed_slots = issued < nslots ? issued : nslots;
-  for (int k = 0; k < armed_slots; ++k) {
-    const long long uses = (issued - 1 - k) / nslots + 1;
-    mbar_wait_bounded(smem_addr(&sh.full[k]), (uint32_t)((uses - 1) & 1));
-  }
+  ring_drain(sh.full, nslots, issued, p.withhold_row1);
 }
 
 template <typename Tin, typename Tout, bool FUSED>
@@ -218,6 +216,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_split_kernel(const __grid
         for (int e2 = 0; e2 < EPV; ++e2) r[e2] = __int_as_float(0x7fc00000);
         store_out<Tout, EPV>(p.out_r + t * sp.out_stride + (long long)rank * sp.out_slice_bytes, v, r);
       }
+      if (rank == 0 && p.out_a && tid < S) p.out_a[t * S + tid] = __int_as_float(0x7fc00000);
       if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
       break;
     }

@@ -97,6 +97,24 @@ FoldPlan fold_plan(int p, int B, int L) {
   return f;
 }
 
+// Sources of layer folded + 1 of a state with every earlier layer output
+// folded: [h_0, b_1 .. b_c, partial (if open)] (Eq. 10).  Returns S.
+int state_sources(const attnres_state* st, const void** out) {
+  int S = 0;
+  out[S++] = st->h0;
+  const int f = st->folded;
+  int completed = 0;
+  bool partial = false;
+  if (f > 0) {
+    const FoldPlan fp = fold_plan(f, st->block_size, st->num_layers);
+    completed = fp.ends_block ? fp.block : fp.block - 1;
+    partial = !fp.ends_block;
+  }
+  for (int k = 0; k < completed; ++k) out[S++] = st->block_reps[k];
+  if (partial) out[S++] = st->partial;
+  return S;
+}
+
 int check_state(const attnres_state* st) {
   if (!st) return fail(ATTNRES_EINVAL, "state is NULL");
   if (!st->h0 || !st->partial) return fail(ATTNRES_EINVAL, "state h0/partial is NULL");
@@ -612,6 +630,15 @@ int attnres_state_init(attnres_state* st, const void* h0, void* const* block_rep
   return ok();
 }
 
+int attnres_state_resume(attnres_state* st, int folded) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (folded < 0 || folded > st->num_layers)
+    return fail(ATTNRES_EINVAL, "folded=%d outside 0..L=%d", folded, st->num_layers);
+  st->folded = folded;
+  return ok();
+}
+
 int attnres_state_reset(attnres_state* st) {
   if (!st) return fail(ATTNRES_EINVAL, "state is NULL");
   st->folded = 0;
@@ -636,19 +663,7 @@ int attnres_layer_sources(const attnres_state* st, int layer_idx, const void** o
   if (st->folded != layer_idx - 1)
     return fail(ATTNRES_ESTATE, "layer %d needs %d folded layer outputs, state has %d", layer_idx, layer_idx - 1,
                 st->folded);
-  int S = 0;
-  out_ptrs[S++] = st->h0;
-  const int f = st->folded;
-  int completed = 0;
-  bool partial = false;
-  if (f > 0) {
-    const FoldPlan fp = fold_plan(f, B, L);
-    completed = fp.ends_block ? fp.block : fp.block - 1;
-    partial = !fp.ends_block;
-  }
-  for (int k = 0; k < completed; ++k) out_ptrs[S++] = st->block_reps[k];
-  if (partial) out_ptrs[S++] = st->partial;
-  *out_S = S;
+  *out_S = state_sources(st, out_ptrs);
   return ok();
 }
 
@@ -688,10 +703,13 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
   if (!w_l || !out_r) return fail(ATTNRES_EINVAL, "w_l/out_r is NULL");
   const int L = st->num_layers, B = st->block_size;
   if (layer_idx < 1 || layer_idx > L + 1) return fail(ATTNRES_EINVAL, "layer_idx %d outside 1..L+1", layer_idx);
-  if ((layer_idx == 1) != (F_prev == nullptr)) return fail(ATTNRES_EINVAL, "F_prev must be NULL exactly at layer 1");
-  const int need = layer_idx >= 2 ? layer_idx - 2 : 0;
+  if (layer_idx == 1 && F_prev) return fail(ATTNRES_EINVAL, "F_prev must be NULL at layer 1");
+  // with F_prev, v_{l-1} is folded here; without, it must have been folded
+  // already (layer 1, or a state resumed at a stage boundary)
+  const int need = F_prev ? layer_idx - 2 : layer_idx - 1;
   if (st->folded != need)
-    return fail(ATTNRES_ESTATE, "layer_step(%d) needs folded == %d, state has %d", layer_idx, need, st->folded);
+    return fail(ATTNRES_ESTATE, "layer_step(%d)%s needs folded == %d, state has %d", layer_idx,
+                F_prev ? "" : " without F_prev", need, st->folded);
   {
     // r and the weights must not share memory with the state's rows or F
     const int64_t row = st->T * st->d * (st->dtype == ATTNRES_BF16 ? 2 : 4);
@@ -720,7 +738,9 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
   a.stream = static_cast<cudaStream_t>(stream);
   a.src[0] = st->h0;
   a.n_stored = 1;
-  if (layer_idx >= 2) {
+  if (!F_prev) {
+    a.n_stored = state_sources(st, a.src);
+  } else {
     const int p = layer_idx - 1;
     const FoldPlan fp = fold_plan(p, B, L);
     for (int k = 0; k < fp.block - 1; ++k) a.src[a.n_stored++] = st->block_reps[k];
@@ -735,7 +755,7 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
     cudaError_t e = launch_aggregate(a, &path);
     if (e != cudaSuccess) return cuda_fail(e, "attnres_layer_step launch");
   }
-  if (layer_idx >= 2) st->folded = layer_idx - 1;
+  st->folded = layer_idx - 1;
   return ok();
 }
 

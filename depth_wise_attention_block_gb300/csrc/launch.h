@@ -148,6 +148,7 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 struct DeviceInfo {
   int sm_count;
   int max_smem_optin;
+  int l2_bytes;
 };
 cudaError_t device_info(DeviceInfo* info);
 

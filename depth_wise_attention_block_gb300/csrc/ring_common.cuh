@@ -42,6 +42,7 @@ struct RingParams {
   int pad_rows;                // rows appended to each token (re-reads of src[0]'s row; multi-group kernel)
   int withhold_row1;           // bounded-wait test: 1 + the row of each CTA's first token armed
                                // without a copy (its waits must run out); 0 = none
+  int keep_src0;               // fused step whose source 0 fits in L2: keep it there, stream the rest
   const char* src[kMaxSources];
   const char* fuse_prev;
   const char* fuse_F;
@@ -257,10 +258,11 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
   long long issued = 0;
   bool ok = true;
   // A fused layer step runs inside a stack, where source 0 (the embedding
-  // h_0) is read again by every layer: its rows are kept in L2 and every
-  // other row streams through once (evict first), which also spares the
-  // rows the previous kernels just wrote.  A single aggregation streams
-  // everything with the default policy.
+  // h_0) is read again by every layer: while h_0 fits in half of L2
+  // (keep_src0) its rows are kept there and every other row streams
+  // through once (evict first), which also spares the rows the previous
+  // kernels just wrote.  A single aggregation, or a fused step over more
+  // tokens, streams everything with the default policy.
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   for (long long t = blockIdx.x; t < T && ok; t += gridDim.x) {
     const long long off = t * (long long)p.row_bytes;
@@ -279,7 +281,7 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
       mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
       // the bounded-wait test arms one row of the first token without its copy
       if (issued + 1 != p.withhold_row1) {
-        if (fused)
+        if (p.keep_src0)
           bulk_copy_g2s_hint(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full,
                              (j == 0 || j >= real_rows) ? keep : stream);
         else

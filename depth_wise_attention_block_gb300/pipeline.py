@@ -10,9 +10,12 @@ first layer of its block.  A receiver keeps (caches) what it was sent, so
 with interleaved (virtual) stages a rank that runs several layer chunks is
 only sent the blocks completed since its previous chunk.
 
-This module is host logic only: it says which [T, d] buffers cross which
-boundary.  The transport (NCCL / gloo send and recv of the buffers) is the
-caller's.
+plan_transfers is host logic: it says which [T, d] buffers cross which
+boundary.  transfer_buffers names those buffers in a stage's AttnResState
+(the same positions on the sending and the receiving side), and hand_off
+moves them between two stages held by one process on one GPU, one device
+copy per buffer, then resumes the receiver.  Between GPUs the transport is
+the caller's (NCCL send / recv of the same buffers, in the same order).
 """
 from __future__ import annotations
 
@@ -104,3 +107,36 @@ def full_attnres_rows(num_layers: int, chunks: list[tuple[int, int, int]]) -> in
             rows += first  # h_0 and v_1 .. v_{first-1}
         prev = rank
     return rows
+
+
+def transfer_buffers(t: Transfer, state) -> list:
+    """The buffers of a stage's AttnResState that transfer `t` moves, in
+    order: h_0 (if sent), the block sums b_k of t.blocks, the open partial
+    sum (if sent).  The sender reads them after its last layer (its chunk
+    ends by folding that layer's output), the receiver writes them into its
+    own state at the same positions."""
+    out = [state.h0] if t.embedding else []
+    out += [state.block_reps[k - 1] for k in t.blocks]
+    if t.partial is not None:
+        out.append(state.partial)
+    return out
+
+
+def hand_off(t: Transfer, src_state, dst_state, stream=None) -> int:
+    """Move transfer `t` from one stage's state to another's when both live
+    in this process on one GPU: one device-to-device copy per buffer (on
+    `stream`, default the current one), then the receiver resumes at layer
+    t.layer - 1.  Returns the bytes copied."""
+    import torch
+    src, dst = transfer_buffers(t, src_state), transfer_buffers(t, dst_state)
+    ctx = torch.cuda.stream(stream) if stream is not None else None
+    if ctx is not None:
+        ctx.__enter__()
+    try:
+        for a, b in zip(src, dst):
+            b.copy_(a, non_blocking=True)
+    finally:
+        if ctx is not None:
+            ctx.__exit__(None, None, None)
+    dst_state.resume(t.layer - 1)
+    return sum(a.numel() * a.element_size() for a in src)

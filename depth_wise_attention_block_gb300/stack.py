@@ -81,7 +81,7 @@ class StackForward:
             return N + (N - 1) + 2 * self.L + 1
         return 2 * self.L + 1
 
-    def _issue_two_phase(self, stream=None) -> None:
+    def _issue_two_phase(self, stream=None, on_layer=None) -> None:
         st, L, B = self.state, self.L, self.B
         st.reset()
         bufs = {t.data_ptr(): t for t in [st.h0] + st.block_reps}
@@ -102,27 +102,68 @@ class StackForward:
                                         self.weights[layer - 1] if self.weights is not None else None,
                                         dev_err=self.dev_err, stream=stream)
                 attnres_synthetic_layer(self.r, self.G[layer - 1], self.Sc[layer - 1], self.F, stream=stream)
+                if on_layer is not None:
+                    on_layer(layer, self)
         attnres_layer_step(st, self.F, self.W[L], L + 1, self.r,
                            self.weights[L] if self.weights is not None else None, dev_err=self.dev_err, stream=stream)
+        if on_layer is not None:
+            on_layer(L + 1, self)
 
-    def _issue(self, stream=None) -> None:
-        if self.schedule == "two_phase":
-            self._issue_two_phase(stream)
-            return
-        self.state.reset()
-        for l in range(1, self.L + 2):
-            attnres_layer_step(self.state, self.F if l > 1 else None, self.W[l - 1], l, self.r,
+    def _issue_layers(self, first: int, last: int, stream=None, on_layer=None) -> None:
+        """Layers first..last from a state with v_1 .. v_{first-1} folded:
+        the first layer aggregates the state's sources as they are, each
+        later one folds its predecessor's output in the same launch.  If
+        last == L the final aggregation follows (folding v_L); otherwise v_last
+        is folded on its own, so that the state holds everything a later
+        stage needs ([Tutorial] ch. 4.6, pipeline stages)."""
+        for l in range(first, last + 1):
+            attnres_layer_step(self.state, self.F if l > first else None, self.W[l - 1], l, self.r,
                                self.weights[l - 1] if self.weights is not None else None,
                                dev_err=self.dev_err, stream=stream)
-            if l <= self.L:
-                attnres_synthetic_layer(self.r, self.G[l - 1], self.Sc[l - 1], self.F, stream=stream)
+            attnres_synthetic_layer(self.r, self.G[l - 1], self.Sc[l - 1], self.F, stream=stream)
+            if on_layer is not None:
+                on_layer(l, self)
+        if last == self.L:
+            attnres_layer_step(self.state, self.F, self.W[self.L], self.L + 1, self.r,
+                               self.weights[self.L] if self.weights is not None else None,
+                               dev_err=self.dev_err, stream=stream)
+            if on_layer is not None:
+                on_layer(self.L + 1, self)
+        else:
+            attnres_block_step(self.state, self.F, last, dev_err=self.dev_err, stream=stream)
 
-    def run(self, stream=None) -> torch.Tensor:
-        """One forward (replays the captured graph if there is one)."""
+    def _issue(self, stream=None, on_layer=None) -> None:
+        if self.schedule == "two_phase":
+            self._issue_two_phase(stream, on_layer)
+            return
+        self.state.reset()
+        self._issue_layers(1, self.L, stream, on_layer)
+
+    def run(self, stream=None, on_layer=None) -> torch.Tensor:
+        """One forward (replays the captured graph if there is one).
+        on_layer(l, self), eager runs only, is called after layer l's step
+        and body have been issued (l = L+1: after the final aggregation)."""
         if self.graph is not None:
+            if on_layer is not None:
+                raise ValueError("on_layer needs an eager run (this forward is a captured graph)")
             self.graph.replay()
         else:
-            self._issue(stream)
+            self._issue(stream, on_layer)
+        return self.r
+
+    def run_chunk(self, first: int, last: int, stream=None, on_layer=None) -> torch.Tensor:
+        """Layers first..last only (a pipeline stage, eager).  first == 1
+        starts the stack; otherwise the state must hold v_1 .. v_{first-1}
+        folded (its own earlier chunk, or buffers received and
+        AttnResState.resume(first - 1)).  Ends with the final aggregation
+        when last == L, else with v_last folded into the state."""
+        if self.schedule != "single":
+            raise ValueError("run_chunk runs the single-pass schedule")
+        if not (1 <= first <= last <= self.L):
+            raise ValueError("need 1 <= first <= last <= L")
+        if first == 1:
+            self.state.reset()
+        self._issue_layers(first, last, stream, on_layer)
         return self.r
 
     def capture(self) -> None:
@@ -199,12 +240,16 @@ class StackBackward:
         self.ws = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=dev)
         self.graph = None
 
-    def _issue(self, dr_out, stream=None) -> None:
+    def _issue(self, dr_out, stream=None, on_call=None) -> None:
         f, st = self.fwd, self.fwd.state
         L, B, eps = f.L, f.B, f.eps
         b = st.block_reps[: self.N]
+        if on_call is not None:
+            on_call(L + 1, [st.h0] + b, dr_out, [self.dh0] + self.gb, self.dW[L], False, "before")
         attnres_aggregate_backward([st.h0] + b, f.W[L], dr_out, [self.dh0] + self.gb, self.dW[L],
                                    workspace=self.ws, eps=eps, accumulate=False, stream=stream)
+        if on_call is not None:
+            on_call(L + 1, [st.h0] + b, dr_out, [self.dh0] + self.gb, self.dW[L], False, "after")
         for n in range(self.N, 0, -1):
             first, last = (n - 1) * B + 1, min(n * B, L)
             cached = [st.h0] + b[: n - 1]
@@ -227,17 +272,26 @@ class StackBackward:
                                                  self.gpart if layer < last else None, self.gr, stream=stream)
                 srcs = cached + ([self.P[i - 1]] if i >= 2 else [])
                 grads = [self.dh0] + self.gb[: n - 1] + ([self.gpart] if i >= 2 else [])
+                if on_call is not None:
+                    on_call(layer, srcs, self.gr, grads, self.dW[layer - 1], True, "before")
                 attnres_aggregate_backward(srcs, f.W[layer - 1], self.gr, grads, self.dW[layer - 1],
                                            workspace=self.ws, eps=eps, accumulate=True, stream=stream)
+                if on_call is not None:
+                    on_call(layer, srcs, self.gr, grads, self.dW[layer - 1], True, "after")
 
-    def run(self, dr_out=None, stream=None):
+    def run(self, dr_out=None, stream=None, on_call=None):
         """One backward (replays the captured graph, recorded for the dr_out
         given to capture(), if there is one); the forward must have run on
-        the same inputs."""
+        the same inputs.  on_call(layer, sources, grad_r, grad_sources,
+        grad_w, accumulate, phase), eager runs only, is called just before
+        (phase "before") and after ("after") each layer's
+        attnres_aggregate_backward is issued."""
         if self.graph is not None:
+            if on_call is not None:
+                raise ValueError("on_call needs an eager run (this backward is a captured graph)")
             self.graph.replay()
         else:
-            self._issue(dr_out, stream)
+            self._issue(dr_out, stream, on_call)
         return self.dh0, self.dW
 
     def capture(self, dr_out) -> None:

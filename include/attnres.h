@@ -206,8 +206,10 @@ int64_t attnres_aggregate_backward_workspace_size(int64_t T, int d);
  * is allocated and no allocating library routine is called.
  *
  * The first call on a device looks up the array's device address (one
- * cudaGetSymbolAddress, with that device current) and caches it: make that
- * first call before any stream capture.  All calls share the array and it
+ * cudaGetSymbolAddress, with that device current) and caches it, keyed by
+ * the device and its current context: make that first call before any
+ * stream capture, and again after the device's context was torn down and
+ * recreated (cudaDeviceReset), when the address is looked up anew.  All calls share the array and it
  * keeps the previous call's contents (every value a call reads it has
  * written first, so nothing needs clearing); calls whose kernels overlap on
  * a GPU (other streams or host threads) race on it and must be serialised.
@@ -229,8 +231,9 @@ int attnres_aggregate_backward_noalloc(const void* const* sources, int S, int64_
  * `folded` = number of layer outputs v_1 .. v_folded already folded into the
  * partial sum / block representations.  Layer outputs must be folded in
  * order: attnres_block_step(p) needs folded == p-1; attnres_layer_step(l)
- * needs folded == l-2 (it folds v_{l-1} itself); attnres_layer_sources(l)
- * needs folded == l-1.  Anything else returns ATTNRES_ESTATE.
+ * needs folded == l-2 when it is given v_{l-1} to fold, folded == l-1
+ * when not; attnres_layer_sources(l) needs folded == l-1.  Anything else
+ * returns ATTNRES_ESTATE.
  * ---------------------------------------------------------------------- */
 typedef struct attnres_state {
   const void* h0;                          /* device [T, d]: b_0, the embedding */
@@ -255,6 +258,20 @@ int attnres_state_init(attnres_state* st, const void* h0, void* const* block_rep
 
 /* Rewind to layer 1 (folded = 0).  Host only; buffers are left as they are. */
 int attnres_state_reset(attnres_state* st);
+
+/* attnres_state_resume -- take up a stack after layer `folded` (0..L), for
+ * a pipeline stage that starts at layer folded + 1 ([Tutorial] ch. 4.6:
+ * cache-based pipeline communication sends a later stage only the blocks
+ * completed since it last received, plus the open partial sum).  Host only:
+ * sets st->folded and touches no buffer.  The caller has already placed in
+ * the state's buffers what layer folded + 1 reads: h0, b_1 .. b_c
+ * (c = completed blocks after layer `folded`) and, when layer `folded`
+ * does not end its block, the partial sum of v_{first..folded} of the open
+ * block; the sender forms them with attnres_block_step(folded) after its
+ * last layer.  The next call is attnres_layer_step(folded + 1) with
+ * F_prev = NULL (or attnres_layer_sources(folded + 1)).  ATTNRES_EINVAL for
+ * folded outside 0..L; other errors as attnres_state_reset. */
+int attnres_state_resume(attnres_state* st, int folded);
 
 /* Number of sources layer `layer_idx` (1..L, or L+1 for the final output
  * aggregation) reads: n + [i >= 2] for layer i of block n, ceil(L/B) + 1 for
@@ -291,13 +308,17 @@ int attnres_block_step(attnres_state* st, const void* F_out, int layer_idx, int*
  * using the freshly formed partial / b_n as the last source without reading
  * it back.  One launch.
  *   layer_idx  1..L+1 (L+1 = the final output aggregation over [h_0, b_1..b_N])
- *   F_prev     device [T, d] of st->dtype; NULL exactly when layer_idx == 1
+ *   F_prev     device [T, d] of st->dtype; NULL when v_{l-1} is already
+ *              folded (layer 1, or a state resumed with attnres_state_resume
+ *              at folded == l-1): then layer l is aggregated over the
+ *              state's sources as they are
  *   w_l        device [d] fp32 pseudo-query of this layer
  *   out_r      device [T, d] of st->dtype; it and out_weights may not share
  *              memory with the state's rows or F_prev (ATTNRES_EINVAL)
  *   out_weights device [T, S_l] fp32 or NULL
- * Needs folded == max(layer_idx - 2, 0); advances folded to layer_idx - 1.
- * Bit-identical to block_step(l-1) + aggregate(layer_sources(l)).
+ * Needs folded == layer_idx - 2 with F_prev, layer_idx - 1 without;
+ * leaves folded at layer_idx - 1.  Bit-identical to block_step(l-1) +
+ * aggregate(layer_sources(l)).
  * ---------------------------------------------------------------------- */
 int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, int layer_idx,
                        void* out_r, float* out_weights, int* dev_err, void* stream);
@@ -395,7 +416,6 @@ int attnres_fold(const void* prev, const void* F, void* dst, int64_t T, int d, i
  * in flight; its copies are drained), the context stays usable.  Outputs of
  * kernels launched in this mode are not meaningful.  (0, -1) restores
  * normal operation.  Process-wide; not for use while other threads launch.
- * The cluster-split variant's producer ignores withhold_row.
  * Returns ATTNRES_OK, or ATTNRES_EINVAL for withhold_row outside -1..7.
  * ---------------------------------------------------------------------- */
 int attnres_debug_wait_test(uint64_t wait_limit_ns, int withhold_row);

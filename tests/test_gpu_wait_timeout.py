@@ -10,6 +10,10 @@ normal operation the same call must give correct results.  Nothing here
 faults or hangs a GPU: every wait is bounded and every issued copy targets
 valid memory and is waited for before the CTA exits.
 """
+import os
+import subprocess
+import sys
+
 import pytest
 import torch
 
@@ -19,6 +23,9 @@ from tests.parity import check_weights, oracle_aggregate, to64
 pytestmark = pytest.mark.gpu
 
 LIMIT_NS = 1_000_000   # 1 ms: far above any healthy copy's latency
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+# the opt-in cluster-split variant for few tokens (read once per process)
+SPLIT = os.environ.get("ATTNRES_SPLIT", "0") not in ("", "0")
 
 
 @pytest.fixture(scope="module")
@@ -114,3 +121,45 @@ def test_backward_times_out_and_recovers(A, TIMEOUT_BIT):
 def test_wait_test_rejects_bad_rows(A):
     with pytest.raises(Exception):
         A.attnres_debug_wait_test(LIMIT_NS, 8)
+
+
+def test_split_variant_times_out_and_recovers(A, TIMEOUT_BIT):
+    # the cluster-split variant shares each token across a cluster of CTAs;
+    # at T = 64, d = 7168, S = 9 it takes clusters of 2, one token each.
+    # Every CTA withholds a row of its (only) token: every token is
+    # abandoned (NaN in r and the weights), the error bit is set, and
+    # normal operation afterwards gives the one-CTA-per-token results.
+    if not SPLIT:
+        pytest.skip("runs in the child process of the next test (ATTNRES_SPLIT=1)")
+    from tests.test_gpu_aggregate import _kernel_names
+    inp = W.block_bf16(T=64, d=7168, seed=6, device="cuda")
+    r = torch.zeros((64, 7168), dtype=torch.bfloat16, device="cuda")
+    a = torch.zeros((64, 9), device="cuda")
+    err = _err()
+    A.attnres_debug_wait_test(LIMIT_NS, 0)
+    try:
+        names = _kernel_names(lambda: A.attnres_aggregate(inp.H, inp.w, r, a, dev_err=err))
+        torch.cuda.synchronize()
+    finally:
+        A.attnres_debug_wait_test(0, -1)
+    if names:
+        assert any("agg_split_kernel" in n for n in names), names
+    assert int(err.item()) & TIMEOUT_BIT
+    assert torch.isnan(r.float()).all() and torch.isnan(a).all()
+    err2 = _err()
+    A.attnres_aggregate(inp.H, inp.w, r, a, dev_err=err2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == 0
+    _, a_ref, _, _ = oracle_aggregate(inp.H, inp.w, 1e-5)
+    check_weights(to64(a), a_ref)
+
+
+def test_split_variant_timeout_in_a_child_process():
+    if SPLIT:
+        pytest.skip("this is the child")
+    env = dict(os.environ, ATTNRES_SPLIT="1")
+    res = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+                          "tests/test_gpu_wait_timeout.py::test_split_variant_times_out_and_recovers"],
+                         env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stdout[-4000:] + res.stderr[-2000:]
+    assert "1 passed" in res.stdout, res.stdout[-2000:]

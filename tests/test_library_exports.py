@@ -100,9 +100,10 @@ def test_stack_calls_enforce_order(native):
     assert native.lib.attnres_block_step(ctypes.byref(st), 0x20000 + 8, 1, None, None) == native.ATTNRES_EINVAL
     assert b"F_out overlaps" in native.lib.attnres_last_error()
     assert native.lib.attnres_block_step(ctypes.byref(st), 0x100000, 1, None, None) == native.ATTNRES_EINVAL
-    # layer_step: F_prev must be NULL exactly at layer 1; layer 3 needs folded == 1
+    # layer_step: F_prev must be NULL at layer 1; without F_prev layer 2 needs
+    # v_1 folded already; with it, layer 3 needs folded == 1
     assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, 1, 0x777, None, None, None) == native.ATTNRES_EINVAL
-    assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 2, 0x777, None, None, None) == native.ATTNRES_EINVAL
+    assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 2, 0x777, None, None, None) == native.ATTNRES_ESTATE
     assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, 3, 0x777, None, None, None) == native.ATTNRES_ESTATE
     assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, L + 2, 0x777, None, None, None) == native.ATTNRES_EINVAL
     # out_r may not share memory with the state (rows of 4 x 8 bf16 = 64 B)
@@ -113,6 +114,27 @@ def test_stack_calls_enforce_order(native):
     assert native.lib.attnres_layer_step(ctypes.byref(st), None, 0x888, 1, 0x10000 - 32, None, None, None) == native.ATTNRES_EINVAL
     assert st.folded == 0
     assert native.lib.attnres_state_reset(ctypes.byref(st)) == 0
+
+
+def test_state_resume_sets_progress_only(native):
+    # a pipeline stage that starts at layer f + 1 resumes the state at f:
+    # the next layer's sources are then those of Eq. 10 after f layers
+    L, B = 93, 12
+    st, h0, partial, reps = _fake_state(native, L, B)
+    out = (ctypes.c_void_p * 128)()
+    n = ctypes.c_int()
+    for bad in (-1, L + 1):
+        assert native.lib.attnres_state_resume(ctypes.byref(st), bad) == native.ATTNRES_EINVAL
+        assert st.folded == 0
+    for f in (0, 11, 12, 47, 92, 93):
+        assert native.lib.attnres_state_resume(ctypes.byref(st), f) == 0 and st.folded == f
+        assert native.lib.attnres_layer_sources(ctypes.byref(st), f + 1, out, ctypes.byref(n)) == 0
+        assert n.value == O.num_sources(f + 1, B, L)
+        # a fused step that folds v_f again is out of order
+        if 1 <= f < L:
+            assert native.lib.attnres_layer_step(ctypes.byref(st), 0x999, 0x888, f + 1, 0x777, None, None,
+                                                 None) == native.ATTNRES_ESTATE
+    assert native.lib.attnres_state_resume(None, 3) == native.ATTNRES_EINVAL
 
 
 def test_state_init_rejects_bad_arguments(native):

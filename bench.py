@@ -53,7 +53,7 @@ METRIC = "AttnRes depth-aggregation tokens/s & HBM GB/s (% of peak), d=7168, 9 s
 T_MAIN, D_MAIN, S_MAIN = 4096, 7168, 9
 WORKLOAD = "block_attnres_single_layer_T4096_d7168_S9"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "aggregate_ring_T4096_d7168_S9.md")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "aggregate_ring_T4096_d7168_S9.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "depth_wise_attention_block_gb300", "csrc", f)
                   for f in ("ring_kernel.cuh", "ring_fixed_s.cu", "ring_common.cuh", "device_common.cuh")]
 
@@ -198,23 +198,20 @@ def hbm_peak():
 
 
 def profiled_traffic():
-    """dram bytes per launch of the aggregation kernel from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+    """DRAM bytes per launch of the aggregation kernel from the committed ncu
+    capture (profiles/aggregate_ring_T4096_d7168_S9.json), if it was taken on
+    the current kernel sources (else None)."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
         with open(p, "rb") as f:
             h.update(f.read())
     digest = h.hexdigest()
     try:
-        kv = {}
-        with open(PROFILE_SUMMARY) as f:
-            for line in f:
-                if ":" in line and line.strip().startswith(("kernel_source_sha256", "dram_bytes_per_launch")):
-                    k, v = line.split(":", 1)
-                    kv[k.strip()] = v.strip().strip("`")
-        if kv.get("kernel_source_sha256") == digest:
-            return int(kv["dram_bytes_per_launch"]), digest
-    except Exception:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_sha256") == digest:
+            return int(rec["dram_bytes_per_launch"]), digest
+    except (OSError, ValueError, KeyError, TypeError):
         pass
     return None, digest
 

@@ -460,13 +460,13 @@ def bench_stacks(A, W, dev, peak):
     out = {}
     for name, T, seed, reps in (("stack_prefill_T2048", 2048, 2, 10), ("stack_decode_T64", 64, 3, 50)):
         stk = W.stack(T=T, seed=seed, device=dev)
-        for schedule in ("single", "two_phase"):
+        for schedule in ("single", "two_phase", "hybrid"):
             fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, schedule=schedule)
             eager_ms = _time_forward(fwd, reps)
             fwd.capture()
             ms = _time_forward(fwd, reps)
             gbs = fwd.bytes_moved() / (ms * 1e-3) / 1e9
-            key = name if schedule == "single" else name + "_two_phase"
+            key = name if schedule == "single" else name + "_" + schedule
             out[key] = {"ms_per_forward": ms, "tokens_per_s": T / (ms * 1e-3), "layers": stk.num_layers,
                         "us_per_layer": 1e3 * ms / (stk.num_layers + 1), "schedule": schedule,
                         "launches_per_forward": fwd.launches_per_forward(), "cuda_graph": True,
@@ -500,6 +500,41 @@ def bench_decode(A, W, dev, peak, reps=20):
     return {"stack_decode_T64": {"ms_per_forward": ms, "us_per_layer": 1e3 * ms / (stk.num_layers + 1),
                                  "launches_per_forward": fwd.launches_per_forward(), "forwards_timed": reps,
                                  "cuda_graph": True}}
+
+
+def bench_interblock(A, W, dev, peak, reps=20, cached=(1, 4, 8), Q=12, T=2048):
+    """The two-phase schedule's inter-block pass alone (attnres_interblock),
+    T = 2048, d = 7168 bf16, for a block with n cached sources and Q = 12
+    layer queries; launches back to back.  Bytes: the n source rows read,
+    the Q fp32 aggregate rows, log-sum-exps and weights written."""
+    d = D_MAIN
+    out = {}
+    g = torch.Generator(device=dev).manual_seed(31)
+    Wq = torch.randn((Q, d), generator=g, device=dev) / math.sqrt(d)
+    R = torch.empty((Q, T, d), device=dev)
+    lse = torch.empty((Q, T), device=dev)
+    for n in cached:
+        inp = W.block_bf16(T=T, d=d, seed=40 + n, device=dev, num_blocks=max(n - 2, 0))
+        H = list(inp.H[:n].contiguous().unbind(0))
+        Aw = torch.empty((Q, T, n), device=dev)
+        for _ in range(3):
+            A.attnres_interblock(H, Wq, R, lse, Aw)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            A.attnres_interblock(H, Wq, R, lse, Aw)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        by = n * T * d * 2 + Q * T * d * 4 + Q * T * 4 + Q * T * n * 4
+        gbs = by / (ms * 1e-3) / 1e9
+        out[f"interblock_T{T}_n{n}_Q{Q}"] = {"ms_per_pass": ms, "bytes": by, "achieved_gbs": gbs,
+                                              "frac_of_hbm_peak": gbs / peak}
+        del inp, H, Aw
+    del R, lse, Wq
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_stack_backward(A, W, dev, peak, reps=5):
@@ -691,7 +726,8 @@ def run_only(args):
         res = fn(A, W, dev, peak, tokens=args.tokens)
     else:
         res = {"stacks": bench_stacks, "backward": bench_backward, "small": bench_small_fp32,
-               "stack_backward": bench_stack_backward, "decode": bench_decode}[args.only](A, W, dev, peak)
+               "stack_backward": bench_stack_backward, "decode": bench_decode,
+               "interblock": bench_interblock}[args.only](A, W, dev, peak)
     print(json.dumps(res), flush=True)
 
 
@@ -810,7 +846,8 @@ def main():
     ap.add_argument("--no-cpu-all-cores", action="store_true", help="time the oracle on one core only")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count of the --only long / --only full workloads (small cases for profiling)")
-    ap.add_argument("--only", choices=["stacks", "long", "full", "small", "backward", "stack_backward", "decode"],
+    ap.add_argument("--only", choices=["stacks", "long", "full", "small", "backward", "stack_backward", "decode",
+                                       "interblock"],
                     help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:

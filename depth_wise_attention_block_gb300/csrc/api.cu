@@ -496,6 +496,7 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
   }
   for (int q = 0; q < Q; ++q) {
     if (!w_queries[q]) return fail(ATTNRES_EINVAL, "w_queries[%d] is NULL", q);
+    if (!twophase_pointers_ok(w_queries[q])) return fail(ATTNRES_EINVAL, "w_queries[%d] not 16-byte aligned", q);
     a.wq[q] = w_queries[q];
   }
   {

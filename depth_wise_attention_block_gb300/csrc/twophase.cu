@@ -5,10 +5,15 @@
 // then folds in its own partial sum with an online-softmax merge.
 //
 //  agg_interblock_kernel (phase 1): the TMA ring of the aggregation kernels
-//      (ring_common.cuh); a token's n <= 9 cached rows are taken into
-//      registers once, then for each of the Q queries w_q: logits, softmax,
-//      the normalised weighted sum (fp32 row), its log-sum-exp and weights.
-//      One cross-warp reduction step per query.
+//      (ring_common.cuh) brings a token's n <= 9 cached rows into shared
+//      memory, where they stay until the token is done.  Phase A: the
+//      Q x n logits and the n sums of squares, queries taken two at a time
+//      (each row vector is unpacked once per pair of queries), each pair's
+//      per-thread partials summed over the warp by one reduce-scatter and
+//      over the warps in shared memory.  One barrier, then the softmax of
+//      every query (one warp per query), one more barrier, then phase C:
+//      the Q weighted sums, four queries at a time (each row vector
+//      unpacked once per four queries), written as fp32 rows.
 //
 //  agg_merge_kernel (phase 2, one layer): p = round(prev + F) (or F) is
 //      stored as the new partial sum / block sum, its logit z_p = w.p/rms(p)
@@ -39,6 +44,17 @@ struct InterParams {
   float* out_a;    // [Q, T, n] or null
 };
 
+constexpr int kInterGA = 2;  // queries per phase-A group (the logits)
+constexpr int kInterGC = 4;  // queries per phase-C group (the weighted sums)
+constexpr int kInterSumsq = kMaxQueries * kRingSmax;  // offset of the sums of squares in a warp's partials
+
+// Shared memory between the ring header and the ring slots.
+struct InterShared {
+  float red[kRingConsumerWarps][kInterSumsq + kRingSmax];  // per-warp totals: logits [q * 9 + s], then sums of squares
+  float2 a2[kMaxQueries][kRingSmax];                       // softmax weights as (a, a) pairs
+};
+constexpr int kInterSharedBytes = (int)((sizeof(InterShared) + 127) / 128 * 128);
+
 template <typename Tin, int VPT, bool EXACT>
 __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const __grid_constant__ InterParams ip) {
   const RingParams& p = ip.rp;
@@ -46,7 +62,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
   constexpr int NP = EPV / 2;
   extern __shared__ __align__(128) unsigned char smem[];
   RingShared& sh = *reinterpret_cast<RingShared*>(smem);
-  const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
+  InterShared& xs = *reinterpret_cast<InterShared*>(smem + kRingHeaderBytes);
+  const uint32_t ring = smem_addr(smem) + kRingHeaderBytes + kInterSharedBytes;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -62,137 +79,220 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
   }
 
   const int S = p.S;
+  const int Q = ip.Q;
   const long long T = p.T;
-  uint32_t slot = 0, lap = 0;
+  const float nan = __int_as_float(0x7fc00000);
+  uint32_t slot = 0, lap = 0;  // ring position of the next token's first row
   bool ok = true;
   int iter = 0;
   bool abort = false;
-  for (long long t = blockIdx.x; t < T && !abort; t += gridDim.x) {
-    uint4 x[kRingSmax][VPT];
+  for (long long t = blockIdx.x; t < T && !abort; t += gridDim.x, ++iter) {
+    const int buf = iter & 1;
+    volatile int* abort_flag = &sh.abort_flag[buf];
+    // wait for the token's n rows; they stay in their slots until phase C
+    // is done with them
+    uint32_t row[kRingSmax];  // shared-memory address of source s's row
+    uint32_t sl_of[kRingSmax];
 #pragma unroll
     for (int s = 0; s < kRingSmax; ++s) {
+      row[s] = 0;
+      sl_of[s] = 0;
       if (s < S) {
-        if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u, p.wait_ns)) ok = false;
-        const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          const int v = tid + k * kRingConsumers;
-          x[s][k] = (EXACT || v < p.nvec) ? ld_shared_v4(base + (uint32_t)v * 16u) : make_uint4(0, 0, 0, 0);
+        uint32_t sl = slot + s, lp = lap;
+        if (sl >= (uint32_t)nslots) {
+          sl -= nslots;
+          ++lp;
         }
-        // Lane 0 releases the slot only while its own waits have all succeeded:
-        // then this phase completed and its copy landed.  After a wait ran out
-        // the copy may still be in flight, and the slot must not be refilled
-        // under it (the producer then runs out of slots, stops and drains).
-        __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
-        if (++slot == (uint32_t)nslots) {
-          slot = 0;
-          ++lap;
-        }
+        if (ok && !mbar_wait_bounded(smem_addr(&sh.full[sl]), lp & 1u, p.wait_ns)) ok = false;
+        row[s] = ring + sl * (uint32_t)p.row_bytes;
+        sl_of[s] = sl;
       }
     }
-    float inv_rho = 0.f;  // lane 2s: 1 / rms(h_s), from the first query's reduction
-    // this thread's channels of query q's w, as pairs; the next query's are
-    // loaded as soon as the current one's dot products are taken, so their
-    // latency hides behind its softmax and weighted sum
-    uint64_t wp[VPT][NP];
-    auto load_w = [&](int q) {
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int v = tid + k * kRingConsumers;
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-          const bool in = EXACT || v < p.nvec;
-          wp[k][j] = f2_pack(in ? __ldg(ip.wq[q] + v * EPV + 2 * j) : 0.f,
-                             in ? __ldg(ip.wq[q] + v * EPV + 2 * j + 1) : 0.f);
-        }
-      }
-    };
-    load_w(0);
-    for (int q = 0; q < ip.Q && !abort; ++q, ++iter) {
-      const int buf = iter & 1;
-      volatile int* abort_flag = &sh.abort_flag[buf];
-      float part[2 * kRingSmax];
-#pragma unroll
-      for (int s = 0; s < kRingSmax; ++s) {
-        uint64_t dot2 = 0, ss2 = 0;
-        if (s < S) {
-#pragma unroll
-          for (int k = 0; k < VPT; ++k) {
-            uint64_t h[NP];
-            Vec<Tin>::pairs(x[s][k], h);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-              dot2 = f2_fma(wp[k][j], h[j], dot2);
-              if (q == 0) ss2 = f2_fma(h[j], h[j], ss2);
-            }
-          }
-        }
-        part[2 * s] = f2_hsum(dot2);
-        part[2 * s + 1] = f2_hsum(ss2);
-      }
-      reduce_scatter18(part, lane);
-      if ((kRsValidLanes >> lane) & 1u) {
-        const int idx = rs_index(lane);
-        if (idx < 2 * S) sh.red[buf][warp][idx] = part[0];
-      }
-      const bool warp_failed = __any_sync(0xffffffffu, !ok);
-      if (lane == 0 && warp_failed) *abort_flag = 1;
-      if (q + 1 < ip.Q) load_w(q + 1);
-      named_barrier_sync(kRingBarrierId, kRingConsumers);
 
-      abort = *abort_flag != 0;
-      float tot = 0.f;
-      if (lane < 2 * S) {
-#pragma unroll
-        for (int w = 0; w < kRingConsumerWarps; ++w) tot += sh.red[buf][w][lane];
-      }
-      const float sumsq = __shfl_down_sync(0xffffffffu, tot, 1);
-      const bool is_src = lane < 2 * S && (lane & 1) == 0;
-      // fast reciprocal square root, exponential, logarithm and division:
-      // a few fp32 ulps, far inside the parity tolerances
-      if (q == 0) inv_rho = rsqrtf(fmaf(sumsq, p.inv_d, p.eps));
-      const float z = is_src ? tot * inv_rho : -INFINITY;
-      const float m = warp_max(z);
-      const float e = is_src ? __expf(z - m) : 0.f;
-      const float esum = warp_sum(e);
-      const float nan = __int_as_float(0x7fc00000);
-      const float a = abort ? nan : __fdividef(e, esum);
-      if (warp == 0) {
-        if (is_src && ip.out_a) ip.out_a[((long long)q * T + t) * S + (lane >> 1)] = a;
-        if (lane == 0) ip.out_lse[(long long)q * T + t] = abort ? nan : m + __logf(esum);
-      }
-      uint64_t a2[kRingSmax];
+    // ---- phase A: logits of every query and the sums of squares
+    for (int q0 = 0; q0 < Q; q0 += kInterGA) {
+      const bool first = q0 == 0;
+      uint64_t acc[kInterGA][kRingSmax];
+      uint64_t ss2[kRingSmax];
 #pragma unroll
       for (int s = 0; s < kRingSmax; ++s) {
-        const float as = __shfl_sync(0xffffffffu, a, 2 * s);
-        a2[s] = f2_pack(as, as);
+        ss2[s] = 0;
+#pragma unroll
+        for (int g = 0; g < kInterGA; ++g) acc[g][s] = 0;
       }
-      char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)q * T + t) * (long long)p.d * 4;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int v = tid + k * kRingConsumers;
         if (EXACT || v < p.nvec) {
-          uint64_t acc[NP];
+          uint64_t wp[kInterGA][NP];
 #pragma unroll
-          for (int j = 0; j < NP; ++j) acc[j] = 0;
+          for (int g = 0; g < kInterGA; ++g) {
+            const bool qin = q0 + g < Q;
+#pragma unroll
+            for (int j = 0; j < NP; j += 2) {
+              const float4 w4 = qin ? __ldg(reinterpret_cast<const float4*>(ip.wq[q0 + g] + v * EPV + 2 * j))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+              wp[g][j] = f2_pack(w4.x, w4.y);
+              wp[g][j + 1] = f2_pack(w4.z, w4.w);
+            }
+          }
 #pragma unroll
           for (int s = 0; s < kRingSmax; ++s) {
             if (s < S) {
               uint64_t h[NP];
-              Vec<Tin>::pairs(x[s][k], h);
+              Vec<Tin>::pairs(ld_shared_v4(row[s] + (uint32_t)v * 16u), h);
 #pragma unroll
-              for (int j = 0; j < NP; ++j) acc[j] = f2_fma(a2[s], h[j], acc[j]);
+              for (int j = 0; j < NP; ++j) {
+#pragma unroll
+                for (int g = 0; g < kInterGA; ++g) acc[g][s] = f2_fma(wp[g][j], h[j], acc[g][s]);
+                if (first) ss2[s] = f2_fma(h[j], h[j], ss2[s]);
+              }
             }
           }
-          float r[EPV];
+        }
+      }
+      // this warp's totals: one reduce-scatter of the pair's 2 x 9 logits
+      // (and, for the first pair, the 9 sums of squares)
+      float part[kInterGA * kRingSmax + kRingSmax];
 #pragma unroll
-          for (int j = 0; j < NP; ++j) f2_unpack(acc[j], r[2 * j], r[2 * j + 1]);
-          store_out<float, EPV>(orow, v, r);
+      for (int g = 0; g < kInterGA; ++g)
+#pragma unroll
+        for (int s = 0; s < kRingSmax; ++s) part[g * kRingSmax + s] = f2_hsum(acc[g][s]);
+      if (first) {
+        constexpr int N = kInterGA * kRingSmax + kRingSmax;
+#pragma unroll
+        for (int s = 0; s < kRingSmax; ++s) part[kInterGA * kRingSmax + s] = f2_hsum(ss2[s]);
+        reduce_scatter<N>(part, lane);
+        const int idx = rs_lane_index<N>(lane);
+        if (idx >= 0) {
+          const int g = idx / kRingSmax, s = idx % kRingSmax;
+          if (g < kInterGA) {
+            if (s < S && q0 + g < Q) xs.red[warp][(q0 + g) * kRingSmax + s] = part[0];
+          } else if (s < S) {
+            xs.red[warp][kInterSumsq + s] = part[0];
+          }
+        }
+      } else {
+        constexpr int N = kInterGA * kRingSmax;
+        reduce_scatter<N>(part, lane);
+        const int idx = rs_lane_index<N>(lane);
+        if (idx >= 0) {
+          const int g = idx / kRingSmax, s = idx % kRingSmax;
+          if (s < S && q0 + g < Q) xs.red[warp][(q0 + g) * kRingSmax + s] = part[0];
         }
       }
     }
-    if (abort && tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+    const bool warp_failed = __any_sync(0xffffffffu, !ok);
+    if (lane == 0 && warp_failed) *abort_flag = 1;
+    named_barrier_sync(kRingBarrierId, kRingConsumers);
+
+    // the CTA-uniform exit test: every warp reads the flag after the barrier
+    abort = *abort_flag != 0;
+    if (abort) {
+      // the token is abandoned: NaN for every output of it, and no slot is
+      // released (a copy may still be landing in one)
+      float r[EPV];
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) r[e] = nan;
+      for (int q = 0; q < Q; ++q) {
+        char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)q * T + t) * (long long)p.d * 4;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          const int v = tid + k * kRingConsumers;
+          if (EXACT || v < p.nvec) store_out<float, EPV>(orow, v, r);
+        }
+      }
+      if (warp == 0) {
+        for (int q = lane; q < Q; q += 32) ip.out_lse[(long long)q * T + t] = nan;
+        if (ip.out_a)
+          for (int i = lane; i < Q * S; i += 32) ip.out_a[((long long)(i / S) * T + t) * S + i % S] = nan;
+      }
+      if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+
+    // ---- softmax of each query over the n sources (one warp per query)
+    for (int q = warp; q < Q; q += kRingConsumerWarps) {
+      const bool is_src = lane < S;
+      float dot = 0.f, ss = 0.f;
+      if (is_src) {
+#pragma unroll
+        for (int w = 0; w < kRingConsumerWarps; ++w) {
+          dot += xs.red[w][q * kRingSmax + lane];
+          ss += xs.red[w][kInterSumsq + lane];
+        }
+      }
+      // fast reciprocal square root, exponential, logarithm and division:
+      // a few fp32 ulps, far inside the parity tolerances
+      const float z = is_src ? dot * rsqrtf(fmaf(ss, p.inv_d, p.eps)) : -INFINITY;
+      const float m = warp_max(z);
+      const float e = is_src ? __expf(z - m) : 0.f;
+      const float esum = warp_sum(e);
+      const float a = __fdividef(e, esum);
+      if (is_src) {
+        xs.a2[q][lane] = make_float2(a, a);
+        if (ip.out_a) ip.out_a[((long long)q * T + t) * S + lane] = a;
+      }
+      if (lane == 0) ip.out_lse[(long long)q * T + t] = m + __logf(esum);
+    }
+    named_barrier_sync(kRingBarrierId, kRingConsumers);
+
+    // ---- phase C: the weighted sums, four queries at a time
+    for (int q0 = 0; q0 < Q; q0 += kInterGC) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * kRingConsumers;
+        if (EXACT || v < p.nvec) {
+          uint64_t acc[kInterGC][NP];
+#pragma unroll
+          for (int g = 0; g < kInterGC; ++g)
+#pragma unroll
+            for (int j = 0; j < NP; ++j) acc[g][j] = 0;
+#pragma unroll
+          for (int s = 0; s < kRingSmax; ++s) {
+            if (s < S) {
+              uint64_t h[NP];
+              Vec<Tin>::pairs(ld_shared_v4(row[s] + (uint32_t)v * 16u), h);
+#pragma unroll
+              for (int g = 0; g < kInterGC; ++g) {
+                if (q0 + g < Q) {
+                  const float2 ag = xs.a2[q0 + g][s];
+                  const uint64_t a2 = f2_pack(ag.x, ag.y);
+#pragma unroll
+                  for (int j = 0; j < NP; ++j) acc[g][j] = f2_fma(a2, h[j], acc[g][j]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < kInterGC; ++g) {
+            if (q0 + g < Q) {
+              float r[EPV];
+#pragma unroll
+              for (int j = 0; j < NP; ++j) f2_unpack(acc[g][j], r[2 * j], r[2 * j + 1]);
+              char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)(q0 + g) * T + t) * (long long)p.d * 4;
+              store_out<float, EPV>(orow, v, r);
+            }
+          }
+        }
+      }
+    }
+
+    // ---- release the token's slots.  Lane 0 releases a slot only while its
+    // own waits have all succeeded: then the phase completed and its copy
+    // landed.  After a wait ran out the copy may still be in flight, and the
+    // slot must not be refilled under it (the producer then runs out of
+    // slots, stops and drains).
+    __syncwarp();
+#pragma unroll
+    for (int s = 0; s < kRingSmax; ++s) {
+      if (s < S && lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[sl_of[s]]));
+    }
+    slot += S;
+    if (slot >= (uint32_t)nslots) {
+      slot -= nslots;
+      ++lap;
+    }
   }
 }
 
@@ -402,9 +502,10 @@ cudaError_t launch_interblock(const InterArgs& a) {
   rp.inv_d = 1.0f / (float)a.d;
   rp.wait_ns = wait_limit_ns();
   rp.withhold_row1 = debug_withhold_row1();
-  int nslots = (di.max_smem_optin - kRingHeaderBytes) / row_bytes;
+  // a token's n rows stay in the ring until it is done: the ring must hold them
+  int nslots = (di.max_smem_optin - kRingHeaderBytes - kInterSharedBytes) / row_bytes;
   if (nslots > kRingMaxSlots) nslots = kRingMaxSlots;
-  if (nslots < 1) return cudaErrorInvalidValue;
+  if (nslots < a.n) return cudaErrorInvalidValue;
   rp.nslots = nslots;
   for (int q = 0; q < a.Q; ++q) ip.wq[q] = a.wq[q];
   ip.Q = a.Q;
@@ -412,7 +513,7 @@ cudaError_t launch_interblock(const InterArgs& a) {
   ip.out_lse = a.out_lse;
   ip.out_a = a.out_a;
   const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
-  const int smem = kRingHeaderBytes + nslots * row_bytes;
+  const int smem = kRingHeaderBytes + kInterSharedBytes + nslots * row_bytes;
   const bool exact = nvec == vpt * kRingConsumers;
   if (bf16) {
     if (vpt == 1) return launch_inter_t<bf16_t, 1, false>(ip, grid, smem, a.stream);

@@ -14,7 +14,9 @@ inference schedule (ch. 4.4, 4.6): at the start of block n the previous
 block is closed (attnres_block_step), one inter-block pass aggregates the
 cached [h_0, b_1 .. b_{n-1}] for all of the block's layer queries
 (attnres_interblock), and each layer merges its partial sum in
-(attnres_intrablock_step).
+(attnres_intrablock_step).  schedule="hybrid" runs the blocks before
+`two_phase_from` in single pass and the later ones (the most cached
+sources, where one shared pass saves the most re-reads) two-phase.
 """
 from __future__ import annotations
 
@@ -47,7 +49,8 @@ class StackForward:
     """
 
     def __init__(self, h0, W, G, Sc, num_layers: int, block_size: int, eps: float = 1e-5,
-                 keep_weights: bool = True, dev_err: torch.Tensor | None = None, schedule: str = "single"):
+                 keep_weights: bool = True, dev_err: torch.Tensor | None = None, schedule: str = "single",
+                 two_phase_from: int = 5):
         self.L, self.B, self.eps = num_layers, block_size, eps
         T, d = h0.shape
         self.T, self.d = T, d
@@ -65,10 +68,12 @@ class StackForward:
                 off += T * s
         self.dev_err = dev_err
         self.graph = None
-        if schedule not in ("single", "two_phase"):
-            raise ValueError("schedule must be 'single' or 'two_phase'")
+        if schedule not in ("single", "two_phase", "hybrid"):
+            raise ValueError("schedule must be 'single', 'two_phase' or 'hybrid'")
         self.schedule = schedule
-        if schedule == "two_phase":
+        # the first block run two-phase
+        self.first_two_phase = {"single": None, "two_phase": 1, "hybrid": max(1, int(two_phase_from))}[schedule]
+        if schedule != "single":
             q = min(block_size, num_layers)
             n_max = -(-num_layers // block_size)          # cached sources of the last block
             self.R_inter = torch.empty((q, T, d), dtype=torch.float32, device=h0.device)
@@ -76,10 +81,12 @@ class StackForward:
             self.A_flat = torch.empty(q * T * n_max, dtype=torch.float32, device=h0.device)
 
     def launches_per_forward(self) -> int:
-        if self.schedule == "two_phase":
-            N = -(-self.L // self.B)
-            return N + (N - 1) + 2 * self.L + 1
-        return 2 * self.L + 1
+        if self.schedule == "single":
+            return 2 * self.L + 1
+        N = -(-self.L // self.B)
+        n2 = max(0, N - self.first_two_phase + 1)            # blocks run two-phase
+        closes = n2 - (1 if self.first_two_phase == 1 else 0)  # block_step closing the block before
+        return n2 + closes + 2 * self.L + 1
 
     def _issue_two_phase(self, stream=None, on_layer=None) -> None:
         st, L, B = self.state, self.L, self.B
@@ -88,6 +95,16 @@ class StackForward:
         T = self.T
         for n in range(1, -(-L // B) + 1):
             first, last = (n - 1) * B + 1, min(n * B, L)
+            if n < self.first_two_phase:
+                # single pass: each step folds the previous layer's output
+                for l in range(first, last + 1):
+                    attnres_layer_step(st, self.F if l > 1 else None, self.W[l - 1], l, self.r,
+                                       self.weights[l - 1] if self.weights is not None else None,
+                                       dev_err=self.dev_err, stream=stream)
+                    attnres_synthetic_layer(self.r, self.G[l - 1], self.Sc[l - 1], self.F, stream=stream)
+                    if on_layer is not None:
+                        on_layer(l, self)
+                continue
             if n >= 2:
                 attnres_block_step(st, self.F, first - 1, dev_err=self.dev_err, stream=stream)
             cached = [bufs[p] for p in attnres_layer_sources(st, first)]
@@ -133,7 +150,7 @@ class StackForward:
             attnres_block_step(self.state, self.F, last, dev_err=self.dev_err, stream=stream)
 
     def _issue(self, stream=None, on_layer=None) -> None:
-        if self.schedule == "two_phase":
+        if self.schedule != "single":
             self._issue_two_phase(stream, on_layer)
             return
         self.state.reset()

@@ -336,7 +336,7 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
  * attnres_interblock -- phase 1 for one block.
  *   sources    host array of n (1..9) device pointers [T, d] of dtype
  *   w_queries  host array of Q (1..16) device pointers [d] fp32 (the
- *              block's layer queries in order)
+ *              block's layer queries in order), each 16-byte aligned
  *   out_r      device [Q, T, d] fp32: per query, the softmax-weighted sum
  *              over the n sources (normalised)
  *   out_lse    device [Q, T] fp32: log sum_s exp(z_qs) of those logits

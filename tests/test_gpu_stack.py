@@ -31,11 +31,11 @@ def _oracle_stack(stk: W.Stack, tokens=None, store=O.round_bf16):
     return O.block_stack_forward(h0, Wq, fn, stk.num_layers, stk.block_size, store=store)
 
 
-def _gpu_stack(A, stk: W.Stack, graph=False, schedule="single"):
+def _gpu_stack(A, stk: W.Stack, graph=False, schedule="single", two_phase_from=5):
     from depth_wise_attention_block_gb300.stack import StackForward
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, dev_err=err,
-                       schedule=schedule)
+                       schedule=schedule, two_phase_from=two_phase_from)
     if graph:
         fwd.capture()
     fwd.run()
@@ -286,6 +286,32 @@ def test_two_phase_stack_matches_the_oracle(A, L, B, T, d, dtype):
     tol = A_ATOL if dtype == torch.float32 else STACK_BF16_A_ATOL
     wa, wr = _check_stack(fwd, tr, slice(None), dtype, tol, check_blocks=(L < 20 or dtype == torch.float32))
     print(f"two-phase stack L={L} B={B} d={d} {dtype}: worst weight error {wa:.3g}, output {wr:.3g} x bound")
+
+
+@pytest.mark.parametrize("L,B,T,d,dtype,start", [
+    (93, 12, 16, 3584, torch.float32, 5),   # K3 layout: blocks 1-4 single pass, 5-8 two-phase
+    (9, 2, 5, 7168, torch.bfloat16, 3),
+    (7, 3, 6, 64, torch.float32, 9),        # start past the last block: all single pass
+])
+def test_hybrid_stack_matches_the_oracle(A, L, B, T, d, dtype, start):
+    stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=73 + L, device="cuda", dtype=dtype)
+    fwd = _gpu_stack(A, stk, schedule="hybrid", two_phase_from=start)
+    N = -(-L // B)
+    assert fwd.launches_per_forward() == 2 * L + 1 + 2 * max(0, N - start + 1)
+    store = O.round_bf16 if dtype == torch.bfloat16 else O.round_fp32
+    tr = _oracle_stack(stk, store=store)
+    tol = A_ATOL if dtype == torch.float32 else STACK_BF16_A_ATOL
+    wa, wr = _check_stack(fwd, tr, slice(None), dtype, tol, check_blocks=(L < 20 or dtype == torch.float32))
+    print(f"hybrid stack L={L} B={B} from block {start}: worst weight error {wa:.3g}, output {wr:.3g} x bound")
+
+
+def test_hybrid_graph_equals_eager(A):
+    stk = W.stack(T=64, num_layers=93, block_size=12, seed=74, device="cuda")
+    eager = _gpu_stack(A, stk, schedule="hybrid")
+    graphed = _gpu_stack(A, stk, graph=True, schedule="hybrid")
+    assert torch.equal(eager.r, graphed.r)
+    for a1, a2 in zip(eager.weights, graphed.weights):
+        assert torch.equal(a1, a2)
 
 
 def test_two_phase_decode_T64_graph(A):

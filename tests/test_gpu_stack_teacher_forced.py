@@ -51,7 +51,7 @@ def _teacher_forced_forward(A, stk, tokens, schedule="single"):
     from depth_wise_attention_block_gb300.stack import StackForward
     L, B = stk.num_layers, stk.block_size
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, L, B, dev_err=err, schedule=schedule)
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, L, B, dev_err=err, schedule=schedule, two_phase_from=5)
     r_at, F_at, partial_at = {}, {}, {}
 
     def hook(l, f):
@@ -101,10 +101,11 @@ def test_decode_stack_T64_every_layer_every_token(A):
     print(f"decode T=64 per layer: worst weight error {wa:.3g}, worst r {wr:.3g} x bar")
 
 
-def test_decode_stack_T64_two_phase_every_layer(A):
+@pytest.mark.parametrize("schedule", ["two_phase", "hybrid"])
+def test_decode_stack_T64_two_phase_every_layer(A, schedule):
     stk = W.stack_T64(device="cuda")
-    wa, wr = _teacher_forced_forward(A, stk, torch.arange(64, device="cuda"), schedule="two_phase")
-    print(f"decode T=64 two-phase per layer: worst weight error {wa:.3g}, worst r {wr:.3g} x bar")
+    wa, wr = _teacher_forced_forward(A, stk, torch.arange(64, device="cuda"), schedule=schedule)
+    print(f"decode T=64 {schedule} per layer: worst weight error {wa:.3g}, worst r {wr:.3g} x bar")
 
 
 def test_prefill_stack_T2048_every_layer_sampled_tokens(A):

@@ -99,6 +99,41 @@ def test_fused_stack_times_out(A, TIMEOUT_BIT, withheld):
     assert int(err.item()) & TIMEOUT_BIT
 
 
+def test_interblock_times_out_and_recovers(A, TIMEOUT_BIT):
+    # the inter-block pass of the two-phase schedule keeps a token's rows in
+    # the ring until the token is done: the withheld row's wait runs out,
+    # the token's outputs for every query are NaN, nothing after it is
+    # written, and the next call is correct again
+    from tests.parity import oracle_aggregate
+    T, n, Q = 600, 8, 12
+    inp = W.block_bf16(T=T, d=7168, seed=7, device="cuda", num_blocks=n - 2)
+    H = inp.H[:n].contiguous()
+    g = torch.Generator(device="cuda").manual_seed(8)
+    Wq = torch.randn((Q, 7168), generator=g, device="cuda") / 7168 ** 0.5
+    R = torch.zeros((Q, T, 7168), device="cuda")
+    lse = torch.zeros((Q, T), device="cuda")
+    Aw = torch.zeros((Q, T, n), device="cuda")
+    err = _err()
+    A.attnres_debug_wait_test(LIMIT_NS, 0)
+    try:
+        A.attnres_interblock(list(H.unbind(0)), Wq, R, lse, Aw, dev_err=err)
+        torch.cuda.synchronize()
+    finally:
+        A.attnres_debug_wait_test(0, -1)
+    assert int(err.item()) & TIMEOUT_BIT
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert torch.isnan(R[:, :sms]).all() and torch.isnan(lse[:, :sms]).all() and torch.isnan(Aw[:, :sms]).all()
+    assert (R[:, sms:] == 0).all() and (lse[:, sms:] == 0).all()
+    err2 = _err()
+    A.attnres_interblock(list(H.unbind(0)), Wq, R, lse, Aw, dev_err=err2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == 0
+    idx = torch.arange(0, T, 37, device="cuda")
+    for q in (0, Q - 1):
+        _, a_ref, _, _ = oracle_aggregate(H[:, idx].contiguous(), Wq[q], 1e-5)
+        check_weights(to64(Aw[q, idx]), a_ref)
+
+
 def test_backward_times_out_and_recovers(A, TIMEOUT_BIT):
     inp = W.block_bf16(T=1024, d=7168, seed=4, device="cuda")
     dr = torch.randn((1024, 7168), device="cuda").to(torch.bfloat16)

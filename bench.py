@@ -463,13 +463,19 @@ def _time_forward(fwd, reps):
 
 def bench_stacks(A, W, dev, peak):
     """The 93-layer stack forwards, replayed from a CUDA graph (the eager
-    Python launch loop is also timed), with the single-pass schedule and the
-    two-phase one (one inter-block pass per block, one merge per layer)."""
+    Python launch loop is also timed), with the single-pass schedule, the
+    two-phase one (one inter-block pass per block, one merge per layer) and
+    the hybrid (blocks 5-8 two-phase); and a 16384-token prefill stack in
+    single pass."""
     from depth_wise_attention_block_gb300.stack import StackForward
     out = {}
-    for name, T, seed, reps in (("stack_prefill_T2048", 2048, 2, 10), ("stack_decode_T64", 64, 3, 50)):
+    # the long-prefill stack (T = 16384: h_0 is 235 MB, more than half of L2,
+    # so its fused steps stream every row with the default L2 policy)
+    for name, T, seed, reps, schedules in (("stack_prefill_T2048", 2048, 2, 10, ("single", "two_phase", "hybrid")),
+                                           ("stack_decode_T64", 64, 3, 50, ("single", "two_phase", "hybrid")),
+                                           ("stack_prefill_T16384", 16384, 2, 3, ("single",))):
         stk = W.stack(T=T, seed=seed, device=dev)
-        for schedule in ("single", "two_phase", "hybrid"):
+        for schedule in schedules:
             fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, schedule=schedule)
             eager_ms = _time_forward(fwd, reps)
             fwd.capture()

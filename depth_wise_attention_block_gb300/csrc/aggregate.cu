@@ -45,6 +45,7 @@
 #include <stdlib.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "attnres.h"
 #include "device_common.cuh"
@@ -177,6 +178,46 @@ cudaError_t device_info(DeviceInfo* info) {
     have[dev] = true;
   }
   *info = di;
+  return cudaSuccess;
+}
+
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != 0 || !ctx) return 0;
+  if (get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+cudaError_t SmemOptIn::ensure(const void* kern) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  const unsigned long long now = current_context_id();
+  if (slot && now != 0 && ctx[dev].load() == now) return cudaSuccess;
+  DeviceInfo di;
+  e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+  if (e != cudaSuccess) return e;
+  if (slot) ctx[dev].store(current_context_id());  // the call above made the context current
   return cudaSuccess;
 }
 

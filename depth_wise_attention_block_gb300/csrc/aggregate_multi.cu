@@ -257,20 +257,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
 
 template <typename Tin, typename Tout, int VPT, bool FUSED, bool EXACT>
 static cudaError_t launch_multi_t(const RingParams& rp, int grid, int smem, cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  static SmemOptIn optin;  // the large shared-memory opt-in, per device and context
   auto kern = agg_ring_multi_kernel<Tin, Tout, VPT, FUSED, EXACT>;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
-    DeviceInfo di;
-    e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
-  }
+  cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
   // pad every token's source list to a whole number of groups
   constexpr int GS = MultiGroup<Tin, VPT>::kSize;
   RingParams padded = rp;

@@ -300,20 +300,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_split_kernel(const __grid
 
 template <typename Tin, typename Tout, bool FUSED>
 static cudaError_t launch_split_t(const SplitParams& sp, int grid, int smem, cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  static SmemOptIn optin;  // the large shared-memory opt-in, per device and context
   auto kern = agg_split_kernel<Tin, Tout, FUSED>;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
-    DeviceInfo di;
-    e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
-  }
+  cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kRingThreads);

@@ -438,20 +438,10 @@ __global__ void __launch_bounds__(kDwThreads) dw_reduce_kernel(const float* ws, 
 
 template <typename T, int VPT, bool ACC>
 static cudaError_t launch_bwd_ring_t(const BwdParams& bp, int grid, int smem, cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  static SmemOptIn optin;  // the large shared-memory opt-in, per device and context
   auto kern = agg_bwd_ring_kernel<T, VPT, ACC>;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
-    DeviceInfo di;
-    e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
-  }
+  cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
   e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, bp);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -555,34 +545,6 @@ cudaError_t launch_aggregate_backward(const BwdArgs& a) {
 constexpr int64_t kNoAllocScratchFloats = 160 * 8192;  // 5 MiB: 160 CTA rows of d <= 8192
 static __device__ __align__(256) float g_noalloc_bwd_scratch[kNoAllocScratchFloats];
 
-// Unique id of the calling thread's current CUDA context (0 if none is
-// current yet), through the driver's own entry points: a context that was
-// torn down and created again (cudaDeviceReset) gets a new id, even where
-// its handle is reused.  cudaErrorNotSupported if the driver lacks them.
-static cudaError_t current_context_id(unsigned long long* id) {
-  using GetCurrent = int (*)(void**);
-  using GetId = int (*)(void*, unsigned long long*);
-  static GetCurrent get_current = nullptr;
-  static GetId get_id = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      get_current = reinterpret_cast<GetCurrent>(f);
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      get_id = reinterpret_cast<GetId>(f);
-  });
-  if (!get_current || !get_id) return cudaErrorNotSupported;
-  void* ctx = nullptr;
-  *id = 0;
-  if (get_current(&ctx) != 0) return cudaErrorDeviceUninitialized;
-  if (ctx && get_id(ctx, id) != 0) return cudaErrorDeviceUninitialized;
-  return cudaSuccess;
-}
-
 // Device address of the scratch array on the current device (a host-side
 // name of a __device__ array is not a device address).  Looked up with
 // cudaGetSymbolAddress the first time on a device, and again whenever the
@@ -597,16 +559,14 @@ cudaError_t noalloc_backward_scratch(float** ptr, int64_t* capacity_floats) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  unsigned long long ctx = 0;
-  const bool have_ctx = current_context_id(&ctx) == cudaSuccess;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> guard(lock);
-  if (!addr[dev] || !have_ctx || ctx == 0 || ctx != ctx_of[dev]) {
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_bwd_scratch);
     if (e != cudaSuccess) return e;
     addr[dev] = static_cast<float*>(p);
-    // the lookup made the device's context current on this thread
-    ctx_of[dev] = (have_ctx && current_context_id(&ctx) == cudaSuccess) ? ctx : 0;
+    ctx_of[dev] = current_context_id();  // the lookup made the device's context current on this thread
   }
   *ptr = addr[dev];
   *capacity_floats = kNoAllocScratchFloats;

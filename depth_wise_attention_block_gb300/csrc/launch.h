@@ -1,6 +1,8 @@
 // Host-side launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -151,5 +153,21 @@ struct DeviceInfo {
   int l2_bytes;
 };
 cudaError_t device_info(DeviceInfo* info);
+
+// Unique id of the calling thread's current CUDA context, 0 if none is
+// current yet or the driver lacks the entry points (cuCtxGetCurrent and
+// cuCtxGetId, reached through cudaGetDriverEntryPointByVersion).  A context
+// torn down and created again (cudaDeviceReset) gets a new id.
+unsigned long long current_context_id();
+
+// The large dynamic shared-memory opt-in of one kernel
+// (cudaFuncAttributeMaxDynamicSharedMemorySize), set once per device and
+// context: a context recreated after cudaDeviceReset reloads the module
+// without it, so a new context id sets it again.
+struct SmemOptIn {
+  static constexpr int kMaxDevices = 64;
+  std::atomic<unsigned long long> ctx[kMaxDevices];  // context the attribute was set in (0: not yet)
+  cudaError_t ensure(const void* kern);
+};
 
 }  // namespace attnres

@@ -442,20 +442,10 @@ __global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_c
 
 template <typename Tin, int VPT, bool EXACT>
 static cudaError_t launch_inter_t(const InterParams& ip, int grid, int smem, cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static std::atomic<bool> configured[kMaxDevices];  // set once the attribute is set
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  static SmemOptIn optin;  // the large shared-memory opt-in, per device and context
   auto kern = agg_interblock_kernel<Tin, VPT, EXACT>;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
-    DeviceInfo di;
-    e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
-  }
+  cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
   e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, ip);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

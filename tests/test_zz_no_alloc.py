@@ -6,11 +6,15 @@ library instead of a caller buffer.
 Checked through the C ABI: two calls in a row (different shapes and dtypes,
 so the second starts on the first one's leftover scratch) give the same
 gradients as attnres_aggregate_backward with a caller workspace, within the
-backward parity bar; a request larger than the built-in scratch is refused.
-This file is collected last so that a run stopping at the first failure
+backward parity bar; a request larger than the built-in scratch is refused;
+and a plain C client gets the same gradients before and after a
+cudaDeviceReset.  This file is collected last so that a run stopping at the first failure
 has run every other test before it.
 """
 import ctypes
+import os
+import shutil
+import subprocess
 
 import numpy as np
 import pytest
@@ -77,3 +81,30 @@ def test_noalloc_backward_refuses_oversize():
     rc, _ = _call_noalloc(A, H, w, dr, gH, gw)
     assert rc == A._N.ATTNRES_ERANGE
     assert b"built-in scratch" in A._N.lib.attnres_last_error()
+
+
+def test_noalloc_backward_survives_a_device_reset(tmp_path):
+    # A caller that resets its device (cudaDeviceReset: a new context, the
+    # library's module loaded again) must get the same gradients from the
+    # no-alloc backward afterwards: the scratch array's address and the
+    # kernels' shared-memory opt-in are looked up again for the new
+    # context.  Run from a plain C client (tests/c_abi/noalloc_reset_client.c)
+    # in a process of its own, so the reset touches nothing else.
+    import __graft_entry__
+    B = __graft_entry__._build_module()
+    if not os.path.exists(B.LIB_PATH):
+        B.build()
+    lib = os.path.abspath(B.LIB_PATH)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    nv = shutil.which("nvcc")
+    cuda = os.environ.get("CUDA_HOME") or (os.path.dirname(os.path.dirname(nv)) if nv else "/usr/local/cuda")
+    exe = tmp_path / "noalloc_reset_client"
+    build = subprocess.run(
+        ["gcc", "-O2", "-std=c11", "-Wall", "-I", os.path.join(root, "include"), "-I", os.path.join(cuda, "include"),
+         os.path.join(root, "tests", "c_abi", "noalloc_reset_client.c"), "-o", str(exe), lib,
+         f"-L{cuda}/lib64", "-lcudart", f"-Wl,-rpath,{os.path.dirname(lib)}", f"-Wl,-rpath,{cuda}/lib64"],
+        capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
+    assert run.returncode == 0, run.stderr + run.stdout
+    assert "equal before and after cudaDeviceReset" in run.stdout

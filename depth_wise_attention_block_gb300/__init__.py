@@ -32,7 +32,7 @@ from ._native import (  # noqa: F401
 
 __all__ = [
     "attnres_aggregate", "attnres_aggregate_backward", "attnres_aggregate_backward_workspace_size",
-    "attnres_interblock", "attnres_intrablock_step", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
+    "attnres_interblock", "attnres_interblock_workspace_size", "attnres_intrablock_step", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
     "attnres_layer_step", "attnres_synthetic_layer", "attnres_synthetic_layer_backward", "attnres_fold",
     "attnres_version", "AttnResState",
     "attnres_aggregate_host", "attnres_aggregate_host_workspace_size", "dtype_code", "AttnresError",
@@ -170,21 +170,40 @@ def attnres_aggregate_backward(sources: Sequence[torch.Tensor] | torch.Tensor, w
     _N.check(rc, "attnres_aggregate_backward")
 
 
+def attnres_interblock_workspace_size(n: int, T: int, d: int, dtype: torch.dtype, Q: int) -> int:
+    """Bytes of workspace attnres_interblock's tensor-core logits need (0: the
+    path does not apply, e.g. fp32 sources)."""
+    return _N.check(_N.lib.attnres_interblock_workspace_size(int(n), int(T), int(d), dtype_code(dtype), int(Q)),
+                    "attnres_interblock_workspace_size")
+
+
 def attnres_interblock(sources: Sequence[torch.Tensor], w_queries: Sequence[torch.Tensor] | torch.Tensor,
                        out_r: torch.Tensor, out_lse: torch.Tensor, out_weights: torch.Tensor | None = None,
-                       eps: float = ATTNRES_DEFAULT_EPS, dev_err: torch.Tensor | None = None, stream=None) -> None:
+                       eps: float = ATTNRES_DEFAULT_EPS, workspace: torch.Tensor | None = None,
+                       tensor_cores: bool = True, dev_err: torch.Tensor | None = None, stream=None) -> None:
     """Phase 1 of the two-phase schedule: the n cached sources aggregated for
     Q queries at once.  out_r [Q, T, d] fp32, out_lse [Q, T] fp32,
-    out_weights [Q, T, n] fp32 or None."""
+    out_weights [Q, T, n] fp32 or None.  With tensor_cores (bf16 sources, d
+    a multiple of 64) the logits run on the tensor cores in a workspace of
+    attnres_interblock_workspace_size bytes (allocated here through torch
+    when None); tensor_cores=False keeps every step on the CUDA cores."""
     srcs = list(sources)
     qs = list(w_queries.unbind(0)) if isinstance(w_queries, torch.Tensor) else list(w_queries)
     T, d = srcs[0].shape
     dt = srcs[0].dtype
+    ws_ptr, ws_bytes = None, 0
+    if tensor_cores:
+        need = attnres_interblock_workspace_size(len(srcs), T, d, dt, len(qs))
+        if need > 0:
+            if workspace is None:
+                workspace = torch.empty(need, dtype=torch.uint8, device=srcs[0].device)
+            ws_ptr = _dev_ptr(workspace, "workspace")
+            ws_bytes = workspace.numel() * workspace.element_size()
     sp = (ctypes.c_void_p * len(srcs))(*[_dev_ptr(t, f"sources[{i}]") for i, t in enumerate(srcs)])
     qp = (ctypes.c_void_p * len(qs))(*[_dev_ptr(q, f"w_queries[{i}]", torch.float32) for i, q in enumerate(qs)])
     rc = _N.lib.attnres_interblock(sp, len(srcs), T, d, dtype_code(dt), qp, len(qs), float(eps),
                                    _dev_ptr(out_r, "out_r", torch.float32), _dev_ptr(out_lse, "out_lse", torch.float32),
-                                   _dev_ptr(out_weights, "out_weights", torch.float32),
+                                   _dev_ptr(out_weights, "out_weights", torch.float32), ws_ptr, ws_bytes,
                                    _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
     _N.check(rc, "attnres_interblock")
 

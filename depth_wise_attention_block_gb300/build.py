@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libattnres.so")
 SOURCES = ["aggregate.cu", "ring_fixed_s.cu", "ring_fixed_s_fused.cu", "ring_fixed_s_fused_noprev.cu",
            "aggregate_multi.cu", "aggregate_split.cu",
-           "backward.cu", "twophase.cu", "elementwise.cu", "api.cu"]
+           "backward.cu", "twophase.cu", "twophase_tc.cu", "elementwise.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-Wall",
                      "-I", INCLUDE, "-I", CSRC]

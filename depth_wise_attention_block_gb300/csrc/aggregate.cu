@@ -205,7 +205,7 @@ unsigned long long current_context_id() {
   return id;
 }
 
-cudaError_t SmemOptIn::ensure(const void* kern) {
+cudaError_t SmemOptIn::ensure(const void* kern, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -215,7 +215,7 @@ cudaError_t SmemOptIn::ensure(const void* kern) {
   DeviceInfo di;
   e = device_info(&di);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes > 0 ? bytes : di.max_smem_optin);
   if (e != cudaSuccess) return e;
   if (slot) ctx[dev].store(current_context_id());  // the call above made the context current
   return cudaSuccess;

@@ -185,7 +185,7 @@ struct HostPipe {
 
 extern "C" {
 
-int attnres_version(void) { return (1 << 16) | 0; }
+int attnres_version(void) { return (1 << 16) | 1; }
 
 const char* attnres_status_string(int status) {
   switch (status) {
@@ -474,9 +474,20 @@ int attnres_aggregate_backward_noalloc(const void* const* sources, int S, int64_
   return ok();
 }
 
+int64_t attnres_interblock_workspace_size(int n, int64_t T, int d, int dtype, int Q) {
+  if (n < 1 || n > 9) return fail(ATTNRES_ERANGE, "n=%d cached sources: 1..9", n);
+  if (Q < 1 || Q > kMaxQueries) return fail(ATTNRES_ERANGE, "Q=%d queries: 1..%d", Q, kMaxQueries);
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (T < 0 || d < 1 || !size_ok(T, d)) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  const int64_t b = interblock_tc_workspace_bytes(n, T, d, dtype, Q);
+  if (b < 0) return fail(ATTNRES_ECUDA, "no CUDA device");
+  ok();
+  return b;
+}
+
 int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int dtype,
                        const float* const* w_queries, int Q, float eps, float* out_r, float* out_lse,
-                       float* out_weights, int* dev_err, void* stream) {
+                       float* out_weights, void* workspace, int64_t workspace_bytes, int* dev_err, void* stream) {
   if (!sources || !w_queries) return fail(ATTNRES_EINVAL, "sources/w_queries is NULL");
   if (n < 1 || n > 9) return fail(ATTNRES_ERANGE, "n=%d cached sources: 1..9", n);
   if (Q < 1 || Q > kMaxQueries) return fail(ATTNRES_ERANGE, "Q=%d queries: 1..%d", Q, kMaxQueries);
@@ -512,6 +523,33 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
       return fail(ATTNRES_EINVAL, "out_lse overlaps another output");
   }
   if (!twophase_pointers_ok(out_r)) return fail(ATTNRES_EINVAL, "out_r not 16-byte aligned");
+  if (workspace) {
+    // the tensor-core logits: the workspace holds the split queries and the
+    // partial dot products; it may not share memory with an input or output
+    const int64_t need = interblock_tc_workspace_bytes(n, T, d, dtype, Q);
+    if (need < 0) return fail(ATTNRES_ECUDA, "no CUDA device");
+    if (need == 0) {
+      workspace = nullptr;  // the path does not apply (fp32 sources, d not a multiple of 64): CUDA cores
+    } else {
+      if (workspace_bytes < need)
+        return fail(ATTNRES_EINVAL, "workspace of %lld bytes, %lld needed", (long long)workspace_bytes,
+                    (long long)need);
+      if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ATTNRES_EINVAL, "workspace not 256-byte aligned");
+      const int64_t row = T * d * (dtype == ATTNRES_BF16 ? 2 : 4);
+      for (int s = 0; s < n; ++s)
+        if (overlaps(workspace, need, sources[s], row)) return fail(ATTNRES_EINVAL, "workspace overlaps source %d", s);
+      if (overlaps(workspace, need, out_r, (int64_t)Q * T * d * 4) ||
+          overlaps(workspace, need, out_lse, (int64_t)Q * T * 4) ||
+          (out_weights && overlaps(workspace, need, out_weights, (int64_t)Q * T * n * 4)))
+        return fail(ATTNRES_EINVAL, "workspace overlaps an output");
+      for (int q = 0; q < Q; ++q)
+        if (overlaps(workspace, need, w_queries[q], (int64_t)d * 4))
+          return fail(ATTNRES_EINVAL, "workspace overlaps w_queries[%d]", q);
+    }
+  }
+  a.workspace = workspace;
+  a.workspace_bytes = workspace ? workspace_bytes : 0;
   a.n = n;
   a.T = T;
   a.d = d;
@@ -524,7 +562,10 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
   a.dev_err = dev_err;
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_interblock(a);
-  if (e != cudaSuccess) return cuda_fail(e, "attnres_interblock launch");
+  if (e != cudaSuccess) {
+    const char* step = interblock_tc_last_step();
+    return cuda_fail(e, *step ? step : "attnres_interblock launch");
+  }
   return ok();
 }
 

@@ -56,8 +56,14 @@ struct InterArgs {
   float* out_r;    // [Q, T, d]
   float* out_lse;  // [Q, T]
   float* out_a;    // [Q, T, n] or null
+  void* workspace;  // the tensor-core logits' scratch (interblock_tc_workspace_bytes), or null
+  int64_t workspace_bytes;
   int* dev_err;
   cudaStream_t stream;
+};
+// the queries of one inter-block pass, as a kernel parameter
+struct InterQueries {
+  const float* w[kMaxQueries];
 };
 struct MergeArgs {
   const void* prev;
@@ -79,6 +85,16 @@ struct MergeArgs {
 bool twophase_supported(int d, int dtype);
 bool twophase_pointers_ok(const void* p);
 cudaError_t launch_interblock(const InterArgs& a);
+// The inter-block logits on the tensor cores (twophase_tc.cu): bf16 sources
+// with d a multiple of 64.  Workspace bytes for n sources, T tokens and Q
+// queries on the current device (0: the path does not apply; -1: error).
+bool interblock_tc_supported(int n, int d, int dtype);
+int64_t interblock_tc_workspace_bytes(int n, long long T, int d, int dtype, int Q);
+// Splits the queries into bf16 terms and computes the partial dot products
+// [ksplit][T][n][Q] into the workspace; returns where they are.
+cudaError_t launch_interblock_tc(const InterArgs& a, void* workspace, float** dots, int* ksplit);
+// the step of the last launch_interblock_tc that failed on this thread ("" if none)
+const char* interblock_tc_last_step();
 cudaError_t launch_merge(const MergeArgs& a);
 
 // Backward of one aggregation (see backward.cu).
@@ -167,7 +183,9 @@ unsigned long long current_context_id();
 struct SmemOptIn {
   static constexpr int kMaxDevices = 64;
   std::atomic<unsigned long long> ctx[kMaxDevices];  // context the attribute was set in (0: not yet)
-  cudaError_t ensure(const void* kern);
+  // bytes: the dynamic shared memory the kernel's launches use, or 0 for the
+  // device's whole opt-in size (kernels without static shared memory)
+  cudaError_t ensure(const void* kern, int bytes = 0);
 };
 
 }  // namespace attnres

@@ -42,9 +42,12 @@ struct InterParams {
   float* out_r;    // [Q, T, d] fp32
   float* out_lse;  // [Q, T]
   float* out_a;    // [Q, T, n] or null
+  const float* dots;  // DOTS kernels: partial dot products w_q . h_s, [ksplit][T][n][Q]
+  int ksplit;
 };
 
 constexpr int kInterGA = 2;  // queries per phase-A group (the logits)
+constexpr int kInterMaxSplit = 16;  // channel splits of the tensor-core logits, at most
 constexpr int kInterGC = 4;  // queries per phase-C group (the weighted sums)
 constexpr int kInterSumsq = kMaxQueries * kRingSmax;  // offset of the sums of squares in a warp's partials
 
@@ -296,6 +299,224 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
   }
 }
 
+// The inter-block pass when the dot products w_q . h_s come precomputed
+// (the tensor-core kernel of twophase_tc.cu, partial sums per channel split
+// in ip.dots, [ksplit][T][n][Q]); bf16 sources.  A consumer thread owns
+// QPT quads of 4 channels (quad tid + m * 448), so that a warp's shared
+// loads read 256 contiguous bytes and its fp32 stores write 512 contiguous
+// bytes.  It takes its quads of the token's n rows into registers and
+// releases the slots at once (the producer keeps the ring full), forms the
+// sums of squares on the way, and loads its warp's partial dots (queries
+// warp, warp + 14) at the token's start, summed in split order.  One
+// barrier, the softmax of every query (one warp per query), one more
+// barrier, then the weighted sums from registers, kInterGCr queries at a
+// time.
+constexpr int kInterGCr = 2;
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+template <int QPT, bool EXACT>
+__global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(const __grid_constant__ InterParams ip) {
+  const RingParams& p = ip.rp;
+  extern __shared__ __align__(128) unsigned char smem[];
+  RingShared& sh = *reinterpret_cast<RingShared*>(smem);
+  InterShared& xs = *reinterpret_cast<InterShared*>(smem + kRingHeaderBytes);
+  const uint32_t ring = smem_addr(smem) + kRingHeaderBytes + kInterSharedBytes;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int nslots = p.nslots;
+  const int nquad = 2 * p.nvec;  // 8-byte quads (4 bf16) per row
+  pdl_trigger();
+  ring_init(p, sh);
+  __syncthreads();
+  pdl_wait();
+
+  if (warp == kRingConsumerWarps) {
+    if (lane == 0) ring_produce(p, sh, ring);
+    return;
+  }
+
+  const int S = p.S;
+  const int Q = ip.Q;
+  const long long T = p.T;
+  const float nan = __int_as_float(0x7fc00000);
+  uint32_t slot = 0, lap = 0;
+  bool ok = true;
+  int iter = 0;
+  bool abort = false;
+  auto consume = [&](uint2* dst) {
+    if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u, p.wait_ns)) ok = false;
+    const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
+#pragma unroll
+    for (int m = 0; m < QPT; ++m) {
+      const int qd = tid + m * kRingConsumers;
+      dst[m] = (EXACT || qd < nquad) ? ld_shared_v2(base + (uint32_t)qd * 8u) : make_uint2(0, 0);
+    }
+    // Lane 0 releases the slot only while its own waits have all succeeded:
+    // then this phase completed and its copy landed.  After a wait ran out
+    // the copy may still be in flight, and the slot must not be refilled
+    // under it (the producer then runs out of slots, stops and drains).
+    __syncwarp();
+    if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
+    if (++slot == (uint32_t)nslots) {
+      slot = 0;
+      ++lap;
+    }
+  };
+  // the 4 channels of a quad as 2 packed fp32 pairs
+  auto pairs = [](const uint2& v, uint64_t* h) {
+    h[0] = f2_pack(bf16lo(v.x), bf16hi(v.x));
+    h[1] = f2_pack(bf16lo(v.y), bf16hi(v.y));
+  };
+
+  for (long long t = blockIdx.x; t < T && !abort; t += gridDim.x, ++iter) {
+    const int buf = iter & 1;
+    volatile int* abort_flag = &sh.abort_flag[buf];
+    // this warp's queries' partial dots, loads issued together
+    float pre_dot[2] = {0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int q = warp + u * kRingConsumerWarps;
+      if (q < Q && lane < S) {
+        float part[kInterMaxSplit];
+#pragma unroll
+        for (int k = 0; k < kInterMaxSplit; ++k)
+          part[k] = k < ip.ksplit ? __ldg(ip.dots + (((long long)k * T + t) * S + lane) * Q + q) : 0.f;
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < kInterMaxSplit; ++k) sum += part[k];
+        pre_dot[u] = sum;
+      }
+    }
+    // the token's rows into registers, the sums of squares on the way
+    uint2 x[kRingSmax][QPT];
+    float part[kRingSmax];
+#pragma unroll
+    for (int s = 0; s < kRingSmax; ++s) {
+      part[s] = 0.f;
+      if (s < S) {
+        consume(x[s]);
+        uint64_t ss2 = 0;
+#pragma unroll
+        for (int m = 0; m < QPT; ++m) {
+          uint64_t h[2];
+          pairs(x[s][m], h);
+          ss2 = f2_fma(h[0], h[0], ss2);
+          ss2 = f2_fma(h[1], h[1], ss2);
+        }
+        part[s] = f2_hsum(ss2);
+      }
+    }
+    reduce_scatter<kRingSmax>(part, lane);
+    {
+      const int idx = rs_lane_index<kRingSmax>(lane);
+      if (idx >= 0 && idx < S) xs.red[warp][kInterSumsq + idx] = part[0];
+    }
+    const bool warp_failed = __any_sync(0xffffffffu, !ok);
+    if (lane == 0 && warp_failed) *abort_flag = 1;
+    named_barrier_sync(kRingBarrierId, kRingConsumers);
+
+    // the CTA-uniform exit test: every warp reads the flag after the barrier
+    abort = *abort_flag != 0;
+    if (abort) {
+      for (int q = 0; q < Q; ++q) {
+        char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)q * T + t) * (long long)p.d * 4;
+#pragma unroll
+        for (int m = 0; m < QPT; ++m) {
+          const int qd = tid + m * kRingConsumers;
+          if (EXACT || qd < nquad) *reinterpret_cast<float4*>(orow + (size_t)qd * 16) = make_float4(nan, nan, nan, nan);
+        }
+      }
+      if (warp == 0) {
+        for (int q = lane; q < Q; q += 32) ip.out_lse[(long long)q * T + t] = nan;
+        if (ip.out_a)
+          for (int i = lane; i < Q * S; i += 32) ip.out_a[((long long)(i / S) * T + t) * S + i % S] = nan;
+      }
+      if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+
+    // ---- softmax of each query over the n sources (one warp per query)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int q = warp + u * kRingConsumerWarps;
+      if (q < Q) {
+        const bool is_src = lane < S;
+        float ss = 0.f;
+        if (is_src) {
+#pragma unroll
+          for (int w = 0; w < kRingConsumerWarps; ++w) ss += xs.red[w][kInterSumsq + lane];
+        }
+        // fast reciprocal square root, exponential, logarithm and division:
+        // a few fp32 ulps, far inside the parity tolerances
+        const float z = is_src ? pre_dot[u] * rsqrtf(fmaf(ss, p.inv_d, p.eps)) : -INFINITY;
+        const float m = warp_max(z);
+        const float e = is_src ? __expf(z - m) : 0.f;
+        const float esum = warp_sum(e);
+        const float a = __fdividef(e, esum);
+        if (is_src) {
+          xs.a2[q][lane] = make_float2(a, a);
+          if (ip.out_a) ip.out_a[((long long)q * T + t) * S + lane] = a;
+        }
+        if (lane == 0) ip.out_lse[(long long)q * T + t] = m + __logf(esum);
+      }
+    }
+    named_barrier_sync(kRingBarrierId, kRingConsumers);
+
+    // ---- the weighted sums from registers, kInterGCr queries at a time:
+    // per source, the group's weights are loaded once and update every quad
+    for (int q0 = 0; q0 < Q; q0 += kInterGCr) {
+      uint64_t acc[QPT][kInterGCr][2];
+#pragma unroll
+      for (int m = 0; m < QPT; ++m)
+#pragma unroll
+        for (int g = 0; g < kInterGCr; ++g) acc[m][g][0] = acc[m][g][1] = 0;
+#pragma unroll
+      for (int s = 0; s < kRingSmax; ++s) {
+        if (s < S) {
+          uint64_t a2[kInterGCr];
+#pragma unroll
+          for (int g = 0; g < kInterGCr; ++g) {
+            const float2 ag = q0 + g < Q ? xs.a2[q0 + g][s] : make_float2(0.f, 0.f);
+            a2[g] = f2_pack(ag.x, ag.y);
+          }
+#pragma unroll
+          for (int m = 0; m < QPT; ++m) {
+            uint64_t h[2];
+            pairs(x[s][m], h);
+#pragma unroll
+            for (int g = 0; g < kInterGCr; ++g) {
+              acc[m][g][0] = f2_fma(a2[g], h[0], acc[m][g][0]);
+              acc[m][g][1] = f2_fma(a2[g], h[1], acc[m][g][1]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kInterGCr; ++g) {
+        if (q0 + g < Q) {
+          char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)(q0 + g) * T + t) * (long long)p.d * 4;
+#pragma unroll
+          for (int m = 0; m < QPT; ++m) {
+            const int qd = tid + m * kRingConsumers;
+            if (EXACT || qd < nquad) {
+              float4 r;
+              f2_unpack(acc[m][g][0], r.x, r.y);
+              f2_unpack(acc[m][g][1], r.z, r.w);
+              *reinterpret_cast<float4*>(orow + (size_t)qd * 16) = r;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------- phase 2 ---
 
 constexpr int kMergeThreads = kRingConsumers;  // 448: two 16-byte vectors each at d = 7168 bf16
@@ -440,10 +661,15 @@ __global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_c
 
 // ---------------------------------------------------------------- launch --
 
-template <typename Tin, int VPT, bool EXACT>
+template <typename Tin, int VPT, bool EXACT, bool DOTS = false>
 static cudaError_t launch_inter_t(const InterParams& ip, int grid, int smem, cudaStream_t stream) {
   static SmemOptIn optin;  // the large shared-memory opt-in, per device and context
-  auto kern = agg_interblock_kernel<Tin, VPT, EXACT>;
+  auto kern = [] {
+    if constexpr (DOTS)
+      return agg_interblock_dots_kernel<2 * VPT, EXACT>;  // bf16 rows: two quads per 16-byte vector
+    else
+      return agg_interblock_kernel<Tin, VPT, EXACT>;
+  }();
   cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
   e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, ip);
@@ -492,7 +718,8 @@ cudaError_t launch_interblock(const InterArgs& a) {
   rp.inv_d = 1.0f / (float)a.d;
   rp.wait_ns = wait_limit_ns();
   rp.withhold_row1 = debug_withhold_row1();
-  // a token's n rows stay in the ring until it is done: the ring must hold them
+  // the one-pass kernel keeps a token's n rows in the ring until it is done:
+  // the ring must hold them
   int nslots = (di.max_smem_optin - kRingHeaderBytes - kInterSharedBytes) / row_bytes;
   if (nslots > kRingMaxSlots) nslots = kRingMaxSlots;
   if (nslots < a.n) return cudaErrorInvalidValue;
@@ -505,6 +732,18 @@ cudaError_t launch_interblock(const InterArgs& a) {
   const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
   const int smem = kRingHeaderBytes + kInterSharedBytes + nslots * row_bytes;
   const bool exact = nvec == vpt * kRingConsumers;
+  if (a.workspace && interblock_tc_supported(a.n, a.d, a.dtype)) {
+    // the logits on the tensor cores, then the softmax and the weighted sums here
+    float* dots = nullptr;
+    int ksplit = 0;
+    e = launch_interblock_tc(a, a.workspace, &dots, &ksplit);
+    if (e != cudaSuccess) return e;
+    ip.dots = dots;
+    ip.ksplit = ksplit;
+    if (vpt == 1) return launch_inter_t<bf16_t, 1, false, true>(ip, grid, smem, a.stream);
+    return exact ? launch_inter_t<bf16_t, 2, true, true>(ip, grid, smem, a.stream)
+                 : launch_inter_t<bf16_t, 2, false, true>(ip, grid, smem, a.stream);
+  }
   if (bf16) {
     if (vpt == 1) return launch_inter_t<bf16_t, 1, false>(ip, grid, smem, a.stream);
     return exact ? launch_inter_t<bf16_t, 2, true>(ip, grid, smem, a.stream)

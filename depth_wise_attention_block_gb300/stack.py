@@ -30,6 +30,7 @@ from . import (
     attnres_block_step,
     attnres_fold,
     attnres_interblock,
+    attnres_interblock_workspace_size,
     attnres_intrablock_step,
     attnres_layer_sources,
     attnres_layer_step,
@@ -79,6 +80,9 @@ class StackForward:
             self.R_inter = torch.empty((q, T, d), dtype=torch.float32, device=h0.device)
             self.lse_inter = torch.empty((q, T), dtype=torch.float32, device=h0.device)
             self.A_flat = torch.empty(q * T * n_max, dtype=torch.float32, device=h0.device)
+            # the tensor-core logits' workspace, sized for the largest block
+            need = max(attnres_interblock_workspace_size(n, T, d, h0.dtype, q) for n in range(1, n_max + 1))
+            self.inter_ws = torch.empty(need, dtype=torch.uint8, device=h0.device) if need > 0 else None
 
     def launches_per_forward(self) -> int:
         if self.schedule == "single":
@@ -111,6 +115,7 @@ class StackForward:
             Q = last - first + 1
             A = self.A_flat[: Q * T * n].view(Q, T, n)
             attnres_interblock(cached, self.W[first - 1:last], self.R_inter[:Q], self.lse_inter[:Q], A,
+                               workspace=self.inter_ws, tensor_cores=self.inter_ws is not None,
                                dev_err=self.dev_err, stream=stream)
             for layer in range(first, last + 1):
                 q = layer - first

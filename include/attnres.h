@@ -341,12 +341,34 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
  *              over the n sources (normalised)
  *   out_lse    device [Q, T] fp32: log sum_s exp(z_qs) of those logits
  *   out_weights device [Q, T, n] fp32 (softmax over the n sources) or NULL
- *   Every source row is read once for all Q queries.  No output may share
- *   memory with a source or with another output (ATTNRES_EINVAL).
+ *   workspace  NULL, or device scratch of at least
+ *              attnres_interblock_workspace_size(n, T, d, dtype, Q) bytes,
+ *              256-byte aligned, owned by the caller, sharing no memory
+ *              with an input or output (its contents on entry do not
+ *              matter).  With it (bf16 sources, d a multiple of 64) the
+ *              Q x n logits of all tokens are taken on the tensor cores
+ *              (tcgen05.mma): the queries split into three bf16 terms
+ *              (hi + mid + lo, fp32 accumulation), tiles of tokens x
+ *              sources loaded by TMA, the channels split across CTAs; the
+ *              softmax and the weighted sums then read the sources again.
+ *              Without it (or when the size is 0) every step runs on the
+ *              CUDA cores in one pass.  Results agree to fp32 rounding.
+ *   workspace_bytes  its size
+ *   Every source row is read once for all Q queries (twice with the
+ *   workspace: once for the logits, once for the weighted sums).  No output
+ *   may share memory with a source or with another output (ATTNRES_EINVAL).
  * ---------------------------------------------------------------------- */
 int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int dtype,
                        const float* const* w_queries, int Q, float eps, float* out_r,
-                       float* out_lse, float* out_weights, int* dev_err, void* stream);
+                       float* out_lse, float* out_weights, void* workspace, int64_t workspace_bytes,
+                       int* dev_err, void* stream);
+
+/* Bytes of workspace attnres_interblock's tensor-core logits need for n
+ * sources of T tokens and d channels and Q queries on the current device
+ * (the split queries, 48 x d bf16, and the partial dot products of every
+ * channel split); 0 when that path does not apply (fp32 sources, d not a
+ * multiple of 64).  Negative attnres_status on bad arguments. */
+int64_t attnres_interblock_workspace_size(int n, int64_t T, int d, int dtype, int Q);
 
 /* attnres_intrablock_step -- phase 2 for layer l (1..L) of block n:
  *   first layer of its block (i = 1): F_prev NULL and the previous block

@@ -251,9 +251,17 @@ def test_bytes_model_counts_k3_sources(A):
 
 # ------------------------------------------------- two-phase schedule -------
 
-@pytest.mark.parametrize("n,Q,dtype,d", [(1, 12, torch.bfloat16, 7168), (5, 3, torch.bfloat16, 7168),
-                                         (9, 12, torch.float32, 3584), (8, 9, torch.bfloat16, 7160)])
-def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d):
+@pytest.mark.parametrize("tensor_cores", [True, False], ids=["tcgen05_logits", "cuda_cores"])
+@pytest.mark.parametrize("n,Q,dtype,d", [
+    (1, 12, torch.bfloat16, 7168),   # tensor cores: 128 tokens per tile, 2 tiles (the second ragged)
+    (5, 3, torch.bfloat16, 7168),    # 16 tokens x 8 rows (3 zero rows), ragged last tile
+    (3, 12, torch.bfloat16, 7168),   # 32 tokens x 4 rows
+    (8, 12, torch.bfloat16, 7168),   # the K3 top block: 16 tokens x 8 rows
+    (9, 16, torch.bfloat16, 1024),   # 8 tokens x 16 rows, 16 channel chunks, Q = 16
+    (9, 12, torch.float32, 3584),    # fp32 sources: CUDA cores either way
+    (8, 9, torch.bfloat16, 7160),    # d not a multiple of 64: CUDA cores either way
+])
+def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d, tensor_cores):
     from tests.parity import oracle_aggregate
     T = 150
     inp = W.block_bf16(T=T, d=d, seed=60 + n + Q, device="cuda", num_blocks=max(n - 2, 0), src_dtype=dtype)
@@ -263,8 +271,10 @@ def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d):
     R = torch.empty((Q, T, d), device="cuda")
     lse = torch.empty((Q, T), device="cuda")
     Aw = torch.empty((Q, T, n), device="cuda")
-    A.attnres_interblock(list(H.unbind(0)), Wq, R, lse, Aw)
+    A.attnres_interblock(list(H.unbind(0)), Wq, R, lse, Aw, tensor_cores=tensor_cores)
     torch.cuda.synchronize()
+    uses_tc = tensor_cores and A.attnres_interblock_workspace_size(n, T, d, dtype, Q) > 0
+    assert uses_tc == (tensor_cores and dtype == torch.bfloat16 and d % 64 == 0)
     for q in range(Q):
         r_ref, a_ref, l_ref = O.depth_attention_lse(to64(H), to64(Wq[q]))
         _, _, cond, M = oracle_aggregate(H, Wq[q], 1e-5)

@@ -137,6 +137,17 @@ def test_state_resume_sets_progress_only(native):
     assert native.lib.attnres_state_resume(None, 3) == native.ATTNRES_EINVAL
 
 
+def test_interblock_workspace_size_checks_its_arguments(native):
+    # host checks before any device query: cached sources 1..9, queries
+    # 1..16, a known dtype
+    lib = native.lib
+    assert lib.attnres_interblock_workspace_size(0, 64, 7168, 1, 12) == native.ATTNRES_ERANGE
+    assert lib.attnres_interblock_workspace_size(10, 64, 7168, 1, 12) == native.ATTNRES_ERANGE
+    assert lib.attnres_interblock_workspace_size(4, 64, 7168, 1, 17) == native.ATTNRES_ERANGE
+    assert lib.attnres_interblock_workspace_size(4, 64, 7168, 7, 12) == native.ATTNRES_EDTYPE
+    assert lib.attnres_interblock_workspace_size(4, -1, 7168, 1, 12) == native.ATTNRES_EINVAL
+
+
 def test_state_init_rejects_bad_arguments(native):
     st = native.AttnresState()
     reps = (ctypes.c_void_p * 3)(0x1000, 0x2000, 0x3000)

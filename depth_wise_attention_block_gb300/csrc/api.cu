@@ -572,7 +572,6 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
 int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* w_l, int layer_idx,
                             const float* r_inter, const float* lse_inter, const float* a_inter, void* out_r,
                             float* out_weights, int* dev_err, void* stream) {
-  (void)dev_err;  // the merge kernel has no waits
   int rc = check_state(st);
   if (rc) return rc;
   const int L = st->num_layers, B = st->block_size;
@@ -627,6 +626,7 @@ int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* 
   a.dtype = st->dtype;
   a.n = n;
   a.eps = st->eps;
+  a.dev_err = dev_err;
   a.stream = static_cast<cudaStream_t>(stream);
   if (st->T > 0) {
     cudaError_t e = launch_merge(a);

@@ -80,6 +80,7 @@ struct MergeArgs {
   int dtype;
   int n;
   float eps;
+  int* dev_err;  // the ring merge's bounded waits (bf16 rows of 2 x 448 vectors)
   cudaStream_t stream;
 };
 bool twophase_supported(int d, int dtype);

@@ -659,6 +659,200 @@ __global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_c
   }
 }
 
+// The merge of a block's later layers (i >= 2) with the TMA ring, for bf16
+// rows of exactly 2 x 448 16-byte vectors (d = 7168).  Per token the
+// producer streams [prev (PREV), F, the fp32 inter-block row's two halves]
+// into the ring; each consumer thread folds its two vectors of F into the
+// partial sum (one rounding, stored), takes their dot product with w and
+// their sum of squares, and after one barrier every warp forms the merge
+// coefficients and writes r = c1 r_inter + c2 p.
+struct MergeRingParams {
+  RingParams rp;         // ring geometry; rp.T, rp.d, rp.nvec, rp.row_bytes, rp.w, rp.eps, rp.inv_d
+  MergeParams mp;        // the merge's rows and outputs
+};
+
+template <bool PREV>
+__device__ __forceinline__ void merge_produce(const MergeRingParams& q, RingShared& sh, uint32_t ring) {
+  const RingParams& p = q.rp;
+  const int nslots = p.nslots;
+  const int rows = (PREV ? 1 : 0) + 1 + 2;
+  uint32_t slot = 0, lap = 0;
+  long long issued = 0;
+  bool ok = true;
+  for (long long t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
+    const long long off = t * (long long)p.row_bytes;
+    for (int j = 0; j < rows; ++j) {
+      const char* g;
+      if (PREV && j == 0) g = q.mp.prev + off;
+      else if (j == rows - 3) g = q.mp.F + off;
+      else g = reinterpret_cast<const char*>(q.mp.r_inter) + 2 * off + (j - (rows - 2)) * (long long)p.row_bytes;
+      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = smem_addr(&sh.full[slot]);
+      mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
+      // the bounded-wait test arms one row of the first token without its copy
+      if (issued + 1 != p.withhold_row1) bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+      ++issued;
+      if (++slot == (uint32_t)nslots) {
+        slot = 0;
+        ++lap;
+      }
+    }
+  }
+  if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+  ring_drain(sh.full, nslots, issued, p.withhold_row1);
+}
+
+template <bool PREV>
+__global__ void __launch_bounds__(kRingThreads, 1) agg_merge_ring_kernel(const __grid_constant__ MergeRingParams q) {
+  const RingParams& p = q.rp;
+  const MergeParams& mp = q.mp;
+  extern __shared__ __align__(128) unsigned char smem[];
+  RingShared& sh = *reinterpret_cast<RingShared*>(smem);
+  const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nslots = p.nslots;
+  pdl_trigger();
+  ring_init(p, sh);
+  __syncthreads();
+  pdl_wait();
+  if (warp == kRingConsumerWarps) {
+    if (lane == 0) merge_produce<PREV>(q, sh, ring);
+    return;
+  }
+
+  uint64_t wp[2][4];  // this thread's channels of w (vectors tid, tid + 448), as pairs
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int v = tid + k * kRingConsumers;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wp[k][j] = f2_pack(__ldg(p.w + v * 8 + 2 * j), __ldg(p.w + v * 8 + 2 * j + 1));
+  }
+  const long long T = p.T;
+  const float nan = __int_as_float(0x7fc00000);
+  uint32_t slot = 0, lap = 0;
+  bool ok = true;
+  int iter = 0;
+  bool abort = false;
+  // take 32 bytes per thread of the next slot: a bf16 row's vectors tid and
+  // tid + 448 (halves = false), or one fp32 half row's bytes [32 tid, +32)
+  auto consume = [&](uint4* dst, bool halves) {
+    if (ok && !mbar_wait_bounded_sh(smem_addr(&sh.full[slot]), lap & 1u, &sh.wait_ns)) ok = false;
+    const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
+    if (halves) {
+      dst[0] = ld_shared_v4(base + (uint32_t)tid * 32u);
+      dst[1] = ld_shared_v4(base + (uint32_t)tid * 32u + 16u);
+    } else {
+      dst[0] = ld_shared_v4(base + (uint32_t)tid * 16u);
+      dst[1] = ld_shared_v4(base + (uint32_t)(tid + kRingConsumers) * 16u);
+    }
+    // Lane 0 releases the slot only while its own waits have all succeeded
+    // (the safe abort protocol of the ring kernels).
+    __syncwarp();
+    if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
+    if (++slot == (uint32_t)nslots) {
+      slot = 0;
+      ++lap;
+    }
+  };
+
+  for (long long t = blockIdx.x; t < T && !abort; t += gridDim.x, ++iter) {
+    const int buf = iter & 1;
+    volatile int* abort_flag = &sh.abort_flag[buf];
+    const float lse = __ldg(mp.lse_inter + t);
+    uint4 pv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)}, fv[2];
+    if (PREV) consume(pv, false);
+    consume(fv, false);
+    // the new partial sum: prev + F, rounded once, stored
+    uint4 x[2];
+    char* drow = mp.dst + t * (long long)p.row_bytes;
+    uint64_t dot2 = 0, ss2 = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float f[8];
+      Vec<bf16_t>::unpack(fv[k], f);
+      if (PREV) {
+        float g[8];
+        Vec<bf16_t>::unpack(pv[k], g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = g[e] + f[e];
+      }
+      if (!ok) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = nan;
+      }
+      x[k] = Vec<bf16_t>::pack(f);
+      *reinterpret_cast<uint4*>(drow + (size_t)(tid + k * kRingConsumers) * 16) = x[k];
+      uint64_t h[4];
+      Vec<bf16_t>::pairs(x[k], h);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        dot2 = f2_fma(wp[k][j], h[j], dot2);
+        ss2 = f2_fma(h[j], h[j], ss2);
+      }
+    }
+    const float dot = warp_sum(f2_hsum(dot2)), ss = warp_sum(f2_hsum(ss2));
+    if (lane == 0) {
+      sh.red[buf][warp][0] = dot;
+      sh.red[buf][warp][1] = ss;
+    }
+    // the fp32 inter-block row: thread tid's vectors' 32 bytes in each half
+    uint4 r0[2], r1[2];
+    consume(r0, true);
+    consume(r1, true);
+    const bool warp_failed = __any_sync(0xffffffffu, !ok);
+    if (lane == 0 && warp_failed) *abort_flag = 1;
+    named_barrier_sync(kRingBarrierId, kRingConsumers);
+    abort = *abort_flag != 0;
+
+    float c1 = nan, c2 = nan;
+    if (!abort) {
+      float dd = 0.f, qq = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRingConsumerWarps; ++w) {
+        dd += sh.red[buf][w][0];
+        qq += sh.red[buf][w][1];
+      }
+      // fast reciprocal square root, exponential and division: a few fp32
+      // ulps, far inside the parity tolerances
+      const float zp = dd * rsqrtf(fmaf(qq, p.inv_d, p.eps));
+      const float m = fmaxf(lse, zp);
+      const float e1 = __expf(lse - m), e2 = __expf(zp - m);
+      const float inv = __fdividef(1.0f, e1 + e2);
+      c1 = e1 * inv;
+      c2 = e2 * inv;
+    }
+    const uint64_t c1p = f2_pack(c1, c1), c2p = f2_pack(c2, c2);
+    char* orow = mp.out_r + t * (long long)p.row_bytes;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4* rr = k == 0 ? r0 : r1;
+      uint64_t ri[4] = {f2_pack(__uint_as_float(rr[0].x), __uint_as_float(rr[0].y)),
+                        f2_pack(__uint_as_float(rr[0].z), __uint_as_float(rr[0].w)),
+                        f2_pack(__uint_as_float(rr[1].x), __uint_as_float(rr[1].y)),
+                        f2_pack(__uint_as_float(rr[1].z), __uint_as_float(rr[1].w))};
+      uint64_t h[4];
+      Vec<bf16_t>::pairs(x[k], h);
+      float out[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t r = f2_fma(c2p, h[j], f2_fma(c1p, ri[j], 0));
+        f2_unpack(r, out[2 * j], out[2 * j + 1]);
+      }
+      store_out<bf16_t, 8>(orow, tid + k * kRingConsumers, out);
+    }
+    if (mp.out_a && warp == 0) {
+      const int na = mp.n + 1;
+      for (int s2 = lane; s2 < mp.n; s2 += 32)
+        mp.out_a[t * na + s2] = (mp.a_inter ? __ldg(mp.a_inter + t * mp.n + s2) : 0.f) * c1;
+      if (lane == 0) mp.out_a[t * na + mp.n] = c2;
+    }
+    if (abort && tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+  }
+}
+
 // ---------------------------------------------------------------- launch --
 
 template <typename Tin, int VPT, bool EXACT, bool DOTS = false>
@@ -754,6 +948,16 @@ cudaError_t launch_interblock(const InterArgs& a) {
                : launch_inter_t<float, 2, false>(ip, grid, smem, a.stream);
 }
 
+template <bool PREV>
+static cudaError_t launch_merge_ring_t(const MergeRingParams& q, int grid, int smem, cudaStream_t stream) {
+  static SmemOptIn optin;  // the large shared-memory opt-in, per device and context
+  auto kern = agg_merge_ring_kernel<PREV>;
+  cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, q);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_merge(const MergeArgs& a) {
   if (a.T <= 0) return cudaSuccess;
   DeviceInfo di;
@@ -761,6 +965,44 @@ cudaError_t launch_merge(const MergeArgs& a) {
   if (e != cudaSuccess) return e;
   int nvec = 0, vpt = 0;
   if (!twophase_geometry(a.d, a.dtype, &nvec, &vpt)) return cudaErrorInvalidValue;
+  if (a.F && a.dtype == ATTNRES_BF16 && nvec == 2 * kRingConsumers) {
+    // a later layer of the block, bf16 rows of 2 x 448 vectors: the ring
+    MergeRingParams q{};
+    RingParams& rp = q.rp;
+    rp.w = a.w;
+    rp.T = a.T;
+    rp.d = a.d;
+    rp.nvec = nvec;
+    rp.row_bytes = nvec * 16;
+    rp.eps = a.eps;
+    rp.inv_d = 1.0f / (float)a.d;
+    rp.wait_ns = wait_limit_ns();
+    rp.withhold_row1 = debug_withhold_row1();
+    rp.dev_err = a.dev_err;
+    int nslots = (di.max_smem_optin - kRingHeaderBytes) / rp.row_bytes;
+    if (nslots > kRingMaxSlots) nslots = kRingMaxSlots;
+    if (nslots < 4) return cudaErrorInvalidValue;
+    rp.nslots = nslots;
+    MergeParams& mp = q.mp;
+    mp.prev = static_cast<const char*>(a.prev);
+    mp.F = static_cast<const char*>(a.F);
+    mp.dst = static_cast<char*>(a.dst);
+    mp.w = a.w;
+    mp.r_inter = a.r_inter;
+    mp.lse_inter = a.lse_inter;
+    mp.a_inter = a.a_inter;
+    mp.out_r = static_cast<char*>(a.out_r);
+    mp.out_a = a.out_a;
+    mp.T = a.T;
+    mp.d = a.d;
+    mp.n = a.n;
+    mp.nvec = nvec;
+    mp.eps = a.eps;
+    mp.inv_d = rp.inv_d;
+    const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
+    const int smem = kRingHeaderBytes + nslots * rp.row_bytes;
+    return a.prev ? launch_merge_ring_t<true>(q, grid, smem, a.stream) : launch_merge_ring_t<false>(q, grid, smem, a.stream);
+  }
   MergeParams mp{};
   mp.prev = static_cast<const char*>(a.prev);
   mp.F = static_cast<const char*>(a.F);

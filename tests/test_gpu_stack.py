@@ -300,6 +300,7 @@ def test_two_phase_stack_matches_the_oracle(A, L, B, T, d, dtype):
 
 @pytest.mark.parametrize("L,B,T,d,dtype,start", [
     (93, 12, 16, 3584, torch.float32, 5),   # K3 layout: blocks 1-4 single pass, 5-8 two-phase
+    (93, 12, 16, 7168, torch.bfloat16, 6),  # the default: blocks 6-8 two-phase (tensor-core logits, ring merge)
     (9, 2, 5, 7168, torch.bfloat16, 3),
     (7, 3, 6, 64, torch.float32, 9),        # start past the last block: all single pass
 ])

@@ -99,6 +99,33 @@ def test_fused_stack_times_out(A, TIMEOUT_BIT, withheld):
     assert int(err.item()) & TIMEOUT_BIT
 
 
+@pytest.mark.parametrize("schedule", ["two_phase", "hybrid"])
+def test_two_phase_stack_times_out_and_recovers(A, TIMEOUT_BIT, schedule):
+    # the two-phase schedule's ring kernels (the softmax / weighted-sum pass
+    # after the tensor-core logits, the ring merge) abandon the withheld
+    # token with the error bit set; run again normally, the same stack is
+    # correct (equal to the single-pass schedule's weights to fp32 rounding)
+    from depth_wise_attention_block_gb300.stack import StackForward
+    stk = W.stack(T=256, num_layers=30, block_size=12, seed=10, device="cuda")
+    err = _err()
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, 30, 12, dev_err=err, schedule=schedule, two_phase_from=2)
+    A.attnres_debug_wait_test(LIMIT_NS, 0)
+    try:
+        fwd.run()
+        torch.cuda.synchronize()
+    finally:
+        A.attnres_debug_wait_test(0, -1)
+    assert int(err.item()) & TIMEOUT_BIT
+    err.zero_()
+    fwd.run()
+    ref = StackForward(stk.h0, stk.W, stk.G, stk.Sc, 30, 12)
+    ref.run()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for a1, a2 in zip(fwd.weights, ref.weights):
+        assert (a1 - a2).abs().max().item() <= 2e-2   # bf16 storage: rounding flips compound (the free-running bar)
+
+
 def test_interblock_times_out_and_recovers(A, TIMEOUT_BIT):
     # the inter-block pass of the two-phase schedule keeps a token's rows in
     # the ring until the token is done: the withheld row's wait runs out,

@@ -383,7 +383,11 @@ int64_t attnres_interblock_workspace_size(int n, int64_t T, int d, int dtype, in
  *     (the cached sources' weights scaled into the merged softmax, then the
  *     partial sum's).
  * Needs folded == l-1 (i = 1) or l-2 (i >= 2); advances folded like
- * attnres_layer_step.  The final aggregation (L+1) uses attnres_layer_step. */
+ * attnres_layer_step.  The final aggregation (L+1) uses attnres_layer_step.
+ * Later layers with bf16 rows of d = 7168 stream their rows (previous
+ * partial, F_prev, r_inter) through the persistent TMA ring; its waits are
+ * bounded, and one that runs out sets ATTNRES_DEVERR_WAIT_TIMEOUT in
+ * dev_err and leaves NaN in that token's outputs. */
 int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* w_l,
                             int layer_idx, const float* r_inter, const float* lse_inter,
                             const float* a_inter, void* out_r, float* out_weights,

@@ -52,9 +52,10 @@ constexpr int kInterGC = 4;  // queries per phase-C group (the weighted sums)
 constexpr int kInterSumsq = kMaxQueries * kRingSmax;  // offset of the sums of squares in a warp's partials
 
 // Shared memory between the ring header and the ring slots.
+constexpr int kInterA2Row = kRingSmax + 1;  // 10 pairs: 80-byte rows, 16-byte aligned
 struct InterShared {
+  float2 a2[kMaxQueries][kInterA2Row];                     // softmax weights as (a, a) pairs
   float red[kRingConsumerWarps][kInterSumsq + kRingSmax];  // per-warp totals: logits [q * 9 + s], then sums of squares
-  float2 a2[kMaxQueries][kRingSmax];                       // softmax weights as (a, a) pairs
 };
 constexpr int kInterSharedBytes = (int)((sizeof(InterShared) + 127) / 128 * 128);
 
@@ -309,9 +310,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
 // sums of squares on the way, and loads its warp's partial dots (queries
 // warp, warp + 14) at the token's start, summed in split order.  One
 // barrier, the softmax of every query (one warp per query), one more
-// barrier, then the weighted sums from registers, kInterGCr queries at a
-// time.
-constexpr int kInterGCr = 2;
+// barrier, then the weighted sums from registers: quad by quad, the n rows'
+// 4 channels unpacked once, then every query's sum over them with its
+// weights read two sources per shared load.  NS > 0 fixes the source count
+// at compile time (no per-source branches in the inner loop).
 
 __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
   uint2 v;
@@ -319,7 +321,7 @@ __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
   return v;
 }
 
-template <int QPT, bool EXACT>
+template <int QPT, bool EXACT, int NS>
 __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(const __grid_constant__ InterParams ip) {
   const RingParams& p = ip.rp;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -341,7 +343,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
     return;
   }
 
-  const int S = p.S;
+  const int S = NS > 0 ? NS : p.S;
+  // sources whose quads stay in registers: the most that fit, with the n
+  // unpacked sources of one quad, under the 128-register cap without spills
+  // (5 up to n = 8, 4 at n = 9 or when n is known only at run time)
+  constexpr int KR = NS == 0 ? (QPT > 2 ? 4 : kRingSmax) : (NS <= 5 ? NS : (NS == 9 ? 4 : 5));
   const int Q = ip.Q;
   const long long T = p.T;
   const float nan = __int_as_float(0x7fc00000);
@@ -349,8 +355,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
   bool ok = true;
   int iter = 0;
   bool abort = false;
-  auto consume = [&](uint2* dst) {
+  // Takes this thread's quads of the next ring slot into dst.  With
+  // `release` the slot goes back to the producer at once; otherwise its
+  // index is returned and the caller releases it after its last read.
+  auto consume = [&](uint2* dst, bool release) -> uint32_t {
     if (ok && !mbar_wait_bounded(smem_addr(&sh.full[slot]), lap & 1u, p.wait_ns)) ok = false;
+    const uint32_t taken = slot;
     const uint32_t base = ring + slot * (uint32_t)p.row_bytes;
 #pragma unroll
     for (int m = 0; m < QPT; ++m) {
@@ -361,12 +371,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
     // then this phase completed and its copy landed.  After a wait ran out
     // the copy may still be in flight, and the slot must not be refilled
     // under it (the producer then runs out of slots, stops and drains).
-    __syncwarp();
-    if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
+    if (release) {
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[slot]));
+    }
     if (++slot == (uint32_t)nslots) {
       slot = 0;
       ++lap;
     }
+    return taken;
   };
   // the 4 channels of a quad as 2 packed fp32 pairs
   auto pairs = [](const uint2& v, uint64_t* h) {
@@ -393,19 +406,27 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
         pre_dot[u] = sum;
       }
     }
-    // the token's rows into registers, the sums of squares on the way
-    uint2 x[kRingSmax][QPT];
+    // the token's rows into registers (the first KR sources; the rest stay
+    // in their slots until the weighted sums are done), the sums of squares
+    // on the way
+    uint2 x[KR][QPT];
+    uint32_t held[kRingSmax];
     float part[kRingSmax];
 #pragma unroll
     for (int s = 0; s < kRingSmax; ++s) {
       part[s] = 0.f;
+      held[s] = 0;
       if (s < S) {
-        consume(x[s]);
+        uint2 xs_[QPT];
+        if (s < KR)
+          consume(x[s], true);
+        else
+          held[s] = consume(xs_, false);
         uint64_t ss2 = 0;
 #pragma unroll
         for (int m = 0; m < QPT; ++m) {
           uint64_t h[2];
-          pairs(x[s][m], h);
+          pairs(s < KR ? x[s][m] : xs_[m], h);
           ss2 = f2_fma(h[0], h[0], ss2);
           ss2 = f2_fma(h[1], h[1], ss2);
         }
@@ -468,52 +489,49 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
     }
     named_barrier_sync(kRingBarrierId, kRingConsumers);
 
-    // ---- the weighted sums from registers, kInterGCr queries at a time:
-    // per source, the group's weights are loaded once and update every quad
-    for (int q0 = 0; q0 < Q; q0 += kInterGCr) {
-      uint64_t acc[QPT][kInterGCr][2];
+    // ---- the weighted sums from registers, one quad at a time
+    const long long qstride = T * (long long)p.d * 4;  // bytes between queries' rows
 #pragma unroll
-      for (int m = 0; m < QPT; ++m)
+    for (int m = 0; m < QPT; ++m) {
+      const int qd = tid + m * kRingConsumers;
+      if (EXACT || qd < nquad) {
+        uint64_t h[kRingSmax][2];
 #pragma unroll
-        for (int g = 0; g < kInterGCr; ++g) acc[m][g][0] = acc[m][g][1] = 0;
-#pragma unroll
-      for (int s = 0; s < kRingSmax; ++s) {
-        if (s < S) {
-          uint64_t a2[kInterGCr];
-#pragma unroll
-          for (int g = 0; g < kInterGCr; ++g) {
-            const float2 ag = q0 + g < Q ? xs.a2[q0 + g][s] : make_float2(0.f, 0.f);
-            a2[g] = f2_pack(ag.x, ag.y);
-          }
-#pragma unroll
-          for (int m = 0; m < QPT; ++m) {
-            uint64_t h[2];
-            pairs(x[s][m], h);
-#pragma unroll
-            for (int g = 0; g < kInterGCr; ++g) {
-              acc[m][g][0] = f2_fma(a2[g], h[0], acc[m][g][0]);
-              acc[m][g][1] = f2_fma(a2[g], h[1], acc[m][g][1]);
-            }
-          }
+        for (int s = 0; s < kRingSmax; ++s) {
+          if (s < S && s < KR) pairs(x[s][m], h[s]);
+          if (s < S && s >= KR) pairs(ld_shared_v2(ring + held[s] * (uint32_t)p.row_bytes + (uint32_t)qd * 8u), h[s]);
         }
-      }
+        char* orow = reinterpret_cast<char*>(ip.out_r) + (t * (long long)p.d + (long long)qd * 4) * 4;
+#pragma unroll 4
+        for (int q = 0; q < Q; ++q) {
+          const float4* aq = reinterpret_cast<const float4*>(&xs.a2[q][0]);
+          uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-      for (int g = 0; g < kInterGCr; ++g) {
-        if (q0 + g < Q) {
-          char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)(q0 + g) * T + t) * (long long)p.d * 4;
-#pragma unroll
-          for (int m = 0; m < QPT; ++m) {
-            const int qd = tid + m * kRingConsumers;
-            if (EXACT || qd < nquad) {
-              float4 r;
-              f2_unpack(acc[m][g][0], r.x, r.y);
-              f2_unpack(acc[m][g][1], r.z, r.w);
-              *reinterpret_cast<float4*>(orow + (size_t)qd * 16) = r;
+          for (int s2 = 0; s2 < kInterA2Row / 2; ++s2) {
+            if (2 * s2 < S) {
+              const float4 w = aq[s2];  // (a_s, a_s, a_s+1, a_s+1)
+              const uint64_t wa = f2_pack(w.x, w.y);
+              acc0 = f2_fma(wa, h[2 * s2][0], acc0);
+              acc1 = f2_fma(wa, h[2 * s2][1], acc1);
+              if (2 * s2 + 1 < S) {
+                const uint64_t wb = f2_pack(w.z, w.w);
+                acc0 = f2_fma(wb, h[2 * s2 + 1][0], acc0);
+                acc1 = f2_fma(wb, h[2 * s2 + 1][1], acc1);
+              }
             }
           }
+          float4 r;
+          f2_unpack(acc0, r.x, r.y);
+          f2_unpack(acc1, r.z, r.w);
+          *reinterpret_cast<float4*>(orow + q * qstride) = r;
         }
       }
     }
+    // the held slots back to the producer (same rule as in consume)
+    __syncwarp();
+#pragma unroll
+    for (int s = KR; s < kRingSmax; ++s)
+      if (s < S && lane == 0 && ok) mbar_arrive(smem_addr(&sh.empty[held[s]]));
   }
 }
 
@@ -855,12 +873,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_merge_ring_kernel(const _
 
 // ---------------------------------------------------------------- launch --
 
-template <typename Tin, int VPT, bool EXACT, bool DOTS = false>
+template <typename Tin, int VPT, bool EXACT, bool DOTS = false, int NS = 0>
 static cudaError_t launch_inter_t(const InterParams& ip, int grid, int smem, cudaStream_t stream) {
   static SmemOptIn optin;  // the large shared-memory opt-in, per device and context
   auto kern = [] {
     if constexpr (DOTS)
-      return agg_interblock_dots_kernel<2 * VPT, EXACT>;  // bf16 rows: two quads per 16-byte vector
+      return agg_interblock_dots_kernel<2 * VPT, EXACT, NS>;  // bf16 rows: two quads per 16-byte vector
     else
       return agg_interblock_kernel<Tin, VPT, EXACT>;
   }();
@@ -935,8 +953,18 @@ cudaError_t launch_interblock(const InterArgs& a) {
     ip.dots = dots;
     ip.ksplit = ksplit;
     if (vpt == 1) return launch_inter_t<bf16_t, 1, false, true>(ip, grid, smem, a.stream);
-    return exact ? launch_inter_t<bf16_t, 2, true, true>(ip, grid, smem, a.stream)
-                 : launch_inter_t<bf16_t, 2, false, true>(ip, grid, smem, a.stream);
+    if (!exact) return launch_inter_t<bf16_t, 2, false, true>(ip, grid, smem, a.stream);
+    switch (a.n) {  // d = 7168: the source count fixed at compile time
+      case 1: return launch_inter_t<bf16_t, 2, true, true, 1>(ip, grid, smem, a.stream);
+      case 2: return launch_inter_t<bf16_t, 2, true, true, 2>(ip, grid, smem, a.stream);
+      case 3: return launch_inter_t<bf16_t, 2, true, true, 3>(ip, grid, smem, a.stream);
+      case 4: return launch_inter_t<bf16_t, 2, true, true, 4>(ip, grid, smem, a.stream);
+      case 5: return launch_inter_t<bf16_t, 2, true, true, 5>(ip, grid, smem, a.stream);
+      case 6: return launch_inter_t<bf16_t, 2, true, true, 6>(ip, grid, smem, a.stream);
+      case 7: return launch_inter_t<bf16_t, 2, true, true, 7>(ip, grid, smem, a.stream);
+      case 8: return launch_inter_t<bf16_t, 2, true, true, 8>(ip, grid, smem, a.stream);
+      default: return launch_inter_t<bf16_t, 2, true, true, 9>(ip, grid, smem, a.stream);
+    }
   }
   if (bf16) {
     if (vpt == 1) return launch_inter_t<bf16_t, 1, false>(ip, grid, smem, a.stream);

@@ -283,6 +283,13 @@ def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d, tensor_cores):
         assert (np.abs(to64(lse[q]) - l_ref) <= 1e-5 * (1 + np.abs(l_ref))).all()
 
 
+@pytest.mark.parametrize("n", [2, 4, 6, 7, 9])
+def test_interblock_every_source_count_at_k3_width(A, n):
+    """The tensor-core pass at d = 7168 fixes the source count at compile
+    time; the shapes above cover n = 1, 3, 5, 8, these the rest."""
+    test_interblock_pass_matches_the_oracle(A, n, 12 if n % 2 else 7, torch.bfloat16, 7168, True)
+
+
 @pytest.mark.parametrize("L,B,T,d,dtype", [
     (7, 3, 6, 64, torch.bfloat16),
     (9, 4, 7, 7168, torch.bfloat16),

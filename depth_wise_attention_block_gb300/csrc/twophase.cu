@@ -44,7 +44,66 @@ struct InterParams {
   float* out_a;    // [Q, T, n] or null
   const float* dots;  // DOTS kernels: partial dot products w_q . h_s, [ksplit][T][n][Q]
   int ksplit;
+  int tail_groups;  // DOTS kernels: query groups each of the last T mod grid tokens is split into
 };
+
+// The DOTS kernels' work units.  CTA b first takes whole tokens b, b + G,
+// ... (G = gridDim.x) while a full round of G tokens remains; the r < G
+// tokens left over are split into g = tail_groups query groups each, so
+// that r g <= G CTAs share the last round: CTA b < r g takes token
+// T_full + b / g, queries [(b mod g) Q / g, (b mod g + 1) Q / g).  Unit k of
+// this CTA: false once there is none.
+__device__ __forceinline__ bool inter_unit(const InterParams& ip, int k, long long* t, int* qlo, int* qhi) {
+  const long long G = gridDim.x, b = blockIdx.x;
+  const long long rounds = ip.rp.T / G;
+  if (k < rounds) {
+    *t = b + k * G;
+    *qlo = 0;
+    *qhi = ip.Q;
+    return true;
+  }
+  const long long r = ip.rp.T - rounds * G;
+  const int g = ip.tail_groups;
+  if (k > rounds || b >= r * g) return false;
+  const int grp = (int)(b % g);
+  *t = rounds * G + b / g;
+  *qlo = grp * ip.Q / g;
+  *qhi = (grp + 1) * ip.Q / g;
+  return true;
+}
+
+// The producer of the DOTS kernels: every source row of this CTA's units'
+// tokens, in unit order (otherwise as ring_produce).
+__device__ __forceinline__ void inter_produce(const InterParams& ip, RingShared& sh, uint32_t ring) {
+  const RingParams& p = ip.rp;
+  const int nslots = p.nslots;
+  uint32_t slot = 0, lap = 0;
+  long long issued = 0;
+  bool ok = true;
+  long long t;
+  int qlo, qhi;
+  for (int k = 0; ok && inter_unit(ip, k, &t, &qlo, &qhi); ++k) {
+    const long long off = t * (long long)p.row_bytes;
+    for (int j = 0; j < p.S; ++j) {
+      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = smem_addr(&sh.full[slot]);
+      mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
+      // the bounded-wait test arms one row of the first token without its copy
+      if (issued + 1 != p.withhold_row1)
+        bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, p.src[j] + off, (uint32_t)p.row_bytes, full);
+      ++issued;
+      if (++slot == (uint32_t)nslots) {
+        slot = 0;
+        ++lap;
+      }
+    }
+  }
+  if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+  ring_drain(sh.full, nslots, issued, p.withhold_row1);
+}
 
 constexpr int kInterGA = 2;  // queries per phase-A group (the logits)
 constexpr int kInterMaxSplit = 16;  // channel splits of the tensor-core logits, at most
@@ -54,8 +113,14 @@ constexpr int kInterSumsq = kMaxQueries * kRingSmax;  // offset of the sums of s
 // Shared memory between the ring header and the ring slots.
 constexpr int kInterA2Row = kRingSmax + 1;  // 10 pairs: 80-byte rows, 16-byte aligned
 struct InterShared {
-  float2 a2[kMaxQueries][kInterA2Row];                     // softmax weights as (a, a) pairs
-  float red[kRingConsumerWarps][kInterSumsq + kRingSmax];  // per-warp totals: logits [q * 9 + s], then sums of squares
+  float2 a2[kMaxQueries][kInterA2Row];  // softmax weights as (a, a) pairs
+  union {
+    float red[kRingConsumerWarps][kInterSumsq + kRingSmax];  // per-warp totals: logits [q * 9 + s], then sums of squares
+    // with precomputed dots: the token's partial dots [q][split][s], each
+    // element copied in (cp.async) and summed by the thread that needs it
+    float pd[kMaxQueries][kInterMaxSplit][kRingSmax];
+  };
+  float ss[kRingConsumerWarps][kRingSmax];  // per-warp sums of squares (precomputed-dots kernel)
 };
 constexpr int kInterSharedBytes = (int)((sizeof(InterShared) + 127) / 128 * 128);
 
@@ -305,10 +370,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
 // in ip.dots, [ksplit][T][n][Q]); bf16 sources.  A consumer thread owns
 // QPT quads of 4 channels (quad tid + m * 448), so that a warp's shared
 // loads read 256 contiguous bytes and its fp32 stores write 512 contiguous
-// bytes.  It takes its quads of the token's n rows into registers and
-// releases the slots at once (the producer keeps the ring full), forms the
-// sums of squares on the way, and loads its warp's partial dots (queries
-// warp, warp + 14) at the token's start, summed in split order.  One
+// bytes.  It takes its quads of the token's n rows into registers (the
+// first KR sources; the others stay in their slots until the weighted sums
+// are done) and releases the slots at once (the producer keeps the ring
+// full), forming the sums of squares on the way.  At the token's start its
+// warp's partial dots (queries warp, warp + 14) are copied into shared
+// memory asynchronously, to be summed in split order in the softmax.  One
 // barrier, the softmax of every query (one warp per query), one more
 // barrier, then the weighted sums from registers: quad by quad, the n rows'
 // 4 channels unpacked once, then every query's sum over them with its
@@ -339,7 +406,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
   pdl_wait();
 
   if (warp == kRingConsumerWarps) {
-    if (lane == 0) ring_produce(p, sh, ring);
+    if (lane == 0) inter_produce(ip, sh, ring);
     return;
   }
 
@@ -387,25 +454,23 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
     h[1] = f2_pack(bf16lo(v.y), bf16hi(v.y));
   };
 
-  for (long long t = blockIdx.x; t < T && !abort; t += gridDim.x, ++iter) {
+  long long t;
+  int qlo, qhi;  // this unit's queries
+  for (int unit = 0; !abort && inter_unit(ip, unit, &t, &qlo, &qhi); ++unit, ++iter) {
     const int buf = iter & 1;
     volatile int* abort_flag = &sh.abort_flag[buf];
-    // this warp's queries' partial dots, loads issued together
-    float pre_dot[2] = {0.f, 0.f};
+    // this warp's queries' partial dots (queries warp, warp + 14; lane =
+    // source), copied into shared memory without holding registers or
+    // stalling: summed in the softmax, by the same thread
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int q = warp + u * kRingConsumerWarps;
-      if (q < Q && lane < S) {
-        float part[kInterMaxSplit];
-#pragma unroll
-        for (int k = 0; k < kInterMaxSplit; ++k)
-          part[k] = k < ip.ksplit ? __ldg(ip.dots + (((long long)k * T + t) * S + lane) * Q + q) : 0.f;
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < kInterMaxSplit; ++k) sum += part[k];
-        pre_dot[u] = sum;
+      if (q >= qlo && q < qhi && lane < S) {
+        for (int k = 0; k < ip.ksplit; ++k)
+          cp_async_4(smem_addr(&xs.pd[q][k][lane]), ip.dots + (((long long)k * T + t) * S + lane) * Q + q);
       }
     }
+    cp_async_commit();
     // the token's rows into registers (the first KR sources; the rest stay
     // in their slots until the weighted sums are done), the sums of squares
     // on the way
@@ -436,7 +501,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
     reduce_scatter<kRingSmax>(part, lane);
     {
       const int idx = rs_lane_index<kRingSmax>(lane);
-      if (idx >= 0 && idx < S) xs.red[warp][kInterSumsq + idx] = part[0];
+      if (idx >= 0 && idx < S) xs.ss[warp][idx] = part[0];
     }
     const bool warp_failed = __any_sync(0xffffffffu, !ok);
     if (lane == 0 && warp_failed) *abort_flag = 1;
@@ -445,7 +510,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
     // the CTA-uniform exit test: every warp reads the flag after the barrier
     abort = *abort_flag != 0;
     if (abort) {
-      for (int q = 0; q < Q; ++q) {
+      for (int q = qlo; q < qhi; ++q) {
         char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)q * T + t) * (long long)p.d * 4;
 #pragma unroll
         for (int m = 0; m < QPT; ++m) {
@@ -454,28 +519,31 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
         }
       }
       if (warp == 0) {
-        for (int q = lane; q < Q; q += 32) ip.out_lse[(long long)q * T + t] = nan;
+        for (int q = qlo + lane; q < qhi; q += 32) ip.out_lse[(long long)q * T + t] = nan;
         if (ip.out_a)
-          for (int i = lane; i < Q * S; i += 32) ip.out_a[((long long)(i / S) * T + t) * S + i % S] = nan;
+          for (int i = qlo * S + lane; i < qhi * S; i += 32) ip.out_a[((long long)(i / S) * T + t) * S + i % S] = nan;
       }
       if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+      cp_async_wait_all();  // no copy outlives the CTA
       break;
     }
 
     // ---- softmax of each query over the n sources (one warp per query)
+    cp_async_wait_all();  // this thread's partial dots
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int q = warp + u * kRingConsumerWarps;
-      if (q < Q) {
+      if (q >= qlo && q < qhi) {
         const bool is_src = lane < S;
-        float ss = 0.f;
+        float ss = 0.f, dot = 0.f;
         if (is_src) {
 #pragma unroll
-          for (int w = 0; w < kRingConsumerWarps; ++w) ss += xs.red[w][kInterSumsq + lane];
+          for (int w = 0; w < kRingConsumerWarps; ++w) ss += xs.ss[w][lane];
+          for (int k = 0; k < ip.ksplit; ++k) dot += xs.pd[q][k][lane];  // split order
         }
         // fast reciprocal square root, exponential, logarithm and division:
         // a few fp32 ulps, far inside the parity tolerances
-        const float z = is_src ? pre_dot[u] * rsqrtf(fmaf(ss, p.inv_d, p.eps)) : -INFINITY;
+        const float z = is_src ? dot * rsqrtf(fmaf(ss, p.inv_d, p.eps)) : -INFINITY;
         const float m = warp_max(z);
         const float e = is_src ? __expf(z - m) : 0.f;
         const float esum = warp_sum(e);
@@ -503,7 +571,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
         }
         char* orow = reinterpret_cast<char*>(ip.out_r) + (t * (long long)p.d + (long long)qd * 4) * 4;
 #pragma unroll 4
-        for (int q = 0; q < Q; ++q) {
+        for (int q = qlo; q < qhi; ++q) {
           const float4* aq = reinterpret_cast<const float4*>(&xs.a2[q][0]);
           uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
@@ -523,7 +591,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
           float4 r;
           f2_unpack(acc0, r.x, r.y);
           f2_unpack(acc1, r.z, r.w);
-          *reinterpret_cast<float4*>(orow + q * qstride) = r;
+          __stcs(reinterpret_cast<float4*>(orow + q * qstride), r);  // streamed: evict first from L2
         }
       }
     }
@@ -941,7 +1009,7 @@ cudaError_t launch_interblock(const InterArgs& a) {
   ip.out_r = a.out_r;
   ip.out_lse = a.out_lse;
   ip.out_a = a.out_a;
-  const int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
+  int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
   const int smem = kRingHeaderBytes + kInterSharedBytes + nslots * row_bytes;
   const bool exact = nvec == vpt * kRingConsumers;
   if (a.workspace && interblock_tc_supported(a.n, a.d, a.dtype)) {
@@ -952,6 +1020,12 @@ cudaError_t launch_interblock(const InterArgs& a) {
     if (e != cudaSuccess) return e;
     ip.dots = dots;
     ip.ksplit = ksplit;
+    // one CTA per SM; the tokens of the last, partial round split by query
+    // groups over the idle CTAs (every token once when T is below the SMs)
+    const int G = di.sm_count;
+    const long long r = a.T % G;
+    ip.tail_groups = r == 0 ? 1 : (int)(G / r < a.Q ? G / r : a.Q);
+    grid = G;
     if (vpt == 1) return launch_inter_t<bf16_t, 1, false, true>(ip, grid, smem, a.stream);
     if (!exact) return launch_inter_t<bf16_t, 2, false, true>(ip, grid, smem, a.stream);
     switch (a.n) {  // d = 7168: the source count fixed at compile time

@@ -261,9 +261,8 @@ def test_bytes_model_counts_k3_sources(A):
     (9, 12, torch.float32, 3584),    # fp32 sources: CUDA cores either way
     (8, 9, torch.bfloat16, 7160),    # d not a multiple of 64: CUDA cores either way
 ])
-def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d, tensor_cores):
+def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d, tensor_cores, T=150):
     from tests.parity import oracle_aggregate
-    T = 150
     inp = W.block_bf16(T=T, d=d, seed=60 + n + Q, device="cuda", num_blocks=max(n - 2, 0), src_dtype=dtype)
     H = inp.H[:n].contiguous()
     g = torch.Generator(device="cuda").manual_seed(n)
@@ -288,6 +287,15 @@ def test_interblock_every_source_count_at_k3_width(A, n):
     """The tensor-core pass at d = 7168 fixes the source count at compile
     time; the shapes above cover n = 1, 3, 5, 8, these the rest."""
     test_interblock_pass_matches_the_oracle(A, n, 12 if n % 2 else 7, torch.bfloat16, 7168, True)
+
+
+@pytest.mark.parametrize("T,n,Q", [(16, 8, 12), (64, 6, 12), (160, 8, 12), (153, 3, 5), (310, 8, 16)])
+def test_interblock_tail_split_by_query_groups(A, T, n, Q):
+    """The tokens of the last, partial round of the persistent grid are
+    split by query groups over the idle CTAs: T = 16 (9 groups, 1-2 queries
+    each), 64 (2 groups), 160 (8 leftover tokens, one query per CTA), 153
+    (one leftover token, Q = 5 groups), 310 (6 leftover tokens, 16 groups)."""
+    test_interblock_pass_matches_the_oracle(A, n, Q, torch.bfloat16, 7168, True, T=T)
 
 
 @pytest.mark.parametrize("L,B,T,d,dtype", [

@@ -142,16 +142,6 @@ __device__ __forceinline__ bool mbar_wait_bounded_sh(uint32_t bar, uint32_t pari
   return mbar_wait_slow(bar, parity, *reinterpret_cast<const volatile uint64_t*>(limit_smem));
 }
 
-// ----------------------------------------------------- small async copies --
-
-// 4 bytes global -> shared without a register (cp.async, cached in L1);
-// complete after cp_async_commit and cp_async_wait_all in the same thread.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // --------------------------------------------------------- bulk copies ----
 
 // One TMA bulk copy global -> this CTA's shared memory, completing `bytes`

@@ -105,6 +105,14 @@ __device__ __forceinline__ void inter_produce(const InterParams& ip, RingShared&
   ring_drain(sh.full, nslots, issued, p.withhold_row1);
 }
 
+// 4 bytes global -> shared without a register (cp.async, cached in L1);
+// complete after cp_async_commit and cp_async_wait_all in the same thread.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 constexpr int kInterGA = 2;  // queries per phase-A group (the logits)
 constexpr int kInterMaxSplit = 16;  // channel splits of the tensor-core logits, at most
 constexpr int kInterGC = 4;  // queries per phase-C group (the weighted sums)

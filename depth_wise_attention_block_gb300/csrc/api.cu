@@ -524,8 +524,8 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
   }
   if (!twophase_pointers_ok(out_r)) return fail(ATTNRES_EINVAL, "out_r not 16-byte aligned");
   if (workspace) {
-    // the tensor-core logits: the workspace holds the split queries and the
-    // partial dot products; it may not share memory with an input or output
+    // the tensor-core logits: the workspace holds the partial dot products;
+    // it may not share memory with an input or output
     const int64_t need = interblock_tc_workspace_bytes(n, T, d, dtype, Q);
     if (need < 0) return fail(ATTNRES_ECUDA, "no CUDA device");
     if (need == 0) {

@@ -8,24 +8,22 @@
 // queries: on the CUDA cores each token would stream the queries again.
 // Here a tile of tt tokens x n sources (128 rows, each source's tt rows one
 // TMA tensor box) is multiplied on the tensor cores against the queries,
-// which are read once per tile:
+// which are read once per tile.
 //
-//   wsplit_kernel      w_q (fp32) = hi + mid + lo, three bf16 terms, so that
-//                      bf16 x bf16 products summed in fp32 keep the fp32
-//                      query's precision; rows [16 j + q] of a [48, d] bf16
-//                      matrix (term j, query q; rows q >= Q are zero).
-//   interblock_dots_kernel
-//                      tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in
-//                      TMEM), M = 128 rows, N = 48, K = 16 per instruction,
-//                      64 channels per pipeline stage.  Warp 0 issues the
-//                      TMA loads, warp 1 the MMAs, warps 2-5 read the
-//                      accumulator back (tcgen05.ld) and store
-//                      hi + mid + lo per query.  The channels are split
-//                      across CTAs (split-K) so that every SM has work;
-//                      each split writes its own partial dots.
+// interblock_dots_kernel: tcgen05.mma kind::f16 (bf16 in, fp32 accumulate
+// in TMEM), M = 128 rows, N = 48, K = 16 per instruction, 64 channels per
+// pipeline stage.  The queries enter as three bf16 terms, w_q (fp32) =
+// hi + mid + lo, so that bf16 x bf16 products summed in fp32 keep the fp32
+// query's precision: rows 16 j + q of the stage's B tile (term j, query q;
+// rows q >= Q zero).  Warp 0 issues the TMA loads of the source rows,
+// warp 1 the MMAs; warps 2-5 first write each stage's B tile (the query
+// split, from the fp32 queries, in the layout the TMA would give), then read
+// the accumulator back (tcgen05.ld) and store hi + mid + lo per query.  The
+// channels are split across CTAs (split-K) so that every SM has work; each
+// split writes its own partial dots.
 //
 // The softmax, the log-sum-exp and the weighted sums follow in
-// agg_interblock_kernel (twophase.cu), which sums the partial dots in a
+// agg_interblock_dots_kernel (twophase.cu), which sums the partial dots in a
 // fixed order.
 #include <cuda.h>
 
@@ -52,7 +50,7 @@ static_assert(kTcStageBytes % 1024 == 0, "stages must keep 1024-byte alignment (
 
 struct DotsParams {
   CUtensorMap src[kRingSmax];  // per cached source: [T, d] bf16, box {64 channels, tt tokens}, 128-byte swizzle
-  CUtensorMap wsplit;          // [48, d] bf16, box {64, 48}, 128-byte swizzle
+  InterQueries wq;             // the Q fp32 queries [d], 16-byte aligned
   float* dots;                 // [ksplit][T][n][Q] fp32 partial dot products
   long long T;
   int n, tt, Q;
@@ -145,31 +143,30 @@ constexpr uint32_t kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(k
 
 // ------------------------------------------------------------- kernels -----
 
-// w_q = hi + mid + lo (each bf16, rounded to nearest even); rows 16 j + q.
-__global__ void __launch_bounds__(256) wsplit_kernel(const InterQueries qs, int Q, int d, uint16_t* out) {
-  pdl_trigger();
-  pdl_wait();
-  const long long n = (long long)kTcN * d;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const int row = (int)(i / d), c = (int)(i % d);
-    const int term = row / 16, q = row % 16;
-    uint16_t bits = 0;
-    if (q < Q) {
-      const float w = qs.w[q][c];
-      const uint32_t hi = f32_to_bf16_bits(w);
-      const float r1 = w - bf16_bits_to_f32(hi);  // exact: w and hi share their leading bits
-      const uint32_t mid = f32_to_bf16_bits(r1);
-      const float r2 = r1 - bf16_bits_to_f32(mid);
-      const uint32_t lo = f32_to_bf16_bits(r2);
-      bits = (uint16_t)(term == 0 ? hi : term == 1 ? mid : lo);
-    }
-    out[i] = bits;
+// Three bf16 terms of 8 fp32 query values (channels 8 j .. 8 j + 7):
+// hi = round(w), mid = round(w - hi), lo = round(w - hi - mid), each
+// subtraction exact; as 16-byte rows of 8 bf16 each.
+__device__ __forceinline__ void split3(const float4& a, const float4& b, uint4* hi, uint4* mid, uint4* lo) {
+  const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t th[4], tm[4], tl[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t h = pack_bf16x2(w[2 * k], w[2 * k + 1]);
+    const float r0 = w[2 * k] - bf16lo(h), r1 = w[2 * k + 1] - bf16hi(h);
+    const uint32_t m = pack_bf16x2(r0, r1);
+    const float s0 = r0 - bf16lo(m), s1 = r1 - bf16hi(m);
+    th[k] = h;
+    tm[k] = m;
+    tl[k] = pack_bf16x2(s0, s1);
   }
+  *hi = make_uint4(th[0], th[1], th[2], th[3]);
+  *mid = make_uint4(tm[0], tm[1], tm[2], tm[3]);
+  *lo = make_uint4(tl[0], tl[1], tl[2], tl[3]);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __grid_constant__ DotsParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], acc_full;
+  __shared__ __align__(8) uint64_t full[kTcStages], bfull[kTcStages], empty[kTcStages], acc_full;
   __shared__ uint32_t tmem_base;
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -180,17 +177,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
   const int nloc = c1 - c0;  // >= 1 (the host sizes the splits so)
   pdl_trigger();
 
-  // rows n * tt .. 127 of every stage's A tile hold no source: zero, once
-  // (the TMA loads never touch them; the tensor cores read them as zeros)
+  // rows n * tt .. 127 of every stage's A tile hold no source, and the B
+  // tiles' rows of queries q >= Q none: zero, once (no later write touches
+  // them; the tensor cores read them as zeros)
   const int used = p.n * p.tt * 128;
-  for (int st = 0; st < kTcStages; ++st)
+  for (int st = 0; st < kTcStages; ++st) {
     for (int off = used + tid * 16; off < kTcABytes; off += kTcThreads * 16)
       asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + st * kTcStageBytes + off), "r"(0)
                    : "memory");
+    for (int off = tid * 16; off < kTcBBytes; off += kTcThreads * 16)
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + st * kTcStageBytes + kTcABytes + off),
+                   "r"(0)
+                   : "memory");
+  }
   fence_proxy_async_smem();  // those generic stores, before the tensor cores read the tiles
   if (tid == 0) {
     for (int st = 0; st < kTcStages; ++st) {
       mbar_init(smem_addr(&full[st]), 1);
+      mbar_init(smem_addr(&bfull[st]), kTcThreads / 32 - 2);  // one arrival per warp of warps 2-5
       mbar_init(smem_addr(&empty[st]), 1);
     }
     mbar_init(smem_addr(&acc_full), 1);
@@ -201,12 +205,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  pdl_wait();  // the sources and the split queries may come from the previous kernels
+  pdl_wait();  // the sources and the queries may come from the previous kernels
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer: the tile's n boxes of tt rows and the queries' box, per stage
-      const uint32_t tx = (uint32_t)(p.n * p.tt * 128 + kTcBBytes);
+      // producer: the tile's n boxes of tt rows, per stage
+      const uint32_t tx = (uint32_t)(p.n * p.tt * 128);
       // the softmax and weighted sums read these rows again next: keep them
       // in L2 ahead of other lines (what fits of them)
       const uint64_t keep = l2_policy_evict_last();
@@ -223,7 +227,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
         const int x = (c0 + i) * kTcChunk;
         const uint32_t a = base + st * kTcStageBytes;
         for (int s = 0; s < p.n; ++s) tma_load_2d_hint(a + s * p.tt * 128, &p.src[s], x, (int)t0, fb, keep);
-        tma_load_2d(a + kTcABytes, &p.wsplit, x, 0, fb);
         ++issued;
       }
       // the CTA never exits under a copy: wait for the latest phase of every
@@ -241,7 +244,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
       for (int i = 0; i < nloc; ++i) {
         const int st = i % kTcStages;
         const uint32_t lap = (uint32_t)(i / kTcStages);
-        if (!mbar_wait_bounded(smem_addr(&full[st]), lap & 1u, p.wait_ns)) {
+        if (!mbar_wait_bounded(smem_addr(&full[st]), lap & 1u, p.wait_ns) ||
+            !mbar_wait_bounded(smem_addr(&bfull[st]), lap & 1u, p.wait_ns)) {
           report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
           break;
         }
@@ -257,6 +261,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
     }
     __syncwarp();
   } else {
+    // the queries' B tiles: thread i writes 16 bytes (channels 8 bj .. + 7,
+    // bj = i mod 8) of query bq = i / 8 into rows bq, 16 + bq, 32 + bq, at
+    // the 128-byte swizzle's position of that chunk (bj ^ row mod 8).  Its
+    // loads run kTcStages chunks ahead (an L2 round trip is longer than a
+    // stage).
+    const int bi = tid - 64, bq = bi >> 3, bj = bi & 7;
+    const bool act = bq < p.Q;
+    const float4* wsrc = reinterpret_cast<const float4*>(act ? p.wq.w[bq] + c0 * kTcChunk + 8 * bj : nullptr);
+    constexpr int kPf = kTcStages;
+    float4 wa[kPf], wb[kPf];
+#pragma unroll
+    for (int u = 0; u < kPf; ++u) {
+      wa[u] = wb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (act && u < nloc) {
+        wa[u] = __ldg(wsrc + u * (kTcChunk / 4));
+        wb[u] = __ldg(wsrc + u * (kTcChunk / 4) + 1);
+      }
+    }
+    bool bok = true;
+    for (int i0 = 0; i0 < nloc && bok; i0 += kPf) {
+#pragma unroll
+      for (int u = 0; u < kPf; ++u) {
+        const int i = i0 + u;
+        if (i < nloc && bok) {
+          const int st = i % kTcStages;
+          const uint32_t lap = (uint32_t)(i / kTcStages);
+          // warp-uniform outcome: the warp arrives once, after all its lanes wrote
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&empty[st]), (lap & 1u) ^ 1u, p.wait_ns))) {
+            if (lane == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
+            bok = false;
+          } else {
+            if (act) {
+              uint4 th, tm, tl;
+              split3(wa[u], wb[u], &th, &tm, &tl);
+              const uint32_t bt = base + st * kTcStageBytes + kTcABytes;
+              const uint4* terms[3] = {&th, &tm, &tl};
+#pragma unroll
+              for (int term = 0; term < 3; ++term) {
+                const int row = 16 * term + bq;
+                const uint4 v = *terms[term];
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + row * 128 + ((bj ^ (row & 7)) << 4)),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+              }
+              if (i + kPf < nloc) {
+                wa[u] = __ldg(wsrc + (i + kPf) * (kTcChunk / 4));
+                wb[u] = __ldg(wsrc + (i + kPf) * (kTcChunk / 4) + 1);
+              }
+            }
+            fence_proxy_async_smem();  // visible to the tensor cores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bfull[st]));
+          }
+        }
+      }
+    }
+
     // epilogue: warp w reads TMEM lanes 32 (w mod 4) .. + 31, one row per thread
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&acc_full), 0u, p.wait_ns));
     if (!ok && lane == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
@@ -324,7 +385,7 @@ bool make_map(CUtensorMap* map, const void* ptr, long long rows, int d, int box_
 
 struct TcGeometry {
   int tt, ntiles, nchunks, chunks_per_split, ksplit;
-  long long wsplit_bytes, dots_bytes;
+  long long dots_bytes;
 };
 
 // tt tokens per tile (n sources each, n rounded up to a power of two so
@@ -346,7 +407,6 @@ TcGeometry tc_geometry(int n, long long T, int d, int Q, int sm_count) {
   if (ks > g.nchunks) ks = g.nchunks;
   g.chunks_per_split = (int)((g.nchunks + ks - 1) / ks);
   g.ksplit = (g.nchunks + g.chunks_per_split - 1) / g.chunks_per_split;  // every split has >= 1 chunk
-  g.wsplit_bytes = (long long)kTcN * d * 2;
   g.dots_bytes = (long long)g.ksplit * T * n * Q * 4;
   return g;
 }
@@ -364,7 +424,7 @@ int64_t interblock_tc_workspace_bytes(int n, long long T, int d, int dtype, int 
   DeviceInfo di;
   if (device_info(&di) != cudaSuccess) return -1;
   const TcGeometry g = tc_geometry(n, T, d, Q, di.sm_count);
-  return align256(g.wsplit_bytes) + align256(g.dots_bytes);
+  return align256(g.dots_bytes);
 }
 
 namespace {
@@ -386,20 +446,12 @@ cudaError_t launch_interblock_tc(const InterArgs& a, void* workspace, float** do
   cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return tc_fail(e, "device query");
   const TcGeometry g = tc_geometry(a.n, a.T, a.d, a.Q, di.sm_count);
-  uint16_t* wsplit = static_cast<uint16_t*>(workspace);
-  float* dots = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(g.wsplit_bytes));
-
-  InterQueries qs{};
-  for (int q = 0; q < a.Q; ++q) qs.w[q] = a.wq[q];
-  const int wgrid = (int)((kTcN * (long long)a.d + 255) / 256);
-  e = launch_kernel(wsplit_kernel, dim3(wgrid < 4 * di.sm_count ? wgrid : 4 * di.sm_count), dim3(256), 0, a.stream,
-                    qs, a.Q, a.d, wsplit);
-  if (e != cudaSuccess) return tc_fail(e, "query split launch");
+  float* dots = static_cast<float*>(workspace);
 
   DotsParams dp{};
   for (int s = 0; s < a.n; ++s)
     if (!make_map(&dp.src[s], a.src[s], a.T, a.d, g.tt)) return tc_fail(cudaErrorInvalidValue, "source tensor map");
-  if (!make_map(&dp.wsplit, wsplit, kTcN, a.d, kTcN)) return tc_fail(cudaErrorInvalidValue, "query tensor map");
+  for (int q = 0; q < a.Q; ++q) dp.wq.w[q] = a.wq[q];
   dp.dots = dots;
   dp.T = a.T;
   dp.n = a.n;

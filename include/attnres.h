@@ -365,9 +365,9 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
 
 /* Bytes of workspace attnres_interblock's tensor-core logits need for n
  * sources of T tokens and d channels and Q queries on the current device
- * (the split queries, 48 x d bf16, and the partial dot products of every
- * channel split); 0 when that path does not apply (fp32 sources, d not a
- * multiple of 64).  Negative attnres_status on bad arguments. */
+ * (the partial dot products of every channel split); 0 when that path does
+ * not apply (fp32 sources, d not a multiple of 64).  Negative
+ * attnres_status on bad arguments. */
 int64_t attnres_interblock_workspace_size(int n, int64_t T, int d, int dtype, int Q);
 
 /* attnres_intrablock_step -- phase 2 for layer l (1..L) of block n:

@@ -26,6 +26,7 @@ from ._native import (  # noqa: F401
     ATTNRES_F32,
     ATTNRES_MAX_BLOCKS,
     ATTNRES_MAX_SOURCES,
+    ATTNRES_STATE_EARLY_LOADS,
     AttnresError,
     LIB_PATH,
 )
@@ -230,7 +231,7 @@ class AttnResState:
     """
 
     def __init__(self, h0: torch.Tensor, block_reps: Sequence[torch.Tensor], partial: torch.Tensor,
-                 num_layers: int, block_size: int, eps: float = ATTNRES_DEFAULT_EPS):
+                 num_layers: int, block_size: int, eps: float = ATTNRES_DEFAULT_EPS, early_loads: bool = False):
         T, d = h0.shape
         for i, b in enumerate(list(block_reps) + [partial]):
             if b.shape != (T, d) or b.dtype != h0.dtype:
@@ -244,12 +245,15 @@ class AttnResState:
                                        _dev_ptr(partial, "partial"), T, d, dtype_code(h0.dtype), num_layers,
                                        block_size, float(eps))
         _N.check(rc, "attnres_state_init")
+        # ATTNRES_STATE_EARLY_LOADS: see include/attnres.h for when it is safe
+        self.struct.flags = ATTNRES_STATE_EARLY_LOADS if early_loads else 0
 
     @classmethod
-    def allocate(cls, h0: torch.Tensor, num_layers: int, block_size: int, eps: float = ATTNRES_DEFAULT_EPS):
+    def allocate(cls, h0: torch.Tensor, num_layers: int, block_size: int, eps: float = ATTNRES_DEFAULT_EPS,
+                 early_loads: bool = False):
         n_blocks = -(-num_layers // block_size)
         reps = [torch.empty_like(h0) for _ in range(n_blocks)]
-        return cls(h0, reps, torch.empty_like(h0), num_layers, block_size, eps)
+        return cls(h0, reps, torch.empty_like(h0), num_layers, block_size, eps, early_loads)
 
     @property
     def folded(self) -> int:

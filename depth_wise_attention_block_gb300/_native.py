@@ -26,6 +26,7 @@ ATTNRES_DEVERR_WAIT_TIMEOUT = 0x1
 ATTNRES_MAX_SOURCES = 128
 ATTNRES_MAX_BLOCKS = ATTNRES_MAX_SOURCES - 1
 ATTNRES_DEFAULT_EPS = 1e-5
+ATTNRES_STATE_EARLY_LOADS = 0x1
 
 # every function declared in include/attnres.h
 EXPORTED = (
@@ -68,6 +69,7 @@ class AttnresState(ctypes.Structure):
         ("block_size", ctypes.c_int),
         ("eps", ctypes.c_float),
         ("folded", ctypes.c_int),
+        ("flags", ctypes.c_int),
     ]
 
 

@@ -80,8 +80,8 @@ __global__ void __launch_bounds__(kGenThreads) agg_generic_kernel(const __grid_c
   __shared__ float s_za[kMaxSources];  // logits, then weights
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d = p.d, S = p.S;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   for (long long t = blockIdx.x; t < p.T; t += gridDim.x) {
     const long long row = t * (long long)d;
     // pass 1: logit of every source (forming the fused source on the way)
@@ -337,6 +337,7 @@ cudaError_t launch_aggregate(const AggArgs& a, AggPath* path) {
     // while all of its rows fit in half of L2; beyond that the marked lines
     // would crowd out the rest, and every row takes the default policy
     rp.keep_src0 = fused && a.T * (long long)row_bytes <= (long long)di.l2_bytes / 2;
+    rp.early_loads = fused && a.early_loads ? 1 : 0;
     if (split_c > 0) {
       *path = kPathRingSplit;
       return launch_ring_split(rp, split_c, fused, in_bf16, out_bf16, di.sm_count, di.max_smem_optin, a.stream);

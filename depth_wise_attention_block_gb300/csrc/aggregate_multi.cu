@@ -46,10 +46,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
   const int lane = tid & 31;
   const int nslots = p.nslots;
   const long long T = p.T;
-  pdl_trigger();
   ring_init(p, sh);
   __syncthreads();
   pdl_wait();  // everything below may read what the previous kernel wrote
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   if (warp == kRingConsumerWarps) {
     if (lane == 0) ring_produce(p, sh, ring);

@@ -94,7 +94,6 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_split_kernel(const __grid
   const uint32_t rank = cluster_ctarank();
   const long long cluster = blockIdx.x / C;
   const long long nclusters = gridDim.x / C;
-  pdl_trigger();
   ring_init(p, sh);
   if (tid == 0) {
     mbar_init(smem_addr(&xs.xbar[0]), C);
@@ -107,6 +106,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_split_kernel(const __grid
   // copies are issued
   cluster_arrive();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   if (warp == kRingConsumerWarps) {
     if (lane == 0) split_produce(sp, sh, ring, rank, cluster, nclusters);

@@ -185,7 +185,7 @@ struct HostPipe {
 
 extern "C" {
 
-int attnres_version(void) { return (1 << 16) | 1; }
+int attnres_version(void) { return (2 << 16) | 0; }
 
 const char* attnres_status_string(int status) {
   switch (status) {
@@ -669,6 +669,7 @@ int attnres_state_init(attnres_state* st, const void* h0, void* const* block_rep
   st->block_size = block_size;
   st->eps = eps;
   st->folded = 0;
+  st->flags = 0;
   return ok();
 }
 
@@ -789,6 +790,7 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
     a.fuse_prev = fp.has_prev ? st->partial : nullptr;
     a.fuse_F = F_prev;
     a.fuse_dst = fp.ends_block ? st->block_reps[fp.block - 1] : st->partial;
+    a.early_loads = (st->flags & ATTNRES_STATE_EARLY_LOADS) != 0;
   }
   if (a.S() != attnres_num_sources(layer_idx, B, L))
     return fail(ATTNRES_ESTATE, "internal: source count mismatch at layer %d", layer_idx);

@@ -111,7 +111,6 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_bwd_ring_kernel(const __g
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int nslots = p.nslots;
-  pdl_trigger();
   if (tid == 0) {
     for (int k = 0; k < nslots; ++k) {
       mbar_init(smem_addr(&sh.full[k]), 1);
@@ -123,6 +122,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_bwd_ring_kernel(const __g
   }
   __syncthreads();
   pdl_wait();  // everything below may read what the previous kernel wrote
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   if (warp == kRingConsumerWarps) {
     if (lane == 0) bwd_produce<ACC>(p, sh, ring);
@@ -323,8 +323,8 @@ __global__ void __launch_bounds__(kBwdGenThreads) agg_bwd_generic_kernel(const _
   __shared__ float s_a[kMaxSources], s_al[kMaxSources], s_be[kMaxSources];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d = p.d, S = p.S;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   float* wrow = p.ws + (size_t)blockIdx.x * d;
   for (int c = tid; c < d; c += kBwdGenThreads) wrow[c] = 0.f;
   for (long long t = blockIdx.x; t < p.T; t += gridDim.x) {
@@ -414,8 +414,8 @@ constexpr int kDwThreads = 32 * kDwSplit;
 
 __global__ void __launch_bounds__(kDwThreads) dw_reduce_kernel(const float* ws, int nb, int d, float* dw) {
   __shared__ float part_sum[kDwSplit][32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   const int cl = threadIdx.x & 31;
   const int part = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + cl;

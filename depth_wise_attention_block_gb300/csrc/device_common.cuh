@@ -291,10 +291,13 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // ------------------------------------------- programmatic dependent launch --
-// Every kernel here lets the next kernel on its stream be launched early
-// (pdl_trigger, first thing) and waits for the previous grid to complete and
-// its memory to be visible (pdl_wait) before its first global-memory access.
-// Both are no-ops when the launch did not opt in.
+// Every kernel here waits for the previous grid to complete and its memory
+// to be visible (pdl_wait) before it touches what that grid may have
+// written, and only then lets the next kernel on its stream be launched
+// (pdl_trigger).  So when a kernel starts, the kernel two launches before it
+// has completed: rows that only such earlier kernels wrote may be read
+// before the wait (the fused stack step's early loads).  Both are no-ops
+// when the launch did not opt in.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -60,8 +60,8 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kEwThreads) fold_kernel(const T* prev, const T* F, T* dst,
                                                           long long n) {
   // dst may alias prev (the partial sum is updated in place)
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
     constexpr int E = Vec16<T>::kElems;
@@ -126,8 +126,8 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kEwThreads) synth_layer_kernel(const T* x, const float* __restrict__ g,
                                                                  const float* __restrict__ s, T* out,
                                                                  long long T_, int d) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   const long long n = T_ * (long long)d;
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {
@@ -182,8 +182,8 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kEwThreads) synth_layer_backward_kernel(const T* x, const float* __restrict__ g,
                                                                           const float* __restrict__ s, const T* dva,
                                                                           const T* dvb, T* dx, long long T_, int d) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   const long long n = T_ * (long long)d;
   const long long stride = (long long)gridDim.x * blockDim.x;
   if constexpr (VEC) {

@@ -32,6 +32,7 @@ struct AggArgs {
   float* out_a;   // [T, S] or null
   int* dev_err;
   cudaStream_t stream;
+  bool early_loads;  // fused: stored rows of the first token loaded before the previous kernel ends
 
   int S() const { return n_stored + (fuse_F ? 1 : 0); }
 };

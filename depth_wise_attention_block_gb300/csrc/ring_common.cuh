@@ -43,6 +43,8 @@ struct RingParams {
   int withhold_row1;           // bounded-wait test: 1 + the row of each CTA's first token armed
                                // without a copy (its waits must run out); 0 = none
   int keep_src0;               // fused step whose source 0 fits in L2: keep it there, stream the rest
+  int early_loads;             // fused step: the first token's stored rows are loaded before the wait
+                               // for the previous kernel (only F needs that kernel)
   const char* src[kMaxSources];
   const char* fuse_prev;
   const char* fuse_F;
@@ -248,6 +250,10 @@ __device__ __forceinline__ void ring_drain(uint64_t* full, int nslots, long long
 // the slot's previous row was released by all consumer warps.  On a wait
 // that runs out it stops issuing; in every case it waits (bounded) for its
 // copies in flight before returning, so the CTA never exits under a copy.
+// It waits for the previous kernel (pdl_wait) before its first row, or,
+// with early_loads, only before the first token's F row: the stored rows
+// (h_0, the block sums, the previous partial sum) were written two or more
+// launches back, which have completed when this kernel starts.
 __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh, uint32_t ring) {
   const int nslots = p.nslots;
   const long long T = p.T;
@@ -264,9 +270,15 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
   // kernels just wrote.  A single aggregation, or a fused step over more
   // tokens, streams everything with the default policy.
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+  bool waited = false;
   for (long long t = blockIdx.x; t < T && ok; t += gridDim.x) {
     const long long off = t * (long long)p.row_bytes;
     for (int j = 0; j < rows; ++j) {
+      if (!waited && !(p.early_loads && t == blockIdx.x && j != real_rows - 1)) {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+      }
       const char* g;
       if (j < p.n_stored) g = p.src[j] + off;
       else if (j >= real_rows) g = p.src[0] + off;  // padding: source 0's row again
@@ -293,6 +305,10 @@ __device__ __forceinline__ void ring_produce(const RingParams& p, RingShared& sh
         ++lap;
       }
     }
+  }
+  if (!waited) {
+    pdl_wait();
+    pdl_trigger();
   }
   if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
   ring_drain(sh.full, nslots, issued, p.withhold_row1);

@@ -40,16 +40,18 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_kernel(const __grid_
   const int lane = tid & 31;
   const int nslots = p.nslots;
   const long long T = p.T;
-  pdl_trigger();
-
   ring_init(p, sh);
   __syncthreads();
-  pdl_wait();  // everything below may read what the previous kernel wrote
 
   if (warp == kRingConsumerWarps) {
+    // the producer waits for the previous kernel itself (early loads)
     if (lane == 0) ring_produce(p, sh, ring);
+    pdl_wait();
+    pdl_trigger();
     return;
   }
+  pdl_wait();  // everything below may read or overwrite what the previous kernel used
+  pdl_trigger();
 
   // ------------------------------------------------------------ consumers --
   constexpr int NP = EPV / 2;  // packed fp32 pairs per 16-byte vector

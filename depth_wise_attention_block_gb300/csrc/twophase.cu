@@ -145,10 +145,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int nslots = p.nslots;
-  pdl_trigger();
   ring_init(p, sh);
   __syncthreads();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   if (warp == kRingConsumerWarps) {
     if (lane == 0) ring_produce(p, sh, ring);
@@ -408,10 +408,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
   const int lane = tid & 31;
   const int nslots = p.nslots;
   const int nquad = 2 * p.nvec;  // 8-byte quads (4 bf16) per row
-  pdl_trigger();
   ring_init(p, sh);
   __syncthreads();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   if (warp == kRingConsumerWarps) {
     if (lane == 0) inter_produce(ip, sh, ring);
@@ -640,8 +640,8 @@ __global__ void __launch_bounds__(kMergeThreads) agg_merge_kernel(const __grid_c
   __shared__ float s_red[kMergeThreads / 32][2];
   __shared__ float s_c[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   const bool has_p = p.F != nullptr;
   uint64_t wp[VPT][NP];
 #pragma unroll
@@ -808,10 +808,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_merge_ring_kernel(const _
   const uint32_t ring = smem_addr(smem) + kRingHeaderBytes;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nslots = p.nslots;
-  pdl_trigger();
   ring_init(p, sh);
   __syncthreads();
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   if (warp == kRingConsumerWarps) {
     if (lane == 0) merge_produce<PREV>(q, sh, ring);
     return;

@@ -175,7 +175,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
   const int c0 = ks * p.chunks_per_split;
   const int c1 = c0 + p.chunks_per_split < p.nchunks ? c0 + p.chunks_per_split : p.nchunks;
   const int nloc = c1 - c0;  // >= 1 (the host sizes the splits so)
-  pdl_trigger();
 
   // rows n * tt .. 127 of every stage's A tile hold no source, and the B
   // tiles' rows of queries q >= Q none: zero, once (no later write touches
@@ -206,6 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   pdl_wait();  // the sources and the queries may come from the previous kernels
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   if (warp == 0) {
     if (lane == 0) {

@@ -49,16 +49,22 @@ class StackForward:
     (row L is the final aggregation's); G, Sc: [L, d] fp32 gains and scales
     of the synthetic layer body.  Outputs: `r` ([T, d], the final residual
     stream after `run()`), `weights[l-1]` ([T, S_l] fp32, l = 1..L+1).
+    With `early_loads` the fused steps load their stored rows before the
+    body before them has finished (ATTNRES_STATE_EARLY_LOADS); the results
+    are the same bits.
     """
 
     def __init__(self, h0, W, G, Sc, num_layers: int, block_size: int, eps: float = 1e-5,
                  keep_weights: bool = True, dev_err: torch.Tensor | None = None, schedule: str = "single",
-                 two_phase_from: int = 6):
+                 two_phase_from: int = 6, early_loads: bool = True):
         self.L, self.B, self.eps = num_layers, block_size, eps
         T, d = h0.shape
         self.T, self.d = T, d
         self.W, self.G, self.Sc = W, G, Sc
-        self.state = AttnResState.allocate(h0, num_layers, block_size, eps)
+        # every kernel between two steps is this library's (or launched by
+        # an on_layer hook without programmatic dependent launch): the fused
+        # steps may load their stored rows early (ATTNRES_STATE_EARLY_LOADS)
+        self.state = AttnResState.allocate(h0, num_layers, block_size, eps, early_loads=early_loads)
         self.r = torch.empty_like(h0)
         self.F = torch.empty_like(h0)
         self.S = [attnres_num_sources(l, block_size, num_layers) for l in range(1, num_layers + 2)]

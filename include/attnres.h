@@ -246,12 +246,25 @@ typedef struct attnres_state {
   int block_size;                          /* B */
   float eps;
   int folded;                              /* progress, maintained by the library */
+  int flags;                               /* ATTNRES_STATE_*, set by the caller after init */
 } attnres_state;
+
+/* attnres_state.flags bit: a layer step that folds F_prev (the fused step)
+ * may load the first token's stored rows -- h0, the block sums, the
+ * partial sum -- before the kernel launched just before it on the stream
+ * has finished (programmatic dependent launch), so that their DRAM latency
+ * overlaps that kernel; only F_prev waits for it.  Set it only when no
+ * kernel issued between two steps writes the state's rows, and each kernel
+ * issued before a step either is launched without programmatic dependent
+ * launch or signals its dependents only after it has waited for its own
+ * prerequisites, as every kernel of this library does.  The stack drivers
+ * of the Python package set it; results are the same bits either way. */
+#define ATTNRES_STATE_EARLY_LOADS 0x1
 
 /* Fill *st.  n_block_reps must be >= ceil(L/B) (ATTNRES_ERANGE if
  * ceil(L/B) > ATTNRES_MAX_BLOCKS).  The buffers may not share memory with
  * each other (ATTNRES_EINVAL; *st is not written then).
- * Host only; sets folded = 0. */
+ * Host only; sets folded = 0 and flags = 0. */
 int attnres_state_init(attnres_state* st, const void* h0, void* const* block_reps,
                        int n_block_reps, void* partial, int64_t T, int d, int dtype,
                        int num_layers, int block_size, float eps);

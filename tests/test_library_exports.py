@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(native):
 
 def test_abi_version_and_status_strings(native):
     v = native.lib.attnres_version()
-    assert v >> 16 == 1
+    assert v >> 16 == 2
     for code in [0, -1, -2, -4, -5, -6]:
         assert native.lib.attnres_status_string(code).startswith(b"ATTNRES_")
     assert b"unknown" in native.lib.attnres_status_string(12345)
@@ -58,10 +58,12 @@ def _fake_state(native, L, B, T=4, d=8, dtype=1):
     """State over fake (never dereferenced) device pointers."""
     N = -(-L // B)
     st = native.AttnresState()
+    st.flags = 0x7F   # init clears the flags
     h0, partial = 0x10000, 0x20000
     reps = (ctypes.c_void_p * N)(*[0x100000 * (k + 1) for k in range(N)])
     rc = native.lib.attnres_state_init(ctypes.byref(st), h0, reps, N, partial, T, d, dtype, L, B, 1e-5)
     assert rc == 0, native.lib.attnres_last_error()
+    assert st.flags == 0
     return st, h0, partial, list(reps)
 
 

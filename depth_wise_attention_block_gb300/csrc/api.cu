@@ -628,6 +628,7 @@ int attnres_intrablock_step(attnres_state* st, const void* F_prev, const float* 
   a.eps = st->eps;
   a.dev_err = dev_err;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.early_loads = F_prev && (st->flags & ATTNRES_STATE_EARLY_LOADS) != 0;
   if (st->T > 0) {
     cudaError_t e = launch_merge(a);
     if (e != cudaSuccess) return cuda_fail(e, "attnres_intrablock_step launch");

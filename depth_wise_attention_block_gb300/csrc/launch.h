@@ -83,6 +83,7 @@ struct MergeArgs {
   float eps;
   int* dev_err;  // the ring merge's bounded waits (bf16 rows of 2 x 448 vectors)
   cudaStream_t stream;
+  bool early_loads;  // the ring merge: prev and r_inter of the first token loaded before the previous kernel ends
 };
 bool twophase_supported(int d, int dtype);
 bool twophase_pointers_ok(const void* p);

@@ -765,35 +765,65 @@ struct MergeRingParams {
   MergeParams mp;        // the merge's rows and outputs
 };
 
+// The merge's producer: per token the rows [prev,] F, r_inter's two halves
+// into consecutive slots.  It waits for the previous kernel (pdl_wait)
+// before its first row, or, with early_loads, before the first token's F
+// only: prev and r_inter were written two or more launches back (see
+// ring_produce), so their copies for the first token go out before the
+// wait, into their own slots.
+// The merge's producer: per token the rows [prev,] F, r_inter's two halves
+// into consecutive slots.  It waits for the previous kernel (pdl_wait)
+// before its first row, or, with early_loads, before the first token's F
+// only: prev and r_inter were written two or more launches back (see
+// ring_produce), so their copies for the first token go out before the
+// wait, into their own slots (all on the ring's first lap, whose empty
+// barriers never hold a wait).
 template <bool PREV>
 __device__ __forceinline__ void merge_produce(const MergeRingParams& q, RingShared& sh, uint32_t ring) {
   const RingParams& p = q.rp;
   const int nslots = p.nslots;
   const int rows = (PREV ? 1 : 0) + 1 + 2;
-  uint32_t slot = 0, lap = 0;
-  long long issued = 0;
-  bool ok = true;
+  const int f_row = rows - 3;
+  long long issued = 0;  // rows armed, in ring order
+  bool ok = true, waited = false;
   for (long long t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
     const long long off = t * (long long)p.row_bytes;
-    for (int j = 0; j < rows; ++j) {
-      const char* g;
-      if (PREV && j == 0) g = q.mp.prev + off;
-      else if (j == rows - 3) g = q.mp.F + off;
-      else g = reinterpret_cast<const char*>(q.mp.r_inter) + 2 * off + (j - (rows - 2)) * (long long)p.row_bytes;
-      if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u, p.wait_ns)) {
-        ok = false;
-        break;
+    const bool early = p.early_loads && !waited;
+    // pass 0 (early only): the rows not from the previous kernel; pass 1: the rest
+    int armed = 0;
+    for (int pass = early ? 0 : 1; pass < 2 && ok; ++pass) {
+      if (pass == 1 && !waited) {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
       }
-      const uint32_t full = smem_addr(&sh.full[slot]);
-      mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
-      // the bounded-wait test arms one row of the first token without its copy
-      if (issued + 1 != p.withhold_row1) bulk_copy_g2s(ring + slot * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
-      ++issued;
-      if (++slot == (uint32_t)nslots) {
-        slot = 0;
-        ++lap;
+      for (int j = 0; j < rows; ++j) {
+        if (pass == 0 ? j == f_row : (early && j != f_row)) continue;
+        const long long pos = issued + j;  // the row's place in ring order
+        const uint32_t s = (uint32_t)(pos % nslots), l = (uint32_t)(pos / nslots);
+        const char* g;
+        if (PREV && j == 0) g = q.mp.prev + off;
+        else if (j == f_row) g = q.mp.F + off;
+        else g = reinterpret_cast<const char*>(q.mp.r_inter) + 2 * off + (j - (rows - 2)) * (long long)p.row_bytes;
+        if (!mbar_wait_bounded(smem_addr(&sh.empty[s]), (l & 1u) ^ 1u, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_addr(&sh.full[s]);
+        mbar_arrive_expect_tx(full, (uint32_t)p.row_bytes);
+        // the bounded-wait test arms one row of the first token without its copy
+        if (pos + 1 != p.withhold_row1) bulk_copy_g2s(ring + s * (uint32_t)p.row_bytes, g, (uint32_t)p.row_bytes, full);
+        ++armed;
       }
     }
+    // rows are armed in ring order except for the early token, where all
+    // of them are (its waits cannot run out): either way the first `armed`
+    // positions of this token hold every copy issued
+    issued += armed;
+  }
+  if (!waited) {
+    pdl_wait();
+    pdl_trigger();
   }
   if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
   ring_drain(sh.full, nslots, issued, p.withhold_row1);
@@ -810,12 +840,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_merge_ring_kernel(const _
   const int nslots = p.nslots;
   ring_init(p, sh);
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
   if (warp == kRingConsumerWarps) {
+    // the producer waits for the previous kernel itself (early loads)
     if (lane == 0) merge_produce<PREV>(q, sh, ring);
+    pdl_wait();
+    pdl_trigger();
     return;
   }
+  pdl_wait();
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   uint64_t wp[2][4];  // this thread's channels of w (vectors tid, tid + 448), as pairs
 #pragma unroll
@@ -1088,6 +1121,7 @@ cudaError_t launch_merge(const MergeArgs& a) {
     rp.inv_d = 1.0f / (float)a.d;
     rp.wait_ns = wait_limit_ns();
     rp.withhold_row1 = debug_withhold_row1();
+    rp.early_loads = a.early_loads ? 1 : 0;
     rp.dev_err = a.dev_err;
     int nslots = (di.max_smem_optin - kRingHeaderBytes) / rp.row_bytes;
     if (nslots > kRingMaxSlots) nslots = kRingMaxSlots;

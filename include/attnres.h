@@ -253,7 +253,8 @@ typedef struct attnres_state {
  * may load the first token's stored rows -- h0, the block sums, the
  * partial sum -- before the kernel launched just before it on the stream
  * has finished (programmatic dependent launch), so that their DRAM latency
- * overlaps that kernel; only F_prev waits for it.  Set it only when no
+ * overlaps that kernel; only F_prev waits for it.  attnres_intrablock_step
+ * with F_prev does the same with the partial sum and r_inter.  Set it only when no
  * kernel issued between two steps writes the state's rows, and each kernel
  * issued before a step either is launched without programmatic dependent
  * launch or signals its dependents only after it has waited for its own

@@ -131,22 +131,25 @@ def test_full_attnres_bf16_93_layers(A):
     print(f"Full AttnRes bf16 93 layers: worst weight error {wa:.3g}, worst output error {wr:.3g} x bound")
 
 
-@pytest.mark.parametrize("T,L,B,dtype,graph", [
-    (64, 93, 12, torch.bfloat16, True),     # the decode stack, replayed from a CUDA graph
-    (64, 93, 12, torch.bfloat16, False),
-    (300, 20, 4, torch.float32, True),      # two tokens per CTA on some SMs
-    (5, 14, 1, torch.bfloat16, False),      # Full AttnRes layout: every step closes a block
+@pytest.mark.parametrize("T,L,B,dtype,graph,schedule", [
+    (64, 93, 12, torch.bfloat16, True, "single"),     # the decode stack, replayed from a CUDA graph
+    (64, 93, 12, torch.bfloat16, False, "single"),
+    (300, 20, 4, torch.float32, True, "single"),      # two tokens per CTA on some SMs
+    (5, 14, 1, torch.bfloat16, False, "single"),      # Full AttnRes layout: every step closes a block
+    (64, 93, 12, torch.bfloat16, True, "hybrid"),     # the ring merges of blocks 6-8
+    (300, 30, 12, torch.bfloat16, False, "two_phase"),
 ])
-def test_early_loads_change_no_bit(A, T, L, B, dtype, graph):
-    """The fused steps' stored rows loaded before the previous kernel ends
-    (the stack drivers' default) give the same bits as loads after it."""
+def test_early_loads_change_no_bit(A, T, L, B, dtype, graph, schedule):
+    """The fused steps' and ring merges' rows that earlier kernels wrote,
+    loaded before the previous kernel ends (the stack drivers' default),
+    give the same bits as loads after it."""
     from depth_wise_attention_block_gb300.stack import StackForward
     stk = W.stack(T=T, d=7168 if dtype == torch.bfloat16 else 1024, num_layers=L, block_size=B, seed=90 + T + L,
                   device="cuda", dtype=dtype)
     outs = []
     for early in (True, False):
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, L, B, dev_err=err, early_loads=early)
+        fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, L, B, dev_err=err, early_loads=early, schedule=schedule)
         assert bool(fwd.state.struct.flags & A.ATTNRES_STATE_EARLY_LOADS) == early
         if graph:
             fwd.capture()

@@ -512,9 +512,22 @@ def bench_decode(A, W, dev, peak, reps=20):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
+    # the same forward with every load after the previous kernel's end
+    late = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, early_loads=False)
+    late.capture()
+    for _ in range(3):
+        late.run()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        late.run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_late = e0.elapsed_time(e1) / reps
     return {"stack_decode_T64": {"ms_per_forward": ms, "us_per_layer": 1e3 * ms / (stk.num_layers + 1),
                                  "launches_per_forward": fwd.launches_per_forward(), "forwards_timed": reps,
-                                 "cuda_graph": True}}
+                                 "cuda_graph": True, "early_loads": True,
+                                 "ms_per_forward_without_early_loads": ms_late}}
 
 
 def bench_interblock(A, W, dev, peak, reps=20, cached=(1, 4, 8), Q=12, T=2048):

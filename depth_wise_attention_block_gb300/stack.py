@@ -61,9 +61,10 @@ class StackForward:
         T, d = h0.shape
         self.T, self.d = T, d
         self.W, self.G, self.Sc = W, G, Sc
-        # every kernel between two steps is this library's (or launched by
-        # an on_layer hook without programmatic dependent launch): the fused
-        # steps may load their stored rows early (ATTNRES_STATE_EARLY_LOADS)
+        # the kernel before each fused step is the layer body, which writes
+        # only F and signals its dependents after its own wait: the steps may
+        # load their stored rows early (ATTNRES_STATE_EARLY_LOADS).  on_layer
+        # hooks must not write the state's rows then.
         self.state = AttnResState.allocate(h0, num_layers, block_size, eps, early_loads=early_loads)
         self.r = torch.empty_like(h0)
         self.F = torch.empty_like(h0)

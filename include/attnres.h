@@ -254,12 +254,16 @@ typedef struct attnres_state {
  * partial sum -- before the kernel launched just before it on the stream
  * has finished (programmatic dependent launch), so that their DRAM latency
  * overlaps that kernel; only F_prev waits for it.  attnres_intrablock_step
- * with F_prev does the same with the partial sum and r_inter.  Set it only when no
- * kernel issued between two steps writes the state's rows, and each kernel
- * issued before a step either is launched without programmatic dependent
- * launch or signals its dependents only after it has waited for its own
- * prerequisites, as every kernel of this library does.  The stack drivers
- * of the Python package set it; results are the same bits either way. */
+ * with F_prev does the same with the partial sum and r_inter.  Set it only
+ * when, before every such step, (a) the kernel launched just before it on
+ * the stream writes none of the rows the step reads other than F_prev (in
+ * a stack that kernel is the layer body; a step issued directly after
+ * another step of the same state breaks this), and (b) that kernel is
+ * launched without programmatic dependent launch, or signals its
+ * dependents only after it has waited for its own prerequisites, as every
+ * kernel of this library does: then everything launched before it has
+ * completed when the step starts.  The stack drivers of the Python package
+ * set it; results are the same bits either way. */
 #define ATTNRES_STATE_EARLY_LOADS 0x1
 
 /* Fill *st.  n_block_reps must be >= ceil(L/B) (ATTNRES_ERANGE if

@@ -69,16 +69,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// the same with an L2 cache-eviction policy (from createpolicy) for the box
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
-      "%3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -211,9 +201,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
     if (lane == 0) {
       // producer: the tile's n boxes of tt rows, per stage
       const uint32_t tx = (uint32_t)(p.n * p.tt * 128);
-      // the softmax and weighted sums read these rows again next: keep them
-      // in L2 ahead of other lines (what fits of them)
-      const uint64_t keep = l2_policy_evict_last();
       int issued = 0;
       for (int i = 0; i < nloc; ++i) {
         const int st = i % kTcStages;
@@ -226,7 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) interblock_dots_kernel(const __
         mbar_arrive_expect_tx(fb, tx);
         const int x = (c0 + i) * kTcChunk;
         const uint32_t a = base + st * kTcStageBytes;
-        for (int s = 0; s < p.n; ++s) tma_load_2d_hint(a + s * p.tt * 128, &p.src[s], x, (int)t0, fb, keep);
+        for (int s = 0; s < p.n; ++s) tma_load_2d(a + s * p.tt * 128, &p.src[s], x, (int)t0, fb);
         ++issued;
       }
       // the CTA never exits under a copy: wait for the latest phase of every

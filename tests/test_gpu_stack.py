@@ -287,7 +287,8 @@ def test_bytes_model_counts_k3_sources(A):
     (5, 3, torch.bfloat16, 7168),    # 16 tokens x 8 rows (3 zero rows), ragged last tile
     (3, 12, torch.bfloat16, 7168),   # 32 tokens x 4 rows
     (8, 12, torch.bfloat16, 7168),   # the K3 top block: 16 tokens x 8 rows
-    (9, 16, torch.bfloat16, 1024),   # 8 tokens x 16 rows, 16 channel chunks, Q = 16
+    (9, 16, torch.bfloat16, 1024),   # 8 tokens x 16 rows, 16 channel atoms, Q = 16
+    (5, 12, torch.bfloat16, 1088),   # 17 channel chunks of 64: an odd count, split over CTAs
     (9, 12, torch.float32, 3584),    # fp32 sources: CUDA cores either way
     (8, 9, torch.bfloat16, 7160),    # d not a multiple of 64: CUDA cores either way
 ])

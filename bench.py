@@ -58,6 +58,14 @@ KERNEL_SOURCES = [os.path.join(ROOT, "depth_wise_attention_block_gb300", "csrc",
                   for f in ("ring_kernel.cuh", "ring_fixed_s.cu", "ring_common.cuh", "device_common.cuh")]
 
 
+
+def main_config(ws: int) -> dict:
+    """The workload of the JSON line, the same on both arms."""
+    return {"workload": WORKLOAD, "T": T_MAIN, "d": D_MAIN, "S": S_MAIN, "storage": "bf16",
+            "out": "r bf16 + weights fp32", "seed": 1,
+            "l2": "inputs larger than L2: 3 rotated input sets of 528 MB each",
+            "parallelism": f"token-sharded x{ws}, no data exchange"}
+
 def algorithmic_bytes(T: int, d: int, S: int, esz: int = 2) -> int:
     """Each source row read once, r written once (bf16), weights once (fp32);
     the 28 KB pseudo-query is negligible and not counted."""
@@ -335,8 +343,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "T": T_MAIN, "d": D_MAIN, "S": S_MAIN, "storage": "bf16",
-                   "tokens_per_step": per_step},
+        "config": main_config(ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -831,10 +838,7 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": T_MAIN, "d": D_MAIN, "S": S_MAIN, "storage": "bf16",
-                       "out": "r bf16 + weights fp32", "seed": 1,
-                       "l2": "inputs larger than L2: 3 rotated input sets of 528 MB each",
-                       "parallelism": f"token-sharded x{ws}, no data exchange"},
+            "config": main_config(ws),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "agg_ring_kernel<bf16,bf16,VPT=2,unfused,exact,S=9>",

@@ -35,6 +35,7 @@ __all__ = [
     "attnres_aggregate", "attnres_aggregate_backward", "attnres_aggregate_backward_workspace_size",
     "attnres_interblock", "attnres_interblock_workspace_size", "attnres_intrablock_step", "attnres_num_sources", "attnres_layer_sources", "attnres_block_step",
     "attnres_layer_step", "attnres_synthetic_layer", "attnres_synthetic_layer_backward", "attnres_fold",
+    "attnres_aggregate_fold",
     "attnres_version", "AttnResState",
     "attnres_aggregate_host", "attnres_aggregate_host_workspace_size", "dtype_code", "AttnresError",
 ]
@@ -331,6 +332,30 @@ def attnres_fold(prev: torch.Tensor | None, F: torch.Tensor, dst: torch.Tensor, 
     rc = _N.lib.attnres_fold(_dev_ptr(prev, "prev", F.dtype), _dev_ptr(F, "F"), _dev_ptr(dst, "dst", F.dtype), T, d,
                              dtype_code(F.dtype), _stream_ptr(stream))
     _N.check(rc, "attnres_fold")
+
+
+def attnres_aggregate_fold(sources: Sequence[torch.Tensor], prev: torch.Tensor | None, F: torch.Tensor,
+                           dst: torch.Tensor, w_l: torch.Tensor, out_r: torch.Tensor,
+                           out_weights: torch.Tensor | None = None, eps: float = ATTNRES_DEFAULT_EPS,
+                           dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """One layer over the stored sources and the partial sum dst = prev + F
+    (or F) formed and stored in the same launch; see include/attnres.h.
+    Every row [T, d] of F's dtype; out_r the same; out_weights
+    [T, len(sources) + 1] float32 or None."""
+    T, d = F.shape
+    srcs = list(sources)
+    for i, t in enumerate(srcs + [dst] + ([prev] if prev is not None else []) + [out_r]):
+        if t.shape != (T, d) or t.dtype != F.dtype:
+            raise ValueError(f"row {i}: expected [{T}, {d}] {F.dtype}, got {list(t.shape)} {t.dtype}")
+    if out_weights is not None and out_weights.shape != (T, len(srcs) + 1):
+        raise ValueError("out_weights must be [T, n_stored + 1]")
+    ptrs = (ctypes.c_void_p * max(1, len(srcs)))(*[_dev_ptr(t, f"sources[{i}]") for i, t in enumerate(srcs)])
+    rc = _N.lib.attnres_aggregate_fold(
+        ptrs, len(srcs), _dev_ptr(prev, "prev"), _dev_ptr(F, "F"), _dev_ptr(dst, "dst"), T, d, dtype_code(F.dtype),
+        _dev_ptr(w_l, "w_l", torch.float32), float(eps), _dev_ptr(out_r, "out_r"),
+        _dev_ptr(out_weights, "out_weights", torch.float32), _dev_ptr(dev_err, "dev_err", torch.int32),
+        _stream_ptr(stream))
+    _N.check(rc, "attnres_aggregate_fold")
 
 
 def attnres_debug_wait_test(wait_limit_ns: int, withhold_row: int) -> None:

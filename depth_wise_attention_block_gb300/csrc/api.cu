@@ -238,6 +238,62 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
   return ok();
 }
 
+int attnres_aggregate_fold(const void* const* sources, int n_stored, const void* prev, const void* F, void* dst,
+                           int64_t T, int d, int dtype, const float* w_l, float eps, void* out_r,
+                           float* out_weights, int* dev_err, void* stream) {
+  if (n_stored < 0) return fail(ATTNRES_EINVAL, "n_stored=%d < 0", n_stored);
+  if (n_stored + 1 > ATTNRES_MAX_SOURCES) return fail(ATTNRES_ERANGE, "S=%d > %d", n_stored + 1, ATTNRES_MAX_SOURCES);
+  if (n_stored > 0 && !sources) return fail(ATTNRES_EINVAL, "sources is NULL");
+  if (!valid_dtype(dtype)) return fail(ATTNRES_EDTYPE, "dtype %d", dtype);
+  if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
+  if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  if (T == 0) return ok();
+  if (!w_l || !out_r || !F || !dst) return fail(ATTNRES_EINVAL, "w_l/out_r/F/dst is NULL");
+  for (int s = 0; s < n_stored; ++s)
+    if (!sources[s]) return fail(ATTNRES_EINVAL, "sources[%d] is NULL", s);
+  {
+    const int S = n_stored + 1;
+    const int64_t row = T * d * (dtype == ATTNRES_BF16 ? 2 : 4);
+    // every row read: the stored sources, prev, F, and dst (the new source)
+    const void* rows[ATTNRES_MAX_SOURCES + 2];
+    int nr = 0;
+    for (int s = 0; s < n_stored; ++s) rows[nr++] = sources[s];
+    if (prev) rows[nr++] = prev;
+    rows[nr++] = F;
+    rows[nr++] = dst;
+    const int rc = check_outputs_apart(rows, nr, row, out_r, row, out_weights, T * S * 4);
+    if (rc != ATTNRES_OK) return rc;
+    // dst is written while the rows are read: apart from all of them, except
+    // that it may be prev itself (the partial sum updated in place)
+    for (int s = 0; s < n_stored; ++s)
+      if (overlaps(dst, row, sources[s], row)) return fail(ATTNRES_EINVAL, "dst overlaps sources[%d]", s);
+    if (overlaps(dst, row, F, row)) return fail(ATTNRES_EINVAL, "dst overlaps F");
+    if (prev && prev != dst && overlaps(dst, row, prev, row))
+      return fail(ATTNRES_EINVAL, "dst overlaps prev without being prev");
+  }
+  AggArgs a{};
+  for (int s = 0; s < n_stored; ++s) a.src[s] = sources[s];
+  a.n_stored = n_stored;
+  a.fuse_prev = prev;
+  a.fuse_F = F;
+  a.fuse_dst = dst;
+  a.T = T;
+  a.d = d;
+  a.src_dtype = dtype;
+  a.w = w_l;
+  a.eps = eps;
+  a.out_r = out_r;
+  a.out_dtype = dtype;
+  a.out_a = out_weights;
+  a.dev_err = dev_err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  AggPath path;
+  cudaError_t e = launch_aggregate(a, &path);
+  if (e != cudaSuccess) return cuda_fail(e, "attnres_aggregate_fold launch");
+  return ok();
+}
+
 int64_t attnres_aggregate_host_workspace_size(int S, int64_t chunk_tokens, int d, int src_dtype, int out_dtype,
                                               int with_weights, int slots) {
   if (S < 1) return fail(ATTNRES_EINVAL, "S=%d < 1", S);

@@ -17,8 +17,8 @@ cached [h_0, b_1 .. b_{n-1}] for all of the block's layer queries
 (attnres_intrablock_step).  schedule="hybrid" runs the blocks before
 `two_phase_from` (default 6) in single pass and the later ones (the most
 cached sources, where one shared pass saves the most re-reads) two-phase:
-on a GB300 the 93-layer T = 2048 prefill then takes 4.53 ms against
-4.66 ms in single pass.
+on a GB300 the 93-layer T = 2048 prefill then takes 4.39 ms against
+4.51 ms in single pass.
 """
 from __future__ import annotations
 
@@ -29,8 +29,8 @@ from . import (
     attnres_aggregate,
     attnres_aggregate_backward,
     attnres_aggregate_backward_workspace_size,
+    attnres_aggregate_fold,
     attnres_block_step,
-    attnres_fold,
     attnres_interblock,
     attnres_interblock_workspace_size,
     attnres_intrablock_step,
@@ -238,9 +238,10 @@ class StackBackward:
     granularity, [Tutorial] ch. 4.6).
 
     Per block n, from the last block down:
-      recompute: r_l = attnres_aggregate([h_0, b_1..b_{n-1}, P_l]) for the
-        block's layers, v_l = F_l(r_l), P_{l+1} = P_l + v_l (attnres_fold),
-        keeping every r_l and partial sum P_l;
+      recompute: v_l = F_l(r_l) and r_{l+1} = aggregate over [h_0,
+        b_1..b_{n-1}, P_{l+1}] with P_{l+1} = P_l + v_l formed in the same
+        launch (attnres_aggregate_fold; the block's first layer a plain
+        attnres_aggregate), keeping every r_l and partial sum P_l;
       backward, layer by layer from the block's last: dL/dv_l is the
         gradient of b_n (from later blocks and the final aggregation) plus
         that of the partial sums of the block's later layers, dL/dr_l =
@@ -286,11 +287,14 @@ class StackBackward:
             cached = [st.h0] + b[: n - 1]
             for layer in range(first, last + 1):
                 i = layer - first + 1
-                srcs = cached + ([self.P[i - 1]] if i >= 2 else [])
-                attnres_aggregate(srcs, f.W[layer - 1], self.R[i - 1], eps=eps, stream=stream)
+                if i == 1:
+                    attnres_aggregate(cached, f.W[layer - 1], self.R[0], eps=eps, stream=stream)
+                else:
+                    # P[i-1] = P[i-2] + v_{i-1} (or v_1) formed in the aggregation's launch
+                    attnres_aggregate_fold(cached, self.P[i - 2] if i >= 3 else None, self.v, self.P[i - 1],
+                                           f.W[layer - 1], self.R[i - 1], eps=eps, stream=stream)
                 if layer < last:
                     attnres_synthetic_layer(self.R[i - 1], f.G[layer - 1], f.Sc[layer - 1], self.v, stream=stream)
-                    attnres_fold(self.P[i - 1] if i >= 2 else None, self.v, self.P[i], stream=stream)
             # the block's partial sums have no gradient yet (one memset)
             if stream is None:
                 self.gpart.zero_()
@@ -346,9 +350,12 @@ class StackBackward:
             q = min(n * B, L) - (n - 1) * B
             for i in range(1, q + 1):
                 S = n + (1 if i >= 2 else 0)
-                rows += S + 1                                  # recompute: aggregate reads S, writes r
+                if i == 1:
+                    rows += n + 1                              # recompute: aggregate reads h_0, b_1.., writes r
+                else:
+                    rows += n + (2 if i >= 3 else 1) + 2       # aggregate_fold: stored, (P +) v in; P', r out
                 if i < q:
-                    rows += 2 + (3 if i >= 2 else 2)           # body: r -> v; fold: (P +) v -> P'
+                    rows += 2                                  # body: r -> v
                 rows += (3 if i < q else 2) + 1                # body backward: r, gb (+ gpart) -> gr
                 rows += (2 * S + 1) + S                        # aggregation backward, accumulating
             rows += 1                                          # memset of the partial-sum gradient
@@ -360,6 +367,6 @@ class StackBackward:
         n = 2                                                  # final aggregation backward (+ its dw reduction)
         for k in range(1, N + 1):
             q = min(k * B, L) - (k - 1) * B
-            n += q + 2 * (q - 1)                               # recompute: aggregate, body, fold
+            n += q + (q - 1)                                   # recompute: aggregate (fold fused), body
             n += q * (1 + 2)                                   # body backward, aggregation backward (+ dw reduction)
         return n

@@ -103,6 +103,32 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
                       float* out_weights, int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * attnres_aggregate_fold -- one layer whose last source is a partial sum
+ * formed in the same launch ([Tutorial] ch. 4.3: the partial sum of a block
+ * is the sum of its layer outputs so far), i.e. attnres_layer_step without
+ * a state:
+ *
+ *   p[t,c] = round(prev[t,c] + F[t,c])   (or round(F[t,c]) when prev is
+ *            NULL; fp32 add, rounded to dtype), stored to dst;
+ *   then attnres_aggregate over [sources[0..n_stored-1], p] (p as read back
+ *   from dst's rounding, so the weights see exactly the stored bits).
+ *
+ * sources     host array of n_stored (0..127) device pointers [T, d] of
+ *             dtype (NULL when n_stored = 0)
+ * prev        device [T, d] or NULL; F: device [T, d]; dst: device [T, d]
+ *             (may be prev itself, updated in place, but no other row)
+ * dtype       of every row and of out_r
+ * w_l, eps, out_r, out_weights ([T, n_stored + 1] fp32 or NULL), dev_err,
+ *             stream: as attnres_aggregate.
+ * Results equal attnres_fold followed by attnres_aggregate bit for bit,
+ * with one launch and one row fewer per token.  Outputs may not share
+ * memory with any row (ATTNRES_EINVAL).
+ * ---------------------------------------------------------------------- */
+int attnres_aggregate_fold(const void* const* sources, int n_stored, const void* prev, const void* F, void* dst,
+                           int64_t T, int d, int dtype, const float* w_l, float eps, void* out_r,
+                           float* out_weights, int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * attnres_aggregate_host -- attnres_aggregate on sources, query and outputs
  * that live in HOST memory.  The pages have no counterpart: this is the
  * library's way in for data that starts on the CPU.

@@ -161,6 +161,37 @@ def test_early_loads_change_no_bit(A, T, L, B, dtype, graph, schedule):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+@pytest.mark.parametrize("n,d,dtype,prev,in_place", [
+    (3, 7168, torch.bfloat16, True, False),    # the ring kernel with the source count fixed
+    (8, 7168, torch.bfloat16, False, False),   # nine sources, the partial from F alone
+    (5, 7168, torch.bfloat16, True, True),     # dst is prev, updated in place
+    (5, 1024, torch.float32, True, False),
+    (15, 7168, torch.bfloat16, True, False),   # sixteen sources: the multi-group kernel
+    (2, 1000, torch.bfloat16, True, False),    # 2000-byte rows: the plain-load kernel
+    (0, 7168, torch.bfloat16, True, False),    # the partial sum is the only source
+])
+def test_aggregate_fold_equals_fold_then_aggregate(A, n, d, dtype, prev, in_place):
+    T = 333
+    g = torch.Generator(device="cuda").manual_seed(n * 7 + d)
+    rows = [(torch.randn((T, d), generator=g, device="cuda") * (0.5 + k)).to(dtype) for k in range(n + 2)]
+    srcs, P, F = rows[:n], rows[n], rows[n + 1]
+    w = torch.randn((d,), generator=g, device="cuda") / d ** 0.5
+    # reference: attnres_fold, then attnres_aggregate over [srcs, P']
+    P_ref = torch.empty_like(F)
+    A.attnres_fold(P if prev else None, F, P_ref)
+    r_ref = torch.empty_like(F)
+    a_ref = torch.empty((T, n + 1), device="cuda")
+    A.attnres_aggregate(srcs + [P_ref], w, r_ref, a_ref)
+    dst = P if in_place else torch.empty_like(F)
+    r = torch.empty_like(F)
+    a = torch.empty((T, n + 1), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    A.attnres_aggregate_fold(srcs, P if prev else None, F, dst, w, r, a, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(dst, P_ref) and torch.equal(r, r_ref) and torch.equal(a, a_ref)
+
+
 def test_fused_equals_unfused_bit_for_bit(A):
     L, B, T, d = 14, 4, 33, 7168
     stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=77, device="cuda")

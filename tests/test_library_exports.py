@@ -327,6 +327,33 @@ def test_fold_and_stand_in_backward_reject_bad_arguments(native):
     assert sb(0x1000, 0x2000, 0x3000, 0x5000, None, 0x4000, 4, 0, 1, None) == native.ATTNRES_EINVAL
 
 
+def test_aggregate_fold_rejects_bad_arguments_before_any_launch(native):
+    """Fake (never dereferenced) pointers; rows of 4 x 8 bf16 = 64 bytes."""
+    af = native.lib.attnres_aggregate_fold
+    err = native.lib.attnres_last_error
+    srcs = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    prev, F, dst, w, r, a = 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000
+
+    def call(s=srcs, n=2, pv=prev, f=F, ds=dst, T=4, d=8, dt=1, ww=w, eps=1e-5, rr=r, aa=a):
+        return af(s, n, pv, f, ds, T, d, dt, ww, eps, rr, aa, None, None)
+
+    assert call(f=None) == native.ATTNRES_EINVAL and b"NULL" in err()
+    assert call(ds=None) == native.ATTNRES_EINVAL
+    assert call(n=-1) == native.ATTNRES_EINVAL
+    assert call(n=128) == native.ATTNRES_ERANGE                      # 128 stored + the partial
+    assert call(dt=5) == native.ATTNRES_EDTYPE
+    assert call(eps=-1.0) == native.ATTNRES_EINVAL
+    assert call(T=0, s=None, n=0, pv=None, f=None, ds=None, ww=None, rr=None, aa=None) == 0
+    # dst may be prev itself (in place) but shares no byte with any other row
+    assert call(ds=0x1000 + 32) == native.ATTNRES_EINVAL and b"dst overlaps sources[0]" in err()
+    assert call(ds=F) == native.ATTNRES_EINVAL and b"dst overlaps F" in err()
+    assert call(ds=prev + 16) == native.ATTNRES_EINVAL and b"dst overlaps prev" in err()
+    # outputs share no byte with any row read or written
+    for row in (0x2000, prev, F, dst):
+        assert call(rr=row + 8) == native.ATTNRES_EINVAL and b"overlaps" in err()
+    assert call(aa=F) == native.ATTNRES_EINVAL
+
+
 def test_debug_wait_test_checks_its_row(native):
     assert native.lib.attnres_debug_wait_test(0, 8) == native.ATTNRES_EINVAL
     assert native.lib.attnres_debug_wait_test(0, -2) == native.ATTNRES_EINVAL

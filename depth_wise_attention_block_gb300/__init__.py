@@ -337,11 +337,13 @@ def attnres_fold(prev: torch.Tensor | None, F: torch.Tensor, dst: torch.Tensor, 
 def attnres_aggregate_fold(sources: Sequence[torch.Tensor], prev: torch.Tensor | None, F: torch.Tensor,
                            dst: torch.Tensor, w_l: torch.Tensor, out_r: torch.Tensor,
                            out_weights: torch.Tensor | None = None, eps: float = ATTNRES_DEFAULT_EPS,
-                           dev_err: torch.Tensor | None = None, stream=None) -> None:
+                           early_loads: bool = False, dev_err: torch.Tensor | None = None, stream=None) -> None:
     """One layer over the stored sources and the partial sum dst = prev + F
     (or F) formed and stored in the same launch; see include/attnres.h.
     Every row [T, d] of F's dtype; out_r the same; out_weights
-    [T, len(sources) + 1] float32 or None."""
+    [T, len(sources) + 1] float32 or None.  early_loads: see
+    ATTNRES_STATE_EARLY_LOADS (only when the kernel just before writes
+    nothing this call reads but F)."""
     T, d = F.shape
     srcs = list(sources)
     for i, t in enumerate(srcs + [dst] + ([prev] if prev is not None else []) + [out_r]):
@@ -353,8 +355,8 @@ def attnres_aggregate_fold(sources: Sequence[torch.Tensor], prev: torch.Tensor |
     rc = _N.lib.attnres_aggregate_fold(
         ptrs, len(srcs), _dev_ptr(prev, "prev"), _dev_ptr(F, "F"), _dev_ptr(dst, "dst"), T, d, dtype_code(F.dtype),
         _dev_ptr(w_l, "w_l", torch.float32), float(eps), _dev_ptr(out_r, "out_r"),
-        _dev_ptr(out_weights, "out_weights", torch.float32), _dev_ptr(dev_err, "dev_err", torch.int32),
-        _stream_ptr(stream))
+        _dev_ptr(out_weights, "out_weights", torch.float32), ATTNRES_STATE_EARLY_LOADS if early_loads else 0,
+        _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
     _N.check(rc, "attnres_aggregate_fold")
 
 

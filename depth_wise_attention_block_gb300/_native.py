@@ -84,8 +84,8 @@ def _load() -> ctypes.CDLL:
     sp = ctypes.POINTER(AttnresState)
     sig = {
         "attnres_aggregate": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, vp, f32, vp, i32, vp, vp, vp]),
-        "attnres_aggregate_fold": (i32, [ctypes.POINTER(vp), i32, vp, vp, vp, i64, i32, i32, vp, f32, vp, vp, vp,
-                                         vp]),
+        "attnres_aggregate_fold": (i32, [ctypes.POINTER(vp), i32, vp, vp, vp, i64, i32, i32, vp, f32, vp, vp, i32,
+                                         vp, vp]),
         "attnres_aggregate_host": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, vp, f32, vp, i32, vp, i64, vp,
                                           i64, vp, vp]),
         "attnres_aggregate_host_workspace_size": (i64, [i32, i64, i32, i32, i32, i32, i32]),

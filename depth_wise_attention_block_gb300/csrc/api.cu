@@ -240,7 +240,7 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
 
 int attnres_aggregate_fold(const void* const* sources, int n_stored, const void* prev, const void* F, void* dst,
                            int64_t T, int d, int dtype, const float* w_l, float eps, void* out_r,
-                           float* out_weights, int* dev_err, void* stream) {
+                           float* out_weights, int flags, int* dev_err, void* stream) {
   if (n_stored < 0) return fail(ATTNRES_EINVAL, "n_stored=%d < 0", n_stored);
   if (n_stored + 1 > ATTNRES_MAX_SOURCES) return fail(ATTNRES_ERANGE, "S=%d > %d", n_stored + 1, ATTNRES_MAX_SOURCES);
   if (n_stored > 0 && !sources) return fail(ATTNRES_EINVAL, "sources is NULL");
@@ -248,6 +248,7 @@ int attnres_aggregate_fold(const void* const* sources, int n_stored, const void*
   if (T < 0 || d < 1) return fail(ATTNRES_EINVAL, "T=%lld d=%d", (long long)T, d);
   if (!size_ok(T, d)) return fail(ATTNRES_ERANGE, "T*d too large");
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ATTNRES_EINVAL, "eps must be finite and >= 0");
+  if (flags & ~ATTNRES_STATE_EARLY_LOADS) return fail(ATTNRES_EINVAL, "flags 0x%x: unknown bits", flags);
   if (T == 0) return ok();
   if (!w_l || !out_r || !F || !dst) return fail(ATTNRES_EINVAL, "w_l/out_r/F/dst is NULL");
   for (int s = 0; s < n_stored; ++s)
@@ -278,6 +279,7 @@ int attnres_aggregate_fold(const void* const* sources, int n_stored, const void*
   a.fuse_prev = prev;
   a.fuse_F = F;
   a.fuse_dst = dst;
+  a.early_loads = (flags & ATTNRES_STATE_EARLY_LOADS) != 0;
   a.T = T;
   a.d = d;
   a.src_dtype = dtype;

@@ -65,6 +65,7 @@ class StackForward:
         # only F and signals its dependents after its own wait: the steps may
         # load their stored rows early (ATTNRES_STATE_EARLY_LOADS).  on_layer
         # hooks must not write the state's rows then.
+        self.early_loads = early_loads
         self.state = AttnResState.allocate(h0, num_layers, block_size, eps, early_loads=early_loads)
         self.r = torch.empty_like(h0)
         self.F = torch.empty_like(h0)
@@ -291,8 +292,11 @@ class StackBackward:
                     attnres_aggregate(cached, f.W[layer - 1], self.R[0], eps=eps, stream=stream)
                 else:
                     # P[i-1] = P[i-2] + v_{i-1} (or v_1) formed in the aggregation's launch
+                    # (early loads: the body just before writes only v, and every kernel
+                    # here signals its dependents after its own wait)
                     attnres_aggregate_fold(cached, self.P[i - 2] if i >= 3 else None, self.v, self.P[i - 1],
-                                           f.W[layer - 1], self.R[i - 1], eps=eps, stream=stream)
+                                           f.W[layer - 1], self.R[i - 1], eps=eps, early_loads=f.early_loads,
+                                           stream=stream)
                 if layer < last:
                     attnres_synthetic_layer(self.R[i - 1], f.G[layer - 1], f.Sc[layer - 1], self.v, stream=stream)
             # the block's partial sums have no gradient yet (one memset)

@@ -120,13 +120,18 @@ int attnres_aggregate(const void* const* sources, int S, int64_t T, int d, int s
  * dtype       of every row and of out_r
  * w_l, eps, out_r, out_weights ([T, n_stored + 1] fp32 or NULL), dev_err,
  *             stream: as attnres_aggregate.
+ * flags       0, or ATTNRES_STATE_EARLY_LOADS: the stored rows and prev of
+ *             the first token are loaded before the kernel launched just
+ *             before this call has finished, only F after it -- under the
+ *             conditions given at that flag (here: that kernel writes
+ *             nothing this call reads except F).
  * Results equal attnres_fold followed by attnres_aggregate bit for bit,
  * with one launch and one row fewer per token.  Outputs may not share
  * memory with any row (ATTNRES_EINVAL).
  * ---------------------------------------------------------------------- */
 int attnres_aggregate_fold(const void* const* sources, int n_stored, const void* prev, const void* F, void* dst,
                            int64_t T, int d, int dtype, const float* w_l, float eps, void* out_r,
-                           float* out_weights, int* dev_err, void* stream);
+                           float* out_weights, int flags, int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * attnres_aggregate_host -- attnres_aggregate on sources, query and outputs

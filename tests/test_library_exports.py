@@ -334,8 +334,8 @@ def test_aggregate_fold_rejects_bad_arguments_before_any_launch(native):
     srcs = (ctypes.c_void_p * 2)(0x1000, 0x2000)
     prev, F, dst, w, r, a = 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000
 
-    def call(s=srcs, n=2, pv=prev, f=F, ds=dst, T=4, d=8, dt=1, ww=w, eps=1e-5, rr=r, aa=a):
-        return af(s, n, pv, f, ds, T, d, dt, ww, eps, rr, aa, None, None)
+    def call(s=srcs, n=2, pv=prev, f=F, ds=dst, T=4, d=8, dt=1, ww=w, eps=1e-5, rr=r, aa=a, flags=0):
+        return af(s, n, pv, f, ds, T, d, dt, ww, eps, rr, aa, flags, None, None)
 
     assert call(f=None) == native.ATTNRES_EINVAL and b"NULL" in err()
     assert call(ds=None) == native.ATTNRES_EINVAL
@@ -343,6 +343,7 @@ def test_aggregate_fold_rejects_bad_arguments_before_any_launch(native):
     assert call(n=128) == native.ATTNRES_ERANGE                      # 128 stored + the partial
     assert call(dt=5) == native.ATTNRES_EDTYPE
     assert call(eps=-1.0) == native.ATTNRES_EINVAL
+    assert call(flags=2) == native.ATTNRES_EINVAL and b"unknown bits" in err()
     assert call(T=0, s=None, n=0, pv=None, f=None, ds=None, ww=None, rr=None, aa=None) == 0
     # dst may be prev itself (in place) but shares no byte with any other row
     assert call(ds=0x1000 + 32) == native.ATTNRES_EINVAL and b"dst overlaps sources[0]" in err()

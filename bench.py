@@ -374,11 +374,24 @@ def bench_main(args, A, W, dev, ws):
     # untimed, into a CUDA graph and replayed in the timed region, so that
     # no host-side launch gap (Python marshalling, the clock sampler's
     # thread) lands between them.
+    # The region is timed twice at once: by event nodes at the graph's first
+    # and last node (the device time of the K steps), and by events on the
+    # stream around the replay (which also hold the host's graph launch and
+    # its upload to the device).  The first is the line's figure.
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
+    try:
+        g0 = torch.cuda.Event(enable_timing=True, external=True)
+        g1 = torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:  # a PyTorch without event nodes in graphs
+        g0 = g1 = None
     with torch.cuda.graph(graph, stream=cap):
+        if g0 is not None:
+            g0.record(cap)
         for i in range(K):
             step(i, on=cap)
+        if g1 is not None:
+            g1.record(cap)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index or 0)
@@ -392,7 +405,8 @@ def bench_main(args, A, W, dev, ws):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     barrier(ws)
-    region_ms = e0.elapsed_time(e1)
+    region_ms_stream = e0.elapsed_time(e1)
+    region_ms = g0.elapsed_time(g1) if g0 is not None else region_ms_stream
     del graph
     # a separate pass with events around every launch: each launch alone,
     # front end included (reported beside the region's average)
@@ -406,7 +420,9 @@ def bench_main(args, A, W, dev, ws):
     torch.cuda.synchronize()
     per_launch = [s.elapsed_time(e) for s, e in ev]           # ms
     assert int(err.item()) == 0, "device error flag set"
-    return {"region_ms": region_ms, "launch_ms_mean": statistics.fmean(per_launch),
+    return {"region_ms": region_ms, "region_ms_stream": region_ms_stream,
+            "region_from": "event nodes in the graph" if g0 is not None else "events on the stream",
+            "launch_ms_mean": statistics.fmean(per_launch),
             "launch_ms_median": statistics.median(per_launch), "per_launch_pass": Kp, "wall_s": t_wall,
             "clocks": sampler.summary(),
             "launches": K, "sets": sets}
@@ -779,6 +795,7 @@ def run_gpu(args):
     peak, peak_src = hbm_peak()
     m = bench_main(args, A, W, dev, ws)
     region_ms = max_over_ranks(m["region_ms"], ws, dev)
+    region_ms_stream = max_over_ranks(m["region_ms_stream"], ws, dev)
     iso_ms = max_over_ranks(m["launch_ms_mean"], ws, dev)
     ms_per_step = region_ms / args.steps
     value = ws * T_MAIN * args.steps / (region_ms * 1e-3)
@@ -844,9 +861,13 @@ def run_gpu(args):
                          "kernel": "agg_ring_kernel<bf16,bf16,VPT=2,unfused,exact,S=9>",
                          "algorithmic_bytes_per_launch": bytes_launch, "peak_source": peak_src,
                          "launch_ms": ms_per_step,
-                         "launch_duration_from": f"CUDA events at the ends of the timed region: {args.steps} "
+                         "launch_duration_from": f"CUDA events at the ends of the timed region ({m['region_from']}"
+                                                 f": the graph's first and last node): {args.steps} "
                                                  "launches of this kernel back to back on its stream, "
                                                  "replayed from a CUDA graph recorded before the region",
+                         "launch_ms_stream_events": region_ms_stream / args.steps,
+                         "stream_events_from": "events on the stream around the graph replay (adds the host's "
+                                               "graph launch and upload to the region)",
                          "isolated_launch_ms_mean": iso_ms, "isolated_launch_ms_median": m["launch_ms_median"],
                          "frac_isolated_launch": achieved_iso / peak,
                          "isolated_from": f"CUDA events around each of {m['per_launch_pass']} launches in a "

@@ -353,12 +353,14 @@ def test_interblock_every_source_count_at_k3_width(A, n):
     test_interblock_pass_matches_the_oracle(A, n, 12 if n % 2 else 7, torch.bfloat16, 7168, True)
 
 
-@pytest.mark.parametrize("T,n,Q", [(16, 8, 12), (64, 6, 12), (160, 8, 12), (153, 3, 5), (310, 8, 16)])
+@pytest.mark.parametrize("T,n,Q", [(16, 8, 12), (64, 6, 12), (160, 8, 12), (153, 3, 5), (310, 8, 16),
+                                   (1, 4, 12), (16, 2, 1)])
 def test_interblock_tail_split_by_query_groups(A, T, n, Q):
     """The tokens of the last, partial round of the persistent grid are
     split by query groups over the idle CTAs: T = 16 (9 groups, 1-2 queries
     each), 64 (2 groups), 160 (8 leftover tokens, one query per CTA), 153
-    (one leftover token, Q = 5 groups), 310 (6 leftover tokens, 16 groups)."""
+    (one leftover token, Q = 5 groups), 310 (6 leftover tokens, 16 groups),
+    one token (12 CTAs, a query each), one query (no split)."""
     test_interblock_pass_matches_the_oracle(A, n, Q, torch.bfloat16, 7168, True, T=T)
 
 

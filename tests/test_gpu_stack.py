@@ -353,6 +353,29 @@ def test_interblock_every_source_count_at_k3_width(A, n):
     test_interblock_pass_matches_the_oracle(A, n, 12 if n % 2 else 7, torch.bfloat16, 7168, True)
 
 
+def _random_interblock_cases(n_cases=12, seed=20261202):
+    """Seeded shapes for the tensor-core pass: T across tile (16-128 tokens)
+    and persistent-round (152) boundaries, every source count, query counts
+    1..16, d any multiple of 64 up to 8192 (so the channel splits vary);
+    sized for an oracle of about a second each."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n_cases:
+        n = int(rng.integers(1, 10))
+        Q = int(rng.integers(1, 17))
+        d = 64 * int(rng.integers(1, 129))
+        T = int(rng.choice([int(rng.integers(1, 40)), int(rng.integers(100, 200)), int(rng.integers(290, 700))]))
+        if n * T * d * Q > 400_000_000:
+            continue
+        cases.append((T, n, Q, d))
+    return cases
+
+
+@pytest.mark.parametrize("T,n,Q,d", _random_interblock_cases())
+def test_interblock_random_shapes(A, T, n, Q, d):
+    test_interblock_pass_matches_the_oracle(A, n, Q, torch.bfloat16, d, True, T=T)
+
+
 @pytest.mark.parametrize("T,n,Q", [(16, 8, 12), (64, 6, 12), (160, 8, 12), (153, 3, 5), (310, 8, 16),
                                    (1, 4, 12), (16, 2, 1)])
 def test_interblock_tail_split_by_query_groups(A, T, n, Q):

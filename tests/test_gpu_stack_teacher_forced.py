@@ -108,17 +108,20 @@ def test_decode_stack_T64_two_phase_every_layer(A, schedule):
     print(f"decode T=64 {schedule} per layer: worst weight error {wa:.3g}, worst r {wr:.3g} x bar")
 
 
-def test_prefill_stack_T2048_every_layer_sampled_tokens(A):
+@pytest.mark.parametrize("schedule", ["single", "hybrid"])
+def test_prefill_stack_T2048_every_layer_sampled_tokens(A, schedule):
     # 93-layer bf16 stack, T = 2048, seed 2; tokens at the persistent CTAs'
     # boundaries (token t goes to CTA t mod 152: CTAs 0..71 take 14 tokens,
-    # 72..151 take 13) plus a seeded random sample, 64 in all
+    # 72..151 take 13; in the inter-block pass tokens 1976..2047 are split in
+    # two query halves) plus a seeded random sample, 64 in all.  Hybrid: the
+    # blocks from the fifth on run two-phase.
     stk = W.stack_T2048(device="cuda")
     edge = [0, 1, 71, 72, 151, 152, 1975, 1976, 2046, 2047]
     g = torch.Generator().manual_seed(2048)
     rest = [t for t in torch.randperm(2048, generator=g).tolist() if t not in edge][: 64 - len(edge)]
     tokens = torch.tensor(sorted(edge + rest), device="cuda")
-    wa, wr = _teacher_forced_forward(A, stk, tokens)
-    print(f"prefill T=2048 per layer ({tokens.numel()} tokens): worst weight error {wa:.3g}, "
+    wa, wr = _teacher_forced_forward(A, stk, tokens, schedule=schedule)
+    print(f"prefill T=2048 {schedule} per layer ({tokens.numel()} tokens): worst weight error {wa:.3g}, "
           f"worst r {wr:.3g} x bar")
 
 

@@ -108,6 +108,15 @@ def test_decode_stack_T64_two_phase_every_layer(A, schedule):
     print(f"decode T=64 {schedule} per layer: worst weight error {wa:.3g}, worst r {wr:.3g} x bar")
 
 
+def test_full_attnres_bf16_stack_every_layer(A):
+    # block size 1 (Full AttnRes): layer l aggregates all l earlier outputs,
+    # up to 94 sources at the final aggregation -- the multi-group kernel
+    # fused into the stack steps, every layer at the single-layer bars
+    stk = W.stack(T=32, num_layers=93, block_size=1, seed=7, device="cuda")
+    wa, wr = _teacher_forced_forward(A, stk, torch.arange(32, device="cuda"))
+    print(f"Full AttnRes bf16 T=32 per layer: worst weight error {wa:.3g}, worst r {wr:.3g} x bar")
+
+
 @pytest.mark.parametrize("schedule", ["single", "hybrid"])
 def test_prefill_stack_T2048_every_layer_sampled_tokens(A, schedule):
     # 93-layer bf16 stack, T = 2048, seed 2; tokens at the persistent CTAs'

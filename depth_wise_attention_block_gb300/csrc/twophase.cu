@@ -73,18 +73,28 @@ __device__ __forceinline__ bool inter_unit(const InterParams& ip, int k, long lo
 }
 
 // The producer of the DOTS kernels: every source row of this CTA's units'
-// tokens, in unit order (otherwise as ring_produce).
+// tokens, in unit order (otherwise as ring_produce).  The kernel before a
+// DOTS kernel is always the tensor-core logits kernel, which waits for its
+// own predecessor before it lets this one launch: the sources, written
+// before that, are complete when this kernel starts.  So the rows fill the
+// ring before the wait for the logits kernel, which comes only when the
+// ring is full (and precedes the signal to this kernel's dependents).
 __device__ __forceinline__ void inter_produce(const InterParams& ip, RingShared& sh, uint32_t ring) {
   const RingParams& p = ip.rp;
   const int nslots = p.nslots;
   uint32_t slot = 0, lap = 0;
   long long issued = 0;
-  bool ok = true;
+  bool ok = true, waited = false;
   long long t;
   int qlo, qhi;
   for (int k = 0; ok && inter_unit(ip, k, &t, &qlo, &qhi); ++k) {
     const long long off = t * (long long)p.row_bytes;
     for (int j = 0; j < p.S; ++j) {
+      if (!waited && issued == nslots) {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+      }
       if (!mbar_wait_bounded(smem_addr(&sh.empty[slot]), (lap & 1u) ^ 1u, p.wait_ns)) {
         ok = false;
         break;
@@ -100,6 +110,10 @@ __device__ __forceinline__ void inter_produce(const InterParams& ip, RingShared&
         ++lap;
       }
     }
+  }
+  if (!waited) {
+    pdl_wait();
+    pdl_trigger();
   }
   if (!ok) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
   ring_drain(sh.full, nslots, issued, p.withhold_row1);
@@ -410,13 +424,16 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
   const int nquad = 2 * p.nvec;  // 8-byte quads (4 bf16) per row
   ring_init(p, sh);
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   if (warp == kRingConsumerWarps) {
+    // the producer streams the rows before it waits for the logits kernel
     if (lane == 0) inter_produce(ip, sh, ring);
+    pdl_wait();
+    pdl_trigger();
     return;
   }
+  pdl_wait();  // the partial dots come from the logits kernel
+  pdl_trigger();  // the next kernel may launch once this one's prerequisites are done
 
   const int S = NS > 0 ? NS : p.S;
   // sources whose quads stay in registers: the most that fit, with the n

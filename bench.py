@@ -784,11 +784,12 @@ def run_only(args):
 
 def run_gpu(args):
     ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    # the rank's GPU first, so that the process group binds to it
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
     import depth_wise_attention_block_gb300 as A
     import workloads as W
 

@@ -182,13 +182,16 @@ def attnres_interblock_workspace_size(n: int, T: int, d: int, dtype: torch.dtype
 def attnres_interblock(sources: Sequence[torch.Tensor], w_queries: Sequence[torch.Tensor] | torch.Tensor,
                        out_r: torch.Tensor, out_lse: torch.Tensor, out_weights: torch.Tensor | None = None,
                        eps: float = ATTNRES_DEFAULT_EPS, workspace: torch.Tensor | None = None,
-                       tensor_cores: bool = True, dev_err: torch.Tensor | None = None, stream=None) -> None:
+                       tensor_cores: bool = True, dev_err: torch.Tensor | None = None, stream=None,
+                       out_r0: torch.Tensor | None = None, out_weights0: torch.Tensor | None = None) -> None:
     """Phase 1 of the two-phase schedule: the n cached sources aggregated for
     Q queries at once.  out_r [Q, T, d] fp32, out_lse [Q, T] fp32,
     out_weights [Q, T, n] fp32 or None.  With tensor_cores (bf16 sources, d
     a multiple of 64) the logits run on the tensor cores in a workspace of
     attnres_interblock_workspace_size bytes (allocated here through torch
-    when None); tensor_cores=False keeps every step on the CUDA cores."""
+    when None); tensor_cores=False keeps every step on the CUDA cores.
+    out_r0 [T, d] of the sources' dtype and out_weights0 [T, n] fp32 (or
+    None): the block's first layer's output and weights, written here."""
     srcs = list(sources)
     qs = list(w_queries.unbind(0)) if isinstance(w_queries, torch.Tensor) else list(w_queries)
     T, d = srcs[0].shape
@@ -205,8 +208,9 @@ def attnres_interblock(sources: Sequence[torch.Tensor], w_queries: Sequence[torc
     qp = (ctypes.c_void_p * len(qs))(*[_dev_ptr(q, f"w_queries[{i}]", torch.float32) for i, q in enumerate(qs)])
     rc = _N.lib.attnres_interblock(sp, len(srcs), T, d, dtype_code(dt), qp, len(qs), float(eps),
                                    _dev_ptr(out_r, "out_r", torch.float32), _dev_ptr(out_lse, "out_lse", torch.float32),
-                                   _dev_ptr(out_weights, "out_weights", torch.float32), ws_ptr, ws_bytes,
-                                   _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
+                                   _dev_ptr(out_weights, "out_weights", torch.float32),
+                                   _dev_ptr(out_r0, "out_r0", dt), _dev_ptr(out_weights0, "out_weights0", torch.float32),
+                                   ws_ptr, ws_bytes, _dev_ptr(dev_err, "dev_err", torch.int32), _stream_ptr(stream))
     _N.check(rc, "attnres_interblock")
 
 

@@ -95,7 +95,7 @@ def _load() -> ctypes.CDLL:
         "attnres_aggregate_backward_noalloc": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, vp, f32, vp,
                                                       ctypes.POINTER(vp), i32, vp, vp, vp]),
         "attnres_interblock": (i32, [ctypes.POINTER(vp), i32, i64, i32, i32, ctypes.POINTER(vp), i32, f32, vp, vp,
-                                      vp, vp, i64, vp, vp]),
+                                      vp, vp, vp, vp, i64, vp, vp]),
         "attnres_interblock_workspace_size": (i64, [i32, i64, i32, i32, i32]),
         "attnres_intrablock_step": (i32, [sp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "attnres_state_init": (i32, [sp, vp, ctypes.POINTER(vp), i32, vp, i64, i32, i32, i32, i32, f32]),

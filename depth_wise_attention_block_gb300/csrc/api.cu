@@ -545,7 +545,8 @@ int64_t attnres_interblock_workspace_size(int n, int64_t T, int d, int dtype, in
 
 int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int dtype,
                        const float* const* w_queries, int Q, float eps, float* out_r, float* out_lse,
-                       float* out_weights, void* workspace, int64_t workspace_bytes, int* dev_err, void* stream) {
+                       float* out_weights, void* out_r0, float* out_weights0, void* workspace,
+                       int64_t workspace_bytes, int* dev_err, void* stream) {
   if (!sources || !w_queries) return fail(ATTNRES_EINVAL, "sources/w_queries is NULL");
   if (n < 1 || n > 9) return fail(ATTNRES_ERANGE, "n=%d cached sources: 1..9", n);
   if (Q < 1 || Q > kMaxQueries) return fail(ATTNRES_ERANGE, "Q=%d queries: 1..%d", Q, kMaxQueries);
@@ -579,8 +580,21 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
       if (overlaps(out_lse, lse_bytes, sources[s], row)) return fail(ATTNRES_EINVAL, "out_lse overlaps source %d", s);
     if (overlaps(out_lse, lse_bytes, out_r, r_bytes) || (out_weights && overlaps(out_lse, lse_bytes, out_weights, a_bytes)))
       return fail(ATTNRES_EINVAL, "out_lse overlaps another output");
+    // the block's first-layer outputs: apart from the sources and every other output
+    const void* outs[5] = {out_r, out_lse, out_weights, out_r0, out_weights0};
+    const int64_t sizes[5] = {r_bytes, lse_bytes, a_bytes, row, (int64_t)T * n * 4};
+    const char* names[5] = {"out_r", "out_lse", "out_weights", "out_r0", "out_weights0"};
+    for (int i = 3; i < 5; ++i) {
+      if (!outs[i]) continue;
+      for (int s = 0; s < n; ++s)
+        if (overlaps(outs[i], sizes[i], sources[s], row)) return fail(ATTNRES_EINVAL, "%s overlaps source %d", names[i], s);
+      for (int j = 0; j < 5; ++j)
+        if (j != i && outs[j] && overlaps(outs[i], sizes[i], outs[j], sizes[j]))
+          return fail(ATTNRES_EINVAL, "%s overlaps %s", names[i], names[j]);
+    }
   }
   if (!twophase_pointers_ok(out_r)) return fail(ATTNRES_EINVAL, "out_r not 16-byte aligned");
+  if (out_r0 && !twophase_pointers_ok(out_r0)) return fail(ATTNRES_EINVAL, "out_r0 not 16-byte aligned");
   if (workspace) {
     // the tensor-core logits: the workspace holds the partial dot products;
     // it may not share memory with an input or output
@@ -599,7 +613,9 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
         if (overlaps(workspace, need, sources[s], row)) return fail(ATTNRES_EINVAL, "workspace overlaps source %d", s);
       if (overlaps(workspace, need, out_r, (int64_t)Q * T * d * 4) ||
           overlaps(workspace, need, out_lse, (int64_t)Q * T * 4) ||
-          (out_weights && overlaps(workspace, need, out_weights, (int64_t)Q * T * n * 4)))
+          (out_weights && overlaps(workspace, need, out_weights, (int64_t)Q * T * n * 4)) ||
+          (out_r0 && overlaps(workspace, need, out_r0, row)) ||
+          (out_weights0 && overlaps(workspace, need, out_weights0, (int64_t)T * n * 4)))
         return fail(ATTNRES_EINVAL, "workspace overlaps an output");
       for (int q = 0; q < Q; ++q)
         if (overlaps(workspace, need, w_queries[q], (int64_t)d * 4))
@@ -617,6 +633,8 @@ int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int 
   a.out_r = out_r;
   a.out_lse = out_lse;
   a.out_a = out_weights;
+  a.out_r0 = out_r0;
+  a.out_a0 = out_weights0;
   a.dev_err = dev_err;
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_interblock(a);

@@ -57,6 +57,8 @@ struct InterArgs {
   float* out_r;    // [Q, T, d]
   float* out_lse;  // [Q, T]
   float* out_a;    // [Q, T, n] or null
+  void* out_r0;    // [T, d] of dtype or null: query 0's row rounded, a block's first layer
+  float* out_a0;   // [T, n] or null: query 0's weights
   void* workspace;  // the tensor-core logits' scratch (interblock_tc_workspace_bytes), or null
   int64_t workspace_bytes;
   int* dev_err;

@@ -42,6 +42,8 @@ struct InterParams {
   float* out_r;    // [Q, T, d] fp32
   float* out_lse;  // [Q, T]
   float* out_a;    // [Q, T, n] or null
+  char* out_r0;    // [T, d] of the sources' type or null: query 0's row, rounded (a block's first layer)
+  float* out_a0;   // [T, n] or null: query 0's weights
   const float* dots;  // DOTS kernels: partial dot products w_q . h_s, [ksplit][T][n][Q]
   int ksplit;
   int tail_groups;  // DOTS kernels: query groups each of the last T mod grid tokens is split into
@@ -126,6 +128,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// A block's first layer takes query 0's row as its output: the merge
+// computes it as 1 * r + 0 before rounding (which turns a -0 into +0);
+// these give the same bits when the pass writes that output itself.
+__device__ __forceinline__ float first_layer_value(float r) { return fmaf(1.0f, r, 0.0f); }
 
 constexpr int kInterGA = 2;  // queries per phase-A group (the logits)
 constexpr int kInterMaxSplit = 16;  // channel splits of the tensor-core logits, at most
@@ -285,6 +292,14 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
       float r[EPV];
 #pragma unroll
       for (int e = 0; e < EPV; ++e) r[e] = nan;
+      if (ip.out_r0) {
+        char* r0row = ip.out_r0 + t * (long long)p.d * (long long)sizeof(Tin);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          const int v = tid + k * kRingConsumers;
+          if (EXACT || v < p.nvec) store_out<Tin, EPV>(r0row, v, r);
+        }
+      }
       for (int q = 0; q < Q; ++q) {
         char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)q * T + t) * (long long)p.d * 4;
 #pragma unroll
@@ -297,6 +312,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
         for (int q = lane; q < Q; q += 32) ip.out_lse[(long long)q * T + t] = nan;
         if (ip.out_a)
           for (int i = lane; i < Q * S; i += 32) ip.out_a[((long long)(i / S) * T + t) * S + i % S] = nan;
+        if (ip.out_a0)
+          for (int s2 = lane; s2 < S; s2 += 32) ip.out_a0[t * S + s2] = nan;
       }
       if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
       break;
@@ -323,6 +340,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
       if (is_src) {
         xs.a2[q][lane] = make_float2(a, a);
         if (ip.out_a) ip.out_a[((long long)q * T + t) * S + lane] = a;
+        if (q == 0 && ip.out_a0) ip.out_a0[t * S + lane] = a;
       }
       if (lane == 0) ip.out_lse[(long long)q * T + t] = m + __logf(esum);
     }
@@ -363,6 +381,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_kernel(const _
               for (int j = 0; j < NP; ++j) f2_unpack(acc[g][j], r[2 * j], r[2 * j + 1]);
               char* orow = reinterpret_cast<char*>(ip.out_r) + ((long long)(q0 + g) * T + t) * (long long)p.d * 4;
               store_out<float, EPV>(orow, v, r);
+              if (q0 + g == 0 && ip.out_r0) {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) r[e] = first_layer_value(r[e]);
+                store_out<Tin, EPV>(ip.out_r0 + t * (long long)p.d * (long long)sizeof(Tin), v, r);
+              }
             }
           }
         }
@@ -543,10 +566,20 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
           if (EXACT || qd < nquad) *reinterpret_cast<float4*>(orow + (size_t)qd * 16) = make_float4(nan, nan, nan, nan);
         }
       }
+      if (qlo == 0 && ip.out_r0) {
+        char* r0row = ip.out_r0 + t * (long long)p.d * 2;
+#pragma unroll
+        for (int m = 0; m < QPT; ++m) {
+          const int qd = tid + m * kRingConsumers;
+          if (EXACT || qd < nquad) *reinterpret_cast<uint2*>(r0row + (size_t)qd * 8) = make_uint2(0x7fc07fc0u, 0x7fc07fc0u);
+        }
+      }
       if (warp == 0) {
         for (int q = qlo + lane; q < qhi; q += 32) ip.out_lse[(long long)q * T + t] = nan;
         if (ip.out_a)
           for (int i = qlo * S + lane; i < qhi * S; i += 32) ip.out_a[((long long)(i / S) * T + t) * S + i % S] = nan;
+        if (qlo == 0 && ip.out_a0)
+          for (int s2 = lane; s2 < S; s2 += 32) ip.out_a0[t * S + s2] = nan;
       }
       if (tid == 0) report_error(p.dev_err, ATTNRES_DEVERR_WAIT_TIMEOUT);
       cp_async_wait_all();  // no copy outlives the CTA
@@ -576,6 +609,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
         if (is_src) {
           xs.a2[q][lane] = make_float2(a, a);
           if (ip.out_a) ip.out_a[((long long)q * T + t) * S + lane] = a;
+          if (q == 0 && ip.out_a0) ip.out_a0[t * S + lane] = a;
         }
         if (lane == 0) ip.out_lse[(long long)q * T + t] = m + __logf(esum);
       }
@@ -617,6 +651,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_interblock_dots_kernel(co
           f2_unpack(acc0, r.x, r.y);
           f2_unpack(acc1, r.z, r.w);
           __stcs(reinterpret_cast<float4*>(orow + q * qstride), r);  // streamed: evict first from L2
+          if (q == 0 && ip.out_r0)  // the block's first layer, in the sources' bf16
+            *reinterpret_cast<uint2*>(ip.out_r0 + (t * (long long)p.d + (long long)qd * 4) * 2) =
+                make_uint2(pack_bf16x2(first_layer_value(r.x), first_layer_value(r.y)),
+                           pack_bf16x2(first_layer_value(r.z), first_layer_value(r.w)));
         }
       }
     }
@@ -1067,6 +1105,8 @@ cudaError_t launch_interblock(const InterArgs& a) {
   ip.out_r = a.out_r;
   ip.out_lse = a.out_lse;
   ip.out_a = a.out_a;
+  ip.out_r0 = static_cast<char*>(a.out_r0);
+  ip.out_a0 = a.out_a0;
   int grid = (int)(a.T < di.sm_count ? a.T : di.sm_count);
   const int smem = kRingHeaderBytes + kInterSharedBytes + nslots * row_bytes;
   const bool exact = nvec == vpt * kRingConsumers;

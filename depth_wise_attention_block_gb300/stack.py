@@ -56,7 +56,7 @@ class StackForward:
 
     def __init__(self, h0, W, G, Sc, num_layers: int, block_size: int, eps: float = 1e-5,
                  keep_weights: bool = True, dev_err: torch.Tensor | None = None, schedule: str = "single",
-                 two_phase_from: int = 6, early_loads: bool = True):
+                 two_phase_from: int = 6, early_loads: bool = True, first_layer_from_pass: bool = True):
         self.L, self.B, self.eps = num_layers, block_size, eps
         T, d = h0.shape
         self.T, self.d = T, d
@@ -66,6 +66,9 @@ class StackForward:
         # load their stored rows early (ATTNRES_STATE_EARLY_LOADS).  on_layer
         # hooks must not write the state's rows then.
         self.early_loads = early_loads
+        # a two-phase block's first layer written by the inter-block pass
+        # itself (its merge would fold nothing and give the same bits)
+        self.first_layer_from_pass = first_layer_from_pass
         self.state = AttnResState.allocate(h0, num_layers, block_size, eps, early_loads=early_loads)
         self.r = torch.empty_like(h0)
         self.F = torch.empty_like(h0)
@@ -100,7 +103,9 @@ class StackForward:
         N = -(-self.L // self.B)
         n2 = max(0, N - self.first_two_phase + 1)            # blocks run two-phase
         closes = n2 - (1 if self.first_two_phase == 1 else 0)  # block_step closing the block before
-        return n2 + closes + 2 * self.L + 1
+        own = n2 if self.first_layer_from_pass else 0        # first layers the pass writes itself
+        per_pass = 2 if self.inter_ws is not None else 1     # tensor-core logits + weighted sums, or one kernel
+        return per_pass * n2 + closes + 2 * self.L + 1 - own
 
     def _issue_two_phase(self, stream=None, on_layer=None) -> None:
         st, L, B = self.state, self.L, self.B
@@ -124,15 +129,18 @@ class StackForward:
             cached = [bufs[p] for p in attnres_layer_sources(st, first)]
             Q = last - first + 1
             A = self.A_flat[: Q * T * n].view(Q, T, n)
+            own = self.first_layer_from_pass
             attnres_interblock(cached, self.W[first - 1:last], self.R_inter[:Q], self.lse_inter[:Q], A,
                                workspace=self.inter_ws, tensor_cores=self.inter_ws is not None,
-                               dev_err=self.dev_err, stream=stream)
+                               dev_err=self.dev_err, stream=stream, out_r0=self.r if own else None,
+                               out_weights0=self.weights[first - 1] if own and self.weights is not None else None)
             for layer in range(first, last + 1):
                 q = layer - first
-                attnres_intrablock_step(st, self.F if layer > first else None, self.W[layer - 1], layer,
-                                        self.R_inter[q], self.lse_inter[q], A[q], self.r,
-                                        self.weights[layer - 1] if self.weights is not None else None,
-                                        dev_err=self.dev_err, stream=stream)
+                if not (own and layer == first):
+                    attnres_intrablock_step(st, self.F if layer > first else None, self.W[layer - 1], layer,
+                                            self.R_inter[q], self.lse_inter[q], A[q], self.r,
+                                            self.weights[layer - 1] if self.weights is not None else None,
+                                            dev_err=self.dev_err, stream=stream)
                 attnres_synthetic_layer(self.r, self.G[layer - 1], self.Sc[layer - 1], self.F, stream=stream)
                 if on_layer is not None:
                     on_layer(layer, self)

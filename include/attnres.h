@@ -390,6 +390,12 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
  *              over the n sources (normalised)
  *   out_lse    device [Q, T] fp32: log sum_s exp(z_qs) of those logits
  *   out_weights device [Q, T, n] fp32 (softmax over the n sources) or NULL
+ *   out_r0     device [T, d] of dtype, 16-byte aligned, or NULL: query 0's
+ *              row rounded to dtype -- the output of the block's first
+ *              layer, the same bits attnres_intrablock_step writes for it
+ *              (which the caller may then skip: it folds nothing there)
+ *   out_weights0 device [T, n] fp32 or NULL: query 0's weights, the first
+ *              layer's (the same bits attnres_intrablock_step writes)
  *   workspace  NULL, or device scratch of at least
  *              attnres_interblock_workspace_size(n, T, d, dtype, Q) bytes,
  *              256-byte aligned, owned by the caller, sharing no memory
@@ -409,8 +415,8 @@ int attnres_layer_step(attnres_state* st, const void* F_prev, const float* w_l, 
  * ---------------------------------------------------------------------- */
 int attnres_interblock(const void* const* sources, int n, int64_t T, int d, int dtype,
                        const float* const* w_queries, int Q, float eps, float* out_r,
-                       float* out_lse, float* out_weights, void* workspace, int64_t workspace_bytes,
-                       int* dev_err, void* stream);
+                       float* out_lse, float* out_weights, void* out_r0, float* out_weights0,
+                       void* workspace, int64_t workspace_bytes, int* dev_err, void* stream);
 
 /* Bytes of workspace attnres_interblock's tensor-core logits need for n
  * sources of T tokens and d channels and Q queries on the current device

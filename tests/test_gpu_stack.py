@@ -131,6 +131,28 @@ def test_full_attnres_bf16_93_layers(A):
     print(f"Full AttnRes bf16 93 layers: worst weight error {wa:.3g}, worst output error {wr:.3g} x bound")
 
 
+@pytest.mark.parametrize("schedule,T,dtype", [("two_phase", 64, torch.bfloat16), ("hybrid", 300, torch.bfloat16),
+                                              ("two_phase", 33, torch.float32)])
+def test_first_layer_from_the_pass_changes_no_bit(A, schedule, T, dtype):
+    """A two-phase block's first layer written by the inter-block pass
+    (out_r0, out_weights0) gives the bits of its merge step."""
+    from depth_wise_attention_block_gb300.stack import StackForward
+    d = 7168 if dtype == torch.bfloat16 else 1024
+    stk = W.stack(T=T, d=d, num_layers=30, block_size=6, seed=11 + T, device="cuda", dtype=dtype)
+    outs = []
+    for own in (True, False):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, 30, 6, dev_err=err, schedule=schedule, two_phase_from=2,
+                           first_layer_from_pass=own)
+        fwd.run()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append((fwd.r.clone(), torch.cat(fwd.weights, dim=1).clone(),
+                     [b.clone() for b in fwd.state.block_reps]))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert all(torch.equal(x, y) for x, y in zip(outs[0][2], outs[1][2]))
+
+
 @pytest.mark.parametrize("T,L,B,dtype,graph,schedule", [
     (64, 93, 12, torch.bfloat16, True, "single"),     # the decode stack, replayed from a CUDA graph
     (64, 93, 12, torch.bfloat16, False, "single"),
@@ -334,8 +356,12 @@ def test_interblock_pass_matches_the_oracle(A, n, Q, dtype, d, tensor_cores, T=1
     R = torch.empty((Q, T, d), device="cuda")
     lse = torch.empty((Q, T), device="cuda")
     Aw = torch.empty((Q, T, n), device="cuda")
-    A.attnres_interblock(list(H.unbind(0)), Wq, R, lse, Aw, tensor_cores=tensor_cores)
+    r0 = torch.empty((T, d), dtype=dtype, device="cuda")
+    a0 = torch.empty((T, n), device="cuda")
+    A.attnres_interblock(list(H.unbind(0)), Wq, R, lse, Aw, tensor_cores=tensor_cores, out_r0=r0, out_weights0=a0)
     torch.cuda.synchronize()
+    # the first layer's outputs: query 0's row rounded (as 1 * r + 0) and its weights
+    assert torch.equal(r0, (R[0] + 0.0).to(dtype)) and torch.equal(a0, Aw[0])
     uses_tc = tensor_cores and A.attnres_interblock_workspace_size(n, T, d, dtype, Q) > 0
     assert uses_tc == (tensor_cores and dtype == torch.bfloat16 and d % 64 == 0)
     for q in range(Q):
@@ -412,7 +438,11 @@ def test_hybrid_stack_matches_the_oracle(A, L, B, T, d, dtype, start):
     stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=73 + L, device="cuda", dtype=dtype)
     fwd = _gpu_stack(A, stk, schedule="hybrid", two_phase_from=start)
     N = -(-L // B)
-    assert fwd.launches_per_forward() == 2 * L + 1 + 2 * max(0, N - start + 1)
+    # per two-phase block: the pass (two kernels with the tensor-core logits,
+    # else one) and the step closing the block before, less the first
+    # layer's merge, which the pass makes unnecessary
+    per_pass = 2 if fwd.inter_ws is not None else 1
+    assert fwd.launches_per_forward() == 2 * L + 1 + per_pass * max(0, N - start + 1)
     store = O.round_bf16 if dtype == torch.bfloat16 else O.round_fp32
     tr = _oracle_stack(stk, store=store)
     tol = A_ATOL if dtype == torch.float32 else STACK_BF16_A_ATOL

@@ -16,7 +16,10 @@ cached [h_0, b_1 .. b_{n-1}] for all of the block's layer queries
 (attnres_interblock), and each layer merges its partial sum in
 (attnres_intrablock_step).  schedule="hybrid" runs the blocks before
 `two_phase_from` (default 6) in single pass and the later ones (the most
-cached sources, where one shared pass saves the most re-reads) two-phase:
+cached sources, where one shared pass saves the most re-reads) two-phase.
+A block whose pass would take more than 9 cached sources or 16 queries
+(more than K3's 8 blocks of 12) runs single pass in either schedule.
+The hybrid schedule is the faster one here:
 on a GB300 the 93-layer T = 2048 prefill then takes 4.35 ms against
 4.51 ms in single pass.
 """
@@ -87,9 +90,10 @@ class StackForward:
         self.schedule = schedule
         # the first block run two-phase
         self.first_two_phase = {"single": None, "two_phase": 1, "hybrid": max(1, int(two_phase_from))}[schedule]
-        if schedule != "single":
+        self.inter_ws = None
+        if any(self._runs_two_phase(n) for n in range(1, -(-num_layers // block_size) + 1)):
             q = min(block_size, num_layers)
-            n_max = -(-num_layers // block_size)          # cached sources of the last block
+            n_max = min(-(-num_layers // block_size), self.PASS_MAX_SOURCES)  # cached sources, at most
             self.R_inter = torch.empty((q, T, d), dtype=torch.float32, device=h0.device)
             self.lse_inter = torch.empty((q, T), dtype=torch.float32, device=h0.device)
             self.A_flat = torch.empty(q * T * n_max, dtype=torch.float32, device=h0.device)
@@ -97,12 +101,26 @@ class StackForward:
             need = max(attnres_interblock_workspace_size(n, T, d, h0.dtype, q) for n in range(1, n_max + 1))
             self.inter_ws = torch.empty(need, dtype=torch.uint8, device=h0.device) if need > 0 else None
 
+    # what one inter-block pass takes (attnres_interblock): cached sources and queries
+    PASS_MAX_SOURCES = 9
+    PASS_MAX_QUERIES = 16
+
+    def _runs_two_phase(self, n: int) -> bool:
+        """Block n runs two-phase: from the schedule's first two-phase block
+        on, while one pass can take its cached sources and its queries (a
+        block beyond that runs single pass)."""
+        if self.first_two_phase is None or n < self.first_two_phase:
+            return False
+        q = min(n * self.B, self.L) - (n - 1) * self.B
+        return n <= self.PASS_MAX_SOURCES and q <= self.PASS_MAX_QUERIES
+
     def launches_per_forward(self) -> int:
         if self.schedule == "single":
             return 2 * self.L + 1
         N = -(-self.L // self.B)
-        n2 = max(0, N - self.first_two_phase + 1)            # blocks run two-phase
-        closes = n2 - (1 if self.first_two_phase == 1 else 0)  # block_step closing the block before
+        two = [n for n in range(1, N + 1) if self._runs_two_phase(n)]
+        n2 = len(two)                                        # blocks run two-phase
+        closes = sum(1 for n in two if n >= 2)               # block_step closing the block before
         own = n2 if self.first_layer_from_pass else 0        # first layers the pass writes itself
         per_pass = 2 if self.inter_ws is not None else 1     # tensor-core logits + weighted sums, or one kernel
         return per_pass * n2 + closes + 2 * self.L + 1 - own
@@ -114,7 +132,7 @@ class StackForward:
         T = self.T
         for n in range(1, -(-L // B) + 1):
             first, last = (n - 1) * B + 1, min(n * B, L)
-            if n < self.first_two_phase:
+            if not self._runs_two_phase(n):
                 # single pass: each step folds the previous layer's output
                 for l in range(first, last + 1):
                     attnres_layer_step(st, self.F if l > 1 else None, self.W[l - 1], l, self.r,

@@ -489,3 +489,38 @@ def test_random_stacks_against_oracle(A, L, B, T, d, dtype):
     tr = _oracle_stack(stk, store=store)
     tol = A_ATOL if dtype == torch.float32 else STACK_BF16_A_ATOL
     _check_stack(fwd, tr, slice(None), dtype, tol, check_blocks=dtype == torch.float32 or L <= 12)
+
+
+def _random_two_phase_stacks(n=10, seed=2026):
+    # seeded layouts for the two-phase and hybrid schedules: L 1..40, block
+    # size 1..12, T 1..300 (the pass's query-split last round included),
+    # widths the two-phase kernels take (tensor-core logits for bf16 with d
+    # a multiple of 64, the CUDA-core pass otherwise), a random first
+    # two-phase block
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        L = int(rng.integers(1, 41))
+        B = int(rng.integers(1, 13))
+        T = int(rng.integers(1, 301))
+        dtype = [torch.bfloat16, torch.float32][int(rng.integers(2))]
+        d = int(rng.choice([64, 256, 1000, 1024, 3584] + ([7168] if dtype == torch.bfloat16 else [])))
+        if dtype == torch.float32 and d == 1000:
+            continue
+        N = -(-L // B)
+        schedule = ["two_phase", "hybrid"][int(rng.integers(2))]
+        start = int(rng.integers(1, N + 1))
+        if T * d * L > 60_000_000:
+            continue
+        out.append((L, B, T, d, dtype, schedule, start))
+    return out
+
+
+@pytest.mark.parametrize("L,B,T,d,dtype,schedule,start", _random_two_phase_stacks())
+def test_random_two_phase_stacks_against_oracle(A, L, B, T, d, dtype, schedule, start):
+    stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=11 * L + B + T, device="cuda", dtype=dtype)
+    fwd = _gpu_stack(A, stk, schedule=schedule, two_phase_from=start)
+    store = O.round_bf16 if dtype == torch.bfloat16 else O.round_fp32
+    tr = _oracle_stack(stk, store=store)
+    tol = A_ATOL if dtype == torch.float32 else STACK_BF16_A_ATOL
+    _check_stack(fwd, tr, slice(None), dtype, tol, check_blocks=dtype == torch.float32 or L <= 12)

@@ -134,18 +134,21 @@ def test_prefill_stack_T2048_every_layer_sampled_tokens(A, schedule):
           f"worst r {wr:.3g} x bar")
 
 
-def test_stack_backward_bf16_every_layer_call(A):
+@pytest.mark.parametrize("schedule", ["single", "hybrid"])
+def test_stack_backward_bf16_every_layer_call(A, schedule):
     # 93-layer bf16 stack backward (block-wise recompute), T = 32, d = 7168:
     # each attnres_aggregate_backward call against the oracle's backward on
     # the bytes it read; source gradients within one bf16 ulp + 1e-3 of the
     # token's largest condition scale (the bar of the single-layer backward
-    # tests), grad_w within 1e-5 of its condition scale
+    # tests), grad_w within 1e-5 of its condition scale.  The forward's
+    # block sums (all the backward keeps) come from either schedule.
     from depth_wise_attention_block_gb300.stack import StackBackward, StackForward
     L, B, T, d = 93, 12, 32, 7168
     stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=17, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(18)
     dr_out = torch.randn((T, d), generator=g, device="cuda").to(torch.bfloat16)
-    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, L, B, keep_weights=False)
+    fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, L, B, keep_weights=False, schedule=schedule,
+                       two_phase_from=5)
     fwd.run()
     bwd = StackBackward(fwd)
     Wq = to64(stk.W)

@@ -216,6 +216,41 @@ def test_aggregate_fold_equals_fold_then_aggregate(A, n, d, dtype, prev, in_plac
     assert torch.equal(dst, P_ref) and torch.equal(r, r_ref) and torch.equal(a, a_ref)
 
 
+def _random_fold_cases(n=12, seed=77):
+    # seeded shapes for the fused fold: stored sources 0..127, T 1..400,
+    # widths on every aggregation kernel, both dtypes, prev or not, in place
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        ns = int(rng.choice([0, 1, 2, 5, 8, 9, 12, 30, 93, 127]))
+        d = int(rng.choice([8, 64, 100, 1000, 3584, 7160, 7168]))
+        T = int(rng.integers(1, 401))
+        dtype = [torch.bfloat16, torch.float32][int(rng.integers(2))]
+        if (ns + 2) * T * d > 40_000_000:
+            continue
+        out.append((ns, d, T, dtype, bool(rng.integers(2)), bool(rng.integers(2))))
+    return out
+
+
+@pytest.mark.parametrize("n,d,T,dtype,prev,in_place", _random_fold_cases())
+def test_aggregate_fold_random_shapes(A, n, d, T, dtype, prev, in_place):
+    """attnres_aggregate_fold = attnres_fold + attnres_aggregate bit for bit
+    on seeded shapes."""
+    g = torch.Generator(device="cuda").manual_seed(n * 131 + d + T)
+    rows = [(torch.randn((T, d), generator=g, device="cuda") * (0.5 + k % 5)).to(dtype) for k in range(n + 2)]
+    srcs, P, F = rows[:n], rows[n], rows[n + 1]
+    w = torch.randn((d,), generator=g, device="cuda") / d ** 0.5
+    P_ref = torch.empty_like(F)
+    A.attnres_fold(P if prev else None, F, P_ref)
+    r_ref, a_ref = torch.empty_like(F), torch.empty((T, n + 1), device="cuda")
+    A.attnres_aggregate(srcs + [P_ref], w, r_ref, a_ref)
+    dst = P if (in_place and prev) else torch.empty_like(F)
+    r, a = torch.empty_like(F), torch.empty((T, n + 1), device="cuda")
+    A.attnres_aggregate_fold(srcs, P if prev else None, F, dst, w, r, a)
+    torch.cuda.synchronize()
+    assert torch.equal(dst, P_ref) and torch.equal(r, r_ref) and torch.equal(a, a_ref)
+
+
 def test_fused_equals_unfused_bit_for_bit(A):
     L, B, T, d = 14, 4, 33, 7168
     stk = W.stack(T=T, d=d, num_layers=L, block_size=B, seed=77, device="cuda")

@@ -488,16 +488,19 @@ def bench_stacks(A, W, dev, peak):
     """The 93-layer stack forwards, replayed from a CUDA graph (the eager
     Python launch loop is also timed), with the single-pass schedule, the
     two-phase one (one inter-block pass per block, one merge per layer) and
-    the hybrid (blocks 5-8 two-phase); and a 16384-token prefill stack in
-    single pass."""
+    the hybrid (blocks 6-8 two-phase); a 16384-token prefill stack in
+    single pass; and a 93-layer Full AttnRes stack (block size 1: layer l
+    aggregates all l earlier outputs, up to 94 sources)."""
     from depth_wise_attention_block_gb300.stack import StackForward
     out = {}
     # the long-prefill stack (T = 16384: h_0 is 235 MB, more than half of L2,
     # so its fused steps stream every row with the default L2 policy)
-    for name, T, seed, reps, schedules in (("stack_prefill_T2048", 2048, 2, 10, ("single", "two_phase", "hybrid")),
-                                           ("stack_decode_T64", 64, 3, 50, ("single", "two_phase", "hybrid")),
-                                           ("stack_prefill_T16384", 16384, 2, 3, ("single",))):
-        stk = W.stack(T=T, seed=seed, device=dev)
+    for name, T, seed, reps, schedules, bs in (
+            ("stack_prefill_T2048", 2048, 2, 10, ("single", "two_phase", "hybrid"), 12),
+            ("stack_decode_T64", 64, 3, 50, ("single", "two_phase", "hybrid"), 12),
+            ("stack_prefill_T16384", 16384, 2, 3, ("single",), 12),
+            ("stack_full_attnres_T2048", 2048, 2, 3, ("single",), 1)):
+        stk = W.stack(T=T, seed=seed, device=dev, block_size=bs)
         for schedule in schedules:
             fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, schedule=schedule)
             eager_ms = _time_forward(fwd, reps)

@@ -21,6 +21,7 @@
 // group has the compile-time size and the per-source guards fold away.
 #include <atomic>
 #include <math.h>
+#include <type_traits>
 
 #include "ring_common.cuh"
 
@@ -113,12 +114,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       volatile int* abort_flag = &sh.abort_flag[buf];
       uint4 x[GS][VPT];
       float part[2 * GS];  // every entry is set below
+      // The group's rows and their partial dots.  Stored sources and padding
+      // rows are single rows; the fused source (index n_stored = S - 1) is
+      // formed from prev and F.  Only the one group that holds it is
+      // compiled with that branch: the others stay straight-line code, so
+      // one row's loads overlap the previous row's arithmetic.
+      auto load_group = [&](auto with_fused) {
 #pragma unroll
-      for (int s = 0; s < GS; ++s) {
-        {
-          // stored sources and padding rows are single rows; the fused
-          // source (index n_stored = S - 1) is formed from prev and F
-          if (!FUSED || g0 + s != p.n_stored) {
+        for (int s = 0; s < GS; ++s) {
+          if (!decltype(with_fused)::value || g0 + s != p.n_stored) {
             consume(x[s]);
           } else {
             // the fused source (the token's last): round(prev + F), stored as
@@ -164,7 +168,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
           part[2 * s] = f2_hsum(dot2[0]) + f2_hsum(dot2[1]);
           part[2 * s + 1] = f2_hsum(ss2[0]) + f2_hsum(ss2[1]);
         }
-      }
+      };
+      if (FUSED && g0 <= p.n_stored && p.n_stored < g0 + GS)
+        load_group(std::true_type{});
+      else
+        load_group(std::false_type{});
 
       // ---- warp totals (a reduce-scatter over the group's 2 GS partials:
       // 13 shuffles for GS = 6), then one CTA-wide step

@@ -89,6 +89,24 @@ def test_multi_group_times_out(A, TIMEOUT_BIT, withheld):
     assert torch.isnan(r[0].float()).all()
 
 
+@pytest.mark.parametrize("prev", [False, True])
+def test_multi_group_fold_times_out(A, TIMEOUT_BIT, withheld, prev):
+    # a fused step over more than 9 sources: the multi-group kernel, which
+    # without prev copies F's ring slot to dst by a bulk copy, with prev
+    # forms round(prev + F) in the consumers
+    inp = W.block_bf16(T=600, d=7168, seed=3, device="cuda", num_blocks=10)
+    stored = [inp.H[s] for s in range(11)]
+    F = inp.H[11].clone()
+    P = torch.zeros_like(F) if prev else None
+    dst = torch.zeros_like(F)
+    r = torch.zeros_like(F)
+    err = _err()
+    A.attnres_aggregate_fold(stored, P, F, dst, inp.w, r, None, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & TIMEOUT_BIT
+    assert torch.isnan(r[0].float()).all()
+
+
 def test_fused_stack_times_out(A, TIMEOUT_BIT, withheld):
     from depth_wise_attention_block_gb300.stack import StackForward
     stk = W.stack(T=256, num_layers=14, block_size=12, seed=9, device="cuda")

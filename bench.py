@@ -484,13 +484,14 @@ def _time_forward(fwd, reps):
     return e0.elapsed_time(e1) / reps
 
 
-def bench_stacks(A, W, dev, peak):
+def bench_stacks(A, W, dev, peak, only=None):
     """The 93-layer stack forwards, replayed from a CUDA graph (the eager
     Python launch loop is also timed), with the single-pass schedule, the
     two-phase one (one inter-block pass per block, one merge per layer) and
     the hybrid (blocks 6-8 two-phase); a 16384-token prefill stack in
     single pass; and a 93-layer Full AttnRes stack (block size 1: layer l
-    aggregates all l earlier outputs, up to 94 sources)."""
+    aggregates all l earlier outputs, up to 94 sources).  only: one stack's
+    name (for profiling)."""
     from depth_wise_attention_block_gb300.stack import StackForward
     out = {}
     # the long-prefill stack (T = 16384: h_0 is 235 MB, more than half of L2,
@@ -500,6 +501,8 @@ def bench_stacks(A, W, dev, peak):
             ("stack_decode_T64", 64, 3, 50, ("single", "two_phase", "hybrid"), 12),
             ("stack_prefill_T16384", 16384, 2, 3, ("single",), 12),
             ("stack_full_attnres_T2048", 2048, 2, 3, ("single",), 1)):
+        if only is not None and name != only:
+            continue
         stk = W.stack(T=T, seed=seed, device=dev, block_size=bs)
         for schedule in schedules:
             fwd = StackForward(stk.h0, stk.W, stk.G, stk.Sc, stk.num_layers, stk.block_size, schedule=schedule)
@@ -781,7 +784,8 @@ def run_only(args):
     else:
         res = {"stacks": bench_stacks, "backward": bench_backward, "small": bench_small_fp32,
                "stack_backward": bench_stack_backward, "decode": bench_decode,
-               "interblock": bench_interblock}[args.only](A, W, dev, peak)
+               "interblock": bench_interblock,
+               "full_stack": lambda *a: bench_stacks(*a, only="stack_full_attnres_T2048")}[args.only](A, W, dev, peak)
     print(json.dumps(res), flush=True)
 
 
@@ -905,7 +909,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count of the --only long / --only full workloads (small cases for profiling)")
     ap.add_argument("--only", choices=["stacks", "long", "full", "small", "backward", "stack_backward", "decode",
-                                       "interblock"],
+                                       "interblock", "full_stack"],
                     help="run one secondary workload alone")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -16,9 +16,13 @@
 //
 // Every source byte is still read from HBM once; each group costs one
 // cross-warp reduction step (one named barrier).  A token's source list is
-// padded to a whole number of groups with re-reads of its source 0 row
-// (L2-resident by then) whose logits are -inf (weight exactly 0), so every
-// group has the compile-time size and the per-source guards fold away.
+// padded to a whole number of groups; a padding position's logit is -inf
+// (weight exactly 0), so every group has the compile-time size and the
+// per-source guards fold away.  In a plain aggregation the padding rows are
+// re-reads of the token's source 0 row (L2-resident by then).  In a fused
+// step the token's last group, which holds the formed source (prev + F),
+// is compiled with per-position checks, and its padding positions take no
+// ring slot and no load: their rows are zero.
 #include <atomic>
 #include <math.h>
 #include <type_traits>
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
   }
 
   const int S = p.S;
-  const int S_pad = S + p.pad_rows;  // a whole number of groups of GS (padding rows weigh 0)
+  const int S_pad = (S + GS - 1) / GS * GS;  // a whole number of groups of GS (padding weighs 0)
   uint32_t slot = 0, lap = 0;
   bool ok = true;
 
@@ -114,15 +118,25 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
       volatile int* abort_flag = &sh.abort_flag[buf];
       uint4 x[GS][VPT];
       float part[2 * GS];  // every entry is set below
-      // The group's rows and their partial dots.  Stored sources and padding
-      // rows are single rows; the fused source (index n_stored = S - 1) is
-      // formed from prev and F.  Only the one group that holds it is
-      // compiled with that branch: the others stay straight-line code, so
-      // one row's loads overlap the previous row's arithmetic.
-      auto load_group = [&](auto with_fused) {
+      // The group's rows and their partial dots.  Stored sources and a plain
+      // aggregation's padding are single rows; a fused step's source (index
+      // n_stored = S - 1) is formed from prev and F, and its padding
+      // positions (index >= S) are zero rows with zero partials, loaded from
+      // nowhere.  Only a fused step's last group is compiled with those
+      // checks: the other groups stay straight-line code, so one row's loads
+      // overlap the previous row's arithmetic.
+      auto load_group = [&](auto last_group) {
+        constexpr bool LAST = decltype(last_group)::value;
 #pragma unroll
         for (int s = 0; s < GS; ++s) {
-          if (!decltype(with_fused)::value || g0 + s != p.n_stored) {
+          if (LAST && g0 + s >= S) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) x[s][k] = make_uint4(0, 0, 0, 0);
+            part[2 * s] = 0.f;
+            part[2 * s + 1] = 0.f;
+            continue;
+          }
+          if (!(LAST && FUSED) || g0 + s != p.n_stored) {
             consume(x[s]);
           } else {
             // the fused source (the token's last): round(prev + F), stored as
@@ -169,7 +183,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) agg_ring_multi_kernel(const _
           part[2 * s + 1] = f2_hsum(ss2[0]) + f2_hsum(ss2[1]);
         }
       };
-      if (FUSED && g0 <= p.n_stored && p.n_stored < g0 + GS)
+      if (FUSED && g0 + GS == S_pad)
         load_group(std::true_type{});
       else
         load_group(std::false_type{});
@@ -269,10 +283,11 @@ static cudaError_t launch_multi_t(const RingParams& rp, int grid, int smem, cuda
   auto kern = agg_ring_multi_kernel<Tin, Tout, VPT, FUSED, EXACT>;
   cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
-  // pad every token's source list to a whole number of groups
+  // a plain aggregation's padding to a whole number of groups: re-reads of
+  // source 0 (a fused step pads without rows)
   constexpr int GS = MultiGroup<Tin, VPT>::kSize;
   RingParams padded = rp;
-  padded.pad_rows = (GS - rp.S % GS) % GS;
+  padded.pad_rows = FUSED ? 0 : (GS - rp.S % GS) % GS;
   e = launch_kernel(kern, dim3(grid), dim3(kRingThreads), (size_t)smem, stream, padded);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

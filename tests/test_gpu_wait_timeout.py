@@ -91,9 +91,9 @@ def test_multi_group_times_out(A, TIMEOUT_BIT, withheld):
 
 @pytest.mark.parametrize("prev", [False, True])
 def test_multi_group_fold_times_out(A, TIMEOUT_BIT, withheld, prev):
-    # a fused step over more than 9 sources: the multi-group kernel, which
-    # without prev copies F's ring slot to dst by a bulk copy, with prev
-    # forms round(prev + F) in the consumers
+    # a fused step over more than 9 sources: the multi-group kernel's fused
+    # form, whose last group forms round(prev + F) (or takes F) and skips
+    # its padding
     inp = W.block_bf16(T=600, d=7168, seed=3, device="cuda", num_blocks=10)
     stored = [inp.H[s] for s in range(11)]
     F = inp.H[11].clone()

@@ -45,6 +45,33 @@ from . import (
 )
 
 
+def stack_forward_bytes(T: int, d: int, esz: int, num_layers: int, block_size: int) -> int:
+    """Byte model of one single-pass stack forward (T tokens of d channels,
+    esz bytes per stored element): each layer step reads its stored sources,
+    the previous partial sum (if the block has one) and F_{l-1} once, and
+    writes the new partial sum or block sum, r and the fp32 weights once;
+    each layer body reads r and writes F (and reads its fp32 g and s)."""
+    L, B = num_layers, block_size
+    row = T * d * esz
+    total = 0
+    for l in range(1, L + 2):
+        S = attnres_num_sources(l, B, L)
+        if l == 1:
+            total += row + row                       # read h_0, write r
+        else:
+            p = l - 1
+            first = (p - 1) // B * B + 1
+            has_prev = p > first
+            total += (S - 1) * row                   # stored sources
+            total += row * (2 if has_prev else 1)    # partial (if any) + F_{l-1}
+            total += row                             # new partial / b_n
+            total += row                             # r_l
+        total += T * S * 4                           # weights
+        if l <= L:
+            total += 2 * row + 2 * d * 4             # F_l: read r, write F (+ g, s)
+    return total
+
+
 class StackForward:
     """Buffers and launch sequence of one stack forward over T tokens.
 
@@ -236,25 +263,7 @@ class StackForward:
     def bytes_moved(self) -> int:
         """Minimum HBM bytes one forward must move (every source row, F row,
         partial/b_n row read once; r, F, partial/b_n and weights written once)."""
-        esz = self.state.h0.element_size()
-        row = self.T * self.d * esz
-        total = 0
-        for l in range(1, self.L + 2):
-            S = self.S[l - 1]
-            if l == 1:
-                total += row + row                       # read h_0, write r
-            else:
-                p = l - 1
-                first = (p - 1) // self.B * self.B + 1
-                has_prev = p > first
-                total += (S - 1) * row                   # stored sources
-                total += row * (2 if has_prev else 1)    # partial (if any) + F_{l-1}
-                total += row                             # new partial / b_n
-                total += row                             # r_l
-            total += self.T * S * 4                      # weights
-            if l <= self.L:
-                total += 2 * row + 2 * self.d * 4        # F_l: read r, write F (+ g, s)
-        return total
+        return stack_forward_bytes(self.T, self.d, self.state.h0.element_size(), self.L, self.B)
 
 
 class StackBackward:
